@@ -1,0 +1,425 @@
+"""Benchmark of the MoBA forward pass on GB300.
+
+One step = one full forward (key pooling, gate + top-k, regroup, attention over
+the selected past blocks, attention over the own block + merge) over one batch
+of seeded synthetic inputs resident in HBM.  Prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload train32k] [--topk 3]
+
+Under torchrun (N > 1) every rank runs the same per-GPU workload on its own
+GPU with its own seed (weak scaling; the heads / sequences of different ranks
+are independent, so there is no data-path collective); rank 0 prints the
+whole-job throughput over the slowest rank's time.  `--impl reference` times
+the CPU oracle on the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoBA fwd tokens/s and effective TFLOP/s (% of BF16 peak) at 32K–1M tokens"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------------------
+# work accounting (exact for the selection rule: past blocks are always full)
+# ---------------------------------------------------------------------------
+
+def issued_pairs(seqlens, block_size: int, topk: int):
+    """(current-block pairs, past-block pairs) of (query, key) with key <= query
+    that the forward attends to, summed over sequences, per head."""
+    cur = past = 0
+    for L in seqlens:
+        n = (L + block_size - 1) // block_size
+        for c in range(n):
+            r = min(block_size, L - c * block_size)
+            cur += r * (r + 1) // 2
+            past += r * min(topk - 1, c) * block_size
+    return cur, past
+
+
+def hbm_bytes(w, topk: int):
+    """Algorithmic HBM bytes of the pooling and gate kernels per forward."""
+    total, H, D = w.total, w.H, w.D
+    nb = sum((L + w.block_size - 1) // w.block_size for L in w.seqlens)
+    pool = total * H * D * 2 + nb * H * D * 4
+    gate = total * H * D * 2 + total * H * topk * 4
+    return {"kpool": pool, "gate": gate}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[3:7]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline and --impl reference)
+# ---------------------------------------------------------------------------
+
+def oracle_rows_rate(w, topk, host, kbar, n_rows, seed):
+    import oracle
+    tok, head = __import__("long_context_sparse_moba_gb300.workloads",
+                           fromlist=["sample_rows"]).sample_rows(w, n_rows, seed=seed)
+    q, k, v = host
+    t0 = time.perf_counter()
+    oracle.moba_rows(q, k, v, w.cu_seqlens(), w.H, w.D, w.block_size, topk, tok, head, kbar=kbar)
+    return len(tok), time.perf_counter() - t0
+
+
+def cpu_oracle_setup(w, inp):
+    import oracle
+    oracle.build()
+    host = tuple(x.reshape(-1, w.H, w.D).cpu() for x in (inp.q, inp.k, inp.v))
+    t0 = time.perf_counter()
+    kbar = oracle.kpool(host[1], inp.cu_seqlens, w.H, w.D, w.block_size)
+    t_pool = time.perf_counter() - t0
+    return host, kbar, t_pool
+
+
+def cpu_baseline(w, inp, topk, budget_s=12.0):
+    """Oracle throughput on a bounded seeded sample of query rows; the pooling
+    of the whole key tensor is charged pro rata to the sampled rows."""
+    import oracle
+    host, kbar, t_pool = cpu_oracle_setup(w, inp)
+    n0, t0 = oracle_rows_rate(w, topk, host, kbar, 512, seed=77)
+    n = int(min(w.total * w.H, max(512, n0 * budget_s / max(t0, 1e-6))))
+    n, t = oracle_rows_rate(w, topk, host, kbar, n, seed=78)
+    frac = n / (w.total * w.H)
+    secs = t + t_pool * frac
+    tokens = n / w.H
+    return {"value": tokens / secs, "unit": "tokens/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"{n} seeded (token, head) rows of the {w.name} workload (top-k {topk}) in "
+                      f"{t:.1f} s plus key pooling of all blocks ({t_pool:.1f} s) charged pro rata "
+                      f"({frac:.3%})"}
+
+
+def run_reference(args, w, topk):
+    """--impl reference: the CPU oracle, timed on the host cores."""
+    import oracle
+    from long_context_sparse_moba_gb300 import workloads
+    inp = workloads.make_inputs(w, device="cpu")
+    host, kbar, t_pool = cpu_oracle_setup(w, inp)
+    n0, t0 = oracle_rows_rate(w, topk, host, kbar, 256, seed=90)
+    rows = int(min(w.total * w.H, max(64, n0 * 0.25 / max(t0, 1e-6))))
+    frac = rows / (w.total * w.H)
+    for s in range(args.warmup):
+        oracle_rows_rate(w, topk, host, kbar, rows, seed=100 + s)
+    times = []
+    for s in range(args.steps):
+        _, t = oracle_rows_rate(w, topk, host, kbar, rows, seed=1000 + s)
+        times.append(t + t_pool * frac)
+    secs = sum(times)
+    tokens = rows / w.H * args.steps
+    value = tokens / secs
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(w, topk),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.max_threads(),
+                             "kind": "oracle",
+                             "sample": f"{rows} seeded (token, head) rows per step plus key "
+                                       f"pooling charged pro rata ({frac:.3%})"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def config_of(w, topk):
+    return {"workload": w.name, "B": w.B, "S": w.S, "H": w.H, "D": w.D,
+            "block_size": w.block_size, "topk": topk, "tokens": w.total,
+            "l2": "inputs larger than L2 (q, k, v %.0f MB)" % (3 * w.total * w.H * w.D * 2 / 1e6)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="train32k")
+    ap.add_argument("--topk", type=int, default=None)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-dense", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from long_context_sparse_moba_gb300 import workloads
+    w = workloads.WORKLOADS[args.workload]
+    topk = args.topk if args.topk is not None else w.topks[0]
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, w, topk)
+        return
+
+    import torch
+    import torch.distributed as dist
+    from long_context_sparse_moba_gb300 import build as _build
+    from long_context_sparse_moba_gb300 import ops
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if rank == 0 or world == 1:
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    ops.lib()
+
+    dev = torch.device("cuda", local)
+    wr = workloads.Workload(**{**w.__dict__, "seed": w.seed + 1000 * rank})
+    inp = workloads.make_inputs(wr, device=dev)
+    q, k, v = inp.q, inp.k, inp.v
+    varlen = w.varlen
+    H, D, bs = w.H, w.D, w.block_size
+    if varlen:
+        cu = torch.tensor(inp.cu_seqlens, dtype=torch.int32, device=dev)
+        ws_bytes = ops.varlen_workspace_size(w.B, w.total, w.S, H, D, bs, topk)
+        lse = torch.empty(H, w.total, dtype=torch.float32, device=dev)
+    else:
+        ws_bytes = ops.workspace_size(w.B, H, w.S, D, bs, topk)
+        lse = torch.empty(w.B, H, w.S, dtype=torch.float32, device=dev)
+    out = torch.empty_like(q)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(topk_=topk, ws_=ws):
+        if varlen:
+            ops.attn_fwd_varlen(q, k, v, cu, w.S, bs, topk_, out=out, lse=lse, workspace=ws_)
+        else:
+            ops.attn_fwd(q, k, v, bs, topk_, out=out, lse=lse, workspace=ws_)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert ops.get_status() == ops.MOBA_OK
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = ops.launch_count()
+    ops.profile_begin(args.steps)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    ncalls, phase_ms = ops.profile_end()
+    launches = ops.launch_count() - launches0
+    clk = clocks.stop()
+    status = ops.get_status()
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_step = elapsed_ms / args.steps
+
+    # dense comparison: same kernels with top-k = number of blocks
+    dense = None
+    n_max = (w.S + bs - 1) // bs
+    if not args.no_dense and topk < n_max:
+        dsteps = 3
+        step(n_max, ws)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(dsteps):
+            step(n_max, ws)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        dms = e0.elapsed_time(e1) / dsteps
+        dcur, dpast = issued_pairs(w.seqlens, bs, n_max)
+        dense = {"topk": n_max, "ms_per_step": dms,
+                 "effective_tflops": 4 * D * (dcur + dpast) * H / (dms * 1e-3) / 1e12,
+                 "sparse_speedup": dms / ms_per_step}
+
+    # end to end through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        esteps = max(3, min(args.steps, 20))
+
+        def e2e_step():
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            step()
+            hout.copy_(out, non_blocking=True)
+            hlse.copy_(lse, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(esteps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = e0.elapsed_time(e1) / esteps
+        if world > 1:
+            t = torch.tensor([ems], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": w.total * world / (ems * 1e-3), "unit": "tokens/s",
+               "h2d_bytes_per_step": 3 * q.numel() * 2,
+               "d2h_bytes_per_step": out.numel() * 2 + lse.numel() * 4,
+               "ms_per_step": ems}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_src = load_peaks()
+    cur, past = issued_pairs(w.seqlens, bs, topk)
+    flops = 4 * D * (cur + past) * H
+    tflops = flops / (ms_per_step * 1e-3) / 1e12
+    per_call = {kk: vv / max(ncalls, 1) for kk, vv in phase_ms.items()}
+    total_phase = sum(per_call.values())
+    hbm = hbm_bytes(w, topk)
+    work = {"kpool": ("hbm", hbm["kpool"]), "gate": ("hbm", hbm["gate"]),
+            "attn_past": ("tensor", 4 * D * past * H), "attn_current": ("tensor", 4 * D * cur * H)}
+    phases = {}
+    for name, ms in per_call.items():
+        ent = {"ms": ms, "share": ms / total_phase if total_phase > 0 else None}
+        if name in work and ms > 0:
+            kind, amount = work[name]
+            if kind == "hbm":
+                ent["gbs"] = amount / (ms * 1e-3) / 1e9
+                ent["frac_hbm"] = ent["gbs"] / peaks["hbm_gbs"]
+            else:
+                ent["tflops"] = amount / (ms * 1e-3) / 1e12
+                ent["frac_bf16"] = ent["tflops"] / peaks["bf16_tflops_sustained"]
+        phases[name] = ent
+    dom = max((n for n in per_call if n in work), key=lambda n: per_call[n])
+    kind, amount = work[dom]
+    dms = per_call[dom]
+    if kind == "hbm":
+        achieved, peak, unit = amount / (dms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
+    else:
+        achieved, peak, unit = (amount / (dms * 1e-3) / 1e12, peaks["bf16_tflops_sustained"],
+                                "TFLOP/s")
+    roofline = {"kernel": dom, "bound": kind, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "traffic": None,
+                "peak_source": f"{peak_src} ({'bf16_tflops_sustained' if kind == 'tensor' else 'hbm_gbs'})"}
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, inp, topk)
+
+    line = {"metric": METRIC, "value": w.total * world / (ms_per_step * 1e-3), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config_of(w, topk),
+            "effective_tflops": tflops * world,
+            "frac_of_bf16_peak": tflops / peaks["bf16_tflops_sustained"],
+            "issued_flops_per_step": flops,
+            "sparsity_vs_dense_causal": None,
+            "roofline": roofline, "phases": phases, "dense": dense, "e2e": e2e,
+            "cpu_baseline": cpu, "gpu_launches": launches, "clocks": clk,
+            "device_status": ops.status_string(status)}
+    dcur, dpast = issued_pairs(w.seqlens, bs, n_max)
+    line["sparsity_vs_dense_causal"] = 1.0 - (cur + past) / (dcur + dpast)
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,177 @@
+/*
+ * moba.h -- C ABI of the MoBA (Mixture of Block Attention) forward pass on
+ * GB300 (sm_103a).
+ *
+ * The method (pages cited by title and section):
+ *   "Moonshot MoBA paper explained" (gsyq.cn/news/227272) section 3.1: the
+ *     context is cut into blocks of block_size tokens; a block is represented
+ *     by the mean of its keys; the gate scores blocks by that mean and masks
+ *     future blocks; each query keeps top_k blocks (section 4.1 sorts the
+ *     block scores and keeps the first top_k).
+ *   "MOBA mixture of block attention for server-side long context"
+ *     (hncyxsy.com/news/197418) section 3: the current block is always kept,
+ *     with a causal mask inside it; the gate score is the inner product of
+ *     the query with the mean-pooled keys.
+ *   "When a MoBA reproduction will not run" (mhpq.cn/news/582794) section 3.3:
+ *     attention over the selected blocks only.
+ *
+ * Selection rule (one rule, also used by the test oracle): query token i of a
+ * sequence lies in block c_i = i / block_size.  It attends to block c_i (keys
+ * up to and including i) and to the top (topk - 1) blocks among 0 .. c_i - 1
+ * by the score <q_i, mean of the block's keys>, ties going to the lower block
+ * index; when c_i <= topk - 1 it attends to every block 0 .. c_i.  Attention
+ * is softmax(q k^T / sqrt(D)) v over those keys.  topk >= number of blocks
+ * gives ordinary causal attention.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers (cudaMalloc / torch CUDA
+ *     memory) unless stated; the caller owns them.  Nothing is retained after
+ *     the call returns.
+ *   - q, k, v, out are bf16, laid out [B][S][H][D] (fixed length) or
+ *     [total_tokens][H][D] (varlen, sequences packed back to back), dense and
+ *     16-byte aligned.  D must be 64 or 128; H >= 1.
+ *   - lse is fp32, natural log of the softmax denominator of the scaled
+ *     logits: [B][H][S] (fixed length) or [H][total_tokens] (varlen).
+ *   - block_size must be a positive multiple of 64; topk >= 1.  topk larger
+ *     than the number of blocks is not an error (all blocks are kept).
+ *     topk - 1 must be <= 31 unless topk covers every block.
+ *   - total tokens (B * S) must be below 2^26.
+ *   - stream is a cudaStream_t (NULL = legacy default stream).  All work is
+ *     enqueued on it; no entry point synchronises the host except
+ *     moba_get_status.
+ *   - Return value: MOBA_OK, or an error code.  Argument errors are detected
+ *     on the host before anything is launched.  MOBA_ERR_CUDA reports a
+ *     failed launch or allocation.  A kernel that gives up a bounded wait
+ *     records MOBA_ERR_TIMEOUT in a device-side status word that
+ *     moba_get_status reads.
+ */
+#ifndef MOBA_GB300_H
+#define MOBA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOBA_OK = 0,
+    MOBA_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, bad block_size/topk */
+    MOBA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (D not 64/128, sizes too large) */
+    MOBA_ERR_CUDA = 3,         /* a CUDA launch / allocation failed */
+    MOBA_ERR_WORKSPACE = 4,    /* caller workspace too small */
+    MOBA_ERR_TIMEOUT = 5       /* a kernel gave up a bounded wait (device status word) */
+} moba_status_t;
+
+/* Number of blocks of a sequence: ceil(len / block_size) (the tail block may
+ * be partial).  "Moonshot MoBA paper explained" section 4.1 divides the
+ * context length by the block size (32768 / 512 = 64). */
+int moba_num_blocks(int len, int block_size);
+
+/*
+ * Mean-pooled keys ("Moonshot MoBA paper explained" section 3.1, mean_pool).
+ *   k    : [B][S][H][D] bf16 (device)
+ *   kbar : [B * n][H][D] fp32 (device, written), n = moba_num_blocks(S, bs);
+ *          kbar[b*n + c][h][:] = mean of k[b][t][h][:] over the tokens t of
+ *          block c (the tail block averages only the tokens it holds).
+ */
+int moba_kpool(const void *k, float *kbar, int B, int H, int S, int D, int block_size,
+               void *stream);
+
+/* Varlen form: k [total_tokens][H][D]; cu_seqlens is a DEVICE int32 array of
+ * num_seqs + 1 prefix offsets (cu_seqlens[num_seqs] == total_tokens).
+ * kbar: [sum over sequences of n_b][H][D], sequence 0's blocks first. */
+int moba_kpool_varlen(const void *k, float *kbar, const int32_t *cu_seqlens, int num_seqs,
+                      int total_tokens, int H, int D, int block_size, void *stream);
+
+/*
+ * Gate and top-k selection ("Moonshot MoBA paper explained" sections 3.1 and
+ * 4.1; "MOBA ... server-side long context" section 3).  Scores are
+ * <q, kbar> in fp32 for the strictly-past blocks only.
+ *   q    : [B][S][H][D] bf16 (device)
+ *   kbar : as written by moba_kpool (device)
+ *   idx  : [B][S][H][topk] int32 (device, written): the selected local block
+ *          ids of each (token, head) in ascending order (the own block is
+ *          therefore last among the valid entries), padded with -1.
+ */
+int moba_gate_topk(const void *q, const float *kbar, int32_t *idx, int B, int H, int S, int D,
+                   int block_size, int topk, void *stream);
+
+/* Varlen form of moba_gate_topk: q [total_tokens][H][D], idx
+ * [total_tokens][H][topk]; cu_seqlens as for moba_kpool_varlen. */
+int moba_gate_topk_varlen(const void *q, const float *kbar, int32_t *idx,
+                          const int32_t *cu_seqlens, int num_seqs, int total_tokens, int H,
+                          int D, int block_size, int topk, void *stream);
+
+/*
+ * Full MoBA forward: pool, gate, regroup of the queries by selected block,
+ * attention over the past blocks, causal attention inside the own block and
+ * the log-sum-exp merge of the partial results.
+ *   q, k, v : [B][S][H][D] bf16 (device);  out : [B][S][H][D] bf16 (device)
+ *   lse     : [B][H][S] fp32 (device)
+ * Scratch is allocated stream-ordered on `stream` (cudaMallocAsync) and
+ * released on the same stream before returning.
+ */
+int moba_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse, int B,
+                  int H, int S, int D, int block_size, int topk, void *stream);
+
+/* Bytes of device scratch moba_attn_fwd_ws needs for these sizes. */
+size_t moba_attn_fwd_workspace_size(int B, int H, int S, int D, int block_size, int topk);
+
+/* moba_attn_fwd with caller-provided device scratch (256-byte aligned,
+ * at least moba_attn_fwd_workspace_size bytes; MOBA_ERR_WORKSPACE if
+ * smaller).  The scratch must not be used by anything else until the work
+ * enqueued on `stream` has finished. */
+int moba_attn_fwd_ws(const void *q, const void *k, const void *v, void *out, float *lse, int B,
+                     int H, int S, int D, int block_size, int topk, void *workspace,
+                     size_t workspace_bytes, void *stream);
+
+/*
+ * Varlen forward: q, k, v, out [total_tokens][H][D] bf16; lse
+ * [H][total_tokens] fp32; cu_seqlens DEVICE int32 [num_seqs + 1];
+ * max_seqlen >= every sequence length.  Each sequence is partitioned into
+ * its own blocks starting at its first token.
+ */
+int moba_attn_fwd_varlen(const void *q, const void *k, const void *v, void *out, float *lse,
+                         const int32_t *cu_seqlens, int num_seqs, int total_tokens,
+                         int max_seqlen, int H, int D, int block_size, int topk, void *stream);
+
+size_t moba_attn_fwd_varlen_workspace_size(int num_seqs, int total_tokens, int max_seqlen, int H,
+                                           int D, int block_size, int topk);
+
+int moba_attn_fwd_varlen_ws(const void *q, const void *k, const void *v, void *out, float *lse,
+                            const int32_t *cu_seqlens, int num_seqs, int total_tokens,
+                            int max_seqlen, int H, int D, int block_size, int topk,
+                            void *workspace, size_t workspace_bytes, void *stream);
+
+/* Synchronises `stream`, returns the device status word (MOBA_OK or
+ * MOBA_ERR_TIMEOUT) of the current device and clears it; MOBA_ERR_CUDA if
+ * the synchronisation itself failed. */
+int moba_get_status(void *stream);
+
+/* Static, human-readable name of a status code. */
+const char *moba_status_string(int code);
+
+/* Number of kernels this library has launched since it was loaded (a
+ * process-wide tally; host only). */
+unsigned long long moba_launch_count(void);
+
+/*
+ * Phase timing of the forward entry points (tracing aid; not thread-safe).
+ * moba_profile_begin(max_calls) starts recording CUDA events on each call's
+ * stream between its phases, for at most max_calls calls; moba_profile_end
+ * stops, waits for the recorded events and writes into phase_ms[0..5] the
+ * milliseconds summed over the recorded calls for: 0 sequence tables,
+ * 1 key pooling, 2 gate + top-k, 3 regroup, 4 attention over past blocks,
+ * 5 attention over the own block + merge.  Returns the number of calls
+ * recorded, or a negated status code.  Phases a call skips read as ~0.
+ */
+int moba_profile_begin(int max_calls);
+int moba_profile_end(float *phase_ms, int n_phases);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOBA_GB300_H */

@@ -1,0 +1,381 @@
+// moba_api.cu -- the C ABI declared in include/moba.h: argument validation,
+// scratch layout and the launch sequence of the MoBA forward pass.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+#include "../../include/moba.h"
+#include "moba_internal.cuh"
+
+#define MOBA_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace moba {
+
+__device__ int g_moba_status;
+
+int *status_word() {
+    static int *addr[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_moba_status) != cudaSuccess) return nullptr;
+        addr[dev] = static_cast<int *>(p);
+    }
+    return addr[dev];
+}
+
+static std::atomic<unsigned long long> g_launches{0};
+void note_launches(int n) { g_launches.fetch_add((unsigned long long)n); }
+
+// Optional phase timing: CUDA events recorded on the caller's stream between
+// the phases of each forward call (setup, kpool, gate, regroup, attention
+// over past blocks, attention over the own block + merge).
+constexpr int kPhases = 6;
+struct Profiler {
+    bool on = false;
+    int used = 0;
+    std::vector<cudaEvent_t> ev;  // (kPhases + 1) per recorded call
+} g_prof;
+
+static void prof_mark(int call, int phase, cudaStream_t st) {
+    if (call >= 0) cudaEventRecord(g_prof.ev[(size_t)call * (kPhases + 1) + phase], st);
+}
+
+static inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t workspace_bytes(const Plan &p, Workspace *ws, char *base) {
+    size_t off = 0;
+    auto take = [&](size_t bytes) -> void * {
+        void *r = base ? static_cast<void *>(base + off) : nullptr;
+        off = align256(off + bytes);
+        return r;
+    };
+    Workspace w;
+    std::memset(&w, 0, sizeof w);
+    w.cu = static_cast<int *>(take(sizeof(int) * (p.num_seqs + 1)));
+    w.blk_base = static_cast<int *>(take(sizeof(int) * (p.num_seqs + 1)));
+    const bool gate = !p.dense && p.km1 > 0;
+    if (gate) {
+        const size_t N = (size_t)p.NBcap * p.H;
+        const size_t rows = (size_t)p.total * p.H;
+        w.kbar = static_cast<float *>(take(sizeof(float) * N * p.D));
+        w.idx = static_cast<int32_t *>(take(sizeof(int32_t) * rows * p.topk));
+        w.counts = static_cast<int *>(take(sizeof(int) * N));
+        w.list_off = static_cast<int *>(take(sizeof(int) * (N + 1)));
+        w.tile_off = static_cast<int *>(take(sizeof(int) * (N + 1)));
+        w.cursor = static_cast<int *>(take(sizeof(int) * N));
+        w.list = static_cast<int *>(take(sizeof(int) * rows * p.km1));
+        w.part_o = static_cast<float *>(take(sizeof(float) * rows * p.km1 * p.D));
+        w.part_lse = static_cast<float *>(take(sizeof(float) * rows * p.km1));
+    }
+    if (ws) *ws = w;
+    return off;
+}
+
+// ---------------------------------------------------------------------------
+// validation
+// ---------------------------------------------------------------------------
+static int make_plan(int num_seqs, long long total, int max_len, int H, int D, int bs, int topk,
+                     bool fixed, Plan *p) {
+    if (num_seqs < 1 || H < 1 || max_len < 1 || total < 1 || bs < 1 || topk < 1)
+        return MOBA_ERR_INVALID_ARG;
+    if (bs % 64 != 0) return MOBA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return MOBA_ERR_UNSUPPORTED;
+    if (total >= kMaxTokens || num_seqs > 65535 || H > 65535) return MOBA_ERR_UNSUPPORTED;
+    const long long n_max = (max_len + (long long)bs - 1) / bs;
+    p->num_seqs = num_seqs;
+    p->total = (int)total;
+    p->max_len = max_len;
+    p->H = H;
+    p->D = D;
+    p->bs = bs;
+    p->topk = topk;
+    p->fixed = fixed;
+    p->dense = topk >= n_max;
+    p->km1 = p->dense ? 0 : topk - 1;
+    const long long nbcap = fixed ? (long long)num_seqs * n_max : total / bs + num_seqs;
+    if (nbcap * H >= (1ll << 31)) return MOBA_ERR_UNSUPPORTED;
+    p->NBcap = (int)nbcap;
+    if (!p->dense && p->km1 > kMaxPastSlots) return MOBA_ERR_UNSUPPORTED;
+    if (total * H * (long long)(p->km1 > 0 ? p->km1 : 1) >= (1ll << 31)) return MOBA_ERR_UNSUPPORTED;
+    return MOBA_OK;
+}
+
+static int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOBA_OK : MOBA_ERR_CUDA; }
+
+#define MOBA_TRY(expr)                                   \
+    do {                                                 \
+        cudaError_t _e = (expr);                         \
+        if (_e != cudaSuccess) return MOBA_ERR_CUDA;     \
+    } while (0)
+
+static int run_forward(const Plan &p, const int *cu_dev, const void *q, const void *k,
+                       const void *v, void *out, float *lse, void *workspace, size_t ws_bytes,
+                       cudaStream_t st) {
+    Workspace ws;
+    const size_t need = workspace_bytes(p, &ws, static_cast<char *>(workspace));
+    if (!workspace || ws_bytes < need) return MOBA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255) return MOBA_ERR_WORKSPACE;
+    const auto *qb = static_cast<const __nv_bfloat16 *>(q);
+    const auto *kb = static_cast<const __nv_bfloat16 *>(k);
+    const auto *vb = static_cast<const __nv_bfloat16 *>(v);
+    int call = -1;
+    if (g_prof.on && (size_t)(g_prof.used + 1) * (kPhases + 1) <= g_prof.ev.size())
+        call = g_prof.used++;
+    prof_mark(call, 0, st);
+    MOBA_TRY(launch_setup(p, cu_dev, ws, st));
+    prof_mark(call, 1, st);
+    const bool gate = !p.dense && p.km1 > 0;
+    if (gate) MOBA_TRY(launch_kpool(p, ws, kb, ws.kbar, st));
+    prof_mark(call, 2, st);
+    if (gate) {
+        MOBA_TRY(cudaMemsetAsync(ws.counts, 0, sizeof(int) * (size_t)p.NBcap * p.H, st));
+        MOBA_TRY(launch_gate(p, ws, qb, ws.kbar, ws.idx, true, st));
+    }
+    prof_mark(call, 3, st);
+    if (gate) MOBA_TRY(launch_regroup(p, ws, st));
+    prof_mark(call, 4, st);
+    MOBA_TRY(launch_attn_past(p, ws, qb, kb, vb, st));
+    prof_mark(call, 5, st);
+    MOBA_TRY(launch_attn_current(p, ws, qb, kb, vb, static_cast<__nv_bfloat16 *>(out), lse, st));
+    prof_mark(call, 6, st);
+    return MOBA_OK;
+}
+
+static bool misaligned(const void *p) { return reinterpret_cast<uintptr_t>(p) & 15; }
+
+// Small scratch for the tables of the pooling / gate entry points.
+static int with_tables(const Plan &p, const int *cu_dev, cudaStream_t st,
+                       int (*body)(const Plan &, Workspace &, void *), void *ctx) {
+    Workspace ws;
+    std::memset(&ws, 0, sizeof ws);
+    const size_t bytes = align256(sizeof(int) * (p.num_seqs + 1)) * 2;
+    void *mem = nullptr;
+    if (cudaMallocAsync(&mem, bytes, st) != cudaSuccess) return MOBA_ERR_CUDA;
+    ws.cu = static_cast<int *>(mem);
+    ws.blk_base = reinterpret_cast<int *>(static_cast<char *>(mem) + bytes / 2);
+    int rc = cuda_status(launch_setup(p, cu_dev, ws, st));
+    if (rc == MOBA_OK) rc = body(p, ws, ctx);
+    if (cudaFreeAsync(mem, st) != cudaSuccess && rc == MOBA_OK) rc = MOBA_ERR_CUDA;
+    return rc;
+}
+
+struct PoolCtx {
+    const void *k;
+    float *kbar;
+    cudaStream_t st;
+};
+struct GateCtx {
+    const void *q;
+    const float *kbar;
+    int32_t *idx;
+    cudaStream_t st;
+};
+
+static int pool_run(const Plan &p, Workspace &ws, void *c) {
+    auto *x = static_cast<PoolCtx *>(c);
+    return cuda_status(
+        launch_kpool(p, ws, static_cast<const __nv_bfloat16 *>(x->k), x->kbar, x->st));
+}
+static int gate_run(const Plan &p, Workspace &ws, void *c) {
+    auto *x = static_cast<GateCtx *>(c);
+    return cuda_status(launch_gate(p, ws, static_cast<const __nv_bfloat16 *>(x->q), x->kbar,
+                                   x->idx, false, x->st));
+}
+
+}  // namespace moba
+
+using namespace moba;
+
+MOBA_EXPORT int moba_num_blocks(int len, int block_size) {
+    if (len <= 0 || block_size <= 0) return 0;
+    return (int)(((long long)len + block_size - 1) / block_size);
+}
+
+MOBA_EXPORT const char *moba_status_string(int code) {
+    switch (code) {
+        case MOBA_OK: return "MOBA_OK";
+        case MOBA_ERR_INVALID_ARG: return "MOBA_ERR_INVALID_ARG";
+        case MOBA_ERR_UNSUPPORTED: return "MOBA_ERR_UNSUPPORTED";
+        case MOBA_ERR_CUDA: return "MOBA_ERR_CUDA";
+        case MOBA_ERR_WORKSPACE: return "MOBA_ERR_WORKSPACE";
+        case MOBA_ERR_TIMEOUT: return "MOBA_ERR_TIMEOUT";
+        default: return "MOBA_ERR_UNKNOWN";
+    }
+}
+
+MOBA_EXPORT int moba_kpool(const void *k, float *kbar, int B, int H, int S, int D, int block_size,
+                           void *stream) {
+    if (!k || !kbar) return MOBA_ERR_INVALID_ARG;
+    Plan p;
+    int rc = make_plan(B, (long long)B * S, S, H, D, block_size, 1, true, &p);
+    if (rc) return rc;
+    if (misaligned(k) || misaligned(kbar)) return MOBA_ERR_INVALID_ARG;
+    PoolCtx c{k, kbar, static_cast<cudaStream_t>(stream)};
+    return with_tables(p, nullptr, c.st, pool_run, &c);
+}
+
+MOBA_EXPORT int moba_kpool_varlen(const void *k, float *kbar, const int32_t *cu_seqlens,
+                                  int num_seqs, int total_tokens, int H, int D, int block_size,
+                                  void *stream) {
+    if (!k || !kbar || !cu_seqlens) return MOBA_ERR_INVALID_ARG;
+    Plan p;
+    int rc = make_plan(num_seqs, total_tokens, total_tokens, H, D, block_size, 1, false, &p);
+    if (rc) return rc;
+    if (misaligned(k) || misaligned(kbar)) return MOBA_ERR_INVALID_ARG;
+    PoolCtx c{k, kbar, static_cast<cudaStream_t>(stream)};
+    return with_tables(p, cu_seqlens, c.st, pool_run, &c);
+}
+
+MOBA_EXPORT int moba_gate_topk(const void *q, const float *kbar, int32_t *idx, int B, int H, int S,
+                               int D, int block_size, int topk, void *stream) {
+    if (!q || !kbar || !idx) return MOBA_ERR_INVALID_ARG;
+    Plan p;
+    int rc = make_plan(B, (long long)B * S, S, H, D, block_size, topk, true, &p);
+    if (rc) return rc;
+    if (topk - 1 > kMaxPastSlots && !p.dense) return MOBA_ERR_UNSUPPORTED;
+    if (misaligned(q) || misaligned(kbar)) return MOBA_ERR_INVALID_ARG;
+    GateCtx c{q, kbar, idx, static_cast<cudaStream_t>(stream)};
+    return with_tables(p, nullptr, c.st, gate_run, &c);
+}
+
+MOBA_EXPORT int moba_gate_topk_varlen(const void *q, const float *kbar, int32_t *idx,
+                                      const int32_t *cu_seqlens, int num_seqs, int total_tokens,
+                                      int H, int D, int block_size, int topk, void *stream) {
+    if (!q || !kbar || !idx || !cu_seqlens) return MOBA_ERR_INVALID_ARG;
+    Plan p;
+    int rc = make_plan(num_seqs, total_tokens, total_tokens, H, D, block_size, topk, false, &p);
+    if (rc) return rc;
+    if (misaligned(q) || misaligned(kbar)) return MOBA_ERR_INVALID_ARG;
+    GateCtx c{q, kbar, idx, static_cast<cudaStream_t>(stream)};
+    return with_tables(p, cu_seqlens, c.st, gate_run, &c);
+}
+
+MOBA_EXPORT size_t moba_attn_fwd_workspace_size(int B, int H, int S, int D, int block_size,
+                                                int topk) {
+    Plan p;
+    if (make_plan(B, (long long)B * S, S, H, D, block_size, topk, true, &p)) return 0;
+    return workspace_bytes(p, nullptr, nullptr);
+}
+
+MOBA_EXPORT size_t moba_attn_fwd_varlen_workspace_size(int num_seqs, int total_tokens,
+                                                       int max_seqlen, int H, int D,
+                                                       int block_size, int topk) {
+    Plan p;
+    if (make_plan(num_seqs, total_tokens, max_seqlen, H, D, block_size, topk, false, &p)) return 0;
+    return workspace_bytes(p, nullptr, nullptr);
+}
+
+static int check_tensors(const void *q, const void *k, const void *v, const void *out,
+                         const void *lse) {
+    if (!q || !k || !v || !out || !lse) return MOBA_ERR_INVALID_ARG;
+    if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(out))
+        return MOBA_ERR_INVALID_ARG;
+    return MOBA_OK;
+}
+
+MOBA_EXPORT int moba_attn_fwd_ws(const void *q, const void *k, const void *v, void *out,
+                                 float *lse, int B, int H, int S, int D, int block_size, int topk,
+                                 void *workspace, size_t workspace_bytes_, void *stream) {
+    int rc = check_tensors(q, k, v, out, lse);
+    if (rc) return rc;
+    Plan p;
+    rc = make_plan(B, (long long)B * S, S, H, D, block_size, topk, true, &p);
+    if (rc) return rc;
+    return run_forward(p, nullptr, q, k, v, out, lse, workspace, workspace_bytes_,
+                       static_cast<cudaStream_t>(stream));
+}
+
+MOBA_EXPORT int moba_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse,
+                              int B, int H, int S, int D, int block_size, int topk, void *stream) {
+    int rc = check_tensors(q, k, v, out, lse);
+    if (rc) return rc;
+    Plan p;
+    rc = make_plan(B, (long long)B * S, S, H, D, block_size, topk, true, &p);
+    if (rc) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t bytes = workspace_bytes(p, nullptr, nullptr);
+    void *ws = nullptr;
+    if (cudaMallocAsync(&ws, bytes, st) != cudaSuccess) return MOBA_ERR_CUDA;
+    rc = run_forward(p, nullptr, q, k, v, out, lse, ws, bytes, st);
+    if (cudaFreeAsync(ws, st) != cudaSuccess && rc == MOBA_OK) rc = MOBA_ERR_CUDA;
+    return rc;
+}
+
+MOBA_EXPORT int moba_attn_fwd_varlen_ws(const void *q, const void *k, const void *v, void *out,
+                                        float *lse, const int32_t *cu_seqlens, int num_seqs,
+                                        int total_tokens, int max_seqlen, int H, int D,
+                                        int block_size, int topk, void *workspace,
+                                        size_t workspace_bytes_, void *stream) {
+    int rc = check_tensors(q, k, v, out, lse);
+    if (rc) return rc;
+    if (!cu_seqlens) return MOBA_ERR_INVALID_ARG;
+    Plan p;
+    rc = make_plan(num_seqs, total_tokens, max_seqlen, H, D, block_size, topk, false, &p);
+    if (rc) return rc;
+    return run_forward(p, cu_seqlens, q, k, v, out, lse, workspace, workspace_bytes_,
+                       static_cast<cudaStream_t>(stream));
+}
+
+MOBA_EXPORT int moba_attn_fwd_varlen(const void *q, const void *k, const void *v, void *out,
+                                     float *lse, const int32_t *cu_seqlens, int num_seqs,
+                                     int total_tokens, int max_seqlen, int H, int D,
+                                     int block_size, int topk, void *stream) {
+    int rc = check_tensors(q, k, v, out, lse);
+    if (rc) return rc;
+    if (!cu_seqlens) return MOBA_ERR_INVALID_ARG;
+    Plan p;
+    rc = make_plan(num_seqs, total_tokens, max_seqlen, H, D, block_size, topk, false, &p);
+    if (rc) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t bytes = workspace_bytes(p, nullptr, nullptr);
+    void *ws = nullptr;
+    if (cudaMallocAsync(&ws, bytes, st) != cudaSuccess) return MOBA_ERR_CUDA;
+    rc = run_forward(p, cu_seqlens, q, k, v, out, lse, ws, bytes, st);
+    if (cudaFreeAsync(ws, st) != cudaSuccess && rc == MOBA_OK) rc = MOBA_ERR_CUDA;
+    return rc;
+}
+
+MOBA_EXPORT int moba_get_status(void *stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return MOBA_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_moba_status, sizeof v) != cudaSuccess) return MOBA_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_moba_status, &zero, sizeof zero) != cudaSuccess) return MOBA_ERR_CUDA;
+    return v;
+}
+
+MOBA_EXPORT unsigned long long moba_launch_count(void) { return g_launches.load(); }
+
+MOBA_EXPORT int moba_profile_begin(int max_calls) {
+    if (max_calls < 1) return MOBA_ERR_INVALID_ARG;
+    const size_t need = (size_t)max_calls * (kPhases + 1);
+    while (g_prof.ev.size() < need) {
+        cudaEvent_t e;
+        if (cudaEventCreate(&e) != cudaSuccess) return MOBA_ERR_CUDA;
+        g_prof.ev.push_back(e);
+    }
+    g_prof.used = 0;
+    g_prof.on = true;
+    return MOBA_OK;
+}
+
+MOBA_EXPORT int moba_profile_end(float *phase_ms, int n_phases) {
+    g_prof.on = false;
+    if (!phase_ms || n_phases < kPhases) return -MOBA_ERR_INVALID_ARG;
+    for (int i = 0; i < kPhases; ++i) phase_ms[i] = 0.f;
+    for (int c = 0; c < g_prof.used; ++c) {
+        cudaEvent_t *e = &g_prof.ev[(size_t)c * (kPhases + 1)];
+        if (cudaEventSynchronize(e[kPhases]) != cudaSuccess) return -MOBA_ERR_CUDA;
+        for (int i = 0; i < kPhases; ++i) {
+            float ms = 0.f;
+            if (cudaEventElapsedTime(&ms, e[i], e[i + 1]) != cudaSuccess) return -MOBA_ERR_CUDA;
+            phase_ms[i] += ms;
+        }
+    }
+    return g_prof.used;
+}

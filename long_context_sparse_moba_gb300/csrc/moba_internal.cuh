@@ -1,0 +1,88 @@
+// moba_internal.cuh -- shared definitions of the MoBA sm_103a kernels.
+//
+// Geometry: sequences are packed token-major ([token][H][D]); a fixed-length
+// batch [B][S][H][D] is the packed case with cu_seqlens = {0, S, 2S, ...}.
+// Every kernel reads the per-sequence tables built by moba_setup_kernel:
+//   cu[b]        first token of sequence b (cu[num_seqs] = total tokens)
+//   blk_base[b]  global id of block 0 of sequence b (blk_base[num_seqs] = NB)
+// Global block g of sequence b, local block c: g = blk_base[b] + c.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moba {
+
+constexpr int kMaxPastSlots = 31;      // topk - 1 limit when gating is needed
+constexpr int kSlotBits = 5;           // regroup entry = token << 5 | slot
+constexpr int kMaxTokens = 1 << 26;
+
+// Device status word of the current device (defined in moba_api.cu); kernels
+// with bounded waits record MOBA_ERR_TIMEOUT there.  moba_get_status reads
+// and clears it.
+int *status_word();
+
+struct Geometry {
+    const int *cu;        // [num_seqs + 1]
+    const int *blk_base;  // [num_seqs + 1]
+    int num_seqs;
+    int total;            // tokens
+    int H, D, bs;
+};
+
+// Largest b in [0, num_seqs) with tab[b] <= x (tab ascending, tab[0] = 0).
+__device__ __forceinline__ int upper_index(const int *__restrict__ tab, int num_seqs, int x) {
+    int lo = 0, hi = num_seqs - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (__ldg(tab + mid) <= x) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Scratch carved out of one workspace allocation (offsets 256-byte aligned).
+struct Workspace {
+    int *cu;          // [num_seqs + 1]
+    int *blk_base;    // [num_seqs + 1]
+    float *kbar;      // [NBcap][H][D]
+    int32_t *idx;     // [total][H][topk]
+    int *counts;      // [NBcap * H]   queries per (block, head) past list
+    int *list_off;    // [NBcap * H + 1]
+    int *tile_off;    // [NBcap * H + 1]
+    int *cursor;      // [NBcap * H]
+    int *list;        // [total * H * km1]  entries token << 5 | slot
+    float *part_o;    // [total * H * km1][D]  normalised partial outputs
+    float *part_lse;  // [total * H * km1]     partial log2-sum-exp
+};
+
+struct Plan {
+    int num_seqs, total, max_len, H, D, bs, topk;
+    int NBcap;        // upper bound of the global block count
+    int km1;          // past slots per row (topk - 1), 0 on the dense path
+    bool dense;       // topk covers every block of every sequence
+    bool fixed;       // [B][S] layout (lse [B][H][S]) rather than varlen
+};
+
+size_t workspace_bytes(const Plan &p, Workspace *ws, char *base);
+
+// ---- launchers (each returns cudaGetLastError() of its launch) ----
+cudaError_t launch_setup(const Plan &p, const int *cu_dev, Workspace &ws, cudaStream_t st);
+cudaError_t launch_kpool(const Plan &p, const Workspace &ws, const __nv_bfloat16 *k,
+                         float *kbar, cudaStream_t st);
+cudaError_t launch_gate(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
+                        const float *kbar, int32_t *idx, bool count, cudaStream_t st);
+cudaError_t launch_regroup(const Plan &p, const Workspace &ws, cudaStream_t st);
+// attention over the selected past blocks (skipped on the dense / top-1 paths)
+cudaError_t launch_attn_past(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
+                             const __nv_bfloat16 *k, const __nv_bfloat16 *v, cudaStream_t st);
+// causal attention inside the own block (every earlier key on the dense path)
+// merged with the past partials
+cudaError_t launch_attn_current(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
+                                const __nv_bfloat16 *k, const __nv_bfloat16 *v,
+                                __nv_bfloat16 *out, float *lse, cudaStream_t st);
+
+// count of kernels this library has launched (for the benchmark's launch tally)
+void note_launches(int n);
+
+}  // namespace moba

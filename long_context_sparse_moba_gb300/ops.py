@@ -1,0 +1,228 @@
+"""Python binding of ``libmoba_gb300.so`` (argument marshalling only).
+
+Every function below calls the C ABI of ``include/moba.h`` with the tensors'
+device pointers and the current CUDA stream; all arithmetic runs in the
+library's kernels.  There is no fallback: if the library is missing or a call
+fails, a ``RuntimeError`` is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoba_gb300.so")
+
+MOBA_OK = 0
+MOBA_ERR_INVALID_ARG = 1
+MOBA_ERR_UNSUPPORTED = 2
+MOBA_ERR_CUDA = 3
+MOBA_ERR_WORKSPACE = 4
+MOBA_ERR_TIMEOUT = 5
+
+_lib = None
+
+_P, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+_SIGNATURES = {
+    "moba_num_blocks": (_I, [_I, _I]),
+    "moba_status_string": (ctypes.c_char_p, [_I]),
+    "moba_kpool": (_I, [_P, _P, _I, _I, _I, _I, _I, _P]),
+    "moba_kpool_varlen": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "moba_gate_topk": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "moba_gate_topk_varlen": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "moba_attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "moba_attn_fwd_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "moba_attn_fwd_ws": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _SZ, _P]),
+    "moba_attn_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]),
+    "moba_attn_fwd_varlen_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "moba_attn_fwd_varlen_ws": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
+                                     _P, _SZ, _P]),
+    "moba_get_status": (_I, [_P]),
+    "moba_launch_count": (ctypes.c_ulonglong, []),
+    "moba_profile_begin": (_I, [_I]),
+    "moba_profile_end": (_I, [_P, _I]),
+}
+
+PHASES = ("tables", "kpool", "gate", "regroup", "attn_past", "attn_current")
+
+
+def lib():
+    """Load the library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -m long_context_sparse_moba_gb300.build` (needs nvcc)")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().moba_status_string(code).decode()
+
+
+def _check(code: int, what: str):
+    if code != MOBA_OK:
+        raise RuntimeError(f"{what} failed: {status_string(code)} ({code})")
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _need(t, dtype, name):
+    if t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
+
+
+def num_blocks(length: int, block_size: int) -> int:
+    return int(lib().moba_num_blocks(int(length), int(block_size)))
+
+
+def _nb_total(cu_host, block_size):
+    return sum(num_blocks(cu_host[b + 1] - cu_host[b], block_size) for b in range(len(cu_host) - 1))
+
+
+def kpool(k, block_size: int, stream=None):
+    """Mean-pooled keys of k [B, S, H, D] -> kbar [B * n, H, D] fp32."""
+    _need(k, torch.bfloat16, "k")
+    B, S, H, D = k.shape
+    kbar = torch.empty(B * num_blocks(S, block_size), H, D, dtype=torch.float32, device=k.device)
+    _check(lib().moba_kpool(_ptr(k), _ptr(kbar), B, H, S, D, block_size, _stream(stream)),
+           "moba_kpool")
+    return kbar
+
+
+def kpool_varlen(k, cu_seqlens, block_size: int, stream=None):
+    """Varlen k [total, H, D], cu_seqlens int32 CUDA [num_seqs + 1]."""
+    _need(k, torch.bfloat16, "k")
+    _need(cu_seqlens, torch.int32, "cu_seqlens")
+    total, H, D = k.shape
+    nb = _nb_total(cu_seqlens.tolist(), block_size)
+    kbar = torch.empty(nb, H, D, dtype=torch.float32, device=k.device)
+    _check(lib().moba_kpool_varlen(_ptr(k), _ptr(kbar), _ptr(cu_seqlens), cu_seqlens.numel() - 1,
+                                   total, H, D, block_size, _stream(stream)), "moba_kpool_varlen")
+    return kbar
+
+
+def gate_topk(q, kbar, block_size: int, topk: int, stream=None):
+    """Selected blocks idx [B, S, H, topk] int32 (ascending, -1 padded)."""
+    _need(q, torch.bfloat16, "q")
+    _need(kbar, torch.float32, "kbar")
+    B, S, H, D = q.shape
+    idx = torch.empty(B, S, H, topk, dtype=torch.int32, device=q.device)
+    _check(lib().moba_gate_topk(_ptr(q), _ptr(kbar), _ptr(idx), B, H, S, D, block_size, topk,
+                                _stream(stream)), "moba_gate_topk")
+    return idx
+
+
+def gate_topk_varlen(q, kbar, cu_seqlens, block_size: int, topk: int, stream=None):
+    _need(q, torch.bfloat16, "q")
+    _need(kbar, torch.float32, "kbar")
+    _need(cu_seqlens, torch.int32, "cu_seqlens")
+    total, H, D = q.shape
+    idx = torch.empty(total, H, topk, dtype=torch.int32, device=q.device)
+    _check(lib().moba_gate_topk_varlen(_ptr(q), _ptr(kbar), _ptr(idx), _ptr(cu_seqlens),
+                                       cu_seqlens.numel() - 1, total, H, D, block_size, topk,
+                                       _stream(stream)), "moba_gate_topk_varlen")
+    return idx
+
+
+def workspace_size(B, H, S, D, block_size, topk) -> int:
+    return int(lib().moba_attn_fwd_workspace_size(B, H, S, D, block_size, topk))
+
+
+def varlen_workspace_size(num_seqs, total, max_seqlen, H, D, block_size, topk) -> int:
+    return int(lib().moba_attn_fwd_varlen_workspace_size(num_seqs, total, max_seqlen, H, D,
+                                                         block_size, topk))
+
+
+def attn_fwd(q, k, v, block_size: int, topk: int, out=None, lse=None, workspace=None,
+             stream=None):
+    """MoBA forward for q, k, v [B, S, H, D] bf16 -> (out [B, S, H, D] bf16, lse [B, H, S] fp32).
+
+    With ``workspace`` (a uint8 CUDA tensor of at least :func:`workspace_size`
+    bytes) the call allocates nothing; otherwise the library allocates its
+    scratch stream-ordered."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, torch.bfloat16, n)
+    B, S, H, D = q.shape
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must have the same shape")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, H, S, dtype=torch.float32, device=q.device)
+    st = _stream(stream)
+    if workspace is None:
+        rc = lib().moba_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, S, D,
+                                 block_size, topk, st)
+    else:
+        rc = lib().moba_attn_fwd_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, S, D,
+                                    block_size, topk, _ptr(workspace), workspace.numel(), st)
+    _check(rc, "moba_attn_fwd")
+    return out, lse
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, block_size: int, topk: int, out=None,
+                    lse=None, workspace=None, stream=None):
+    """Varlen MoBA forward: q, k, v [total, H, D] bf16, cu_seqlens int32 CUDA
+    [num_seqs + 1] -> (out [total, H, D] bf16, lse [H, total] fp32)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, torch.bfloat16, n)
+    _need(cu_seqlens, torch.int32, "cu_seqlens")
+    total, H, D = q.shape
+    ns = cu_seqlens.numel() - 1
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(H, total, dtype=torch.float32, device=q.device)
+    st = _stream(stream)
+    if workspace is None:
+        rc = lib().moba_attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                        _ptr(cu_seqlens), ns, total, max_seqlen, H, D,
+                                        block_size, topk, st)
+    else:
+        rc = lib().moba_attn_fwd_varlen_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                           _ptr(cu_seqlens), ns, total, max_seqlen, H, D,
+                                           block_size, topk, _ptr(workspace), workspace.numel(),
+                                           st)
+    _check(rc, "moba_attn_fwd_varlen")
+    return out, lse
+
+
+def get_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status word."""
+    return int(lib().moba_get_status(_stream(stream)))
+
+
+def launch_count() -> int:
+    """Kernels launched by the library so far in this process."""
+    return int(lib().moba_launch_count())
+
+
+def profile_begin(max_calls: int):
+    _check(lib().moba_profile_begin(int(max_calls)), "moba_profile_begin")
+
+
+def profile_end() -> tuple:
+    """(calls recorded, {phase: total ms}) of the forward calls since profile_begin."""
+    buf = (ctypes.c_float * len(PHASES))()
+    n = lib().moba_profile_end(ctypes.cast(buf, ctypes.c_void_p), len(PHASES))
+    if n < 0:
+        raise RuntimeError(f"moba_profile_end failed: {status_string(-n)}")
+    return n, dict(zip(PHASES, (float(x) for x in buf)))

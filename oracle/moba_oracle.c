@@ -90,24 +90,29 @@ int moba_oracle_kpool(const uint16_t *k, const int64_t *cu, int num_seqs,
 {
     if (!k || !cu || !kbar || num_seqs < 1 || H < 1 || D < 1 || block_size < 1)
         return -1;
-    int64_t g = 0;
+    int64_t *base = block_bases(cu, num_seqs, block_size);
+    if (!base) return -2;
+    const int64_t HD = (int64_t)H * D;
     for (int b = 0; b < num_seqs; ++b) {
         int64_t t_begin = cu[b], len = cu[b + 1] - cu[b];
-        int64_t n = moba_oracle_num_blocks(len, block_size);
-        for (int64_t c = 0; c < n; ++c, ++g) {
+        int64_t n = base[b + 1] - base[b];
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int64_t c = 0; c < n; ++c) {
+            int64_t g = base[b] + c;
             int64_t t0 = t_begin + c * block_size;
             int64_t t1 = t0 + block_size;
             if (t1 > t_begin + len) t1 = t_begin + len;
-            for (int h = 0; h < H; ++h) {
-                for (int d = 0; d < D; ++d) {
-                    double sum = 0.0;
-                    for (int64_t t = t0; t < t1; ++t)
-                        sum += widen_bf16(k[(t * H + h) * D + d]);
-                    kbar[(g * H + h) * D + d] = sum / (double)(t1 - t0);
-                }
+            double *sum = kbar + g * HD;
+            for (int64_t e = 0; e < HD; ++e) sum[e] = 0.0;
+            /* every element sums its block's tokens in ascending order */
+            for (int64_t t = t0; t < t1; ++t) {
+                const uint16_t *row = k + t * HD;
+                for (int64_t e = 0; e < HD; ++e) sum[e] += widen_bf16(row[e]);
             }
+            for (int64_t e = 0; e < HD; ++e) sum[e] /= (double)(t1 - t0);
         }
     }
+    free(base);
     return 0;
 }
 

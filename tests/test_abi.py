@@ -1,0 +1,106 @@
+"""C ABI checks that need no GPU: the library builds and loads, exports every
+entry point include/moba.h declares, and rejects bad arguments on the host
+before touching the device."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+from long_context_sparse_moba_gb300 import ops
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moba.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(ops.LIB_PATH):
+        if not shutil.which("nvcc") and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+            pytest.skip("nvcc not available to build the library")
+        from long_context_sparse_moba_gb300 import build
+        build.build()
+    return ops.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moba_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("moba_attn_fwd", "moba_kpool", "moba_gate_topk", "moba_attn_fwd_varlen",
+                     "moba_get_status", "moba_status_string", "moba_attn_fwd_ws",
+                     "moba_attn_fwd_workspace_size"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in ops._SIGNATURES, f"binding lacks {name}"
+
+
+def test_status_strings(lib):
+    assert ops.status_string(0) == "MOBA_OK"
+    assert ops.status_string(5) == "MOBA_ERR_TIMEOUT"
+    assert ops.status_string(99) == "MOBA_ERR_UNKNOWN"
+
+
+def test_num_blocks(lib):
+    assert ops.num_blocks(32768, 512) == 64
+    assert ops.num_blocks(131072, 2048) == 64
+    assert ops.num_blocks(1048576, 4096) == 256
+    assert ops.num_blocks(2049, 256) == 9
+    assert ops.num_blocks(0, 256) == 0
+
+
+FAKE = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
+
+
+@pytest.mark.parametrize("B,H,S,D,bs,topk,code", [
+    (0, 1, 64, 64, 64, 1, ops.MOBA_ERR_INVALID_ARG),
+    (1, 0, 64, 64, 64, 1, ops.MOBA_ERR_INVALID_ARG),
+    (1, 1, 0, 64, 64, 1, ops.MOBA_ERR_INVALID_ARG),
+    (1, 1, 64, 64, 0, 1, ops.MOBA_ERR_INVALID_ARG),
+    (1, 1, 64, 64, 96, 1, ops.MOBA_ERR_INVALID_ARG),     # block size not a multiple of 64
+    (1, 1, 64, 64, 64, 0, ops.MOBA_ERR_INVALID_ARG),     # topk < 1
+    (1, 1, 64, 96, 64, 1, ops.MOBA_ERR_UNSUPPORTED),     # head dim
+    (1, 1, 64 * 64, 64, 64, 40, ops.MOBA_ERR_UNSUPPORTED),  # more than 31 past slots
+    (1, 1, 1 << 26, 64, 64, 3, ops.MOBA_ERR_UNSUPPORTED),   # too many tokens
+])
+def test_attn_rejects_bad_sizes(lib, B, H, S, D, bs, topk, code):
+    rc = lib.moba_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, B, H, S, D, bs, topk, None)
+    assert rc == code
+    assert lib.moba_attn_fwd_workspace_size(B, H, S, D, bs, topk) == 0
+
+
+def test_null_and_misaligned_pointers(lib):
+    assert lib.moba_attn_fwd(None, FAKE, FAKE, FAKE, FAKE, 1, 1, 64, 64, 64, 1, None) == 1
+    assert lib.moba_attn_fwd(FAKE, FAKE, FAKE, FAKE, None, 1, 1, 64, 64, 64, 1, None) == 1
+    odd = ctypes.c_void_p(0x10002)
+    assert lib.moba_attn_fwd(odd, FAKE, FAKE, FAKE, FAKE, 1, 1, 64, 64, 64, 1, None) == 1
+    assert lib.moba_kpool(None, FAKE, 1, 1, 64, 64, 64, None) == 1
+    assert lib.moba_gate_topk(FAKE, FAKE, None, 1, 1, 64, 64, 64, 3, None) == 1
+    assert lib.moba_attn_fwd_varlen(FAKE, FAKE, FAKE, FAKE, FAKE, None, 1, 64, 64, 1, 64, 64, 1,
+                                    None) == 1
+
+
+def test_workspace_too_small_is_rejected_before_launch(lib):
+    need = lib.moba_attn_fwd_workspace_size(1, 2, 4096, 128, 512, 3)
+    assert need > 0
+    rc = lib.moba_attn_fwd_ws(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 4096, 128, 512, 3,
+                              ctypes.c_void_p(0x100000), need - 1, None)
+    assert rc == ops.MOBA_ERR_WORKSPACE
+
+
+def test_workspace_grows_with_topk_and_dense_needs_little(lib):
+    sparse = lib.moba_attn_fwd_workspace_size(1, 32, 32768, 128, 512, 3)
+    wider = lib.moba_attn_fwd_workspace_size(1, 32, 32768, 128, 512, 8)
+    dense = lib.moba_attn_fwd_workspace_size(1, 32, 32768, 128, 512, 64)
+    assert wider > sparse > dense > 0
+    # the partial outputs dominate: tokens * heads * (topk - 1) * D * 4 bytes
+    assert sparse >= 32768 * 32 * 2 * 128 * 4

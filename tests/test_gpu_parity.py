@@ -1,0 +1,164 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from long_context_sparse_moba_gb300 import ops, workloads
+
+from .parity import compare, flat, gpu_forward, gpu_select
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from long_context_sparse_moba_gb300 import build
+    build.build()
+    oracle.build()
+    ops.lib()
+
+
+def run_case(w, topk, rows=None, device="cuda"):
+    inp = workloads.make_inputs(w, device=device)
+    kbar_g, idx = gpu_select(inp, w, topk)
+    out, lse = gpu_forward(inp, w, topk)
+    assert ops.get_status() == ops.MOBA_OK
+    return inp, kbar_g, idx, out, lse, compare(w, inp, topk, out, lse, idx_gpu=idx, rows=rows)
+
+
+# ---------------------------------------------------------------------------
+# per-kernel parity
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("seqlens,H,D,bs", [((2048,), 1, 64, 256), ((1000, 777), 3, 128, 128),
+                                            ((4096,), 4, 128, 512)])
+def test_kpool_matches_oracle(seqlens, H, D, bs):
+    w = workloads.custom(seqlens, H, D, bs, topk=3, seed=11)
+    inp = workloads.make_inputs(w, device="cuda")
+    if w.varlen:
+        cu = torch.tensor(inp.cu_seqlens, dtype=torch.int32, device="cuda")
+        kbar = ops.kpool_varlen(inp.k, cu, bs)
+    else:
+        kbar = ops.kpool(inp.k, bs)
+    ref = oracle.kpool(flat(inp.k).cpu(), inp.cu_seqlens, H, D, bs)
+    got = kbar.cpu().numpy().astype(np.float64)
+    np.testing.assert_allclose(got, ref, rtol=1e-5, atol=1e-6)
+
+
+@pytest.mark.parametrize("topk", [1, 2, 3, 5, 8])
+def test_gate_matches_oracle(topk):
+    w = workloads.custom((3000, 5000), 2, 128, 128, topk=topk, seed=12)
+    inp = workloads.make_inputs(w, device="cuda")
+    _, idx = gpu_select(inp, w, topk)
+    q, k = flat(inp.q).cpu(), flat(inp.k).cpu()
+    tok, head = oracle.all_rows(w.total, w.H)
+    ref = oracle.moba_rows(q, k, flat(inp.v).cpu(), inp.cu_seqlens, w.H, w.D, w.block_size, topk,
+                           tok, head)
+    gi = idx.cpu().numpy().reshape(-1, topk)
+    differ = (gi != ref["idx"]).any(axis=1)
+    assert not (differ & (ref["gap"] >= 1e-5)).any()
+
+
+# ---------------------------------------------------------------------------
+# end-to-end parity on the workloads
+# ---------------------------------------------------------------------------
+
+def test_tiny_workload_all_rows():
+    w = workloads.WORKLOADS["tiny"]
+    *_, st = run_case(w, 3)
+    print("tiny", st)
+
+
+@pytest.mark.parametrize("topk", [3, 64])
+def test_train32k_sampled(topk):
+    w = workloads.WORKLOADS["train32k"]
+    rows = workloads.sample_rows(w, 4096)
+    *_, st = run_case(w, topk, rows=rows)
+    print("train32k", topk, st)
+
+
+def test_long128k_sampled_with_needles():
+    w = workloads.WORKLOADS["long128k"]
+    inp = workloads.make_inputs(w, device="cuda")
+    rows = workloads.sample_rows(w, 4096, needle_queries=inp.needle_queries)
+    _, idx = gpu_select(inp, w, 3)
+    out, lse = gpu_forward(inp, w, 3)
+    st = compare(w, inp, 3, out, lse, idx_gpu=idx, rows=rows)
+    print("long128k", st)
+
+
+def test_prefill1m_sampled():
+    w = workloads.WORKLOADS["prefill1m"]
+    rows = workloads.sample_rows(w, 4096)
+    *_, st = run_case(w, 3, rows=rows)
+    print("prefill1m", st)
+
+
+@pytest.mark.parametrize("topk", [1, 2, 3, 4, 8])
+def test_varlen_sampled(topk):
+    w = workloads.WORKLOADS["varlen"]
+    rows = workloads.sample_rows(w, 4096)
+    *_, st = run_case(w, topk, rows=rows)
+    print("varlen", topk, st)
+
+
+# ---------------------------------------------------------------------------
+# edge cases: tiny / ragged sizes, k >= n, k = 1, several sequences and heads
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("seqlens,H,D,bs,topk", [
+    ((1,), 1, 64, 64, 3),          # a single token
+    ((63,), 2, 64, 64, 3),         # one partial block
+    ((65,), 1, 128, 64, 3),        # tail block with one token
+    ((64 * 5,), 2, 128, 64, 2),    # several tiles, n > k
+    ((700,), 3, 64, 64, 4),        # ragged tail, many blocks
+    ((300,), 1, 128, 64, 1),       # top-k 1: own block only
+    ((512,), 2, 128, 128, 4),      # top-k == number of blocks (dense)
+    ((512,), 2, 64, 128, 9),       # top-k > number of blocks (dense)
+    ((200, 1, 64, 129), 2, 128, 64, 3),  # varlen with tiny sequences
+    ((4096, 4096), 2, 128, 256, 3),      # B = 2, fixed length
+    ((4096,), 2, 128, 64, 32),     # 31 past slots
+])
+def test_edge_cases(seqlens, H, D, bs, topk):
+    w = workloads.custom(seqlens, H, D, bs, topk=topk, seed=13)
+    *_, st = run_case(w, topk)
+    print(seqlens, st)
+
+
+def test_deterministic_and_workspace_variant():
+    w = workloads.custom((8192,), 4, 128, 512, topk=3, seed=14)
+    inp = workloads.make_inputs(w, device="cuda")
+    o1, l1 = ops.attn_fwd(inp.q, inp.k, inp.v, 512, 3)
+    o2, l2 = ops.attn_fwd(inp.q, inp.k, inp.v, 512, 3)
+    ws = torch.empty(ops.workspace_size(1, 4, 8192, 128, 512, 3), dtype=torch.uint8,
+                     device="cuda")
+    o3, l3 = ops.attn_fwd(inp.q, inp.k, inp.v, 512, 3, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert torch.equal(o1, o3) and torch.equal(l1, l3)
+
+
+def test_causality_on_gpu():
+    """Changing the future never changes earlier outputs."""
+    w = workloads.custom((4096,), 2, 128, 256, topk=3, seed=15)
+    inp = workloads.make_inputs(w, device="cuda")
+    o1, l1 = ops.attn_fwd(inp.q, inp.k, inp.v, 256, 3)
+    i = 2500
+    q2, k2, v2 = (x.clone() for x in (inp.q, inp.k, inp.v))
+    for x in (q2, k2, v2):
+        x[:, i + 1:] = torch.randn_like(x[:, i + 1:].float()).mul(3).to(torch.bfloat16)
+    o2, l2 = ops.attn_fwd(q2, k2, v2, 256, 3)
+    assert torch.equal(o1[:, :i + 1], o2[:, :i + 1])
+    assert torch.equal(l1[:, :, :i + 1], l2[:, :, :i + 1])
+
+
+def test_workspace_too_small_on_device():
+    w = workloads.custom((1024,), 1, 64, 64, topk=3, seed=16)
+    inp = workloads.make_inputs(w, device="cuda")
+    need = ops.workspace_size(1, 1, 1024, 64, 64, 3)
+    ws = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(RuntimeError, match="WORKSPACE"):
+        ops.attn_fwd(inp.q, inp.k, inp.v, 64, 3, workspace=ws)
