@@ -170,6 +170,20 @@ unsigned long long moba_launch_count(void);
 int moba_profile_begin(int max_calls);
 int moba_profile_end(float *phase_ms, int n_phases);
 
+/* Attention implementation used by the forward entry points (process-wide,
+ * not thread-safe): 0 = tcgen05 MMA with TMEM accumulators and TMA-staged
+ * K/V (default); 1 = the warp-level mma.sync kernels, kept as the measured
+ * baseline.  Both give the same selection and results within the stated
+ * tolerances.  MOBA_ERR_INVALID_ARG for any other value. */
+int moba_set_attention_kernel(int kind);
+
+/* Test hooks of the bounded waits in the tcgen05 kernels (process-wide):
+ * wait_limit_cycles is the clock64 budget of one mbarrier wait (<= 0 restores
+ * the default, about 2 s); flags bit 0 makes the K/V producer skip its first
+ * load so that the consumer's wait runs out and MOBA_ERR_TIMEOUT is recorded
+ * (read it with moba_get_status) instead of hanging the GPU. */
+int moba_debug_set(int flags, long long wait_limit_cycles);
+
 #ifdef __cplusplus
 }
 #endif

@@ -28,6 +28,21 @@ int *status_word() {
 }
 
 static std::atomic<unsigned long long> g_launches{0};
+
+// attention implementation: 0 = tcgen05 / TMEM / TMA, 1 = warp-level mma.sync
+static int g_attn_kind = 0;
+int past_tile_rows() { return g_attn_kind == 0 ? tc_tile_rows() : mma_tile_rows(); }
+cudaError_t launch_attn_past(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
+                             const __nv_bfloat16 *k, const __nv_bfloat16 *v, cudaStream_t st) {
+    return g_attn_kind == 0 ? launch_attn_past_tc(p, ws, q, k, v, st)
+                            : launch_attn_past_mma(p, ws, q, k, v, st);
+}
+cudaError_t launch_attn_current(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
+                                const __nv_bfloat16 *k, const __nv_bfloat16 *v,
+                                __nv_bfloat16 *out, float *lse, cudaStream_t st) {
+    return g_attn_kind == 0 ? launch_attn_current_tc(p, ws, q, k, v, out, lse, st)
+                            : launch_attn_current_mma(p, ws, q, k, v, out, lse, st);
+}
 void note_launches(int n) { g_launches.fetch_add((unsigned long long)n); }
 
 // Optional phase timing: CUDA events recorded on the caller's stream between
@@ -66,7 +81,7 @@ size_t workspace_bytes(const Plan &p, Workspace *ws, char *base) {
         w.counts = static_cast<int *>(take(sizeof(int) * N));
         w.list_off = static_cast<int *>(take(sizeof(int) * (N + 1)));
         w.tile_off = static_cast<int *>(take(sizeof(int) * (N + 1)));
-        w.cursor = static_cast<int *>(take(sizeof(int) * N));
+        w.ticket = static_cast<int *>(take(sizeof(int) * rows * p.km1));
         w.list = static_cast<int *>(take(sizeof(int) * rows * p.km1));
         w.part_o = static_cast<float *>(take(sizeof(float) * rows * p.km1 * p.D));
         w.part_lse = static_cast<float *>(take(sizeof(float) * rows * p.km1));
@@ -378,4 +393,16 @@ MOBA_EXPORT int moba_profile_end(float *phase_ms, int n_phases) {
         }
     }
     return g_prof.used;
+}
+
+MOBA_EXPORT int moba_set_attention_kernel(int kind) {
+    if (kind != 0 && kind != 1) return MOBA_ERR_INVALID_ARG;
+    g_attn_kind = kind;
+    return MOBA_OK;
+}
+
+MOBA_EXPORT int moba_debug_set(int flags, long long wait_limit_cycles) {
+    if (flags < 0) return MOBA_ERR_INVALID_ARG;
+    tc_debug_set(flags, wait_limit_cycles);
+    return MOBA_OK;
 }

@@ -382,7 +382,7 @@ __global__ __launch_bounds__(kThreads, 2) void current_kernel(Args a) {
 
 }  // namespace mma_path
 
-int past_tile_rows() { return mma_path::kM; }
+int mma_tile_rows() { return mma_path::kM; }
 
 static int sm_count() {
     int dev = 0, n = 0;
@@ -444,14 +444,14 @@ static cudaError_t launch_current_d(const Plan &p, const mma_path::Args &a, cuda
     return cudaGetLastError();
 }
 
-cudaError_t launch_attn_past(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
+cudaError_t launch_attn_past_mma(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
                              const __nv_bfloat16 *k, const __nv_bfloat16 *v, cudaStream_t st) {
     if (p.dense || p.km1 == 0) return cudaSuccess;
     auto a = make_args(p, ws, q, k, v, nullptr, nullptr);
     return p.D == 64 ? launch_past_d<64>(a, st) : launch_past_d<128>(a, st);
 }
 
-cudaError_t launch_attn_current(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
+cudaError_t launch_attn_current_mma(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
                                 const __nv_bfloat16 *k, const __nv_bfloat16 *v,
                                 __nv_bfloat16 *out, float *lse, cudaStream_t st) {
     auto a = make_args(p, ws, q, k, v, out, lse);

@@ -1,0 +1,749 @@
+// moba_attn_tc.cu -- block-sparse attention on the sm_103a tensor cores
+// (tcgen05.mma, accumulators in tensor memory, K/V staged by TMA).
+//
+// Pages: "When a MoBA reproduction will not run" (mhpq.cn/news/582794) section
+// 3.3 (softmax attention over the batched selected blocks, causal mask inside
+// the current block) and "MOBA mixture of block attention for server-side long
+// context" (hncyxsy.com/news/197418) section 3 (force_current_block).
+//
+// One CTA = one work tile of 128 query rows (M = 128) against a run of 64-key
+// K/V tiles, 192 threads in four roles:
+//   warp 0      TMA producer: the Q tile (contiguous rows) and a 2-stage ring
+//               of K/V tiles, each as two 64-dim boxes with the 128-byte swizzle
+//               that the tensor core's K-major / MN-major layouts expect;
+//   warp 1      allocates 256 TMEM columns; lane 0 issues the MMAs:
+//                 S_j = Q K_j^T   (M128 N64 K=D, into one of two S buffers)
+//                 O  += P_j V_j   (M128 N=D K64, P from shared memory)
+//               and signals completion through tcgen05.commit on mbarriers;
+//   warps 2..5  softmax: thread r owns query row r (its TMEM lane), reads its
+//               64 scores with tcgen05.ld, keeps the running max / sum, writes
+//               P_j (bf16) to shared memory in the swizzled K-major layout and,
+//               when the running max grows by more than 2^8, rescales its O row
+//               in TMEM.  They also run the epilogue.
+// Two CTAs share an SM (~113 KB shared memory and 256 TMEM columns each), so
+// one CTA's softmax overlaps the other's MMAs.
+//
+// Modes:
+//   kPast     gathered rows: the rows of one regroup list tile (rows that
+//             selected the same past block of the same head); the softmax warps
+//             gather Q with cp.async; output = normalised fp32 partial O and
+//             its log2-sum-exp per (row, slot);
+//   kCurrent  rows [r0, r0 + 128) of a sequence: causal attention over the own
+//             block (every key up to the row on the dense path), then the
+//             log-sum-exp merge with the row's past partials -> bf16 out, lse.
+//
+// Every mbarrier wait is bounded (clock64 budget); a wait that runs out sets
+// MOBA_ERR_TIMEOUT in the device status word and an abort flag that makes the
+// other roles leave their loops; the producer then waits (bounded) for its
+// copies in flight and the MMA lane for its MMAs before TMEM is freed.
+#include <cuda.h>
+
+#include "../../include/moba.h"
+#include "moba_internal.cuh"
+
+namespace moba {
+namespace tc {
+
+constexpr int kM = 128;           // query rows per tile
+constexpr int kN = 64;            // keys per K/V tile
+constexpr int kStages = 2;        // K/V ring depth
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 256;    // S0 [0,64) S1 [64,128) O [128,128+D)
+constexpr uint32_t kBox = 64;     // dims per TMA box (128 bytes of bf16)
+
+enum Mode { kPast = 0, kCurrent = 1 };
+
+struct Args {
+    Geometry g;
+    const __nv_bfloat16 *q;
+    __nv_bfloat16 *out;
+    float *lse;
+    int topk, km1, dense, fixed, S_fixed;
+    const int32_t *idx;
+    const int *list, *list_off, *tile_off;
+    int n_lists;
+    float *part_o, *part_lse;
+    float scale_log2;
+    int *status;
+    long long wait_limit;  // clock64 budget of one wait
+    int debug_flags;       // bit 0: the producer skips its first K/V load
+};
+
+// ----------------------------------------------------------------------------
+// PTX wrappers
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t saddr(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool pred) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(pred ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+// tcgen05
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     bar)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Shared-memory matrix descriptor (tcgen05 format): start address, leading
+// byte offset, stride byte offset (all >> 4), version 1 at bit 46, 128-byte
+// swizzle (layout type 2) at bits 61-63.
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
+}
+// Instruction descriptor of kind::f16: fp32 accumulate, bf16 A and B, A
+// K-major, B K-major (b_mn = 0) or MN-major (b_mn = 1), M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// ----------------------------------------------------------------------------
+// shared memory plan (offsets from a 1024-byte aligned base)
+// ----------------------------------------------------------------------------
+template <int D>
+struct Smem {
+    static constexpr int NB = D / kBox;                       // 64-dim boxes per row
+    static constexpr uint32_t kQBox = kM * 128;               // 16 KB
+    static constexpr uint32_t kKVBox = kN * 128;              // 8 KB
+    static constexpr uint32_t kQ = 0;
+    static constexpr uint32_t kK = kQ + NB * kQBox;           // stages of K
+    static constexpr uint32_t kV = kK + kStages * NB * kKVBox;
+    static constexpr uint32_t kP = kV + kStages * NB * kKVBox;
+    static constexpr uint32_t kTiles = kP + kM * 128;         // end of the tiles
+    // mbarriers q_full, kv_full[2], kv_empty[2], s_full[2], p_full, pv_done,
+    // drain; then the TMEM address slot and the abort flag
+    static constexpr int kNumBars = 10;
+    static constexpr uint32_t kMisc = kNumBars * 8 + 8;
+    // The tiles need a 1024-byte aligned base; the dynamic window is at least
+    // 16-byte aligned, so up to 1008 bytes of slack.  The misc words go into
+    // the slack when it is large enough, else right after the tiles.  For
+    // D = 128 this keeps two CTAs per SM (2 x (115696 + 1024) <= 233472).
+    static constexpr uint32_t kRequest =
+        (kTiles + 1008 > 80 * 1024) ? kTiles + 1008 : 80 * 1024;  // never a third CTA
+};
+
+struct Ctl {
+    volatile int *abort;
+    int *status;
+    long long limit;
+};
+
+// Bounded wait; false when it ran out (status set) or another role aborted.
+__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl &c) {
+    if (mbar_test(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (mbar_test(bar, parity)) return true;
+        if (*c.abort) return false;
+        if (clock64() - t0 > c.limit) {
+            *c.abort = 1;
+            atomicExch(c.status, (int)MOBA_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+// Bounded wait that ignores the abort flag (draining copies / MMAs in flight).
+__device__ __noinline__ void drain_bar(uint32_t bar, uint32_t parity, long long limit) {
+    const long long t0 = clock64();
+    while (!mbar_test(bar, parity) && clock64() - t0 <= limit) {
+    }
+}
+
+template <int D, int MODE>
+__global__ void __launch_bounds__(kThreads, 2)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                   const __grid_constant__ CUtensorMap tmap_k,
+                   const __grid_constant__ CUtensorMap tmap_v, Args a) {
+    using L = Smem<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = saddr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t misc = (base - raw >= L::kMisc) ? raw : base + L::kTiles;
+    uint8_t *gmisc = smem_raw + (misc - raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = a.g.H;
+
+    // ---------------- work tile ----------------
+    int h, seq0, L_len, r0 = 0, nrows = kM, kv_tok0, kv_end, nkv;
+    int lbeg = 0, kv_lo = 0;
+    if (MODE == kPast) {
+        const int tile = blockIdx.x;
+        if (tile >= __ldg(a.tile_off + a.n_lists)) return;
+        int lo = 0, hi = a.n_lists - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(a.tile_off + mid) <= tile) lo = mid; else hi = mid - 1;
+        }
+        const int Lid = lo;
+        const int gblk = Lid / H;
+        h = Lid % H;
+        const int b = upper_index(a.g.blk_base, a.g.num_seqs, gblk);
+        const int c = gblk - __ldg(a.g.blk_base + b);
+        seq0 = __ldg(a.g.cu + b);
+        L_len = __ldg(a.g.cu + b + 1) - seq0;
+        kv_tok0 = seq0 + c * a.g.bs;
+        kv_end = min(kv_tok0 + a.g.bs, seq0 + L_len);
+        lbeg = __ldg(a.list_off + Lid);
+        const int lcnt = __ldg(a.list_off + Lid + 1) - lbeg;
+        r0 = (tile - __ldg(a.tile_off + Lid)) * kM;
+        nrows = min(kM, lcnt - r0);
+        lbeg += r0;
+    } else {
+        h = blockIdx.y;
+        const int b = blockIdx.z;
+        seq0 = __ldg(a.g.cu + b);
+        L_len = __ldg(a.g.cu + b + 1) - seq0;
+        // heavy (late) tiles first
+        r0 = (gridDim.x - 1 - blockIdx.x) * kM;
+        if (r0 >= L_len) return;
+        nrows = min(kM, L_len - r0);
+        kv_lo = a.dense ? 0 : (r0 / a.g.bs) * a.g.bs;
+        kv_tok0 = seq0 + kv_lo;
+        kv_end = seq0 + min(r0 + kM, L_len);
+    }
+    nkv = (kv_end - kv_tok0 + kN - 1) / kN;
+
+    // ---------------- set-up ----------------
+    const uint32_t sQ = base + L::kQ, sK = base + L::kK, sV = base + L::kV, sP = base + L::kP;
+    const uint32_t bar0 = misc;
+    const uint32_t b_qfull = bar0, b_kvfull = bar0 + 8, b_kvempty = bar0 + 24,
+                   b_sfull = bar0 + 40, b_pfull = bar0 + 56, b_pvdone = bar0 + 64,
+                   b_drain = bar0 + 72;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gmisc + L::kNumBars * 8);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(gmisc + L::kNumBars * 8 + 4);
+    Ctl ctl{abort_flag, a.status, a.wait_limit};
+
+    if (tid == 0) {
+        mbar_init(b_qfull, MODE == kPast ? 4 : 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(b_kvfull + 8 * s, 1);
+            mbar_init(b_kvempty + 8 * s, 1);
+        }
+        mbar_init(b_sfull, 1);
+        mbar_init(b_sfull + 8, 1);
+        mbar_init(b_pfull, 4);
+        mbar_init(b_pvdone, 1);
+        mbar_init(b_drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         saddr(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ================= TMA producer =================
+        if (lane == 0) {
+            constexpr uint32_t kKVBytes = 2u * L::NB * L::kKVBox;
+            if (MODE == kCurrent) {
+                mbar_expect_tx(b_qfull, L::NB * L::kQBox);
+                for (int x = 0; x < L::NB; ++x)
+                    tma_load_3d(sQ + x * L::kQBox, &tmap_q, b_qfull, x * kBox, h, seq0 + r0);
+            }
+            int pending[kStages];  // tile whose load sits in each stage, -1 if none
+            for (int s = 0; s < kStages; ++s) pending[s] = -1;
+            for (int j = 0; j < nkv; ++j) {
+                const int s = j % kStages;
+                if (j >= kStages &&
+                    !wait_bar(b_kvempty + 8 * s, ((j / kStages) - 1) & 1, ctl))
+                    break;
+                pending[s] = -1;
+                if ((a.debug_flags & 1) && j == 0) continue;  // fault-injection knob
+                const uint32_t kb = sK + s * L::NB * L::kKVBox, vb = sV + s * L::NB * L::kKVBox;
+                mbar_expect_tx(b_kvfull + 8 * s, kKVBytes);
+                for (int x = 0; x < L::NB; ++x) {
+                    tma_load_3d(kb + x * L::kKVBox, &tmap_k, b_kvfull + 8 * s, x * kBox, h,
+                                kv_tok0 + j * kN);
+                    tma_load_3d(vb + x * L::kKVBox, &tmap_v, b_kvfull + 8 * s, x * kBox, h,
+                                kv_tok0 + j * kN);
+                }
+                pending[s] = j;
+            }
+            if (*abort_flag) {
+                // let the copies still in flight land before the CTA exits
+                for (int s = 0; s < kStages; ++s)
+                    if (pending[s] >= 0)
+                        drain_bar(b_kvfull + 8 * s, (pending[s] / kStages) & 1, a.wait_limit);
+            }
+        }
+    } else if (warp == 1) {
+        // ================= MMA issuer =================
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_bf16(kM, kN, 0);
+            constexpr uint32_t idesc_o = idesc_bf16(kM, D, 1);
+            const uint32_t tO = tmem + 128;
+            bool ok = wait_bar(b_qfull, 0, ctl);
+            int j = 0;
+            for (; ok && j <= nkv; ++j) {
+                if (j < nkv) {
+                    const int s = j % kStages;
+                    if (!wait_bar(b_kvfull + 8 * s, (j / kStages) & 1, ctl)) break;
+                    tc_fence_after();
+                    const uint32_t kb = sK + s * L::NB * L::kKVBox;
+                    const uint32_t tS = tmem + (j & 1) * kN;
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint32_t off = (uint32_t)(k % 4) * 32;  // 16 dims = 32 B
+                        const uint64_t ad = sdesc(sQ + (k / 4) * L::kQBox + off, 16, 1024);
+                        const uint64_t bd = sdesc(kb + (k / 4) * L::kKVBox + off, 16, 1024);
+                        tc_mma(tS, ad, bd, idesc_s, k > 0);
+                    }
+                    tc_commit(b_sfull + 8 * (j & 1));
+                }
+                if (j >= 1) {
+                    const int jp = j - 1;
+                    if (!wait_bar(b_pfull, jp & 1, ctl)) break;
+                    tc_fence_after();
+                    const uint32_t vb = sV + (jp % kStages) * L::NB * L::kKVBox;
+#pragma unroll
+                    for (int k = 0; k < kN / 16; ++k) {
+                        const uint64_t ad = sdesc(sP + k * 32, 16, 1024);
+                        const uint64_t bd = sdesc(vb + k * 2048, L::kKVBox, 1024);
+                        tc_mma(tO, ad, bd, idesc_o, (jp > 0 || k > 0) ? 1u : 0u);
+                    }
+                    tc_commit(b_pvdone);
+                    tc_commit(b_kvempty + 8 * (jp % kStages));
+                }
+            }
+            // every MMA this thread issued has finished before TMEM is freed
+            tc_commit(b_drain);
+            drain_bar(b_drain, 0, a.wait_limit);
+        }
+    } else {
+        // ================= softmax + epilogue (warps 2..5) =================
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        int row_tok = -1, slot = 0;
+        bool row_valid = row < nrows;
+        if (MODE == kPast) {
+            // gather this row of Q into the swizzled K-major tile
+            int e = 0;
+            if (row_valid) e = __ldg(a.list + lbeg + row);
+            row_tok = e >> kSlotBits;
+            slot = e & ((1 << kSlotBits) - 1);
+            const __nv_bfloat16 *src = a.q + ((size_t)row_tok * H + h) * D;
+#pragma unroll
+            for (int ch = 0; ch < D / 8; ++ch) {
+                const uint32_t dst = sQ + (ch / 8) * L::kQBox + row * 128 +
+                                     ((uint32_t)((ch % 8) ^ (row & 7)) << 4);
+                cp_async16(dst, row_valid ? (const void *)(src + ch * 8) : (const void *)a.q,
+                           row_valid);
+            }
+            cp_async_wait_all();
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_qfull);
+        } else {
+            row_tok = seq0 + r0 + row;
+        }
+        const int i_loc = row_tok - seq0;  // position inside the sequence
+        const int rb = (MODE == kCurrent && !a.dense) ? (i_loc / a.g.bs) * a.g.bs : 0;
+        const int r_min = r0, r_last = r0 + nrows - 1;
+        const int rb_max = (MODE == kCurrent && !a.dense) ? (r_last / a.g.bs) * a.g.bs : 0;
+
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nkv; ++j) {
+            if (!__all_sync(0xffffffffu, wait_bar(b_sfull + 8 * (j & 1), (j >> 1) & 1, ctl))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sr[2][32];
+            const uint32_t tS = tmem + lane_off + (j & 1) * kN;
+            tc_ld32(tS, sr[0]);
+            tc_ld32(tS + 32, sr[1]);
+            tc_wait_ld();
+            float x[64];
+            const int key0 = kv_lo + j * kN;  // sequence-local position of column 0
+            const bool need_mask = MODE == kCurrent &&
+                                   (key0 + kN - 1 > r_min || key0 < rb_max ||
+                                    seq0 + key0 + kN > kv_end);
+            float mt = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                float v = __uint_as_float(sr[c >> 5][c & 31]) * a.scale_log2;
+                if (MODE == kPast) {
+                    if (kv_tok0 + j * kN + c >= kv_end) v = -INFINITY;
+                } else if (need_mask) {
+                    const int kp = key0 + c;
+                    if (kp > i_loc || kp < rb || seq0 + kp >= kv_end) v = -INFINITY;
+                }
+                x[c] = v;
+                mt = fmaxf(mt, v);
+            }
+            const float m_new = fmaxf(m_run, mt);
+            // rescale only when the max grew by more than 2^8 (P stays <= 256)
+            const bool need = (j > 0) && (m_new > m_run + 8.f);
+            if (j > 0) {
+                if (!__all_sync(0xffffffffu, wait_bar(b_pvdone, (j - 1) & 1, ctl))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, need)) {
+                    const float alpha = need ? fast_exp2(m_run - m_new) : 1.f;
+#pragma unroll
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t o[32];
+                        tc_ld32(tmem + lane_off + 128 + c0, o);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                        tc_st32(tmem + lane_off + 128 + c0, o);
+                    }
+                    tc_wait_st();
+                    if (need) l_run *= alpha;
+                }
+                if (need) m_run = m_new;
+            } else {
+                m_run = m_new;
+            }
+            const float mu = (m_run == -INFINITY) ? 0.f : m_run;
+            // P_j (bf16) into the swizzled K-major tile: row `row`, 8 chunks
+            float lsum = 0.f;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+                uint32_t pk[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float p0 = fast_exp2(x[ch * 8 + 2 * e] - mu);
+                    const float p1 = fast_exp2(x[ch * 8 + 2 * e + 1] - mu);
+                    lsum += p0 + p1;
+                    __nv_bfloat162 bb = __floats2bfloat162_rn(p0, p1);
+                    pk[e] = *reinterpret_cast<uint32_t *>(&bb);
+                }
+                const uint32_t dst = sP + row * 128 + ((uint32_t)(ch ^ (row & 7)) << 4);
+                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(pk[0]),
+                             "r"(pk[1]), "r"(pk[2]), "r"(pk[3])
+                             : "memory");
+            }
+            l_run += lsum;
+            fence_proxy_async();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_pfull);
+        }
+        // ---------------- epilogue ----------------
+        if (ok && nkv > 0) ok = __all_sync(0xffffffffu, wait_bar(b_pvdone, (nkv - 1) & 1, ctl));
+        tc_fence_after();
+        if (ok) {
+            const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+            const float lse2 = m_run + __log2f(l_run);
+            if (MODE == kPast) {
+                const size_t pslot = ((size_t)row_tok * H + h) * a.km1 + slot;
+                float *dst = a.part_o + pslot * D;
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[32];
+                    tc_ld32(tmem + lane_off + 128 + c0, o);
+                    tc_wait_ld();
+                    if (row_valid) {
+#pragma unroll
+                        for (int c = 0; c < 32; c += 4)
+                            *reinterpret_cast<float4 *>(dst + c0 + c) = make_float4(
+                                __uint_as_float(o[c]) * inv, __uint_as_float(o[c + 1]) * inv,
+                                __uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv);
+                    }
+                }
+                if (row_valid) a.part_lse[pslot] = lse2;
+            } else {
+                // log-sum-exp merge with the row's past partials (ascending blocks)
+                float w_cur = 1.f, wsum = 1.f, mmax = lse2;
+                int np = 0;
+                const size_t rowid = (size_t)row_tok * H + h;
+                if (row_valid && !a.dense && a.km1 > 0) {
+                    const int ci = i_loc / a.g.bs;
+                    const int32_t *sel = a.idx + rowid * a.topk;
+                    for (; np < a.km1; ++np) {
+                        const int c = __ldg(sel + np);
+                        if (c < 0 || c >= ci) break;
+                        mmax = fmaxf(mmax, __ldg(a.part_lse + rowid * a.km1 + np));
+                    }
+                    if (np > 0) {
+                        w_cur = fast_exp2(lse2 - mmax);
+                        wsum = w_cur;
+                        for (int s = 0; s < np; ++s)
+                            wsum += fast_exp2(__ldg(a.part_lse + rowid * a.km1 + s) - mmax);
+                    }
+                }
+                const float iw = 1.f / wsum;
+                const float fcur = w_cur * inv * iw;
+                __nv_bfloat16 *dst = a.out + rowid * D;
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[32];
+                    tc_ld32(tmem + lane_off + 128 + c0, o);
+                    tc_wait_ld();
+                    if (row_valid) {
+                        float acc[32];
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) acc[c] = __uint_as_float(o[c]) * fcur;
+                        for (int s = 0; s < np; ++s) {
+                            const size_t ps = rowid * a.km1 + s;
+                            const float w = fast_exp2(__ldg(a.part_lse + ps) - mmax) * iw;
+                            const float4 *src =
+                                reinterpret_cast<const float4 *>(a.part_o + ps * D + c0);
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) {
+                                const float4 f = __ldg(src + c);
+                                acc[4 * c] = fmaf(w, f.x, acc[4 * c]);
+                                acc[4 * c + 1] = fmaf(w, f.y, acc[4 * c + 1]);
+                                acc[4 * c + 2] = fmaf(w, f.z, acc[4 * c + 2]);
+                                acc[4 * c + 3] = fmaf(w, f.w, acc[4 * c + 3]);
+                            }
+                        }
+#pragma unroll
+                        for (int c = 0; c < 32; c += 8) {
+                            uint4 pk;
+                            __nv_bfloat162 b0 = __floats2bfloat162_rn(acc[c], acc[c + 1]);
+                            __nv_bfloat162 b1 = __floats2bfloat162_rn(acc[c + 2], acc[c + 3]);
+                            __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[c + 4], acc[c + 5]);
+                            __nv_bfloat162 b3 = __floats2bfloat162_rn(acc[c + 6], acc[c + 7]);
+                            pk.x = *reinterpret_cast<uint32_t *>(&b0);
+                            pk.y = *reinterpret_cast<uint32_t *>(&b1);
+                            pk.z = *reinterpret_cast<uint32_t *>(&b2);
+                            pk.w = *reinterpret_cast<uint32_t *>(&b3);
+                            *reinterpret_cast<uint4 *>(dst + c0 + c) = pk;
+                        }
+                    }
+                }
+                if (row_valid) {
+                    const float lse_out = (np > 0) ? mmax + __log2f(wsum) : lse2;
+                    const size_t li = a.fixed
+                                          ? ((size_t)blockIdx.z * H + h) * a.S_fixed + i_loc
+                                          : (size_t)h * a.g.total + row_tok;
+                    a.lse[li] = lse_out * 0.69314718055994530942f;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+}  // namespace tc
+
+// ----------------------------------------------------------------------------
+// host side
+// ----------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// [total][H][D] bf16 viewed as a 3-D tensor (D, H, total); box = 64 dims x 1
+// head x `rows` tokens, 128-byte swizzle.
+static bool make_map(CUtensorMap *m, const void *ptr, int total, int H, int D, int rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)total};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)rows};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static long long g_wait_limit = 4000000000ll;  // ~2 s at 2 GHz
+static int g_debug_flags = 0;
+
+void tc_debug_set(int flags, long long wait_limit) {
+    g_debug_flags = flags;
+    g_wait_limit = wait_limit > 0 ? wait_limit : 4000000000ll;
+}
+
+int tc_tile_rows() { return tc::kM; }
+
+static tc::Args make_tc_args(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
+                             __nv_bfloat16 *out, float *lse) {
+    tc::Args a;
+    a.g.cu = ws.cu;
+    a.g.blk_base = ws.blk_base;
+    a.g.num_seqs = p.num_seqs;
+    a.g.total = p.total;
+    a.g.H = p.H;
+    a.g.D = p.D;
+    a.g.bs = p.bs;
+    a.q = q;
+    a.out = out;
+    a.lse = lse;
+    a.topk = p.topk;
+    a.km1 = p.km1;
+    a.dense = p.dense ? 1 : 0;
+    a.fixed = p.fixed ? 1 : 0;
+    a.S_fixed = p.max_len;
+    a.idx = ws.idx;
+    a.list = ws.list;
+    a.list_off = ws.list_off;
+    a.tile_off = ws.tile_off;
+    a.n_lists = p.NBcap * p.H;
+    a.part_o = ws.part_o;
+    a.part_lse = ws.part_lse;
+    a.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)p.D));
+    a.status = status_word();
+    a.wait_limit = g_wait_limit;
+    a.debug_flags = g_debug_flags;
+    return a;
+}
+
+template <int D, int MODE>
+static cudaError_t launch_tc(const Plan &p, const tc::Args &a, const __nv_bfloat16 *q,
+                             const __nv_bfloat16 *k, const __nv_bfloat16 *v, cudaStream_t st) {
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, q, p.total, p.H, D, tc::kM) || !make_map(&mk, k, p.total, p.H, D, tc::kN) ||
+        !make_map(&mv, v, p.total, p.H, D, tc::kN))
+        return cudaErrorInvalidValue;
+    const int smem = tc::Smem<D>::kRequest;
+    auto kern = tc::attn_tc_kernel<D, MODE>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid;
+    if (MODE == tc::kPast) {
+        // an upper bound of the tiles; CTAs past the real count exit at once
+        const long long rows = (long long)p.total * p.H * p.km1;
+        const long long tiles = rows / tc::kM + (long long)p.NBcap * p.H + 1;
+        grid = dim3((unsigned)tiles);
+    } else {
+        grid = dim3((p.max_len + tc::kM - 1) / tc::kM, p.H, p.num_seqs);
+    }
+    kern<<<grid, tc::kThreads, smem, st>>>(mq, mk, mv, a);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_attn_past_tc(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
+                                const __nv_bfloat16 *k, const __nv_bfloat16 *v, cudaStream_t st) {
+    if (p.dense || p.km1 == 0) return cudaSuccess;
+    auto a = make_tc_args(p, ws, q, nullptr, nullptr);
+    return p.D == 64 ? launch_tc<64, tc::kPast>(p, a, q, k, v, st)
+                     : launch_tc<128, tc::kPast>(p, a, q, k, v, st);
+}
+
+cudaError_t launch_attn_current_tc(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
+                                   const __nv_bfloat16 *k, const __nv_bfloat16 *v,
+                                   __nv_bfloat16 *out, float *lse, cudaStream_t st) {
+    auto a = make_tc_args(p, ws, q, out, lse);
+    return p.D == 64 ? launch_tc<64, tc::kCurrent>(p, a, q, k, v, st)
+                     : launch_tc<128, tc::kCurrent>(p, a, q, k, v, st);
+}
+
+}  // namespace moba

@@ -101,9 +101,27 @@ __global__ __launch_bounds__(kPoolThreads) void kpool_kernel(Geometry g,
     const int TG = kPoolThreads / CW;
     const int colx = threadIdx.x % CW, tg = threadIdx.x / CW;
     const int col = blockIdx.y * CW + colx;
-    float acc[8];
+    // compensated (Kahan) fp32 sums: the mean of a 4096-token block stays
+    // within ~1 ulp, which keeps the gate scores close to exact
+    float acc[8], comp[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    for (int e = 0; e < 8; ++e) acc[e] = comp[e] = 0.f;
+    auto add8 = [&](const uint4 &u) {
+        const __nv_bfloat162 *p = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(p[e]);
+            const float xs[2] = {f.x, f.y};
+#pragma unroll
+            for (int o = 0; o < 2; ++o) {
+                const int k = 2 * e + o;
+                const float y = xs[o] - comp[k];
+                const float t = acc[k] + y;
+                comp[k] = (t - acc[k]) - y;
+                acc[k] = t;
+            }
+        }
+    };
     if (tg < TG && col < HD8) {
         const uint4 *base = reinterpret_cast<const uint4 *>(k) + col;
         const size_t row = (size_t)HD8;
@@ -113,26 +131,9 @@ __global__ __launch_bounds__(kPoolThreads) void kpool_kernel(Geometry g,
 #pragma unroll
             for (int j = 0; j < 4; ++j) u[j] = __ldcs(base + (size_t)(t + j * TG) * row);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const __nv_bfloat162 *p = reinterpret_cast<const __nv_bfloat162 *>(&u[j]);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float2 f = __bfloat1622float2(p[e]);
-                    acc[2 * e] += f.x;
-                    acc[2 * e + 1] += f.y;
-                }
-            }
+            for (int j = 0; j < 4; ++j) add8(u[j]);
         }
-        for (; t < t1; t += TG) {
-            uint4 u = __ldcs(base + (size_t)t * row);
-            const __nv_bfloat162 *p = reinterpret_cast<const __nv_bfloat162 *>(&u);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float2 f = __bfloat1622float2(p[e]);
-                acc[2 * e] += f.x;
-                acc[2 * e + 1] += f.y;
-            }
-        }
+        for (; t < t1; t += TG) add8(__ldcs(base + (size_t)t * row));
     }
 #pragma unroll
     for (int e = 0; e < 8; ++e) red[threadIdx.x][e] = acc[e];
@@ -174,131 +175,223 @@ cudaError_t launch_kpool(const Plan &p, const Workspace &ws, const __nv_bfloat16
 }
 
 // ---------------------------------------------------------------------------
-// K2: gate + top-k.  One thread per (token, head); a CTA holds 128
-// consecutive tokens of one head, so the lanes of a warp read the same
-// mean-pooled key (an L1 broadcast).  Scores are fp32 dot products with four
-// interleaved partial sums.  The running top list keeps the KCAP best
-// (score desc, block asc) candidates; since blocks are visited in ascending
-// order, a strictly greater score is needed to move ahead of an earlier block,
-// which gives the lower-index tie-break.  Rows whose own block has at most
-// topk - 1 predecessors take them all without scoring.
-// With COUNT, every past selection is also counted per (block, head) for the
-// regroup.
+// K2: gate + top-k.  A CTA scores 128 consecutive query rows of one (sequence,
+// head) against the pooled keys of that sequence's past blocks.  Four lanes
+// share a row: lane j of a quad holds dims [j*D/4, (j+1)*D/4) of the quad's 4
+// rows in fp32 registers, so every pooled-key load from shared memory feeds 16
+// FMAs.  The quad adds its four partial dot products with two butterfly
+// shuffles (all four lanes end with bit-identical sums) and lane j keeps the
+// running top list of row j.  Pooled keys are staged 64 blocks at a time; the
+// 16-byte chunks of a staged row are XOR-swizzled by the reading lane so the
+// four distinct addresses of a load hit distinct banks.
+// The top list keeps the KCAP best (score desc, block asc) candidates; blocks
+// arrive in ascending order and a strictly greater score is needed to move
+// ahead of an earlier block, which is the lower-index tie-break.  Rows whose
+// own block has at most topk - 1 predecessors take them all without scoring.
+// With COUNT, each past selection also gets a ticket (its position inside the
+// (block, head) query list): ranks come from a shared-memory histogram and one
+// global atomic per non-empty bin reserves the CTA's range.
 // ---------------------------------------------------------------------------
 constexpr int kGateThreads = 128;
+constexpr int kGateRows = 128;
+constexpr int kGateChunk = 64;
+constexpr int kHistBins = 512;
+constexpr int kEmpty = 0x7fffffff;
 
 template <int D, int KCAP, bool COUNT>
-__global__ __launch_bounds__(kGateThreads) void gate_kernel(Geometry g,
-                                                             const __nv_bfloat16 *__restrict__ q,
-                                                             const float *__restrict__ kbar,
-                                                             int32_t *__restrict__ idx, int topk,
-                                                             int *__restrict__ counts) {
-    const int h = blockIdx.y;
-    const int t = blockIdx.x * kGateThreads + threadIdx.x;
-    if (t >= g.total) return;
-    const int H = g.H;
-    const int b = upper_index(g.cu, g.num_seqs, t);
-    const int i = t - __ldg(g.cu + b);
-    const int ci = i / g.bs;
+__global__ __launch_bounds__(kGateThreads) void gate_kernel(
+    Geometry g, const __nv_bfloat16 *__restrict__ q, const float *__restrict__ kbar,
+    int32_t *__restrict__ idx, int *__restrict__ ticket, int topk, int *__restrict__ counts) {
+    constexpr int DL = D / 4;  // dims per lane
+    constexpr int M = DL / 4;  // float4 chunks per lane
+    __shared__ __align__(16) float skb[kGateChunk * D];
+    __shared__ int hist[kHistBins];
+    __shared__ int s_cmax, s_call;
+    const int h = blockIdx.y, b = blockIdx.z, H = g.H;
+    const int seq0 = __ldg(g.cu + b), L = __ldg(g.cu + b + 1) - seq0;
+    const int i0 = blockIdx.x * kGateRows;
+    if (i0 >= L) return;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int j = lane & 3, rbase = 32 * warp + 4 * (lane >> 2);
     const int km1 = topk - 1;
     const int bbase = __ldg(g.blk_base + b);
-    int32_t *out = idx + ((size_t)t * H + h) * topk;
 
-    if (km1 == 0) {  // top-1: the own block only
-        out[0] = ci;
-        return;
-    }
-    if (ci <= km1) {
-        for (int j = 0; j < topk; ++j) out[j] = (j <= ci) ? j : -1;
-        if (COUNT)
-            for (int c = 0; c < ci; ++c) atomicAdd(counts + (size_t)(bbase + c) * H + h, 1);
-        return;
-    }
+    const int my_i = i0 + rbase + j;
+    const bool my_valid = my_i < L;
+    const int my_ci = my_valid ? my_i / g.bs : 0;
+    const int my_tok = seq0 + my_i;
+    const bool my_scored = my_valid && km1 > 0 && my_ci > km1;
 
-    float qf[D];
-    {
-        const uint4 *qp = reinterpret_cast<const uint4 *>(q + ((size_t)t * H + h) * D);
+    if (tid == 0) {
+        s_cmax = 0;
+        s_call = 0;
+    }
+    if (COUNT)
+        for (int x = tid; x < kHistBins; x += kGateThreads) hist[x] = 0;
+    __syncthreads();
+    if (my_scored) atomicMax(&s_cmax, my_ci);
+    if (my_valid) atomicMax(&s_call, my_ci);
+
+    float qf[4][DL];
 #pragma unroll
-        for (int j = 0; j < D / 8; ++j) {
-            uint4 u = __ldcs(qp + j);
+    for (int r = 0; r < 4; ++r) {
+        const int i = i0 + rbase + r;
+        const uint4 *qp = reinterpret_cast<const uint4 *>(q + ((size_t)(seq0 + i) * H + h) * D + j * DL);
+#pragma unroll
+        for (int c8 = 0; c8 < DL / 8; ++c8) {
+            uint4 u = (i < L) ? __ldcs(qp + c8) : make_uint4(0, 0, 0, 0);
             const __nv_bfloat162 *p2 = reinterpret_cast<const __nv_bfloat162 *>(&u);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 float2 f = __bfloat1622float2(p2[e]);
-                qf[8 * j + 2 * e] = f.x;
-                qf[8 * j + 2 * e + 1] = f.y;
+                qf[r][8 * c8 + 2 * e] = f.x;
+                qf[r][8 * c8 + 2 * e + 1] = f.y;
             }
         }
     }
+    const int wneed = __reduce_max_sync(0xffffffffu, my_scored ? my_ci : 0);
+    __syncthreads();
+    const int cmax = s_cmax;
+
     float ts[KCAP];
     int ti[KCAP];
 #pragma unroll
-    for (int j = 0; j < KCAP; ++j) {
-        ts[j] = -INFINITY;
-        ti[j] = 0x7fffffff;
+    for (int x = 0; x < KCAP; ++x) {
+        ts[x] = -INFINITY;
+        ti[x] = kEmpty;
     }
-    const float4 *kb = reinterpret_cast<const float4 *>(kbar + ((size_t)bbase * H + h) * D);
-    const size_t kstride = (size_t)H * D / 4;
-    for (int c = 0; c < ci; ++c) {
-        const float4 *row = kb + (size_t)c * kstride;
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-        for (int j = 0; j < D / 4; ++j) {
-            float4 m = __ldg(row + j);
-            a0 = fmaf(qf[4 * j + 0], m.x, a0);
-            a1 = fmaf(qf[4 * j + 1], m.y, a1);
-            a2 = fmaf(qf[4 * j + 2], m.z, a2);
-            a3 = fmaf(qf[4 * j + 3], m.w, a3);
+    const float *kb_head = kbar + ((size_t)bbase * H + h) * D;
+    for (int c0 = 0; c0 < cmax; c0 += kGateChunk) {
+        const int nrow = min(kGateChunk, cmax - c0);
+        __syncthreads();
+        for (int x = tid; x < nrow * (D / 4); x += kGateThreads) {
+            const int row = x / (D / 4), ch = x % (D / 4);
+            const int jj = ch / M, mm = ch % M;
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(kb_head + (size_t)(c0 + row) * H * D) + ch);
+            reinterpret_cast<float4 *>(skb + row * D)[jj * M + (mm ^ jj)] = v;
         }
-        float cur = (a0 + a1) + (a2 + a3);
-        if (cur != cur) cur = -INFINITY;  // a NaN score ranks last
-        int curi = c;
-        bool ins = false;
+        __syncthreads();
+        const int cend = min(c0 + kGateChunk, wneed);
+        for (int c = c0; c < cend; ++c) {
+            const float4 *kr = reinterpret_cast<const float4 *>(skb + (c - c0) * D) + j * M;
+            float acc[4][4];
 #pragma unroll
-        for (int j = 0; j < KCAP; ++j) {
-            // an empty slot (index INT_MAX) takes any candidate, so every slot
-            // is filled once km1 candidates have been seen
-            bool take = (j < km1) && (ins || cur > ts[j] || ti[j] == 0x7fffffff);
-            if (take) {
-                float fs = ts[j];
-                int fi = ti[j];
-                ts[j] = cur;
-                ti[j] = curi;
-                cur = fs;
-                curi = fi;
-                ins = true;
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[r][e] = 0.f;
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                const float4 kv = kr[m ^ j];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    acc[r][0] = fmaf(qf[r][4 * m + 0], kv.x, acc[r][0]);
+                    acc[r][1] = fmaf(qf[r][4 * m + 1], kv.y, acc[r][1]);
+                    acc[r][2] = fmaf(qf[r][4 * m + 2], kv.z, acc[r][2]);
+                    acc[r][3] = fmaf(qf[r][4 * m + 3], kv.w, acc[r][3]);
+                }
+            }
+            float sc[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                float x = (acc[r][0] + acc[r][1]) + (acc[r][2] + acc[r][3]);
+                x += __shfl_xor_sync(0xffffffffu, x, 1);
+                x += __shfl_xor_sync(0xffffffffu, x, 2);
+                sc[r] = x;
+            }
+            float cur = (j == 0) ? sc[0] : (j == 1) ? sc[1] : (j == 2) ? sc[2] : sc[3];
+            if (my_scored && c < my_ci) {
+                if (cur != cur) cur = -INFINITY;  // a NaN score ranks last
+                int curi = c;
+                bool ins = false;
+#pragma unroll
+                for (int x = 0; x < KCAP; ++x) {
+                    // an empty slot takes any candidate, so all km1 slots fill
+                    const bool take = (x < km1) && (ins || cur > ts[x] || ti[x] == kEmpty);
+                    if (take) {
+                        const float fs = ts[x];
+                        const int fi = ti[x];
+                        ts[x] = cur;
+                        ti[x] = curi;
+                        cur = fs;
+                        curi = fi;
+                        ins = true;
+                    }
+                }
             }
         }
     }
-    // ascending block order (odd-even transposition sort; unused slots hold INT_MAX)
+
+    // selected past blocks of my row, ascending
+    int npast = 0;
+    if (my_valid) {
+        if (my_scored) {
 #pragma unroll
-    for (int j = 0; j < KCAP; ++j)
-        if (j >= km1) ti[j] = 0x7fffffff;
+            for (int x = 0; x < KCAP; ++x)
+                if (x >= km1) ti[x] = kEmpty;
 #pragma unroll
-    for (int pass = 0; pass < KCAP; ++pass) {
+            for (int pass = 0; pass < KCAP; ++pass) {
 #pragma unroll
-        for (int j = pass & 1; j + 1 < KCAP; j += 2) {
-            int lo = min(ti[j], ti[j + 1]), hi = max(ti[j], ti[j + 1]);
-            ti[j] = lo;
-            ti[j + 1] = hi;
+                for (int x = pass & 1; x + 1 < KCAP; x += 2) {
+                    const int lo = min(ti[x], ti[x + 1]), hi = max(ti[x], ti[x + 1]);
+                    ti[x] = lo;
+                    ti[x + 1] = hi;
+                }
+            }
+            npast = km1;
+        } else {
+            npast = (km1 == 0) ? 0 : my_ci;  // every past block (my_ci <= km1)
+#pragma unroll
+            for (int x = 0; x < KCAP; ++x) ti[x] = x;
+        }
+        int32_t *out = idx + ((size_t)my_tok * H + h) * topk;
+        if (my_scored) {
+#pragma unroll
+            for (int x = 0; x < KCAP; ++x)
+                if (x < npast) out[x] = ti[x];
+        } else {
+            for (int x = 0; x < npast; ++x) out[x] = x;  // npast may exceed KCAP here
+        }
+        out[npast] = my_ci;
+        for (int x = npast + 1; x < topk; ++x) out[x] = -1;
+    }
+    if (COUNT) {
+        int rank[KCAP];
+#pragma unroll
+        for (int x = 0; x < KCAP; ++x) {
+            rank[x] = 0;
+            if (x < npast) {
+                const int c = ti[x];
+                rank[x] = (c < kHistBins) ? atomicAdd(&hist[c], 1)
+                                          : atomicAdd(counts + (size_t)(bbase + c) * H + h, 1);
+            }
+        }
+        __syncthreads();
+        const int nbins = min(kHistBins, s_call);
+        for (int x = tid; x < nbins; x += kGateThreads) {
+            const int n = hist[x];
+            hist[x] = n ? atomicAdd(counts + (size_t)(bbase + x) * H + h, n) : 0;
+        }
+        __syncthreads();
+        if (my_valid) {
+            int *tk = ticket + ((size_t)my_tok * H + h) * km1;
+#pragma unroll
+            for (int x = 0; x < KCAP; ++x) {
+                if (x < npast) {
+                    const int c = ti[x];
+                    tk[x] = (c < kHistBins) ? hist[c] + rank[x] : rank[x];
+                }
+            }
         }
     }
-#pragma unroll
-    for (int j = 0; j < KCAP; ++j) {
-        if (j < km1) {
-            out[j] = ti[j];
-            if (COUNT) atomicAdd(counts + (size_t)(bbase + ti[j]) * H + h, 1);
-        }
-    }
-    out[km1] = ci;
 }
 
 template <int D, bool COUNT>
 static void launch_gate_d(dim3 grid, cudaStream_t st, Geometry g, const __nv_bfloat16 *q,
-                          const float *kbar, int32_t *idx, int topk, int *counts) {
+                          const float *kbar, int32_t *idx, int *ticket, int topk, int *counts) {
     const int km1 = topk - 1;
-#define MOBA_GATE_CASE(KC)                                                                     \
-    gate_kernel<D, KC, COUNT><<<grid, kGateThreads, 0, st>>>(g, q, kbar, idx, topk, counts); \
+#define MOBA_GATE_CASE(KC)                                                               \
+    gate_kernel<D, KC, COUNT><<<grid, kGateThreads, 0, st>>>(g, q, kbar, idx, ticket, topk, \
+                                                              counts);                  \
     return;
     if (km1 <= 1) { MOBA_GATE_CASE(1) }
     if (km1 <= 2) { MOBA_GATE_CASE(2) }
@@ -311,14 +404,14 @@ static void launch_gate_d(dim3 grid, cudaStream_t st, Geometry g, const __nv_bfl
 
 cudaError_t launch_gate(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
                         const float *kbar, int32_t *idx, bool count, cudaStream_t st) {
-    dim3 grid((p.total + kGateThreads - 1) / kGateThreads, p.H);
+    dim3 grid((p.max_len + kGateRows - 1) / kGateRows, p.H, p.num_seqs);
     Geometry g = make_geo(p, ws);
     if (p.D == 64) {
-        if (count) launch_gate_d<64, true>(grid, st, g, q, kbar, idx, p.topk, ws.counts);
-        else launch_gate_d<64, false>(grid, st, g, q, kbar, idx, p.topk, nullptr);
+        if (count) launch_gate_d<64, true>(grid, st, g, q, kbar, idx, ws.ticket, p.topk, ws.counts);
+        else launch_gate_d<64, false>(grid, st, g, q, kbar, idx, nullptr, p.topk, nullptr);
     } else {
-        if (count) launch_gate_d<128, true>(grid, st, g, q, kbar, idx, p.topk, ws.counts);
-        else launch_gate_d<128, false>(grid, st, g, q, kbar, idx, p.topk, nullptr);
+        if (count) launch_gate_d<128, true>(grid, st, g, q, kbar, idx, ws.ticket, p.topk, ws.counts);
+        else launch_gate_d<128, false>(grid, st, g, q, kbar, idx, nullptr, p.topk, nullptr);
     }
     note_launches(1);
     return cudaGetLastError();
@@ -326,52 +419,48 @@ cudaError_t launch_gate(const Plan &p, const Workspace &ws, const __nv_bfloat16 
 
 // ---------------------------------------------------------------------------
 // K3: regroup.  (a) one CTA scans the per-(block, head) counts into list and
-// tile offsets; (b) every past selection is scattered into its list.  The
-// order inside a list depends on atomic arrival; each row's result does not
-// depend on which rows share its tile, so outputs stay deterministic.
+// tile offsets; (b) every past selection is written at its list offset plus
+// the ticket the gate gave it (no atomics).  The order inside a list depends
+// on which CTA reserved its range first; each row's result does not depend on
+// which rows share its attention tile, so outputs stay deterministic.
 // ---------------------------------------------------------------------------
 __global__ void regroup_scan_kernel(const int *__restrict__ counts, int N, int tile_m,
-                                    int *__restrict__ list_off, int *__restrict__ tile_off,
-                                    int *__restrict__ cursor) {
+                                    int *__restrict__ list_off, int *__restrict__ tile_off) {
     cta_exclusive_scan(
-        N, [&](int i) { return counts[i]; },
-        [&](int i, int v) {
-            list_off[i] = v;
-            if (i < N) cursor[i] = v;
-        });
+        N, [&](int i) { return counts[i]; }, [&](int i, int v) { list_off[i] = v; });
     cta_exclusive_scan(
         N, [&](int i) { return (counts[i] + tile_m - 1) / tile_m; },
         [&](int i, int v) { tile_off[i] = v; });
 }
 
-__global__ void regroup_scatter_kernel(Geometry g, const int32_t *__restrict__ idx, int topk,
-                                       int *__restrict__ cursor, int *__restrict__ list) {
-    const int h = blockIdx.y;
-    const int t = blockIdx.x * blockDim.x + threadIdx.x;
-    if (t >= g.total) return;
+__global__ void regroup_scatter_kernel(Geometry g, const int32_t *__restrict__ idx,
+                                       const int *__restrict__ ticket, int topk,
+                                       const int *__restrict__ list_off, int *__restrict__ list) {
+    const size_t r = (size_t)blockIdx.x * blockDim.x + threadIdx.x;  // token * H + head
+    if (r >= (size_t)g.total * g.H) return;
+    const int t = (int)(r / g.H), h = (int)(r % g.H);
     const int b = upper_index(g.cu, g.num_seqs, t);
     const int ci = (t - __ldg(g.cu + b)) / g.bs;
     const int bbase = __ldg(g.blk_base + b);
-    const int32_t *row = idx + ((size_t)t * g.H + h) * topk;
-    for (int s = 0; s < topk - 1; ++s) {
+    const int km1 = topk - 1;
+    const int32_t *row = idx + r * topk;
+    const int *tk = ticket + r * km1;
+    for (int s = 0; s < km1; ++s) {
         const int c = row[s];
         if (c < 0 || c >= ci) break;
-        const int pos = atomicAdd(cursor + (size_t)(bbase + c) * g.H + h, 1);
-        list[pos] = (t << kSlotBits) | s;
+        list[__ldg(list_off + (size_t)(bbase + c) * g.H + h) + tk[s]] = (t << kSlotBits) | s;
     }
 }
-
-int past_tile_rows();  // rows per tile of the past-block attention kernel
 
 cudaError_t launch_regroup(const Plan &p, const Workspace &ws, cudaStream_t st) {
     const int N = p.NBcap * p.H;
     regroup_scan_kernel<<<1, 1024, 0, st>>>(ws.counts, N, past_tile_rows(), ws.list_off,
-                                            ws.tile_off, ws.cursor);
+                                            ws.tile_off);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    dim3 grid((p.total + 255) / 256, p.H);
-    regroup_scatter_kernel<<<grid, 256, 0, st>>>(make_geo(p, ws), ws.idx, p.topk, ws.cursor,
-                                                 ws.list);
+    const size_t rows = (size_t)p.total * p.H;
+    regroup_scatter_kernel<<<(unsigned)((rows + 255) / 256), 256, 0, st>>>(
+        make_geo(p, ws), ws.idx, ws.ticket, p.topk, ws.list_off, ws.list);
     note_launches(2);
     return cudaGetLastError();
 }

@@ -50,7 +50,7 @@ struct Workspace {
     int *counts;      // [NBcap * H]   queries per (block, head) past list
     int *list_off;    // [NBcap * H + 1]
     int *tile_off;    // [NBcap * H + 1]
-    int *cursor;      // [NBcap * H]
+    int *ticket;      // [total * H * km1]  position of a selection inside its list
     int *list;        // [total * H * km1]  entries token << 5 | slot
     float *part_o;    // [total * H * km1][D]  normalised partial outputs
     float *part_lse;  // [total * H * km1]     partial log2-sum-exp
@@ -84,5 +84,24 @@ cudaError_t launch_attn_current(const Plan &p, const Workspace &ws, const __nv_b
 
 // count of kernels this library has launched (for the benchmark's launch tally)
 void note_launches(int n);
+
+// rows per tile of the past-block attention kernel in use (regroup tiling)
+int past_tile_rows();
+
+// the two attention implementations: tcgen05 / TMEM / TMA (default) and the
+// warp-level mma.sync baseline
+cudaError_t launch_attn_past_tc(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
+                                const __nv_bfloat16 *k, const __nv_bfloat16 *v, cudaStream_t st);
+cudaError_t launch_attn_current_tc(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
+                                   const __nv_bfloat16 *k, const __nv_bfloat16 *v,
+                                   __nv_bfloat16 *out, float *lse, cudaStream_t st);
+cudaError_t launch_attn_past_mma(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
+                                 const __nv_bfloat16 *k, const __nv_bfloat16 *v, cudaStream_t st);
+cudaError_t launch_attn_current_mma(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
+                                    const __nv_bfloat16 *k, const __nv_bfloat16 *v,
+                                    __nv_bfloat16 *out, float *lse, cudaStream_t st);
+int tc_tile_rows();
+int mma_tile_rows();
+void tc_debug_set(int flags, long long wait_limit);
 
 }  // namespace moba

@@ -43,6 +43,8 @@ _SIGNATURES = {
     "moba_launch_count": (ctypes.c_ulonglong, []),
     "moba_profile_begin": (_I, [_I]),
     "moba_profile_end": (_I, [_P, _I]),
+    "moba_set_attention_kernel": (_I, [_I]),
+    "moba_debug_set": (_I, [_I, ctypes.c_longlong]),
 }
 
 PHASES = ("tables", "kpool", "gate", "regroup", "attn_past", "attn_current")
@@ -226,3 +228,17 @@ def profile_end() -> tuple:
     if n < 0:
         raise RuntimeError(f"moba_profile_end failed: {status_string(-n)}")
     return n, dict(zip(PHASES, (float(x) for x in buf)))
+
+
+ATTN_TCGEN05 = 0
+ATTN_MMA_SYNC = 1
+
+
+def set_attention_kernel(kind: int):
+    """0: tcgen05 / TMEM / TMA kernels (default); 1: warp-level mma.sync baseline."""
+    _check(lib().moba_set_attention_kernel(int(kind)), "moba_set_attention_kernel")
+
+
+def debug_set(flags: int = 0, wait_limit_cycles: int = 0):
+    """Fault-injection hooks of the bounded waits (flags bit 0: skip a K/V load)."""
+    _check(lib().moba_debug_set(int(flags), int(wait_limit_cycles)), "moba_debug_set")
