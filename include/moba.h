@@ -145,6 +145,33 @@ int moba_attn_fwd_varlen_ws(const void *q, const void *k, const void *v, void *o
                             int max_seqlen, int H, int D, int block_size, int topk,
                             void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * moba_attn_fwd for callers that cannot allocate device memory: for example
+ * code running under a memory manager that owns the whole device (where an
+ * extra cudaMalloc can fail or fragment its pool), or a serving loop that must
+ * not allocate on its latency path.  The pages describe no such entry point;
+ * it is an addition of this library.
+ *   Arguments, layouts and results are those of moba_attn_fwd; the caller
+ *   still passes q, k, v, out and lse.
+ *   Scratch: one file-scope device array of moba_attn_fwd_noalloc_capacity()
+ *   bytes (64 MiB), held by every device that loads this library until the
+ *   process exits.  Sizes whose scratch (moba_attn_fwd_workspace_size) does not
+ *   fit return MOBA_ERR_WORKSPACE before anything is launched.
+ *   No cudaMalloc, cudaFree or allocating library routine is called.  The
+ *   first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any stream
+ *   capture.
+ *   Every call shares the one array and it keeps the previous call's contents
+ *   (what must start at zero is cleared by the call): calls whose work
+ *   overlaps on the GPU, e.g. on two streams, race and must be serialised by
+ *   the caller.
+ */
+int moba_attn_fwd_noalloc(const void *q, const void *k, const void *v, void *out, float *lse,
+                          int B, int H, int S, int D, int block_size, int topk, void *stream);
+
+/* Bytes of the static scratch array used by moba_attn_fwd_noalloc. */
+size_t moba_attn_fwd_noalloc_capacity(void);
+
 /* Synchronises `stream`, returns the device status word (MOBA_OK or
  * MOBA_ERR_TIMEOUT) of the current device and clears it; MOBA_ERR_CUDA if
  * the synchronisation itself failed. */

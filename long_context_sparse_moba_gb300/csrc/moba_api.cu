@@ -406,3 +406,43 @@ MOBA_EXPORT int moba_debug_set(int flags, long long wait_limit_cycles) {
     tc_debug_set(flags, wait_limit_cycles);
     return MOBA_OK;
 }
+
+// ---------------------------------------------------------------------------
+// Forward pass that allocates nothing.  Its scratch lives in one file-scope
+// device array that every device loading this library keeps until the process
+// exits.  Host code only sees a stand-in for the array's name, so the device
+// address is looked up once per device with cudaGetSymbolAddress.
+// ---------------------------------------------------------------------------
+static constexpr size_t kStaticScratchBytes = 64ull << 20;  // 64 MiB
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+static void *static_scratch() {
+    static void *addr[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) return nullptr;
+        addr[dev] = p;
+    }
+    return addr[dev];
+}
+
+MOBA_EXPORT size_t moba_attn_fwd_noalloc_capacity(void) { return kStaticScratchBytes; }
+
+MOBA_EXPORT int moba_attn_fwd_noalloc(const void *q, const void *k, const void *v, void *out,
+                                      float *lse, int B, int H, int S, int D, int block_size,
+                                      int topk, void *stream) {
+    int rc = check_tensors(q, k, v, out, lse);
+    if (rc) return rc;
+    Plan p;
+    rc = make_plan(B, (long long)B * S, S, H, D, block_size, topk, true, &p);
+    if (rc) return rc;
+    if (workspace_bytes(p, nullptr, nullptr) > kStaticScratchBytes) return MOBA_ERR_WORKSPACE;
+    void *scratch = static_scratch();
+    if (!scratch) return MOBA_ERR_CUDA;
+    // run_forward clears the per-(block, head) counters itself (a memset, not
+    // an allocation); every other scratch area is written before it is read
+    return run_forward(p, nullptr, q, k, v, out, lse, scratch, kStaticScratchBytes,
+                       static_cast<cudaStream_t>(stream));
+}

@@ -44,6 +44,8 @@ _SIGNATURES = {
     "moba_profile_begin": (_I, [_I]),
     "moba_profile_end": (_I, [_P, _I]),
     "moba_set_attention_kernel": (_I, [_I]),
+    "moba_attn_fwd_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "moba_attn_fwd_noalloc_capacity": (_SZ, []),
     "moba_debug_set": (_I, [_I, ctypes.c_longlong]),
 }
 
@@ -242,3 +244,21 @@ def set_attention_kernel(kind: int):
 def debug_set(flags: int = 0, wait_limit_cycles: int = 0):
     """Fault-injection hooks of the bounded waits (flags bit 0: skip a K/V load)."""
     _check(lib().moba_debug_set(int(flags), int(wait_limit_cycles)), "moba_debug_set")
+
+
+def attn_fwd_noalloc(q, k, v, block_size: int, topk: int, out, lse, stream=None):
+    """moba_attn_fwd without any device allocation: the scratch is the
+    library's static device array (see include/moba.h); `out` and `lse` must be
+    provided by the caller."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        _need(t, torch.bfloat16, n)
+    _need(lse, torch.float32, "lse")
+    B, S, H, D = q.shape
+    _check(lib().moba_attn_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, S,
+                                       D, block_size, topk, _stream(stream)),
+           "moba_attn_fwd_noalloc")
+    return out, lse
+
+
+def noalloc_capacity() -> int:
+    return int(lib().moba_attn_fwd_noalloc_capacity())

@@ -162,3 +162,37 @@ def test_workspace_too_small_on_device():
     ws = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
     with pytest.raises(RuntimeError, match="WORKSPACE"):
         ops.attn_fwd(inp.q, inp.k, inp.v, 64, 3, workspace=ws)
+
+
+# ---------------------------------------------------------------------------
+# bounded waits, and the warp-level mma.sync baseline kernels
+# ---------------------------------------------------------------------------
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """A producer told to skip its first K/V load leaves the MMA lane waiting on
+    an mbarrier nothing will complete: the wait gives up, MOBA_ERR_TIMEOUT is
+    recorded, and the next call on the same context is correct."""
+    w = workloads.custom((2048,), 1, 128, 256, topk=3, seed=6)
+    inp = workloads.make_inputs(w, device="cuda")
+    try:
+        ops.debug_set(1, 20_000_000)  # ~10 ms per wait
+        gpu_forward(inp, w, 3)
+        assert ops.get_status() == ops.MOBA_ERR_TIMEOUT
+    finally:
+        ops.debug_set(0, 0)
+    out, lse = gpu_forward(inp, w, 3)
+    assert ops.get_status() == ops.MOBA_OK
+    compare(w, inp, 3, out, lse)
+
+
+@pytest.mark.parametrize("seqlens,H,D,bs,topk", [
+    ((2048,), 1, 64, 256, 3), ((700,), 3, 64, 64, 4), ((4096, 4096), 2, 128, 256, 3),
+    ((512,), 2, 128, 128, 4), ((200, 1, 64, 129), 2, 128, 64, 3)])
+def test_mma_sync_baseline_path(seqlens, H, D, bs, topk):
+    w = workloads.custom(seqlens, H, D, bs, topk=topk, seed=17)
+    try:
+        ops.set_attention_kernel(ops.ATTN_MMA_SYNC)
+        *_, st = run_case(w, topk)
+    finally:
+        ops.set_attention_kernel(ops.ATTN_TCGEN05)
+    print("mma.sync", seqlens, st)
