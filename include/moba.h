@@ -180,6 +180,10 @@ int moba_get_status(void *stream);
 /* Static, human-readable name of a status code. */
 const char *moba_status_string(int code);
 
+/* Text of the CUDA error behind the calling thread's last MOBA_ERR_CUDA
+ * ("no error" if there was none). */
+const char *moba_last_cuda_error(void);
+
 /* Number of kernels this library has launched since it was loaded (a
  * process-wide tally; host only). */
 unsigned long long moba_launch_count(void);

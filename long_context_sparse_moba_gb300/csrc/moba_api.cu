@@ -6,7 +6,7 @@
 #include <cstring>
 #include <vector>
 
-#include "../../include/moba.h"
+#include "moba.h"
 #include "moba_internal.cuh"
 
 #define MOBA_EXPORT extern "C" __attribute__((visibility("default")))
@@ -119,12 +119,17 @@ static int make_plan(int num_seqs, long long total, int max_len, int H, int D, i
     return MOBA_OK;
 }
 
-static int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOBA_OK : MOBA_ERR_CUDA; }
+static int cuda_status(cudaError_t e);
+
+static thread_local cudaError_t g_last_cuda_error = cudaSuccess;
 
 #define MOBA_TRY(expr)                                   \
     do {                                                 \
         cudaError_t _e = (expr);                         \
-        if (_e != cudaSuccess) return MOBA_ERR_CUDA;     \
+        if (_e != cudaSuccess) {                         \
+            g_last_cuda_error = _e;                      \
+            return MOBA_ERR_CUDA;                        \
+        }                                                \
     } while (0)
 
 static int run_forward(const Plan &p, const int *cu_dev, const void *q, const void *k,
@@ -158,6 +163,12 @@ static int run_forward(const Plan &p, const int *cu_dev, const void *q, const vo
     MOBA_TRY(launch_attn_current(p, ws, qb, kb, vb, static_cast<__nv_bfloat16 *>(out), lse, st));
     prof_mark(call, 6, st);
     return MOBA_OK;
+}
+
+static int cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return MOBA_OK;
+    g_last_cuda_error = e;
+    return MOBA_ERR_CUDA;
 }
 
 static bool misaligned(const void *p) { return reinterpret_cast<uintptr_t>(p) & 15; }
@@ -445,4 +456,8 @@ MOBA_EXPORT int moba_attn_fwd_noalloc(const void *q, const void *k, const void *
     // an allocation); every other scratch area is written before it is read
     return run_forward(p, nullptr, q, k, v, out, lse, scratch, kStaticScratchBytes,
                        static_cast<cudaStream_t>(stream));
+}
+
+MOBA_EXPORT const char *moba_last_cuda_error(void) {
+    return cudaGetErrorString(g_last_cuda_error);
 }

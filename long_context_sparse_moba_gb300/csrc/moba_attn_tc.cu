@@ -6,31 +6,39 @@
 // the current block) and "MOBA mixture of block attention for server-side long
 // context" (hncyxsy.com/news/197418) section 3 (force_current_block).
 //
-// One CTA = one work tile of 128 query rows (M = 128) against a run of 64-key
-// K/V tiles, 192 threads in four roles:
-//   warp 0      TMA producer: the Q tile (contiguous rows) and a 2-stage ring
-//               of K/V tiles, each as two 64-dim boxes with the 128-byte swizzle
-//               that the tensor core's K-major / MN-major layouts expect;
-//   warp 1      allocates 256 TMEM columns; lane 0 issues the MMAs:
-//                 S_j = Q K_j^T   (M128 N64 K=D, into one of two S buffers)
-//                 O  += P_j V_j   (M128 N=D K64, P from shared memory)
-//               and signals completion through tcgen05.commit on mbarriers;
-//   warps 2..5  softmax: thread r owns query row r (its TMEM lane), reads its
-//               64 scores with tcgen05.ld, keeps the running max / sum, writes
-//               P_j (bf16) to shared memory in the swizzled K-major layout and,
-//               when the running max grows by more than 2^8, rescales its O row
-//               in TMEM.  They also run the epilogue.
-// Two CTAs share an SM (~113 KB shared memory and 256 TMEM columns each), so
-// one CTA's softmax overlaps the other's MMAs.
+// One CTA = one job of up to 256 query rows held as two 128-row tiles (g = 0,
+// 1) that share every 128-key K/V tile, 352 threads in five roles:
+//   warp 0      TMA producers: lane 0 loads the Q tiles (contiguous rows) and a
+//               2-stage ring of K tiles, lane 1 a 2-stage ring of V tiles (one
+//               TMA stream per thread tops out well below what the tensor core
+//               consumes);
+//   warp 1      allocates all 512 TMEM columns; lane 0 issues the MMAs
+//                 S_g = Q_g K_j^T   (M128 N128 K=D, A and B from shared memory)
+//                 O_g += P_g V_j    (M128 N=D K128, A = P_g from TMEM)
+//               in the order PV_0(j-1), S_0(j), PV_1(j-1), S_1(j): the
+//               tensor core runs one tile's MMAs while the other tile's
+//               softmax works, and because MMAs from one thread execute in
+//               order, S_g(j) may overwrite the TMEM columns that P_g(j-1)
+//               occupies;
+//   warps 2..9  softmax of tile 0 (warps 2..5) and tile 1 (6..9): thread r owns
+//               row r (its TMEM lane); it reads its 128 scores, updates the
+//               running max / sum, rescales its O row in TMEM when the max grew
+//               by more than 2^8, and writes P (bf16 pairs) back over the first
+//               64 columns of its S.  Epilogue per tile.
+// TMEM: S_g at columns 256g .. 256g+127 (P_g in the first 64), O_g at
+// 256g+128 .. 256g+128+D.  One CTA per SM (192 KB of shared memory).
+// Per 128 keys the shared-memory traffic is Q + K for each S MMA and V for
+// each PV MMA, which balances the tensor core and the exponential unit.
 //
 // Modes:
-//   kPast     gathered rows: the rows of one regroup list tile (rows that
+//   kPast     gathered rows: up to 256 rows of one regroup list (rows that
 //             selected the same past block of the same head); the softmax warps
 //             gather Q with cp.async; output = normalised fp32 partial O and
 //             its log2-sum-exp per (row, slot);
-//   kCurrent  rows [r0, r0 + 128) of a sequence: causal attention over the own
+//   kCurrent  rows [r0, r0 + 256) of a sequence: causal attention over the own
 //             block (every key up to the row on the dense path), then the
 //             log-sum-exp merge with the row's past partials -> bf16 out, lse.
+//             Each tile only visits the K/V tiles its rows can see.
 //
 // Every mbarrier wait is bounded (clock64 budget); a wait that runs out sets
 // MOBA_ERR_TIMEOUT in the device status word and an abort flag that makes the
@@ -38,17 +46,22 @@
 // copies in flight and the MMA lane for its MMAs before TMEM is freed.
 #include <cuda.h>
 
-#include "../../include/moba.h"
+#include "moba.h"
 #include "moba_internal.cuh"
 
 namespace moba {
 namespace tc {
 
-constexpr int kM = 128;           // query rows per tile
-constexpr int kN = 64;            // keys per K/V tile
-constexpr int kStages = 2;        // K/V ring depth
-constexpr int kThreads = 192;
-constexpr int kTmemCols = 256;    // S0 [0,64) S1 [64,128) O [128,128+D)
+constexpr int kM = 128;           // rows per Q tile (the MMA's M)
+constexpr int kG = 2;             // Q tiles (softmax groups) per CTA
+constexpr int kRows = kM * kG;    // rows per job
+constexpr int kN = 128;           // keys per K/V tile
+constexpr int kStages = 2;        // depth of the K ring and of the V ring
+constexpr int kThreads = 64 + 128 * kG;  // producers, MMA, 2 x 4 softmax warps
+// Warps are budgeted four at a time, so 10 warps get 65536 / 384 registers
+// each: the kernel is built for (and the host checks) 168.
+constexpr int kRegLaunch = 168;
+constexpr int kTmemCols = 512;
 constexpr uint32_t kBox = 64;     // dims per TMA box (128 bytes of bf16)
 
 enum Mode { kPast = 0, kCurrent = 1 };
@@ -137,6 +150,15 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// A operand from tensor memory (M lanes x K/2 columns of packed bf16 pairs)
+__device__ __forceinline__ void tc_mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
@@ -159,6 +181,24 @@ __device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32])
         "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
         "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
         "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
         : "memory");
 }
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
@@ -192,21 +232,24 @@ struct Smem {
     static constexpr int NB = D / kBox;                       // 64-dim boxes per row
     static constexpr uint32_t kQBox = kM * 128;               // 16 KB
     static constexpr uint32_t kKVBox = kN * 128;              // 8 KB
-    static constexpr uint32_t kQ = 0;
-    static constexpr uint32_t kK = kQ + NB * kQBox;           // stages of K
+    static constexpr uint32_t kQ = 0;                         // [g][box]
+    static constexpr uint32_t kK = kQ + kG * NB * kQBox;      // [stage][box]
     static constexpr uint32_t kV = kK + kStages * NB * kKVBox;
-    static constexpr uint32_t kP = kV + kStages * NB * kKVBox;
-    static constexpr uint32_t kTiles = kP + kM * 128;         // end of the tiles
-    // mbarriers q_full, kv_full[2], kv_empty[2], s_full[2], p_full, pv_done,
-    // drain; then the TMEM address slot and the abort flag
-    static constexpr int kNumBars = 10;
+    static constexpr uint32_t kTiles = kV + kStages * NB * kKVBox;  // end of the tiles
+    // mbarriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2],
+    // s_full[g], p_full[g], pv_done[g], drain; then the TMEM address slot and
+    // the abort flag
+    static constexpr int kBarQ = 0, kBarKF = 1, kBarKE = kBarKF + kStages,
+                         kBarVF = kBarKE + kStages, kBarVE = kBarVF + kStages,
+                         kBarS = kBarVE + kStages, kBarP = kBarS + kG, kBarPV = kBarP + kG,
+                         kBarDrain = kBarPV + kG, kNumBars = kBarDrain + 1;
     static constexpr uint32_t kMisc = kNumBars * 8 + 8;
     // The tiles need a 1024-byte aligned base; the dynamic window is at least
-    // 16-byte aligned, so up to 1008 bytes of slack.  The misc words go into
-    // the slack when it is large enough, else right after the tiles.  For
-    // D = 128 this keeps two CTAs per SM (2 x (115696 + 1024) <= 233472).
-    static constexpr uint32_t kRequest =
-        (kTiles + 1008 > 80 * 1024) ? kTiles + 1008 : 80 * 1024;  // never a third CTA
+    // 16-byte aligned, so up to 1008 bytes of slack; the misc words go into
+    // the slack when it is large enough, else right after the tiles.  The
+    // request keeps a single CTA per SM (it owns all of TMEM).
+    static constexpr uint32_t kNeed = kTiles + 1008 + kMisc;
+    static constexpr uint32_t kRequest = kNeed > 120 * 1024 ? kNeed : 120 * 1024;
 };
 
 struct Ctl {
@@ -237,7 +280,7 @@ __device__ __noinline__ void drain_bar(uint32_t bar, uint32_t parity, long long 
 }
 
 template <int D, int MODE>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                    const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v, Args a) {
@@ -250,16 +293,19 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.g.H;
 
-    // ---------------- work tile ----------------
-    int h, seq0, L_len, r0 = 0, nrows = kM, kv_tok0, kv_end, nkv;
+    // ---------------- the job ----------------
+    // rows: tile g holds job rows [g*128, g*128 + nrows_g); K/V tiles
+    // [0, nkv) start at token kv_tok0; tile g visits K/V tiles [tb[g], te[g]).
+    int h, seq0, L_len, r0 = 0, nrows = kRows, kv_tok0, kv_end, nkv;
     int lbeg = 0, kv_lo = 0;
+    int tb[kG], te[kG];
     if (MODE == kPast) {
-        const int tile = blockIdx.x;
-        if (tile >= __ldg(a.tile_off + a.n_lists)) return;
+        const int job = blockIdx.x;
+        if (job >= __ldg(a.tile_off + a.n_lists)) return;
         int lo = 0, hi = a.n_lists - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (__ldg(a.tile_off + mid) <= tile) lo = mid; else hi = mid - 1;
+            if (__ldg(a.tile_off + mid) <= job) lo = mid; else hi = mid - 1;
         }
         const int Lid = lo;
         const int gblk = Lid / H;
@@ -272,45 +318,62 @@ __global__ void __launch_bounds__(kThreads, 2)
         kv_end = min(kv_tok0 + a.g.bs, seq0 + L_len);
         lbeg = __ldg(a.list_off + Lid);
         const int lcnt = __ldg(a.list_off + Lid + 1) - lbeg;
-        r0 = (tile - __ldg(a.tile_off + Lid)) * kM;
-        nrows = min(kM, lcnt - r0);
+        r0 = (job - __ldg(a.tile_off + Lid)) * kRows;
+        nrows = min(kRows, lcnt - r0);
         lbeg += r0;
+        nkv = (kv_end - kv_tok0 + kN - 1) / kN;
+#pragma unroll
+        for (int g = 0; g < kG; ++g) {
+            tb[g] = 0;
+            te[g] = (nrows > g * kM) ? nkv : 0;
+        }
     } else {
         h = blockIdx.y;
         const int b = blockIdx.z;
         seq0 = __ldg(a.g.cu + b);
         L_len = __ldg(a.g.cu + b + 1) - seq0;
-        // heavy (late) tiles first
-        r0 = (gridDim.x - 1 - blockIdx.x) * kM;
+        r0 = (gridDim.x - 1 - blockIdx.x) * kRows;  // heavy (late) jobs first
         if (r0 >= L_len) return;
-        nrows = min(kM, L_len - r0);
-        kv_lo = a.dense ? 0 : (r0 / a.g.bs) * a.g.bs;
+        nrows = min(kRows, L_len - r0);
+        const int bs = a.g.bs;
+        kv_lo = a.dense ? 0 : (r0 / bs) * bs;
         kv_tok0 = seq0 + kv_lo;
-        kv_end = seq0 + min(r0 + kM, L_len);
+        kv_end = seq0 + r0 + nrows;
+        nkv = (kv_end - kv_tok0 + kN - 1) / kN;
+#pragma unroll
+        for (int g = 0; g < kG; ++g) {
+            const int first = r0 + g * kM, last = min(r0 + (g + 1) * kM, r0 + nrows) - 1;
+            if (last < first) {
+                tb[g] = te[g] = 0;
+                continue;
+            }
+            const int lo_key = a.dense ? 0 : (first / bs) * bs;
+            tb[g] = (lo_key - kv_lo) / kN;
+            te[g] = (last - kv_lo) / kN + 1;
+        }
     }
-    nkv = (kv_end - kv_tok0 + kN - 1) / kN;
 
     // ---------------- set-up ----------------
-    const uint32_t sQ = base + L::kQ, sK = base + L::kK, sV = base + L::kV, sP = base + L::kP;
-    const uint32_t bar0 = misc;
-    const uint32_t b_qfull = bar0, b_kvfull = bar0 + 8, b_kvempty = bar0 + 24,
-                   b_sfull = bar0 + 40, b_pfull = bar0 + 56, b_pvdone = bar0 + 64,
-                   b_drain = bar0 + 72;
+    const uint32_t sQ = base + L::kQ, sK = base + L::kK, sV = base + L::kV;
+    auto bar = [&](int i) -> uint32_t { return misc + 8u * (uint32_t)i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gmisc + L::kNumBars * 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gmisc + L::kNumBars * 8 + 4);
     Ctl ctl{abort_flag, a.status, a.wait_limit};
 
     if (tid == 0) {
-        mbar_init(b_qfull, MODE == kPast ? 4 : 1);
+        mbar_init(bar(L::kBarQ), MODE == kPast ? 4 * kG : 1);
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(b_kvfull + 8 * s, 1);
-            mbar_init(b_kvempty + 8 * s, 1);
+            mbar_init(bar(L::kBarKF + s), 1);
+            mbar_init(bar(L::kBarKE + s), 1);
+            mbar_init(bar(L::kBarVF + s), 1);
+            mbar_init(bar(L::kBarVE + s), 1);
         }
-        mbar_init(b_sfull, 1);
-        mbar_init(b_sfull + 8, 1);
-        mbar_init(b_pfull, 4);
-        mbar_init(b_pvdone, 1);
-        mbar_init(b_drain, 1);
+        for (int g = 0; g < kG; ++g) {
+            mbar_init(bar(L::kBarS + g), 1);
+            mbar_init(bar(L::kBarP + g), 4);
+            mbar_init(bar(L::kBarPV + g), 1);
+        }
+        mbar_init(bar(L::kBarDrain), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -327,38 +390,38 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ================= TMA producer =================
-        if (lane == 0) {
-            constexpr uint32_t kKVBytes = 2u * L::NB * L::kKVBox;
-            if (MODE == kCurrent) {
-                mbar_expect_tx(b_qfull, L::NB * L::kQBox);
-                for (int x = 0; x < L::NB; ++x)
-                    tma_load_3d(sQ + x * L::kQBox, &tmap_q, b_qfull, x * kBox, h, seq0 + r0);
+        // ================= TMA producers (lane 0: Q and K, lane 1: V) =================
+        if (lane < 2) {
+            const bool is_k = lane == 0;
+            constexpr uint32_t kTileBytes = L::NB * L::kKVBox;
+            if (MODE == kCurrent && is_k) {
+                mbar_expect_tx(bar(L::kBarQ), kG * L::NB * L::kQBox);
+                for (int g = 0; g < kG; ++g)
+                    for (int x = 0; x < L::NB; ++x)
+                        tma_load_3d(sQ + (g * L::NB + x) * L::kQBox, &tmap_q, bar(L::kBarQ),
+                                    x * kBox, h, seq0 + r0 + g * kM);
             }
-            int pending[kStages];  // tile whose load sits in each stage, -1 if none
-            for (int s = 0; s < kStages; ++s) pending[s] = -1;
+            const int bfull = is_k ? L::kBarKF : L::kBarVF, bempty = is_k ? L::kBarKE : L::kBarVE;
+            const uint32_t ring = is_k ? sK : sV;
+            const CUtensorMap *map = is_k ? &tmap_k : &tmap_v;
+            int pend[kStages];  // tile whose copy is in flight per slot
+            for (int s = 0; s < kStages; ++s) pend[s] = -1;
             for (int j = 0; j < nkv; ++j) {
-                const int s = j % kStages;
-                if (j >= kStages &&
-                    !wait_bar(b_kvempty + 8 * s, ((j / kStages) - 1) & 1, ctl))
-                    break;
-                pending[s] = -1;
-                if ((a.debug_flags & 1) && j == 0) continue;  // fault-injection knob
-                const uint32_t kb = sK + s * L::NB * L::kKVBox, vb = sV + s * L::NB * L::kKVBox;
-                mbar_expect_tx(b_kvfull + 8 * s, kKVBytes);
-                for (int x = 0; x < L::NB; ++x) {
-                    tma_load_3d(kb + x * L::kKVBox, &tmap_k, b_kvfull + 8 * s, x * kBox, h,
-                                kv_tok0 + j * kN);
-                    tma_load_3d(vb + x * L::kKVBox, &tmap_v, b_kvfull + 8 * s, x * kBox, h,
-                                kv_tok0 + j * kN);
-                }
-                pending[s] = j;
+                const int s = j % kStages, use = j / kStages;
+                if (j >= kStages && !wait_bar(bar(bempty + s), (use - 1) & 1, ctl)) break;
+                pend[s] = -1;
+                if (is_k && (a.debug_flags & 1) && j == 0) continue;  // fault-injection knob
+                mbar_expect_tx(bar(bfull + s), kTileBytes);
+                for (int x = 0; x < L::NB; ++x)
+                    tma_load_3d(ring + (s * L::NB + x) * L::kKVBox, map, bar(bfull + s), x * kBox,
+                                h, kv_tok0 + j * kN);
+                pend[s] = j;
             }
             if (*abort_flag) {
                 // let the copies still in flight land before the CTA exits
                 for (int s = 0; s < kStages; ++s)
-                    if (pending[s] >= 0)
-                        drain_bar(b_kvfull + 8 * s, (pending[s] / kStages) & 1, a.wait_limit);
+                    if (pend[s] >= 0)
+                        drain_bar(bar(bfull + s), (pend[s] / kStages) & 1, a.wait_limit);
             }
         }
     } else if (warp == 1) {
@@ -366,61 +429,79 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16(kM, kN, 0);
             constexpr uint32_t idesc_o = idesc_bf16(kM, D, 1);
-            const uint32_t tO = tmem + 128;
-            bool ok = wait_bar(b_qfull, 0, ctl);
-            int j = 0;
-            for (; ok && j <= nkv; ++j) {
+            bool ok = wait_bar(bar(L::kBarQ), 0, ctl);
+            for (int j = 0; ok && j <= nkv; ++j) {
+                const int s = j % kStages;
                 if (j < nkv) {
-                    const int s = j % kStages;
-                    if (!wait_bar(b_kvfull + 8 * s, (j / kStages) & 1, ctl)) break;
+                    if (!wait_bar(bar(L::kBarKF + s), (j / kStages) & 1, ctl)) break;
                     tc_fence_after();
-                    const uint32_t kb = sK + s * L::NB * L::kKVBox;
-                    const uint32_t tS = tmem + (j & 1) * kN;
-#pragma unroll
-                    for (int k = 0; k < D / 16; ++k) {
-                        const uint32_t off = (uint32_t)(k % 4) * 32;  // 16 dims = 32 B
-                        const uint64_t ad = sdesc(sQ + (k / 4) * L::kQBox + off, 16, 1024);
-                        const uint64_t bd = sdesc(kb + (k / 4) * L::kKVBox + off, 16, 1024);
-                        tc_mma(tS, ad, bd, idesc_s, k > 0);
-                    }
-                    tc_commit(b_sfull + 8 * (j & 1));
                 }
-                if (j >= 1) {
-                    const int jp = j - 1;
-                    if (!wait_bar(b_pfull, jp & 1, ctl)) break;
-                    tc_fence_after();
-                    const uint32_t vb = sV + (jp % kStages) * L::NB * L::kKVBox;
+                const int jp = j - 1, sp = (j + kStages - 1) % kStages;
+                if (jp >= 0 && !wait_bar(bar(L::kBarVF + sp), (jp / kStages) & 1, ctl)) break;
+                const uint32_t kb = sK + s * L::NB * L::kKVBox;
+                const uint32_t vb = sV + sp * L::NB * L::kKVBox;
+                bool stop = false;
 #pragma unroll
-                    for (int k = 0; k < kN / 16; ++k) {
-                        const uint64_t ad = sdesc(sP + k * 32, 16, 1024);
-                        const uint64_t bd = sdesc(vb + k * 2048, L::kKVBox, 1024);
-                        tc_mma(tO, ad, bd, idesc_o, (jp > 0 || k > 0) ? 1u : 0u);
+                for (int g = 0; g < kG; ++g) {
+                    const uint32_t tS = tmem + g * 256, tO = tS + 128;
+                    if (jp >= tb[g] && jp < te[g]) {
+                        // O_g += P_g(jp) V(jp): P_g sits in the first 64 columns of S_g
+                        const int jl = jp - tb[g];
+                        if (!wait_bar(bar(L::kBarP + g), jl & 1, ctl)) {
+                            stop = true;
+                            break;
+                        }
+                        tc_fence_after();
+#pragma unroll
+                        for (int k = 0; k < kN / 16; ++k) {
+                            const uint64_t bd = sdesc(vb + k * 2048, L::kKVBox, 1024);
+                            tc_mma_ta(tO, tS + k * 8, bd, idesc_o, (jl > 0 || k > 0) ? 1u : 0u);
+                        }
+                        if (jp == te[g] - 1) tc_commit(bar(L::kBarPV + g));
                     }
-                    tc_commit(b_pvdone);
-                    tc_commit(b_kvempty + 8 * (jp % kStages));
+                    if (j < nkv && j >= tb[g] && j < te[g]) {
+                        // S_g(j) = Q_g K(j)^T (runs after the PV above: same thread, in order)
+                        const uint32_t qb = sQ + g * L::NB * L::kQBox;
+#pragma unroll
+                        for (int k = 0; k < D / 16; ++k) {
+                            const uint32_t off = (uint32_t)(k % 4) * 32;  // 16 dims = 32 B
+                            const uint64_t ad = sdesc(qb + (k / 4) * L::kQBox + off, 16, 1024);
+                            const uint64_t bd = sdesc(kb + (k / 4) * L::kKVBox + off, 16, 1024);
+                            tc_mma(tS, ad, bd, idesc_s, k > 0);
+                        }
+                        tc_commit(bar(L::kBarS + g));
+                    }
                 }
+                if (stop) break;
+                if (j < nkv) tc_commit(bar(L::kBarKE + s));
+                if (jp >= 0) tc_commit(bar(L::kBarVE + sp));
             }
             // every MMA this thread issued has finished before TMEM is freed
-            tc_commit(b_drain);
-            drain_bar(b_drain, 0, a.wait_limit);
+            tc_commit(bar(L::kBarDrain));
+            drain_bar(bar(L::kBarDrain), 0, a.wait_limit);
         }
     } else {
-        // ================= softmax + epilogue (warps 2..5) =================
-        const int quarter = warp & 3;
+        // ================= softmax + epilogue (warps 2..9) =================
+        const int g = (warp - 2) >> 2;  // Q tile of this warp
+        const int quarter = warp & 3;   // TMEM lane quarter this warp may access
         const int row = quarter * 32 + lane;
+        const int jrow = g * kM + row;  // row inside the job
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tSg = tmem + lane_off + g * 256;
+        const uint32_t tOg = tSg + 128;
+        const uint32_t sQg = sQ + g * L::NB * L::kQBox;
         int row_tok = -1, slot = 0;
-        bool row_valid = row < nrows;
+        const bool row_valid = jrow < nrows;
         if (MODE == kPast) {
             // gather this row of Q into the swizzled K-major tile
             int e = 0;
-            if (row_valid) e = __ldg(a.list + lbeg + row);
+            if (row_valid) e = __ldg(a.list + lbeg + jrow);
             row_tok = e >> kSlotBits;
             slot = e & ((1 << kSlotBits) - 1);
             const __nv_bfloat16 *src = a.q + ((size_t)row_tok * H + h) * D;
 #pragma unroll
             for (int ch = 0; ch < D / 8; ++ch) {
-                const uint32_t dst = sQ + (ch / 8) * L::kQBox + row * 128 +
+                const uint32_t dst = sQg + (ch / 8) * L::kQBox + row * 128 +
                                      ((uint32_t)((ch % 8) ^ (row & 7)) << 4);
                 cp_async16(dst, row_valid ? (const void *)(src + ch * 8) : (const void *)a.q,
                            row_valid);
@@ -428,103 +509,115 @@ __global__ void __launch_bounds__(kThreads, 2)
             cp_async_wait_all();
             fence_proxy_async();
             __syncwarp();
-            if (lane == 0) mbar_arrive(b_qfull);
+            if (lane == 0) mbar_arrive(bar(L::kBarQ));
         } else {
-            row_tok = seq0 + r0 + row;
+            row_tok = seq0 + r0 + jrow;
         }
         const int i_loc = row_tok - seq0;  // position inside the sequence
         const int rb = (MODE == kCurrent && !a.dense) ? (i_loc / a.g.bs) * a.g.bs : 0;
-        const int r_min = r0, r_last = r0 + nrows - 1;
-        const int rb_max = (MODE == kCurrent && !a.dense) ? (r_last / a.g.bs) * a.g.bs : 0;
+        const int g_first = r0 + g * kM;
+        const int g_last = min(r0 + (g + 1) * kM, r0 + nrows) - 1;
+        const int rb_max = (MODE == kCurrent && !a.dense) ? (g_last / a.g.bs) * a.g.bs : 0;
+        const int my_tb = (g == 0) ? tb[0] : tb[kG - 1];
+        const int ntile = ((g == 0) ? te[0] : te[kG - 1]) - my_tb;
 
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
-        for (int j = 0; j < nkv; ++j) {
-            if (!__all_sync(0xffffffffu, wait_bar(b_sfull + 8 * (j & 1), (j >> 1) & 1, ctl))) {
+        for (int jl = 0; jl < ntile; ++jl) {
+            const int j = my_tb + jl;
+            // S_g(j) is ready; the commit behind it also covers PV_g(j-1), so
+            // O_g is stable and P_g's columns are free
+            if (!__all_sync(0xffffffffu, wait_bar(bar(L::kBarS + g), jl & 1, ctl))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            uint32_t sr[2][32];
-            const uint32_t tS = tmem + lane_off + (j & 1) * kN;
-            tc_ld32(tS, sr[0]);
-            tc_ld32(tS + 32, sr[1]);
-            tc_wait_ld();
-            float x[64];
             const int key0 = kv_lo + j * kN;  // sequence-local position of column 0
-            const bool need_mask = MODE == kCurrent &&
-                                   (key0 + kN - 1 > r_min || key0 < rb_max ||
-                                    seq0 + key0 + kN > kv_end);
-            float mt = -INFINITY;
+            const bool need_mask =
+                (MODE == kPast) ? (kv_tok0 + (j + 1) * kN > kv_end)
+                                : (key0 + kN - 1 > g_first || key0 < rb_max ||
+                                   seq0 + key0 + kN > kv_end);
+            // masked columns are set to -inf (raw fp32 bits) in place; only the
+            // tiles on the diagonal / at the end of a block need it
+            const int kt0 = kv_tok0 + j * kN;  // token of column 0
+#define MOBA_MASK64(SR, BASE)                                                         \
+    if (need_mask) {                                                                  \
+        _Pragma("unroll") for (int c = 0; c < 64; ++c) {                              \
+            const int col = (BASE) + c;                                               \
+            const int kp = key0 + col;                                                \
+            if (kt0 + col >= kv_end || (MODE == kCurrent && (kp > i_loc || kp < rb))) \
+                SR[c >> 5][c & 31] = 0xff800000u;                                     \
+        }                                                                             \
+    }
+            // pass 1: row max of the raw scores (the scale is positive)
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                float v = __uint_as_float(sr[c >> 5][c & 31]) * a.scale_log2;
-                if (MODE == kPast) {
-                    if (kv_tok0 + j * kN + c >= kv_end) v = -INFINITY;
-                } else if (need_mask) {
-                    const int kp = key0 + c;
-                    if (kp > i_loc || kp < rb || seq0 + kp >= kv_end) v = -INFINITY;
-                }
-                x[c] = v;
-                mt = fmaxf(mt, v);
+            for (int h2 = 0; h2 < 2; ++h2) {
+                uint32_t sr[2][32];
+                tc_ld32(tSg + 64 * h2, sr[0]);
+                tc_ld32(tSg + 64 * h2 + 32, sr[1]);
+                tc_wait_ld();
+                MOBA_MASK64(sr, 64 * h2)
+#pragma unroll
+                for (int c = 0; c < 64; ++c)
+                    mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(sr[c >> 5][c & 31]));
             }
+            const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
             const float m_new = fmaxf(m_run, mt);
             // rescale only when the max grew by more than 2^8 (P stays <= 256)
-            const bool need = (j > 0) && (m_new > m_run + 8.f);
-            if (j > 0) {
-                if (!__all_sync(0xffffffffu, wait_bar(b_pvdone, (j - 1) & 1, ctl))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (__any_sync(0xffffffffu, need)) {
-                    const float alpha = need ? fast_exp2(m_run - m_new) : 1.f;
+            const bool need = (jl > 0) && (m_new > m_run + 8.f);
+            const float m_use = (jl == 0 || need) ? m_new : m_run;
+            const float mu = (m_use == -INFINITY) ? 0.f : m_use;
+            if (jl > 0 && __any_sync(0xffffffffu, need)) {
+                const float alpha = need ? fast_exp2(m_run - m_new) : 1.f;
 #pragma unroll
-                    for (int c0 = 0; c0 < D; c0 += 32) {
-                        uint32_t o[32];
-                        tc_ld32(tmem + lane_off + 128 + c0, o);
-                        tc_wait_ld();
+                for (int c0 = 0; c0 < D; c0 += 16) {
+                    uint32_t o[16];
+                    tc_ld16(tOg + c0, o);
+                    tc_wait_ld();
 #pragma unroll
-                        for (int c = 0; c < 32; ++c)
-                            o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-                        tc_st32(tmem + lane_off + 128 + c0, o);
-                    }
-                    tc_wait_st();
-                    if (need) l_run *= alpha;
+                    for (int c = 0; c < 16; ++c)
+                        o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                    tc_st16(tOg + c0, o);
                 }
-                if (need) m_run = m_new;
-            } else {
-                m_run = m_new;
+                if (need) l_run *= alpha;
             }
-            const float mu = (m_run == -INFINITY) ? 0.f : m_run;
-            // P_j (bf16) into the swizzled K-major tile: row `row`, 8 chunks
-            float lsum = 0.f;
+            m_run = m_use;
+            // pass 2: p = 2^(s * scale - mu) as bf16 pairs (keys 2c, 2c+1 in
+            // column c) over the first 64 columns of S; half h2 of the keys goes
+            // to columns 32*h2 .. 32*h2+31, already read when h2 = 1 is written
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                uint32_t pk[4];
+            for (int h2 = 0; h2 < 2; ++h2) {
+                uint32_t sr[2][32];
+                tc_ld32(tSg + 64 * h2, sr[0]);
+                tc_ld32(tSg + 64 * h2 + 32, sr[1]);
+                tc_wait_ld();
+                MOBA_MASK64(sr, 64 * h2)
+                uint32_t pk[32];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p0 = fast_exp2(x[ch * 8 + 2 * e] - mu);
-                    const float p1 = fast_exp2(x[ch * 8 + 2 * e + 1] - mu);
-                    lsum += p0 + p1;
+                for (int c = 0; c < 32; ++c) {
+                    const float p0 = fast_exp2(fmaf(__uint_as_float(sr[(2 * c) >> 5][(2 * c) & 31]), a.scale_log2, -mu));
+                    const float p1 = fast_exp2(fmaf(__uint_as_float(sr[(2 * c + 1) >> 5][(2 * c + 1) & 31]), a.scale_log2, -mu));
+                    ls[c & 3] += p0 + p1;
                     __nv_bfloat162 bb = __floats2bfloat162_rn(p0, p1);
-                    pk[e] = *reinterpret_cast<uint32_t *>(&bb);
+                    pk[c] = *reinterpret_cast<uint32_t *>(&bb);
                 }
-                const uint32_t dst = sP + row * 128 + ((uint32_t)(ch ^ (row & 7)) << 4);
-                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(pk[0]),
-                             "r"(pk[1]), "r"(pk[2]), "r"(pk[3])
-                             : "memory");
+                tc_st32(tSg + 32 * h2, pk);
             }
+#undef MOBA_MASK64
+            const float lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
             l_run += lsum;
-            fence_proxy_async();
+            tc_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(b_pfull);
+            if (lane == 0) mbar_arrive(bar(L::kBarP + g));
         }
         // ---------------- epilogue ----------------
-        if (ok && nkv > 0) ok = __all_sync(0xffffffffu, wait_bar(b_pvdone, (nkv - 1) & 1, ctl));
+        if (ok && ntile > 0)
+            ok = __all_sync(0xffffffffu, wait_bar(bar(L::kBarPV + g), 0, ctl));
         tc_fence_after();
-        if (ok) {
+        if (ok && ntile > 0) {
             const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
             const float lse2 = m_run + __log2f(l_run);
             if (MODE == kPast) {
@@ -533,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                 for (int c0 = 0; c0 < D; c0 += 32) {
                     uint32_t o[32];
-                    tc_ld32(tmem + lane_off + 128 + c0, o);
+                    tc_ld32(tOg + c0, o);
                     tc_wait_ld();
                     if (row_valid) {
 #pragma unroll
@@ -568,21 +661,21 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const float fcur = w_cur * inv * iw;
                 __nv_bfloat16 *dst = a.out + rowid * D;
 #pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    uint32_t o[32];
-                    tc_ld32(tmem + lane_off + 128 + c0, o);
+                for (int c0 = 0; c0 < D; c0 += 16) {
+                    uint32_t o[16];
+                    tc_ld16(tOg + c0, o);
                     tc_wait_ld();
                     if (row_valid) {
-                        float acc[32];
+                        float acc[16];
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) acc[c] = __uint_as_float(o[c]) * fcur;
+                        for (int c = 0; c < 16; ++c) acc[c] = __uint_as_float(o[c]) * fcur;
                         for (int s = 0; s < np; ++s) {
                             const size_t ps = rowid * a.km1 + s;
                             const float w = fast_exp2(__ldg(a.part_lse + ps) - mmax) * iw;
                             const float4 *src =
                                 reinterpret_cast<const float4 *>(a.part_o + ps * D + c0);
 #pragma unroll
-                            for (int c = 0; c < 8; ++c) {
+                            for (int c = 0; c < 4; ++c) {
                                 const float4 f = __ldg(src + c);
                                 acc[4 * c] = fmaf(w, f.x, acc[4 * c]);
                                 acc[4 * c + 1] = fmaf(w, f.y, acc[4 * c + 1]);
@@ -591,17 +684,17 @@ __global__ void __launch_bounds__(kThreads, 2)
                             }
                         }
 #pragma unroll
-                        for (int c = 0; c < 32; c += 8) {
-                            uint4 pk;
+                        for (int c = 0; c < 16; c += 8) {
+                            uint4 pkd;
                             __nv_bfloat162 b0 = __floats2bfloat162_rn(acc[c], acc[c + 1]);
                             __nv_bfloat162 b1 = __floats2bfloat162_rn(acc[c + 2], acc[c + 3]);
                             __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[c + 4], acc[c + 5]);
                             __nv_bfloat162 b3 = __floats2bfloat162_rn(acc[c + 6], acc[c + 7]);
-                            pk.x = *reinterpret_cast<uint32_t *>(&b0);
-                            pk.y = *reinterpret_cast<uint32_t *>(&b1);
-                            pk.z = *reinterpret_cast<uint32_t *>(&b2);
-                            pk.w = *reinterpret_cast<uint32_t *>(&b3);
-                            *reinterpret_cast<uint4 *>(dst + c0 + c) = pk;
+                            pkd.x = *reinterpret_cast<uint32_t *>(&b0);
+                            pkd.y = *reinterpret_cast<uint32_t *>(&b1);
+                            pkd.z = *reinterpret_cast<uint32_t *>(&b2);
+                            pkd.w = *reinterpret_cast<uint32_t *>(&b3);
+                            *reinterpret_cast<uint4 *>(dst + c0 + c) = pkd;
                         }
                     }
                 }
@@ -671,7 +764,7 @@ void tc_debug_set(int flags, long long wait_limit) {
     g_wait_limit = wait_limit > 0 ? wait_limit : 4000000000ll;
 }
 
-int tc_tile_rows() { return tc::kM; }
+int tc_tile_rows() { return tc::kRows; }
 
 static tc::Args make_tc_args(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
                              __nv_bfloat16 *out, float *lse) {
@@ -714,16 +807,27 @@ static cudaError_t launch_tc(const Plan &p, const tc::Args &a, const __nv_bfloat
         return cudaErrorInvalidValue;
     const int smem = tc::Smem<D>::kRequest;
     auto kern = tc::attn_tc_kernel<D, MODE>;
+    // The block needs all of its 320 threads resident (warp roles are fixed);
+    // refuse to launch if the build's register use would not allow that.
+    static int checked[2][2] = {{0, 0}, {0, 0}};
+    int &chk = checked[D == 128][MODE];
+    if (!chk) {
+        cudaFuncAttributes fa;
+        cudaError_t e0 = cudaFuncGetAttributes(&fa, kern);
+        if (e0 != cudaSuccess) return e0;
+        chk = (fa.numRegs <= tc::kRegLaunch && fa.maxThreadsPerBlock >= tc::kThreads) ? 1 : -1;
+    }
+    if (chk < 0) return cudaErrorInvalidConfiguration;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dim3 grid;
     if (MODE == tc::kPast) {
         // an upper bound of the tiles; CTAs past the real count exit at once
         const long long rows = (long long)p.total * p.H * p.km1;
-        const long long tiles = rows / tc::kM + (long long)p.NBcap * p.H + 1;
+        const long long tiles = rows / tc::kRows + (long long)p.NBcap * p.H + 1;
         grid = dim3((unsigned)tiles);
     } else {
-        grid = dim3((p.max_len + tc::kM - 1) / tc::kM, p.H, p.num_seqs);
+        grid = dim3((p.max_len + tc::kRows - 1) / tc::kRows, p.H, p.num_seqs);
     }
     kern<<<grid, tc::kThreads, smem, st>>>(mq, mk, mv, a);
     note_launches(1);

@@ -28,6 +28,7 @@ _P, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
 _SIGNATURES = {
     "moba_num_blocks": (_I, [_I, _I]),
     "moba_status_string": (ctypes.c_char_p, [_I]),
+    "moba_last_cuda_error": (ctypes.c_char_p, []),
     "moba_kpool": (_I, [_P, _P, _I, _I, _I, _I, _I, _P]),
     "moba_kpool_varlen": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "moba_gate_topk": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
@@ -75,7 +76,10 @@ def status_string(code: int) -> str:
 
 def _check(code: int, what: str):
     if code != MOBA_OK:
-        raise RuntimeError(f"{what} failed: {status_string(code)} ({code})")
+        extra = ""
+        if code == MOBA_ERR_CUDA:
+            extra = ": " + lib().moba_last_cuda_error().decode()
+        raise RuntimeError(f"{what} failed: {status_string(code)} ({code}){extra}")
 
 
 def _stream(stream=None):
