@@ -424,6 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         drain_bar(bar(bfull + s), (pend[s] / kStages) & 1, a.wait_limit);
             }
         }
+        __syncwarp();  // reconverge before the CTA barrier (bar.sync is per warp)
     } else if (warp == 1) {
         // ================= MMA issuer =================
         if (lane == 0) {
@@ -480,6 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_commit(bar(L::kBarDrain));
             drain_bar(bar(L::kBarDrain), 0, a.wait_limit);
         }
+        __syncwarp();  // reconverge before the CTA barrier (bar.sync is per warp)
     } else {
         // ================= softmax + epilogue (warps 2..9) =================
         const int g = (warp - 2) >> 2;  // Q tile of this warp
@@ -512,6 +514,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(bar(L::kBarQ));
         } else {
             row_tok = seq0 + r0 + jrow;
+            // warm L2 with this row's past partials; the merge reads them only
+            // after the last tile, so the fetch overlaps the attention loop
+            if (row_valid && !a.dense && a.km1 > 0) {
+                const int ci = (row_tok - seq0) / a.g.bs;
+                const size_t rowid = (size_t)row_tok * H + h;
+                const int32_t *sel = a.idx + rowid * a.topk;
+                for (int s2 = 0; s2 < a.km1; ++s2) {
+                    const int c = __ldg(sel + s2);
+                    if (c < 0 || c >= ci) break;
+                    const char *po = reinterpret_cast<const char *>(a.part_o + (rowid * a.km1 + s2) * D);
+#pragma unroll
+                    for (int ln = 0; ln < D * 4; ln += 128)
+                        asm volatile("prefetch.global.L2 [%0];" ::"l"(po + ln));
+                }
+            }
         }
         const int i_loc = row_tok - seq0;  // position inside the sequence
         const int rb = (MODE == kCurrent && !a.dense) ? (i_loc / a.g.bs) * a.g.bs : 0;
@@ -661,39 +678,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float fcur = w_cur * inv * iw;
                 __nv_bfloat16 *dst = a.out + rowid * D;
 #pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 16) {
-                    uint32_t o[16];
-                    tc_ld16(tOg + c0, o);
+                for (int c0 = 0; c0 < D; c0 += 64) {
+                    // 64 columns of O from TMEM in one go, then the partials'
+                    // loads of those columns all in flight together
+                    uint32_t o[2][32];
+                    tc_ld32(tOg + c0, o[0]);
+                    tc_ld32(tOg + c0 + 32, o[1]);
                     tc_wait_ld();
                     if (row_valid) {
-                        float acc[16];
 #pragma unroll
-                        for (int c = 0; c < 16; ++c) acc[c] = __uint_as_float(o[c]) * fcur;
+                        for (int c = 0; c < 64; ++c)
+                            o[c >> 5][c & 31] = __float_as_uint(__uint_as_float(o[c >> 5][c & 31]) * fcur);
                         for (int s = 0; s < np; ++s) {
                             const size_t ps = rowid * a.km1 + s;
                             const float w = fast_exp2(__ldg(a.part_lse + ps) - mmax) * iw;
                             const float4 *src =
                                 reinterpret_cast<const float4 *>(a.part_o + ps * D + c0);
+                            float4 f[16];
 #pragma unroll
-                            for (int c = 0; c < 4; ++c) {
-                                const float4 f = __ldg(src + c);
-                                acc[4 * c] = fmaf(w, f.x, acc[4 * c]);
-                                acc[4 * c + 1] = fmaf(w, f.y, acc[4 * c + 1]);
-                                acc[4 * c + 2] = fmaf(w, f.z, acc[4 * c + 2]);
-                                acc[4 * c + 3] = fmaf(w, f.w, acc[4 * c + 3]);
+                            for (int c = 0; c < 16; ++c) f[c] = __ldg(src + c);
+#pragma unroll
+                            for (int c = 0; c < 16; ++c) {
+                                const float fv[4] = {f[c].x, f[c].y, f[c].z, f[c].w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const int col = 4 * c + e;
+                                    o[col >> 5][col & 31] = __float_as_uint(
+                                        fmaf(w, fv[e], __uint_as_float(o[col >> 5][col & 31])));
+                                }
                             }
                         }
 #pragma unroll
-                        for (int c = 0; c < 16; c += 8) {
+                        for (int c = 0; c < 64; c += 8) {
                             uint4 pkd;
-                            __nv_bfloat162 b0 = __floats2bfloat162_rn(acc[c], acc[c + 1]);
-                            __nv_bfloat162 b1 = __floats2bfloat162_rn(acc[c + 2], acc[c + 3]);
-                            __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[c + 4], acc[c + 5]);
-                            __nv_bfloat162 b3 = __floats2bfloat162_rn(acc[c + 6], acc[c + 7]);
-                            pkd.x = *reinterpret_cast<uint32_t *>(&b0);
-                            pkd.y = *reinterpret_cast<uint32_t *>(&b1);
-                            pkd.z = *reinterpret_cast<uint32_t *>(&b2);
-                            pkd.w = *reinterpret_cast<uint32_t *>(&b3);
+                            uint32_t *pw = reinterpret_cast<uint32_t *>(&pkd);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int col = c + 2 * e;
+                                __nv_bfloat162 bb = __floats2bfloat162_rn(
+                                    __uint_as_float(o[col >> 5][col & 31]),
+                                    __uint_as_float(o[(col + 1) >> 5][(col + 1) & 31]));
+                                pw[e] = *reinterpret_cast<uint32_t *>(&bb);
+                            }
                             *reinterpret_cast<uint4 *>(dst + c0 + c) = pkd;
                         }
                     }
