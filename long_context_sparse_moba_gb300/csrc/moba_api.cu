@@ -83,7 +83,7 @@ size_t workspace_bytes(const Plan &p, Workspace *ws, char *base) {
         w.tile_off = static_cast<int *>(take(sizeof(int) * (N + 1)));
         w.ticket = static_cast<int *>(take(sizeof(int) * rows * p.km1));
         w.list = static_cast<int *>(take(sizeof(int) * rows * p.km1));
-        w.part_o = static_cast<float *>(take(sizeof(float) * rows * p.km1 * p.D));
+        w.part_o = static_cast<__nv_bfloat16 *>(take(sizeof(__nv_bfloat16) * rows * p.km1 * p.D));
         w.part_lse = static_cast<float *>(take(sizeof(float) * rows * p.km1));
     }
     if (ws) *ws = w;

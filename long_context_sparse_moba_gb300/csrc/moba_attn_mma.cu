@@ -35,7 +35,8 @@ struct Args {
     const int32_t *idx;
     const int *list, *list_off, *tile_off;
     int n_lists;
-    float *part_o, *part_lse;
+    __nv_bfloat16 *part_o;
+    float *part_lse;
     float scale_log2;
 };
 
@@ -282,11 +283,11 @@ __global__ __launch_bounds__(kThreads, 2) void past_kernel(Args a) {
             const int e = __ldg(ent + row);
             const size_t slot = ((size_t)(e >> kSlotBits) * H + h) * a.km1 + (e & ((1 << kSlotBits) - 1));
             const float inv = 1.f / st.l[r];
-            float *dst = a.part_o + slot * D + 2 * (lane & 3);
+            __nv_bfloat16 *dst = a.part_o + slot * D + 2 * (lane & 3);
 #pragma unroll
             for (int j = 0; j < D / 8; ++j)
-                *reinterpret_cast<float2 *>(dst + j * 8) =
-                    make_float2(st.o[j][2 * r] * inv, st.o[j][2 * r + 1] * inv);
+                *reinterpret_cast<__nv_bfloat162 *>(dst + j * 8) =
+                    __floats2bfloat162_rn(st.o[j][2 * r] * inv, st.o[j][2 * r + 1] * inv);
             if ((lane & 3) == 0) a.part_lse[slot] = st.m[r] + __log2f(st.l[r]);
         }
         __syncthreads();
@@ -350,10 +351,11 @@ __global__ __launch_bounds__(kThreads, 2) void current_kernel(Args a) {
                     const size_t slot = ((size_t)tok * H + h) * a.km1 + s;
                     const float w = fast_exp2(__ldg(a.part_lse + slot) - mmax);
                     wsum += w;
-                    const float *src = a.part_o + slot * D + 2 * (lane & 3);
+                    const __nv_bfloat16 *src = a.part_o + slot * D + 2 * (lane & 3);
 #pragma unroll
                     for (int j = 0; j < D / 8; ++j) {
-                        const float2 f = __ldg(reinterpret_cast<const float2 *>(src + j * 8));
+                        const float2 f = __bfloat1622float2(
+                            __ldg(reinterpret_cast<const __nv_bfloat162 *>(src + j * 8)));
                         acc[j][0] = fmaf(w, f.x, acc[j][0]);
                         acc[j][1] = fmaf(w, f.y, acc[j][1]);
                     }

@@ -75,7 +75,8 @@ struct Args {
     const int32_t *idx;
     const int *list, *list_off, *tile_off;
     int n_lists;
-    float *part_o, *part_lse;
+    __nv_bfloat16 *part_o;  // partial outputs, bf16
+    float *part_lse;
     float scale_log2;
     int *status;
     long long wait_limit;  // clock64 budget of one wait
@@ -525,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (c < 0 || c >= ci) break;
                     const char *po = reinterpret_cast<const char *>(a.part_o + (rowid * a.km1 + s2) * D);
 #pragma unroll
-                    for (int ln = 0; ln < D * 4; ln += 128)
+                    for (int ln = 0; ln < D * 2; ln += 128)
                         asm volatile("prefetch.global.L2 [%0];" ::"l"(po + ln));
                 }
             }
@@ -639,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float lse2 = m_run + __log2f(l_run);
             if (MODE == kPast) {
                 const size_t pslot = ((size_t)row_tok * H + h) * a.km1 + slot;
-                float *dst = a.part_o + pslot * D;
+                __nv_bfloat16 *dst = a.part_o + pslot * D;
 #pragma unroll
                 for (int c0 = 0; c0 < D; c0 += 32) {
                     uint32_t o[32];
@@ -647,10 +648,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_wait_ld();
                     if (row_valid) {
 #pragma unroll
-                        for (int c = 0; c < 32; c += 4)
-                            *reinterpret_cast<float4 *>(dst + c0 + c) = make_float4(
-                                __uint_as_float(o[c]) * inv, __uint_as_float(o[c + 1]) * inv,
-                                __uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv);
+                        for (int c = 0; c < 32; c += 8) {
+                            uint4 pkd;
+                            uint32_t *pw = reinterpret_cast<uint32_t *>(&pkd);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                __nv_bfloat162 bb =
+                                    __floats2bfloat162_rn(__uint_as_float(o[c + 2 * e]) * inv,
+                                                          __uint_as_float(o[c + 2 * e + 1]) * inv);
+                                pw[e] = *reinterpret_cast<uint32_t *>(&bb);
+                            }
+                            *reinterpret_cast<uint4 *>(dst + c0 + c) = pkd;
+                        }
                     }
                 }
                 if (row_valid) a.part_lse[pslot] = lse2;
@@ -692,19 +701,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int s = 0; s < np; ++s) {
                             const size_t ps = rowid * a.km1 + s;
                             const float w = fast_exp2(__ldg(a.part_lse + ps) - mmax) * iw;
-                            const float4 *src =
-                                reinterpret_cast<const float4 *>(a.part_o + ps * D + c0);
-                            float4 f[16];
+                            const uint4 *src =
+                                reinterpret_cast<const uint4 *>(a.part_o + ps * D + c0);
+                            uint4 f[8];
 #pragma unroll
-                            for (int c = 0; c < 16; ++c) f[c] = __ldg(src + c);
+                            for (int c = 0; c < 8; ++c) f[c] = __ldg(src + c);
 #pragma unroll
-                            for (int c = 0; c < 16; ++c) {
-                                const float fv[4] = {f[c].x, f[c].y, f[c].z, f[c].w};
+                            for (int c = 0; c < 8; ++c) {
+                                const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&f[c]);
 #pragma unroll
                                 for (int e = 0; e < 4; ++e) {
-                                    const int col = 4 * c + e;
+                                    const float2 fv = __bfloat1622float2(b2[e]);
+                                    const int col = 8 * c + 2 * e;
                                     o[col >> 5][col & 31] = __float_as_uint(
-                                        fmaf(w, fv[e], __uint_as_float(o[col >> 5][col & 31])));
+                                        fmaf(w, fv.x, __uint_as_float(o[col >> 5][col & 31])));
+                                    o[(col + 1) >> 5][(col + 1) & 31] = __float_as_uint(
+                                        fmaf(w, fv.y, __uint_as_float(o[(col + 1) >> 5][(col + 1) & 31])));
                                 }
                             }
                         }

@@ -52,7 +52,7 @@ struct Workspace {
     int *tile_off;    // [NBcap * H + 1]
     int *ticket;      // [total * H * km1]  position of a selection inside its list
     int *list;        // [total * H * km1]  entries token << 5 | slot
-    float *part_o;    // [total * H * km1][D]  normalised partial outputs
+    __nv_bfloat16 *part_o;  // [total * H * km1][D]  normalised partial outputs (bf16)
     float *part_lse;  // [total * H * km1]     partial log2-sum-exp
 };
 
