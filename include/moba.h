@@ -208,6 +208,14 @@ int moba_profile_end(float *phase_ms, int n_phases);
  * tolerances.  MOBA_ERR_INVALID_ARG for any other value. */
 int moba_set_attention_kernel(int kind);
 
+/* Gate implementation (process-wide, not thread-safe): 0 = block scores on
+ * the tensor cores (q times the pooled keys split into two bf16 terms, fp32
+ * accumulation) followed by an exact fp32 re-score of the blocks within a
+ * proven error margin of the top-(k-1) boundary (default; used when the
+ * longest sequence has at most 256 blocks); 1 = all scores on the CUDA cores.
+ * Both select exactly the same blocks.  MOBA_ERR_INVALID_ARG otherwise. */
+int moba_set_gate_kernel(int kind);
+
 /* Test hooks of the bounded waits in the tcgen05 kernels (process-wide):
  * wait_limit_cycles is the clock64 budget of one mbarrier wait (<= 0 restores
  * the default, about 2 s); flags bit 0 makes the K/V producer skip its first

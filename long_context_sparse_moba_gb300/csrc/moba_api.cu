@@ -31,6 +31,8 @@ static std::atomic<unsigned long long> g_launches{0};
 
 // attention implementation: 0 = tcgen05 / TMEM / TMA, 1 = warp-level mma.sync
 static int g_attn_kind = 0;
+// gate implementation: 0 = tcgen05 scores + exact candidates, 1 = CUDA cores
+static int g_gate_kind = 0;
 int past_tile_rows() { return g_attn_kind == 0 ? tc_tile_rows() : mma_tile_rows(); }
 cudaError_t launch_attn_past(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
                              const __nv_bfloat16 *k, const __nv_bfloat16 *v, cudaStream_t st) {
@@ -82,6 +84,9 @@ size_t workspace_bytes(const Plan &p, Workspace *ws, char *base) {
         w.list_off = static_cast<int *>(take(sizeof(int) * (N + 1)));
         w.tile_off = static_cast<int *>(take(sizeof(int) * (N + 1)));
         w.ticket = static_cast<int *>(take(sizeof(int) * rows * p.km1));
+        w.kbhi = static_cast<__nv_bfloat16 *>(take(sizeof(__nv_bfloat16) * N * p.D));
+        w.kblo = static_cast<__nv_bfloat16 *>(take(sizeof(__nv_bfloat16) * N * p.D));
+        w.knorm = static_cast<float *>(take(sizeof(float) * N));
         w.list = static_cast<int *>(take(sizeof(int) * rows * p.km1));
         w.part_o = static_cast<__nv_bfloat16 *>(take(sizeof(__nv_bfloat16) * rows * p.km1 * p.D));
         w.part_lse = static_cast<float *>(take(sizeof(float) * rows * p.km1));
@@ -153,7 +158,13 @@ static int run_forward(const Plan &p, const int *cu_dev, const void *q, const vo
     prof_mark(call, 2, st);
     if (gate) {
         MOBA_TRY(cudaMemsetAsync(ws.counts, 0, sizeof(int) * (size_t)p.NBcap * p.H, st));
-        MOBA_TRY(launch_gate(p, ws, qb, ws.kbar, ws.idx, true, st));
+        if (g_gate_kind == 0 && gate_tc_supported(p)) {
+            MOBA_TRY(launch_kbar_split(p, ws.kbar, ws.kbhi, ws.kblo, ws.knorm, st));
+            MOBA_TRY(launch_gate_tc(p, ws, qb, ws.kbar, ws.kbhi, ws.kblo, ws.knorm, ws.idx, true,
+                                    st));
+        } else {
+            MOBA_TRY(launch_gate(p, ws, qb, ws.kbar, ws.idx, true, st));
+        }
     }
     prof_mark(call, 3, st);
     if (gate) MOBA_TRY(launch_regroup(p, ws, st));
@@ -208,8 +219,23 @@ static int pool_run(const Plan &p, Workspace &ws, void *c) {
 }
 static int gate_run(const Plan &p, Workspace &ws, void *c) {
     auto *x = static_cast<GateCtx *>(c);
-    return cuda_status(launch_gate(p, ws, static_cast<const __nv_bfloat16 *>(x->q), x->kbar,
-                                   x->idx, false, x->st));
+    const auto *q = static_cast<const __nv_bfloat16 *>(x->q);
+    if (g_gate_kind != 0 || !gate_tc_supported(p))
+        return cuda_status(launch_gate(p, ws, q, x->kbar, x->idx, false, x->st));
+    // bf16 split of the caller's kbar in stream-ordered scratch
+    const size_t n = (size_t)p.NBcap * p.H * p.D;
+    void *mem = nullptr;
+    if (cudaMallocAsync(&mem, 2 * n * sizeof(__nv_bfloat16) + sizeof(float) * p.NBcap * p.H,
+                        x->st) != cudaSuccess)
+        return MOBA_ERR_CUDA;
+    auto *hi = static_cast<__nv_bfloat16 *>(mem);
+    auto *nrm = reinterpret_cast<float *>(hi + 2 * n);
+    int rc = cuda_status(launch_kbar_split(p, x->kbar, hi, hi + n, nrm, x->st));
+    if (rc == MOBA_OK)
+        rc = cuda_status(
+            launch_gate_tc(p, ws, q, x->kbar, hi, hi + n, nrm, x->idx, false, x->st));
+    if (cudaFreeAsync(mem, x->st) != cudaSuccess && rc == MOBA_OK) rc = MOBA_ERR_CUDA;
+    return rc;
 }
 
 }  // namespace moba
@@ -409,6 +435,12 @@ MOBA_EXPORT int moba_profile_end(float *phase_ms, int n_phases) {
 MOBA_EXPORT int moba_set_attention_kernel(int kind) {
     if (kind != 0 && kind != 1) return MOBA_ERR_INVALID_ARG;
     g_attn_kind = kind;
+    return MOBA_OK;
+}
+
+MOBA_EXPORT int moba_set_gate_kernel(int kind) {
+    if (kind != 0 && kind != 1) return MOBA_ERR_INVALID_ARG;
+    g_gate_kind = kind;
     return MOBA_OK;
 }
 

@@ -48,9 +48,11 @@
 
 #include "moba.h"
 #include "moba_internal.cuh"
+#include "moba_ptx.cuh"
 
 namespace moba {
 namespace tc {
+using namespace ptx;
 
 constexpr int kM = 128;           // rows per Q tile (the MMA's M)
 constexpr int kG = 2;             // Q tiles (softmax groups) per CTA
@@ -84,148 +86,6 @@ struct Args {
 };
 
 // ----------------------------------------------------------------------------
-// PTX wrappers
-// ----------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t saddr(const void *p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ void fence_proxy_async() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void fence_mbar_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                            int c0, int c1, int c2) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
-        : "memory");
-}
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool pred) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-                 "r"(pred ? 16 : 0)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.wait_all;" ::: "memory");
-}
-// tcgen05
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     bar)
-                 : "memory");
-}
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// A operand from tensor memory (M lanes x K/2 columns of packed bf16 pairs)
-__device__ __forceinline__ void tc_mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                          uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-          "=r"(r[31])
-        : "r"(taddr));
-}
-__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-        "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
-            taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-        "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-        "%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-}
-__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-        "%13,%14,%15,%16};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-        "r"(r[15])
-        : "memory");
-}
-__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-__device__ __forceinline__ float fast_exp2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-// Shared-memory matrix descriptor (tcgen05 format): start address, leading
-// byte offset, stride byte offset (all >> 4), version 1 at bit 46, 128-byte
-// swizzle (layout type 2) at bits 61-63.
-__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-    return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
-}
-// Instruction descriptor of kind::f16: fp32 accumulate, bf16 A and B, A
-// K-major, B K-major (b_mn = 0) or MN-major (b_mn = 1), M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn << 16) |
-           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-// ----------------------------------------------------------------------------
 // shared memory plan (offsets from a 1024-byte aligned base)
 // ----------------------------------------------------------------------------
 template <int D>
@@ -252,33 +112,6 @@ struct Smem {
     static constexpr uint32_t kNeed = kTiles + 1008 + kMisc;
     static constexpr uint32_t kRequest = kNeed > 120 * 1024 ? kNeed : 120 * 1024;
 };
-
-struct Ctl {
-    volatile int *abort;
-    int *status;
-    long long limit;
-};
-
-// Bounded wait; false when it ran out (status set) or another role aborted.
-__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl &c) {
-    if (mbar_test(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (true) {
-        if (mbar_test(bar, parity)) return true;
-        if (*c.abort) return false;
-        if (clock64() - t0 > c.limit) {
-            *c.abort = 1;
-            atomicExch(c.status, (int)MOBA_ERR_TIMEOUT);
-            return false;
-        }
-    }
-}
-// Bounded wait that ignores the abort flag (draining copies / MMAs in flight).
-__device__ __noinline__ void drain_bar(uint32_t bar, uint32_t parity, long long limit) {
-    const long long t0 = clock64();
-    while (!mbar_test(bar, parity) && clock64() - t0 <= limit) {
-    }
-}
 
 template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -781,7 +614,7 @@ static EncodeTiledFn encode_fn() {
 
 // [total][H][D] bf16 viewed as a 3-D tensor (D, H, total); box = 64 dims x 1
 // head x `rows` tokens, 128-byte swizzle.
-static bool make_map(CUtensorMap *m, const void *ptr, int total, int H, int D, int rows) {
+bool make_tma_3d(CUtensorMap *m, const void *ptr, int total, int H, int D, int rows) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)total};
@@ -803,6 +636,7 @@ void tc_debug_set(int flags, long long wait_limit) {
 }
 
 int tc_tile_rows() { return tc::kRows; }
+long long tc_wait_limit() { return g_wait_limit; }
 
 static tc::Args make_tc_args(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
                              __nv_bfloat16 *out, float *lse) {
@@ -840,8 +674,9 @@ template <int D, int MODE>
 static cudaError_t launch_tc(const Plan &p, const tc::Args &a, const __nv_bfloat16 *q,
                              const __nv_bfloat16 *k, const __nv_bfloat16 *v, cudaStream_t st) {
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, q, p.total, p.H, D, tc::kM) || !make_map(&mk, k, p.total, p.H, D, tc::kN) ||
-        !make_map(&mv, v, p.total, p.H, D, tc::kN))
+    if (!make_tma_3d(&mq, q, p.total, p.H, D, tc::kM) ||
+        !make_tma_3d(&mk, k, p.total, p.H, D, tc::kN) ||
+        !make_tma_3d(&mv, v, p.total, p.H, D, tc::kN))
         return cudaErrorInvalidValue;
     const int smem = tc::Smem<D>::kRequest;
     auto kern = tc::attn_tc_kernel<D, MODE>;

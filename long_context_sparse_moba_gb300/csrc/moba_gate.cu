@@ -152,6 +152,38 @@ __global__ __launch_bounds__(kPoolThreads) void kpool_kernel(Geometry g,
     }
 }
 
+// kbar -> (hi, lo) bf16 terms for the tensor-core gate, and the L2 norm of
+// every pooled key; one warp per (block, head) row of D values
+__global__ void kbar_split_kernel(const float *__restrict__ kbar, __nv_bfloat16 *__restrict__ hi,
+                                  __nv_bfloat16 *__restrict__ lo, float *__restrict__ norm,
+                                  int rows, int D) {
+    const int lane = threadIdx.x & 31;
+    for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows;
+         r += (gridDim.x * blockDim.x) >> 5) {
+        float ss = 0.f;
+        for (int d = lane; d < D; d += 32) {
+            const size_t i = (size_t)r * D + d;
+            const float x = kbar[i];
+            const __nv_bfloat16 h = __float2bfloat16_rn(x);
+            hi[i] = h;
+            lo[i] = __float2bfloat16_rn(x - __bfloat162float(h));
+            ss = fmaf(x, x, ss);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (lane == 0) norm[r] = sqrtf(ss);
+    }
+}
+
+cudaError_t launch_kbar_split(const Plan &p, const float *kbar, __nv_bfloat16 *hi,
+                              __nv_bfloat16 *lo, float *norm, cudaStream_t st) {
+    const int rows = p.NBcap * p.H;
+    const unsigned blocks = (unsigned)((rows + 7) / 8 < 8192 ? (rows + 7) / 8 : 8192);
+    kbar_split_kernel<<<blocks, 256, 0, st>>>(kbar, hi, lo, norm, rows, p.D);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
 static Geometry make_geo(const Plan &p, const Workspace &ws) {
     Geometry g;
     g.cu = ws.cu;

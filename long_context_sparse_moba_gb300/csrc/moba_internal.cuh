@@ -8,6 +8,7 @@
 // Global block g of sequence b, local block c: g = blk_base[b] + c.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -51,6 +52,8 @@ struct Workspace {
     int *list_off;    // [NBcap * H + 1]
     int *tile_off;    // [NBcap * H + 1]
     int *ticket;      // [total * H * km1]  position of a selection inside its list
+    __nv_bfloat16 *kbhi, *kblo;  // [NBcap][H][D] bf16 split of kbar (tensor-core gate)
+    float *knorm;                // [NBcap][H] L2 norm of each pooled key
     int *list;        // [total * H * km1]  entries token << 5 | slot
     __nv_bfloat16 *part_o;  // [total * H * km1][D]  normalised partial outputs (bf16)
     float *part_lse;  // [total * H * km1]     partial log2-sum-exp
@@ -101,6 +104,17 @@ cudaError_t launch_attn_current_mma(const Plan &p, const Workspace &ws, const __
                                     const __nv_bfloat16 *k, const __nv_bfloat16 *v,
                                     __nv_bfloat16 *out, float *lse, cudaStream_t st);
 int tc_tile_rows();
+long long tc_wait_limit();
+// [total][H][D] bf16 as a 3-D TMA tensor (D, H, total), box 64 x 1 x rows, 128B swizzle
+bool make_tma_3d(CUtensorMap *m, const void *ptr, int total, int H, int D, int rows);
+// kbar (fp32) -> hi = bf16(kbar), lo = bf16(kbar - hi)
+cudaError_t launch_kbar_split(const Plan &p, const float *kbar, __nv_bfloat16 *hi,
+                              __nv_bfloat16 *lo, float *norm, cudaStream_t st);
+// tensor-core gate (scores on tcgen05, exact fp32 re-score of the candidates)
+bool gate_tc_supported(const Plan &p);
+cudaError_t launch_gate_tc(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
+                           const float *kbar, const __nv_bfloat16 *khi, const __nv_bfloat16 *klo,
+                           const float *knorm, int32_t *idx, bool count, cudaStream_t st);
 int mma_tile_rows();
 void tc_debug_set(int flags, long long wait_limit);
 

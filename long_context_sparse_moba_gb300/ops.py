@@ -45,6 +45,7 @@ _SIGNATURES = {
     "moba_profile_begin": (_I, [_I]),
     "moba_profile_end": (_I, [_P, _I]),
     "moba_set_attention_kernel": (_I, [_I]),
+    "moba_set_gate_kernel": (_I, [_I]),
     "moba_attn_fwd_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "moba_attn_fwd_noalloc_capacity": (_SZ, []),
     "moba_debug_set": (_I, [_I, ctypes.c_longlong]),
@@ -266,3 +267,12 @@ def attn_fwd_noalloc(q, k, v, block_size: int, topk: int, out, lse, stream=None)
 
 def noalloc_capacity() -> int:
     return int(lib().moba_attn_fwd_noalloc_capacity())
+
+
+GATE_TCGEN05 = 0
+GATE_CUDA_CORES = 1
+
+
+def set_gate_kernel(kind: int):
+    """0: tensor-core scores + exact re-score of candidates (default); 1: CUDA cores."""
+    _check(lib().moba_set_gate_kernel(int(kind)), "moba_set_gate_kernel")

@@ -196,3 +196,26 @@ def test_mma_sync_baseline_path(seqlens, H, D, bs, topk):
     finally:
         ops.set_attention_kernel(ops.ATTN_TCGEN05)
     print("mma.sync", seqlens, st)
+
+
+@pytest.mark.parametrize("seqlens,H,D,bs,topk", [
+    ((32768,), 4, 128, 512, 3),       # one 128-block chunk
+    ((16384,), 2, 128, 64, 5),        # 256 blocks: two chunks in TMEM
+    ((3000, 9000), 3, 64, 64, 8),     # varlen, D = 64
+    ((20000,), 2, 128, 64, 3),        # 313 blocks: falls back to the CUDA-core gate
+    ((65536,), 2, 128, 256, 17),      # wide top-k
+])
+def test_tensor_core_gate_equals_cuda_core_gate(seqlens, H, D, bs, topk):
+    """The tensor-core gate re-scores its candidates exactly, so it must pick
+    the very same blocks as the all-CUDA-core gate."""
+    w = workloads.custom(seqlens, H, D, bs, topk=topk, seed=31)
+    inp = workloads.make_inputs(w, device="cuda")
+    try:
+        ops.set_gate_kernel(ops.GATE_CUDA_CORES)
+        _, ref = gpu_select(inp, w, topk)
+        ops.set_gate_kernel(ops.GATE_TCGEN05)
+        _, got = gpu_select(inp, w, topk)
+    finally:
+        ops.set_gate_kernel(ops.GATE_TCGEN05)
+    assert ops.get_status() == ops.MOBA_OK
+    assert torch.equal(ref, got)
