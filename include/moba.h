@@ -223,6 +223,10 @@ int moba_set_gate_kernel(int kind);
  * (read it with moba_get_status) instead of hanging the GPU. */
 int moba_debug_set(int flags, long long wait_limit_cycles);
 
+/* Where the timeout reported by the last moba_get_status happened: out4 =
+ * {barrier shared-memory address, parity, block index, thread index}. */
+void moba_debug_timeout_info(int *out4);
+
 #ifdef __cplusplus
 }
 #endif

@@ -13,7 +13,9 @@
 
 namespace moba {
 
-__device__ int g_moba_status;
+// [0] status word; [1..4] where the first timeout happened (barrier shared
+// address, parity, block, thread)
+__device__ int g_moba_status[8];
 
 int *status_word() {
     static int *addr[64] = {nullptr};
@@ -391,14 +393,22 @@ MOBA_EXPORT int moba_attn_fwd_varlen(const void *q, const void *k, const void *v
     return rc;
 }
 
+static int g_last_timeout[4] = {0, 0, 0, 0};
+
+MOBA_EXPORT void moba_debug_timeout_info(int *out4) {
+    if (out4)
+        for (int i = 0; i < 4; ++i) out4[i] = g_last_timeout[i];
+}
+
 MOBA_EXPORT int moba_get_status(void *stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return MOBA_ERR_CUDA;
-    int v = 0;
-    if (cudaMemcpyFromSymbol(&v, g_moba_status, sizeof v) != cudaSuccess) return MOBA_ERR_CUDA;
-    const int zero = 0;
-    if (cudaMemcpyToSymbol(g_moba_status, &zero, sizeof zero) != cudaSuccess) return MOBA_ERR_CUDA;
-    return v;
+    int v[8];
+    if (cudaMemcpyFromSymbol(v, g_moba_status, sizeof v) != cudaSuccess) return MOBA_ERR_CUDA;
+    for (int i = 0; i < 4; ++i) g_last_timeout[i] = v[1 + i];
+    const int zero[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (cudaMemcpyToSymbol(g_moba_status, zero, sizeof zero) != cudaSuccess) return MOBA_ERR_CUDA;
+    return v[0];
 }
 
 MOBA_EXPORT unsigned long long moba_launch_count(void) { return g_launches.load(); }

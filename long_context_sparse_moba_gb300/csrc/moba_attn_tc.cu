@@ -77,6 +77,7 @@ struct Args {
     const int32_t *idx;
     const int *list, *list_off, *tile_off;
     int n_lists;
+    int n_jobs, n_rtiles;   // own-block mode: jobs = n_rtiles x num_seqs x H
     __nv_bfloat16 *part_o;  // partial outputs, bf16
     float *part_lse;
     float scale_log2;
@@ -97,10 +98,10 @@ struct Smem {
     static constexpr uint32_t kK = kQ + kG * NB * kQBox;      // [stage][box]
     static constexpr uint32_t kV = kK + kStages * NB * kKVBox;
     static constexpr uint32_t kTiles = kV + kStages * NB * kKVBox;  // end of the tiles
-    // mbarriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2],
+    // mbarriers: q_full, q_empty, k_full[2], k_empty[2], v_full[2], v_empty[2],
     // s_full[g], p_full[g], pv_done[g], drain; then the TMEM address slot and
     // the abort flag
-    static constexpr int kBarQ = 0, kBarKF = 1, kBarKE = kBarKF + kStages,
+    static constexpr int kBarQ = 0, kBarQE = 1, kBarKF = 2, kBarKE = kBarKF + kStages,
                          kBarVF = kBarKE + kStages, kBarVE = kBarVF + kStages,
                          kBarS = kBarVE + kStages, kBarP = kBarS + kG, kBarPV = kBarP + kG,
                          kBarDrain = kBarPV + kG, kNumBars = kBarDrain + 1;
@@ -113,6 +114,80 @@ struct Smem {
     static constexpr uint32_t kRequest = kNeed > 120 * 1024 ? kNeed : 120 * 1024;
 };
 
+// One unit of work: up to 256 query rows and the K/V tiles they visit.
+// rows: tile g holds job rows [g*128, g*128 + 128) (valid below nrows); K/V
+// tiles [0, nkv) start at token kv_tok0; tile g visits K/V tiles [tb[g], te[g]).
+struct Job {
+    int h, b, seq0, L_len, r0, nrows, kv_tok0, kv_end, kv_lo, nkv, lbeg;
+    int tb[kG], te[kG];
+};
+
+template <int MODE>
+__device__ __forceinline__ bool get_job(const Args &a, int job, Job &J) {
+    const int H = a.g.H;
+    if (MODE == kPast) {
+        int lo = 0, hi = a.n_lists - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(a.tile_off + mid) <= job) lo = mid; else hi = mid - 1;
+        }
+        const int Lid = lo;
+        const int gblk = Lid / H;
+        J.h = Lid % H;
+        J.b = upper_index(a.g.blk_base, a.g.num_seqs, gblk);
+        const int c = gblk - __ldg(a.g.blk_base + J.b);
+        J.seq0 = __ldg(a.g.cu + J.b);
+        J.L_len = __ldg(a.g.cu + J.b + 1) - J.seq0;
+        J.kv_lo = 0;
+        J.kv_tok0 = J.seq0 + c * a.g.bs;
+        J.kv_end = min(J.kv_tok0 + a.g.bs, J.seq0 + J.L_len);
+        const int lbeg = __ldg(a.list_off + Lid);
+        const int lcnt = __ldg(a.list_off + Lid + 1) - lbeg;
+        J.r0 = (job - __ldg(a.tile_off + Lid)) * kRows;
+        J.nrows = min(kRows, lcnt - J.r0);
+        J.lbeg = lbeg + J.r0;
+        J.nkv = (J.kv_end - J.kv_tok0 + kN - 1) / kN;
+#pragma unroll
+        for (int g = 0; g < kG; ++g) {
+            J.tb[g] = 0;
+            J.te[g] = (J.nrows > g * kM) ? J.nkv : 0;
+        }
+        return true;
+    }
+    // own-block mode: heavy (late) row tiles first
+    J.h = job % H;
+    const int t = job / H;
+    J.b = t % a.g.num_seqs;
+    const int x = a.n_rtiles - 1 - t / a.g.num_seqs;
+    J.seq0 = __ldg(a.g.cu + J.b);
+    J.L_len = __ldg(a.g.cu + J.b + 1) - J.seq0;
+    J.r0 = x * kRows;
+    if (J.r0 >= J.L_len) return false;
+    J.nrows = min(kRows, J.L_len - J.r0);
+    const int bs = a.g.bs;
+    J.kv_lo = a.dense ? 0 : (J.r0 / bs) * bs;
+    J.kv_tok0 = J.seq0 + J.kv_lo;
+    J.kv_end = J.seq0 + J.r0 + J.nrows;
+    J.nkv = (J.kv_end - J.kv_tok0 + kN - 1) / kN;
+    J.lbeg = 0;
+#pragma unroll
+    for (int g = 0; g < kG; ++g) {
+        const int first = J.r0 + g * kM, last = min(J.r0 + (g + 1) * kM, J.r0 + J.nrows) - 1;
+        if (last < first) {
+            J.tb[g] = J.te[g] = 0;
+            continue;
+        }
+        const int lo_key = a.dense ? 0 : (first / bs) * bs;
+        J.tb[g] = (lo_key - J.kv_lo) / kN;
+        J.te[g] = (last - J.kv_lo) / kN + 1;
+    }
+    return true;
+}
+
+// Persistent kernel: one CTA per SM walks the jobs blockIdx.x, +gridDim.x,
+// ...; every barrier phase is counted across jobs, the K/V rings run ahead
+// into the next job, and in the past-block mode the next job's Q rows are
+// gathered while the current job's partial outputs are written.
 template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
@@ -126,68 +201,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *gmisc = smem_raw + (misc - raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.g.H;
+    const int njobs = (MODE == kPast) ? __ldg(a.tile_off + a.n_lists) : a.n_jobs;
+    if ((int)blockIdx.x >= njobs) return;
 
-    // ---------------- the job ----------------
-    // rows: tile g holds job rows [g*128, g*128 + nrows_g); K/V tiles
-    // [0, nkv) start at token kv_tok0; tile g visits K/V tiles [tb[g], te[g]).
-    int h, seq0, L_len, r0 = 0, nrows = kRows, kv_tok0, kv_end, nkv;
-    int lbeg = 0, kv_lo = 0;
-    int tb[kG], te[kG];
-    if (MODE == kPast) {
-        const int job = blockIdx.x;
-        if (job >= __ldg(a.tile_off + a.n_lists)) return;
-        int lo = 0, hi = a.n_lists - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (__ldg(a.tile_off + mid) <= job) lo = mid; else hi = mid - 1;
-        }
-        const int Lid = lo;
-        const int gblk = Lid / H;
-        h = Lid % H;
-        const int b = upper_index(a.g.blk_base, a.g.num_seqs, gblk);
-        const int c = gblk - __ldg(a.g.blk_base + b);
-        seq0 = __ldg(a.g.cu + b);
-        L_len = __ldg(a.g.cu + b + 1) - seq0;
-        kv_tok0 = seq0 + c * a.g.bs;
-        kv_end = min(kv_tok0 + a.g.bs, seq0 + L_len);
-        lbeg = __ldg(a.list_off + Lid);
-        const int lcnt = __ldg(a.list_off + Lid + 1) - lbeg;
-        r0 = (job - __ldg(a.tile_off + Lid)) * kRows;
-        nrows = min(kRows, lcnt - r0);
-        lbeg += r0;
-        nkv = (kv_end - kv_tok0 + kN - 1) / kN;
-#pragma unroll
-        for (int g = 0; g < kG; ++g) {
-            tb[g] = 0;
-            te[g] = (nrows > g * kM) ? nkv : 0;
-        }
-    } else {
-        h = blockIdx.y;
-        const int b = blockIdx.z;
-        seq0 = __ldg(a.g.cu + b);
-        L_len = __ldg(a.g.cu + b + 1) - seq0;
-        r0 = (gridDim.x - 1 - blockIdx.x) * kRows;  // heavy (late) jobs first
-        if (r0 >= L_len) return;
-        nrows = min(kRows, L_len - r0);
-        const int bs = a.g.bs;
-        kv_lo = a.dense ? 0 : (r0 / bs) * bs;
-        kv_tok0 = seq0 + kv_lo;
-        kv_end = seq0 + r0 + nrows;
-        nkv = (kv_end - kv_tok0 + kN - 1) / kN;
-#pragma unroll
-        for (int g = 0; g < kG; ++g) {
-            const int first = r0 + g * kM, last = min(r0 + (g + 1) * kM, r0 + nrows) - 1;
-            if (last < first) {
-                tb[g] = te[g] = 0;
-                continue;
-            }
-            const int lo_key = a.dense ? 0 : (first / bs) * bs;
-            tb[g] = (lo_key - kv_lo) / kN;
-            te[g] = (last - kv_lo) / kN + 1;
-        }
-    }
-
-    // ---------------- set-up ----------------
+    // ---------------- set-up (once per CTA) ----------------
     const uint32_t sQ = base + L::kQ, sK = base + L::kK, sV = base + L::kV;
     auto bar = [&](int i) -> uint32_t { return misc + 8u * (uint32_t)i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gmisc + L::kNumBars * 8);
@@ -196,6 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         mbar_init(bar(L::kBarQ), MODE == kPast ? 4 * kG : 1);
+        mbar_init(bar(L::kBarQE), 1);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(L::kBarKF + s), 1);
             mbar_init(bar(L::kBarKE + s), 1);
@@ -228,28 +246,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane < 2) {
             const bool is_k = lane == 0;
             constexpr uint32_t kTileBytes = L::NB * L::kKVBox;
-            if (MODE == kCurrent && is_k) {
-                mbar_expect_tx(bar(L::kBarQ), kG * L::NB * L::kQBox);
-                for (int g = 0; g < kG; ++g)
-                    for (int x = 0; x < L::NB; ++x)
-                        tma_load_3d(sQ + (g * L::NB + x) * L::kQBox, &tmap_q, bar(L::kBarQ),
-                                    x * kBox, h, seq0 + r0 + g * kM);
-            }
             const int bfull = is_k ? L::kBarKF : L::kBarVF, bempty = is_k ? L::kBarKE : L::kBarVE;
             const uint32_t ring = is_k ? sK : sV;
             const CUtensorMap *map = is_k ? &tmap_k : &tmap_v;
-            int pend[kStages];  // tile whose copy is in flight per slot
+            int pend[kStages];  // tile (global count) whose copy is in flight per slot
             for (int s = 0; s < kStages; ++s) pend[s] = -1;
-            for (int j = 0; j < nkv; ++j) {
-                const int s = j % kStages, use = j / kStages;
-                if (j >= kStages && !wait_bar(bar(bempty + s), (use - 1) & 1, ctl)) break;
-                pend[s] = -1;
-                if (is_k && (a.debug_flags & 1) && j == 0) continue;  // fault-injection knob
-                mbar_expect_tx(bar(bfull + s), kTileBytes);
-                for (int x = 0; x < L::NB; ++x)
-                    tma_load_3d(ring + (s * L::NB + x) * L::kKVBox, map, bar(bfull + s), x * kBox,
-                                h, kv_tok0 + j * kN);
-                pend[s] = j;
+            int t = 0, qj = 0;  // K/V tiles and Q tiles loaded so far
+            bool go = true;
+            for (int job = blockIdx.x; go && job < njobs; job += gridDim.x) {
+                Job J;
+                if (!get_job<MODE>(a, job, J)) continue;
+                if (MODE == kCurrent && is_k) {
+                    // the previous job's S MMAs have read Q before it is replaced
+                    if (qj > 0 && !wait_bar(bar(L::kBarQE), (qj - 1) & 1, ctl)) break;
+                    mbar_expect_tx(bar(L::kBarQ), kG * L::NB * L::kQBox);
+                    for (int g = 0; g < kG; ++g)
+                        for (int x = 0; x < L::NB; ++x)
+                            tma_load_3d(sQ + (g * L::NB + x) * L::kQBox, &tmap_q, bar(L::kBarQ),
+                                        x * kBox, J.h, J.seq0 + J.r0 + g * kM);
+                    ++qj;
+                }
+                for (int j = 0; j < J.nkv; ++j, ++t) {
+                    const int s = t % kStages, use = t / kStages;
+                    if (t >= kStages && !wait_bar(bar(bempty + s), (use - 1) & 1, ctl)) {
+                        go = false;
+                        break;
+                    }
+                    pend[s] = -1;
+                    if (is_k && (a.debug_flags & 1) && t == 0) continue;  // fault-injection knob
+                    mbar_expect_tx(bar(bfull + s), kTileBytes);
+                    for (int x = 0; x < L::NB; ++x)
+                        tma_load_3d(ring + (s * L::NB + x) * L::kKVBox, map, bar(bfull + s),
+                                    x * kBox, J.h, J.kv_tok0 + j * kN);
+                    pend[s] = t;
+                }
             }
             if (*abort_flag) {
                 // let the copies still in flight land before the CTA exits
@@ -264,52 +294,72 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16(kM, kN, 0);
             constexpr uint32_t idesc_o = idesc_bf16(kM, D, 1);
-            bool ok = wait_bar(bar(L::kBarQ), 0, ctl);
-            for (int j = 0; ok && j <= nkv; ++j) {
-                const int s = j % kStages;
-                if (j < nkv) {
-                    if (!wait_bar(bar(L::kBarKF + s), (j / kStages) & 1, ctl)) break;
-                    tc_fence_after();
-                }
-                const int jp = j - 1, sp = (j + kStages - 1) % kStages;
-                if (jp >= 0 && !wait_bar(bar(L::kBarVF + sp), (jp / kStages) & 1, ctl)) break;
-                const uint32_t kb = sK + s * L::NB * L::kKVBox;
-                const uint32_t vb = sV + sp * L::NB * L::kKVBox;
-                bool stop = false;
-#pragma unroll
-                for (int g = 0; g < kG; ++g) {
-                    const uint32_t tS = tmem + g * 256, tO = tS + 128;
-                    if (jp >= tb[g] && jp < te[g]) {
-                        // O_g += P_g(jp) V(jp): P_g sits in the first 64 columns of S_g
-                        const int jl = jp - tb[g];
-                        if (!wait_bar(bar(L::kBarP + g), jl & 1, ctl)) {
-                            stop = true;
+            int t = 0, qj = 0;          // K/V tiles consumed, jobs started
+            int gt[kG] = {0, 0};        // per tile g: S/P tiles so far
+            bool ok = true;
+            for (int job = blockIdx.x; ok && job < njobs; job += gridDim.x) {
+                Job J;
+                if (!get_job<MODE>(a, job, J)) continue;
+                if (!wait_bar(bar(L::kBarQ), qj & 1, ctl)) break;
+                ++qj;
+                for (int j = 0; j <= J.nkv; ++j) {
+                    const int tk = t + j, s = tk % kStages;
+                    if (j < J.nkv) {
+                        if (!wait_bar(bar(L::kBarKF + s), (tk / kStages) & 1, ctl)) {
+                            ok = false;
                             break;
                         }
                         tc_fence_after();
-#pragma unroll
-                        for (int k = 0; k < kN / 16; ++k) {
-                            const uint64_t bd = sdesc(vb + k * 2048, L::kKVBox, 1024);
-                            tc_mma_ta(tO, tS + k * 8, bd, idesc_o, (jl > 0 || k > 0) ? 1u : 0u);
-                        }
-                        if (jp == te[g] - 1) tc_commit(bar(L::kBarPV + g));
                     }
-                    if (j < nkv && j >= tb[g] && j < te[g]) {
-                        // S_g(j) = Q_g K(j)^T (runs after the PV above: same thread, in order)
-                        const uint32_t qb = sQ + g * L::NB * L::kQBox;
-#pragma unroll
-                        for (int k = 0; k < D / 16; ++k) {
-                            const uint32_t off = (uint32_t)(k % 4) * 32;  // 16 dims = 32 B
-                            const uint64_t ad = sdesc(qb + (k / 4) * L::kQBox + off, 16, 1024);
-                            const uint64_t bd = sdesc(kb + (k / 4) * L::kKVBox + off, 16, 1024);
-                            tc_mma(tS, ad, bd, idesc_s, k > 0);
-                        }
-                        tc_commit(bar(L::kBarS + g));
+                    const int jp = j - 1, tp = tk - 1, sp = (tp + kStages) % kStages;
+                    if (jp >= 0 && !wait_bar(bar(L::kBarVF + sp), (tp / kStages) & 1, ctl)) {
+                        ok = false;
+                        break;
                     }
+                    const uint32_t kb = sK + s * L::NB * L::kKVBox;
+                    const uint32_t vb = sV + sp * L::NB * L::kKVBox;
+#pragma unroll
+                    for (int g = 0; g < kG; ++g) {
+                        const uint32_t tS = tmem + g * 256, tO = tS + 128;
+                        if (ok && jp >= J.tb[g] && jp < J.te[g]) {
+                            // O_g += P_g V: P_g sits in the first 64 columns of S_g
+                            const int jl = jp - J.tb[g];
+                            if (!wait_bar(bar(L::kBarP + g), (gt[g] + jl) & 1, ctl)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+#pragma unroll
+                            for (int k = 0; k < kN / 16; ++k) {
+                                const uint64_t bd = sdesc(vb + k * 2048, L::kKVBox, 1024);
+                                tc_mma_ta(tO, tS + k * 8, bd, idesc_o, (jl > 0 || k > 0) ? 1u : 0u);
+                            }
+                            if (jp == J.te[g] - 1) tc_commit(bar(L::kBarPV + g));
+                        }
+                        if (j < J.nkv && j >= J.tb[g] && j < J.te[g]) {
+                            // S_g = Q_g K^T (runs after the PV above: same thread, in order)
+                            const uint32_t qb = sQ + g * L::NB * L::kQBox;
+#pragma unroll
+                            for (int k = 0; k < D / 16; ++k) {
+                                const uint32_t off = (uint32_t)(k % 4) * 32;  // 16 dims = 32 B
+                                const uint64_t ad = sdesc(qb + (k / 4) * L::kQBox + off, 16, 1024);
+                                const uint64_t bd = sdesc(kb + (k / 4) * L::kKVBox + off, 16, 1024);
+                                tc_mma(tS, ad, bd, idesc_s, k > 0);
+                            }
+                            tc_commit(bar(L::kBarS + g));
+                        }
+                    }
+                    if (!ok) break;
+                    if (j < J.nkv) {
+                        // the job's last S: Q may be replaced once it completes
+                        if (MODE == kCurrent && j == J.nkv - 1) tc_commit(bar(L::kBarQE));
+                        tc_commit(bar(L::kBarKE + s));
+                    }
+                    if (jp >= 0) tc_commit(bar(L::kBarVE + sp));
                 }
-                if (stop) break;
-                if (j < nkv) tc_commit(bar(L::kBarKE + s));
-                if (jp >= 0) tc_commit(bar(L::kBarVE + sp));
+                t += J.nkv;
+#pragma unroll
+                for (int g = 0; g < kG; ++g) gt[g] += J.te[g] - J.tb[g];
             }
             // every MMA this thread issued has finished before TMEM is freed
             tc_commit(bar(L::kBarDrain));
@@ -326,71 +376,95 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tSg = tmem + lane_off + g * 256;
         const uint32_t tOg = tSg + 128;
         const uint32_t sQg = sQ + g * L::NB * L::kQBox;
-        int row_tok = -1, slot = 0;
-        const bool row_valid = jrow < nrows;
-        if (MODE == kPast) {
-            // gather this row of Q into the swizzled K-major tile
-            int e = 0;
-            if (row_valid) e = __ldg(a.list + lbeg + jrow);
-            row_tok = e >> kSlotBits;
-            slot = e & ((1 << kSlotBits) - 1);
-            const __nv_bfloat16 *src = a.q + ((size_t)row_tok * H + h) * D;
+        // past mode: gather job J's rows of Q for tile g (cp.async, zero rows
+        // past nrows); the arrival on q_full happens later
+        auto gather = [&](const Job &J) {
+            const bool valid = jrow < J.nrows;
+            const int e = valid ? __ldg(a.list + J.lbeg + jrow) : 0;
+            const __nv_bfloat16 *src = a.q + ((size_t)(e >> kSlotBits) * H + J.h) * D;
 #pragma unroll
             for (int ch = 0; ch < D / 8; ++ch) {
                 const uint32_t dst = sQg + (ch / 8) * L::kQBox + row * 128 +
                                      ((uint32_t)((ch % 8) ^ (row & 7)) << 4);
-                cp_async16(dst, row_valid ? (const void *)(src + ch * 8) : (const void *)a.q,
-                           row_valid);
+                cp_async16(dst, valid ? (const void *)(src + ch * 8) : (const void *)a.q, valid);
             }
+        };
+        auto q_ready = [&]() {
             cp_async_wait_all();
             fence_proxy_async();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(L::kBarQ));
-        } else {
-            row_tok = seq0 + r0 + jrow;
-            // warm L2 with this row's past partials; the merge reads them only
-            // after the last tile, so the fetch overlaps the attention loop
-            if (row_valid && !a.dense && a.km1 > 0) {
-                const int ci = (row_tok - seq0) / a.g.bs;
-                const size_t rowid = (size_t)row_tok * H + h;
-                const int32_t *sel = a.idx + rowid * a.topk;
-                for (int s2 = 0; s2 < a.km1; ++s2) {
-                    const int c = __ldg(sel + s2);
-                    if (c < 0 || c >= ci) break;
-                    const char *po = reinterpret_cast<const char *>(a.part_o + (rowid * a.km1 + s2) * D);
+        };
+        int gt = 0, gj = 0, qj = 0;  // S/P tiles of tile g, jobs with rows in tile g, jobs
+        bool ok = true;
+        int job = blockIdx.x;
+        Job J;
+        while (job < njobs && !get_job<MODE>(a, job, J)) job += gridDim.x;
+        if (MODE == kPast && job < njobs) {
+            gather(J);
+            q_ready();
+        }
+        while (ok && job < njobs) {
+            // past mode: this job's Q is in place before the next job may be
+            // gathered (the softmax warps drive q_full, so it cannot run ahead).
+            // Own-block mode: the softmax warps never read Q and do not wait
+            // on it -- the producer may already be two phases ahead.
+            if (MODE == kPast) {
+                if (!__all_sync(0xffffffffu, wait_bar(bar(L::kBarQ), qj & 1, ctl))) break;
+                ++qj;
+            }
+            const int seq0 = J.seq0, h = J.h;
+            const bool row_valid = jrow < J.nrows;
+            int row_tok = -1, slot = 0;
+            if (MODE == kPast) {
+                const int e = row_valid ? __ldg(a.list + J.lbeg + jrow) : 0;
+                row_tok = e >> kSlotBits;
+                slot = e & ((1 << kSlotBits) - 1);
+            } else {
+                row_tok = seq0 + J.r0 + jrow;
+                // warm L2 with this row's past partials; the merge reads them only
+                // after the last tile, so the fetch overlaps the attention loop
+                if (row_valid && !a.dense && a.km1 > 0) {
+                    const int ci = (row_tok - seq0) / a.g.bs;
+                    const size_t rowid = (size_t)row_tok * H + h;
+                    const int32_t *sel = a.idx + rowid * a.topk;
+                    for (int s2 = 0; s2 < a.km1; ++s2) {
+                        const int c = __ldg(sel + s2);
+                        if (c < 0 || c >= ci) break;
+                        const char *po = reinterpret_cast<const char *>(a.part_o + (rowid * a.km1 + s2) * D);
 #pragma unroll
-                    for (int ln = 0; ln < D * 2; ln += 128)
-                        asm volatile("prefetch.global.L2 [%0];" ::"l"(po + ln));
+                        for (int ln = 0; ln < D * 2; ln += 128)
+                            asm volatile("prefetch.global.L2 [%0];" ::"l"(po + ln));
+                    }
                 }
             }
-        }
-        const int i_loc = row_tok - seq0;  // position inside the sequence
-        const int rb = (MODE == kCurrent && !a.dense) ? (i_loc / a.g.bs) * a.g.bs : 0;
-        const int g_first = r0 + g * kM;
-        const int g_last = min(r0 + (g + 1) * kM, r0 + nrows) - 1;
-        const int rb_max = (MODE == kCurrent && !a.dense) ? (g_last / a.g.bs) * a.g.bs : 0;
-        const int my_tb = (g == 0) ? tb[0] : tb[kG - 1];
-        const int ntile = ((g == 0) ? te[0] : te[kG - 1]) - my_tb;
+            const int i_loc = row_tok - seq0;  // position inside the sequence
+            const int rb = (MODE == kCurrent && !a.dense) ? (i_loc / a.g.bs) * a.g.bs : 0;
+            const int g_first = J.r0 + g * kM;
+            const int g_last = min(J.r0 + (g + 1) * kM, J.r0 + J.nrows) - 1;
+            const int rb_max = (MODE == kCurrent && !a.dense) ? (g_last / a.g.bs) * a.g.bs : 0;
+            const int my_tb = (g == 0) ? J.tb[0] : J.tb[kG - 1];
+            const int ntile = ((g == 0) ? J.te[0] : J.te[kG - 1]) - my_tb;
+            const int kv_lo = J.kv_lo, kv_tok0 = J.kv_tok0, kv_end = J.kv_end;
 
-        float m_run = -INFINITY, l_run = 0.f;
-        bool ok = true;
-        for (int jl = 0; jl < ntile; ++jl) {
-            const int j = my_tb + jl;
-            // S_g(j) is ready; the commit behind it also covers PV_g(j-1), so
-            // O_g is stable and P_g's columns are free
-            if (!__all_sync(0xffffffffu, wait_bar(bar(L::kBarS + g), jl & 1, ctl))) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const int key0 = kv_lo + j * kN;  // sequence-local position of column 0
-            const bool need_mask =
-                (MODE == kPast) ? (kv_tok0 + (j + 1) * kN > kv_end)
-                                : (key0 + kN - 1 > g_first || key0 < rb_max ||
-                                   seq0 + key0 + kN > kv_end);
-            // masked columns are set to -inf (raw fp32 bits) in place; only the
-            // tiles on the diagonal / at the end of a block need it
-            const int kt0 = kv_tok0 + j * kN;  // token of column 0
+            float m_run = -INFINITY, l_run = 0.f;
+            for (int jl = 0; jl < ntile; ++jl) {
+                const int j = my_tb + jl;
+                // S_g(j) is ready; the commit behind it also covers PV_g(j-1), so
+                // O_g is stable and P_g's columns are free
+                if (!__all_sync(0xffffffffu, wait_bar(bar(L::kBarS + g), (gt + jl) & 1, ctl))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int key0 = kv_lo + j * kN;  // sequence-local position of column 0
+                const bool need_mask =
+                    (MODE == kPast) ? (kv_tok0 + (j + 1) * kN > kv_end)
+                                    : (key0 + kN - 1 > g_first || key0 < rb_max ||
+                                       seq0 + key0 + kN > kv_end);
+                // masked columns are set to -inf (raw fp32 bits) in place; only the
+                // tiles on the diagonal / at the end of a block need it
+                const int kt0 = kv_tok0 + j * kN;  // token of column 0
 #define MOBA_MASK64(SR, BASE)                                                         \
     if (need_mask) {                                                                  \
         _Pragma("unroll") for (int c = 0; c < 64; ++c) {                              \
@@ -400,184 +474,202 @@ __global__ void __launch_bounds__(kThreads, 1)
                 SR[c >> 5][c & 31] = 0xff800000u;                                     \
         }                                                                             \
     }
-            // pass 1: row max of the raw scores (the scale is positive)
-            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                // pass 1: row max of the raw scores (the scale is positive)
+                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                uint32_t sr[2][32];
-                tc_ld32(tSg + 64 * h2, sr[0]);
-                tc_ld32(tSg + 64 * h2 + 32, sr[1]);
-                tc_wait_ld();
-                MOBA_MASK64(sr, 64 * h2)
-#pragma unroll
-                for (int c = 0; c < 64; ++c)
-                    mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(sr[c >> 5][c & 31]));
-            }
-            const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
-            const float m_new = fmaxf(m_run, mt);
-            // rescale only when the max grew by more than 2^8 (P stays <= 256)
-            const bool need = (jl > 0) && (m_new > m_run + 8.f);
-            const float m_use = (jl == 0 || need) ? m_new : m_run;
-            const float mu = (m_use == -INFINITY) ? 0.f : m_use;
-            if (jl > 0 && __any_sync(0xffffffffu, need)) {
-                const float alpha = need ? fast_exp2(m_run - m_new) : 1.f;
-#pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 16) {
-                    uint32_t o[16];
-                    tc_ld16(tOg + c0, o);
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    uint32_t sr[2][32];
+                    tc_ld32(tSg + 64 * h2, sr[0]);
+                    tc_ld32(tSg + 64 * h2 + 32, sr[1]);
                     tc_wait_ld();
+                    MOBA_MASK64(sr, 64 * h2)
 #pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-                    tc_st16(tOg + c0, o);
+                    for (int c = 0; c < 64; ++c)
+                        mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(sr[c >> 5][c & 31]));
                 }
-                if (need) l_run *= alpha;
-            }
-            m_run = m_use;
-            // pass 2: p = 2^(s * scale - mu) as bf16 pairs (keys 2c, 2c+1 in
-            // column c) over the first 64 columns of S; half h2 of the keys goes
-            // to columns 32*h2 .. 32*h2+31, already read when h2 = 1 is written
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+                const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
+                const float m_new = fmaxf(m_run, mt);
+                // rescale only when the max grew by more than 2^8 (P stays <= 256)
+                const bool need = (jl > 0) && (m_new > m_run + 8.f);
+                const float m_use = (jl == 0 || need) ? m_new : m_run;
+                const float mu = (m_use == -INFINITY) ? 0.f : m_use;
+                if (jl > 0 && __any_sync(0xffffffffu, need)) {
+                    const float alpha = need ? fast_exp2(m_run - m_new) : 1.f;
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                uint32_t sr[2][32];
-                tc_ld32(tSg + 64 * h2, sr[0]);
-                tc_ld32(tSg + 64 * h2 + 32, sr[1]);
-                tc_wait_ld();
-                MOBA_MASK64(sr, 64 * h2)
-                uint32_t pk[32];
+                    for (int c0 = 0; c0 < D; c0 += 16) {
+                        uint32_t o[16];
+                        tc_ld16(tOg + c0, o);
+                        tc_wait_ld();
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    const float p0 = fast_exp2(fmaf(__uint_as_float(sr[(2 * c) >> 5][(2 * c) & 31]), a.scale_log2, -mu));
-                    const float p1 = fast_exp2(fmaf(__uint_as_float(sr[(2 * c + 1) >> 5][(2 * c + 1) & 31]), a.scale_log2, -mu));
-                    ls[c & 3] += p0 + p1;
-                    __nv_bfloat162 bb = __floats2bfloat162_rn(p0, p1);
-                    pk[c] = *reinterpret_cast<uint32_t *>(&bb);
+                        for (int c = 0; c < 16; ++c)
+                            o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                        tc_st16(tOg + c0, o);
+                    }
+                    if (need) l_run *= alpha;
                 }
-                tc_st32(tSg + 32 * h2, pk);
-            }
+                m_run = m_use;
+                // pass 2: p = 2^(s * scale - mu) as bf16 pairs (keys 2c, 2c+1 in
+                // column c) over the first 64 columns of S; half h2 of the keys goes
+                // to columns 32*h2 .. 32*h2+31, already read when h2 = 1 is written
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    uint32_t sr[2][32];
+                    tc_ld32(tSg + 64 * h2, sr[0]);
+                    tc_ld32(tSg + 64 * h2 + 32, sr[1]);
+                    tc_wait_ld();
+                    MOBA_MASK64(sr, 64 * h2)
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        const float p0 = fast_exp2(fmaf(__uint_as_float(sr[(2 * c) >> 5][(2 * c) & 31]), a.scale_log2, -mu));
+                        const float p1 = fast_exp2(fmaf(__uint_as_float(sr[(2 * c + 1) >> 5][(2 * c + 1) & 31]), a.scale_log2, -mu));
+                        ls[c & 3] += p0 + p1;
+                        __nv_bfloat162 bb = __floats2bfloat162_rn(p0, p1);
+                        pk[c] = *reinterpret_cast<uint32_t *>(&bb);
+                    }
+                    tc_st32(tSg + 32 * h2, pk);
+                }
 #undef MOBA_MASK64
-            const float lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            l_run += lsum;
-            tc_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::kBarP + g));
-        }
-        // ---------------- epilogue ----------------
-        if (ok && ntile > 0)
-            ok = __all_sync(0xffffffffu, wait_bar(bar(L::kBarPV + g), 0, ctl));
-        tc_fence_after();
-        if (ok && ntile > 0) {
-            const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
-            const float lse2 = m_run + __log2f(l_run);
-            if (MODE == kPast) {
-                const size_t pslot = ((size_t)row_tok * H + h) * a.km1 + slot;
-                __nv_bfloat16 *dst = a.part_o + pslot * D;
-#pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    uint32_t o[32];
-                    tc_ld32(tOg + c0, o);
-                    tc_wait_ld();
-                    if (row_valid) {
-#pragma unroll
-                        for (int c = 0; c < 32; c += 8) {
-                            uint4 pkd;
-                            uint32_t *pw = reinterpret_cast<uint32_t *>(&pkd);
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                __nv_bfloat162 bb =
-                                    __floats2bfloat162_rn(__uint_as_float(o[c + 2 * e]) * inv,
-                                                          __uint_as_float(o[c + 2 * e + 1]) * inv);
-                                pw[e] = *reinterpret_cast<uint32_t *>(&bb);
-                            }
-                            *reinterpret_cast<uint4 *>(dst + c0 + c) = pkd;
-                        }
-                    }
+                l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                tc_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(L::kBarP + g));
+            }
+            if (!ok) break;
+            gt += ntile;
+            // the next job; in past mode its Q rows are gathered now (this tile's
+            // S MMAs are done) and land while this job's epilogue runs
+            int njob = job + gridDim.x;
+            Job NJ;
+            while (njob < njobs && !get_job<MODE>(a, njob, NJ)) njob += gridDim.x;
+            if (MODE == kPast && njob < njobs) gather(NJ);
+
+            // ---------------- epilogue ----------------
+            if (ntile > 0) {
+                if (!__all_sync(0xffffffffu, wait_bar(bar(L::kBarPV + g), gj & 1, ctl))) {
+                    ok = false;
+                    break;
                 }
-                if (row_valid) a.part_lse[pslot] = lse2;
-            } else {
-                // log-sum-exp merge with the row's past partials (ascending blocks)
-                float w_cur = 1.f, wsum = 1.f, mmax = lse2;
-                int np = 0;
-                const size_t rowid = (size_t)row_tok * H + h;
-                if (row_valid && !a.dense && a.km1 > 0) {
-                    const int ci = i_loc / a.g.bs;
-                    const int32_t *sel = a.idx + rowid * a.topk;
-                    for (; np < a.km1; ++np) {
-                        const int c = __ldg(sel + np);
-                        if (c < 0 || c >= ci) break;
-                        mmax = fmaxf(mmax, __ldg(a.part_lse + rowid * a.km1 + np));
-                    }
-                    if (np > 0) {
-                        w_cur = fast_exp2(lse2 - mmax);
-                        wsum = w_cur;
-                        for (int s = 0; s < np; ++s)
-                            wsum += fast_exp2(__ldg(a.part_lse + rowid * a.km1 + s) - mmax);
-                    }
-                }
-                const float iw = 1.f / wsum;
-                const float fcur = w_cur * inv * iw;
-                __nv_bfloat16 *dst = a.out + rowid * D;
+                ++gj;
+                tc_fence_after();
+                const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+                const float lse2 = m_run + __log2f(l_run);
+                if (MODE == kPast) {
+                    const size_t pslot = ((size_t)row_tok * H + h) * a.km1 + slot;
+                    __nv_bfloat16 *dst = a.part_o + pslot * D;
 #pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 64) {
-                    // 64 columns of O from TMEM in one go, then the partials'
-                    // loads of those columns all in flight together
-                    uint32_t o[2][32];
-                    tc_ld32(tOg + c0, o[0]);
-                    tc_ld32(tOg + c0 + 32, o[1]);
-                    tc_wait_ld();
-                    if (row_valid) {
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t o[32];
+                        tc_ld32(tOg + c0, o);
+                        tc_wait_ld();
+                        if (row_valid) {
 #pragma unroll
-                        for (int c = 0; c < 64; ++c)
-                            o[c >> 5][c & 31] = __float_as_uint(__uint_as_float(o[c >> 5][c & 31]) * fcur);
-                        for (int s = 0; s < np; ++s) {
-                            const size_t ps = rowid * a.km1 + s;
-                            const float w = fast_exp2(__ldg(a.part_lse + ps) - mmax) * iw;
-                            const uint4 *src =
-                                reinterpret_cast<const uint4 *>(a.part_o + ps * D + c0);
-                            uint4 f[8];
-#pragma unroll
-                            for (int c = 0; c < 8; ++c) f[c] = __ldg(src + c);
-#pragma unroll
-                            for (int c = 0; c < 8; ++c) {
-                                const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&f[c]);
+                            for (int c = 0; c < 32; c += 8) {
+                                uint4 pkd;
+                                uint32_t *pw = reinterpret_cast<uint32_t *>(&pkd);
 #pragma unroll
                                 for (int e = 0; e < 4; ++e) {
-                                    const float2 fv = __bfloat1622float2(b2[e]);
-                                    const int col = 8 * c + 2 * e;
-                                    o[col >> 5][col & 31] = __float_as_uint(
-                                        fmaf(w, fv.x, __uint_as_float(o[col >> 5][col & 31])));
-                                    o[(col + 1) >> 5][(col + 1) & 31] = __float_as_uint(
-                                        fmaf(w, fv.y, __uint_as_float(o[(col + 1) >> 5][(col + 1) & 31])));
+                                    __nv_bfloat162 bb =
+                                        __floats2bfloat162_rn(__uint_as_float(o[c + 2 * e]) * inv,
+                                                              __uint_as_float(o[c + 2 * e + 1]) * inv);
+                                    pw[e] = *reinterpret_cast<uint32_t *>(&bb);
                                 }
+                                *reinterpret_cast<uint4 *>(dst + c0 + c) = pkd;
                             }
-                        }
-#pragma unroll
-                        for (int c = 0; c < 64; c += 8) {
-                            uint4 pkd;
-                            uint32_t *pw = reinterpret_cast<uint32_t *>(&pkd);
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int col = c + 2 * e;
-                                __nv_bfloat162 bb = __floats2bfloat162_rn(
-                                    __uint_as_float(o[col >> 5][col & 31]),
-                                    __uint_as_float(o[(col + 1) >> 5][(col + 1) & 31]));
-                                pw[e] = *reinterpret_cast<uint32_t *>(&bb);
-                            }
-                            *reinterpret_cast<uint4 *>(dst + c0 + c) = pkd;
                         }
                     }
+                    if (row_valid) a.part_lse[pslot] = lse2;
+                } else {
+                    // log-sum-exp merge with the row's past partials (ascending blocks)
+                    float w_cur = 1.f, wsum = 1.f, mmax = lse2;
+                    int np = 0;
+                    const size_t rowid = (size_t)row_tok * H + h;
+                    if (row_valid && !a.dense && a.km1 > 0) {
+                        const int ci = i_loc / a.g.bs;
+                        const int32_t *sel = a.idx + rowid * a.topk;
+                        for (; np < a.km1; ++np) {
+                            const int c = __ldg(sel + np);
+                            if (c < 0 || c >= ci) break;
+                            mmax = fmaxf(mmax, __ldg(a.part_lse + rowid * a.km1 + np));
+                        }
+                        if (np > 0) {
+                            w_cur = fast_exp2(lse2 - mmax);
+                            wsum = w_cur;
+                            for (int s2 = 0; s2 < np; ++s2)
+                                wsum += fast_exp2(__ldg(a.part_lse + rowid * a.km1 + s2) - mmax);
+                        }
+                    }
+                    const float iw = 1.f / wsum;
+                    const float fcur = w_cur * inv * iw;
+                    __nv_bfloat16 *dst = a.out + rowid * D;
+#pragma unroll
+                    for (int c0 = 0; c0 < D; c0 += 64) {
+                        // 64 columns of O from TMEM in one go, then the partials'
+                        // loads of those columns all in flight together
+                        uint32_t o[2][32];
+                        tc_ld32(tOg + c0, o[0]);
+                        tc_ld32(tOg + c0 + 32, o[1]);
+                        tc_wait_ld();
+                        if (row_valid) {
+#pragma unroll
+                            for (int c = 0; c < 64; ++c)
+                                o[c >> 5][c & 31] = __float_as_uint(__uint_as_float(o[c >> 5][c & 31]) * fcur);
+                            for (int s2 = 0; s2 < np; ++s2) {
+                                const size_t ps = rowid * a.km1 + s2;
+                                const float w = fast_exp2(__ldg(a.part_lse + ps) - mmax) * iw;
+                                const uint4 *src =
+                                    reinterpret_cast<const uint4 *>(a.part_o + ps * D + c0);
+                                uint4 f[8];
+#pragma unroll
+                                for (int c = 0; c < 8; ++c) f[c] = __ldg(src + c);
+#pragma unroll
+                                for (int c = 0; c < 8; ++c) {
+                                    const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&f[c]);
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        const float2 fv = __bfloat1622float2(b2[e]);
+                                        const int col = 8 * c + 2 * e;
+                                        o[col >> 5][col & 31] = __float_as_uint(
+                                            fmaf(w, fv.x, __uint_as_float(o[col >> 5][col & 31])));
+                                        o[(col + 1) >> 5][(col + 1) & 31] = __float_as_uint(
+                                            fmaf(w, fv.y, __uint_as_float(o[(col + 1) >> 5][(col + 1) & 31])));
+                                    }
+                                }
+                            }
+#pragma unroll
+                            for (int c = 0; c < 64; c += 8) {
+                                uint4 pkd;
+                                uint32_t *pw = reinterpret_cast<uint32_t *>(&pkd);
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const int col = c + 2 * e;
+                                    __nv_bfloat162 bb = __floats2bfloat162_rn(
+                                        __uint_as_float(o[col >> 5][col & 31]),
+                                        __uint_as_float(o[(col + 1) >> 5][(col + 1) & 31]));
+                                    pw[e] = *reinterpret_cast<uint32_t *>(&bb);
+                                }
+                                *reinterpret_cast<uint4 *>(dst + c0 + c) = pkd;
+                            }
+                        }
+                    }
+                    if (row_valid) {
+                        const float lse_out = (np > 0) ? mmax + __log2f(wsum) : lse2;
+                        const size_t li = a.fixed
+                                              ? ((size_t)J.b * H + h) * a.S_fixed + i_loc
+                                              : (size_t)h * a.g.total + row_tok;
+                        a.lse[li] = lse_out * 0.69314718055994530942f;
+                    }
                 }
-                if (row_valid) {
-                    const float lse_out = (np > 0) ? mmax + __log2f(wsum) : lse2;
-                    const size_t li = a.fixed
-                                          ? ((size_t)blockIdx.z * H + h) * a.S_fixed + i_loc
-                                          : (size_t)h * a.g.total + row_tok;
-                    a.lse[li] = lse_out * 0.69314718055994530942f;
-                }
+                // O_g has been read: the next job's first PV may overwrite it
+                tc_fence_before();
             }
+            if (MODE == kPast && njob < njobs) q_ready();
+            job = njob;
+            J = NJ;
         }
+        if (!ok) cp_async_wait_all();  // no copy of ours may land after the exit
     }
     tc_fence_before();
     __syncthreads();
@@ -628,6 +720,19 @@ bool make_tma_3d(CUtensorMap *m, const void *ptr, int total, int H, int D, int r
 }
 
 static long long g_wait_limit = 4000000000ll;  // ~2 s at 2 GHz
+
+static int sm_count_tc() {
+    static int cached[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (!cached[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = n > 0 ? n : 1;
+    }
+    return cached[dev];
+}
 static int g_debug_flags = 0;
 
 void tc_debug_set(int flags, long long wait_limit) {
@@ -661,6 +766,8 @@ static tc::Args make_tc_args(const Plan &p, const Workspace &ws, const __nv_bflo
     a.list_off = ws.list_off;
     a.tile_off = ws.tile_off;
     a.n_lists = p.NBcap * p.H;
+    a.n_rtiles = (p.max_len + tc::kRows - 1) / tc::kRows;
+    a.n_jobs = a.n_rtiles * p.num_seqs * p.H;
     a.part_o = ws.part_o;
     a.part_lse = ws.part_lse;
     a.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)p.D));
@@ -693,15 +800,10 @@ static cudaError_t launch_tc(const Plan &p, const tc::Args &a, const __nv_bfloat
     if (chk < 0) return cudaErrorInvalidConfiguration;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    dim3 grid;
-    if (MODE == tc::kPast) {
-        // an upper bound of the tiles; CTAs past the real count exit at once
-        const long long rows = (long long)p.total * p.H * p.km1;
-        const long long tiles = rows / tc::kRows + (long long)p.NBcap * p.H + 1;
-        grid = dim3((unsigned)tiles);
-    } else {
-        grid = dim3((p.max_len + tc::kRows - 1) / tc::kRows, p.H, p.num_seqs);
-    }
+    // persistent: one CTA per SM (fewer when there are fewer own-block jobs)
+    int ctas = sm_count_tc();
+    if (MODE == tc::kCurrent && a.n_jobs < ctas) ctas = a.n_jobs;
+    const dim3 grid(ctas > 0 ? ctas : 1);
     kern<<<grid, tc::kThreads, smem, st>>>(mq, mk, mv, a);
     note_launches(1);
     return cudaGetLastError();

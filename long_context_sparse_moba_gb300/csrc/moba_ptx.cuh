@@ -170,7 +170,13 @@ static __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, cons
         if (*c.abort) return false;
         if (clock64() - t0 > c.limit) {
             *c.abort = 1;
-            atomicExch(c.status, (int)MOBA_ERR_TIMEOUT);
+            if (atomicExch(c.status, (int)MOBA_ERR_TIMEOUT) == 0) {
+                // first timeout of this device: which wait gave up
+                c.status[1] = (int)(bar & 0xffff);
+                c.status[2] = (int)parity;
+                c.status[3] = (int)blockIdx.x;
+                c.status[4] = (int)threadIdx.x;
+            }
             return false;
         }
     }

@@ -49,6 +49,7 @@ _SIGNATURES = {
     "moba_attn_fwd_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "moba_attn_fwd_noalloc_capacity": (_SZ, []),
     "moba_debug_set": (_I, [_I, ctypes.c_longlong]),
+    "moba_debug_timeout_info": (None, [_P]),
 }
 
 PHASES = ("tables", "kpool", "gate", "regroup", "attn_past", "attn_current")
@@ -276,3 +277,10 @@ GATE_CUDA_CORES = 1
 def set_gate_kernel(kind: int):
     """0: tensor-core scores + exact re-score of candidates (default); 1: CUDA cores."""
     _check(lib().moba_set_gate_kernel(int(kind)), "moba_set_gate_kernel")
+
+
+def debug_timeout_info():
+    """(barrier address, parity, block, thread) of the last reported timeout."""
+    buf = (ctypes.c_int * 4)()
+    lib().moba_debug_timeout_info(ctypes.cast(buf, ctypes.c_void_p))
+    return tuple(buf)
