@@ -85,6 +85,8 @@ size_t workspace_bytes(const Plan &p, Workspace *ws, char *base) {
         w.counts = static_cast<int *>(take(sizeof(int) * N));
         w.list_off = static_cast<int *>(take(sizeof(int) * (N + 1)));
         w.tile_off = static_cast<int *>(take(sizeof(int) * (N + 1)));
+        w.job_list = static_cast<int *>(
+            take(sizeof(int) * (rows * p.km1 / (size_t)past_tile_rows() + N + 1)));
         w.ticket = static_cast<int *>(take(sizeof(int) * rows * p.km1));
         w.kbhi = static_cast<__nv_bfloat16 *>(take(sizeof(__nv_bfloat16) * N * p.D));
         w.kblo = static_cast<__nv_bfloat16 *>(take(sizeof(__nv_bfloat16) * N * p.D));

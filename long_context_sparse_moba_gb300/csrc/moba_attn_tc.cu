@@ -75,7 +75,7 @@ struct Args {
     float *lse;
     int topk, km1, dense, fixed, S_fixed;
     const int32_t *idx;
-    const int *list, *list_off, *tile_off;
+    const int *list, *list_off, *tile_off, *job_list;
     int n_lists;
     int n_jobs, n_rtiles;   // own-block mode: jobs = n_rtiles x num_seqs x H
     __nv_bfloat16 *part_o;  // partial outputs, bf16
@@ -126,12 +126,7 @@ template <int MODE>
 __device__ __forceinline__ bool get_job(const Args &a, int job, Job &J) {
     const int H = a.g.H;
     if (MODE == kPast) {
-        int lo = 0, hi = a.n_lists - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (__ldg(a.tile_off + mid) <= job) lo = mid; else hi = mid - 1;
-        }
-        const int Lid = lo;
+        const int Lid = __ldg(a.job_list + job);
         const int gblk = Lid / H;
         J.h = Lid % H;
         J.b = upper_index(a.g.blk_base, a.g.num_seqs, gblk);
@@ -253,9 +248,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < kStages; ++s) pend[s] = -1;
             int t = 0, qj = 0;  // K/V tiles and Q tiles loaded so far
             bool go = true;
-            for (int job = blockIdx.x; go && job < njobs; job += gridDim.x) {
-                Job J;
-                if (!get_job<MODE>(a, job, J)) continue;
+            int job = blockIdx.x;
+            Job J;
+            while (job < njobs && !get_job<MODE>(a, job, J)) job += gridDim.x;
+            while (go && job < njobs) {
+                // the next job's descriptor is fetched one job ahead
+                int njob = job + gridDim.x;
+                Job NJ;
+                while (njob < njobs && !get_job<MODE>(a, njob, NJ)) njob += gridDim.x;
                 if (MODE == kCurrent && is_k) {
                     // the previous job's S MMAs have read Q before it is replaced
                     if (qj > 0 && !wait_bar(bar(L::kBarQE), (qj - 1) & 1, ctl)) break;
@@ -280,6 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     x * kBox, J.h, J.kv_tok0 + j * kN);
                     pend[s] = t;
                 }
+                job = njob;
+                J = NJ;
             }
             if (*abort_flag) {
                 // let the copies still in flight land before the CTA exits
@@ -297,9 +299,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             int t = 0, qj = 0;          // K/V tiles consumed, jobs started
             int gt[kG] = {0, 0};        // per tile g: S/P tiles so far
             bool ok = true;
-            for (int job = blockIdx.x; ok && job < njobs; job += gridDim.x) {
-                Job J;
-                if (!get_job<MODE>(a, job, J)) continue;
+            int job = blockIdx.x;
+            Job J;
+            while (job < njobs && !get_job<MODE>(a, job, J)) job += gridDim.x;
+            while (ok && job < njobs) {
+                int njob = job + gridDim.x;  // next descriptor, fetched one job ahead
+                Job NJ;
+                while (njob < njobs && !get_job<MODE>(a, njob, NJ)) njob += gridDim.x;
                 if (!wait_bar(bar(L::kBarQ), qj & 1, ctl)) break;
                 ++qj;
                 for (int j = 0; j <= J.nkv; ++j) {
@@ -360,6 +366,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 t += J.nkv;
 #pragma unroll
                 for (int g = 0; g < kG; ++g) gt[g] += J.te[g] - J.tb[g];
+                job = njob;
+                J = NJ;
             }
             // every MMA this thread issued has finished before TMEM is freed
             tc_commit(bar(L::kBarDrain));
@@ -378,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sQg = sQ + g * L::NB * L::kQBox;
         // past mode: gather job J's rows of Q for tile g (cp.async, zero rows
         // past nrows); the arrival on q_full happens later
-        auto gather = [&](const Job &J) {
+        auto gather = [&](const Job &J) -> int {
             const bool valid = jrow < J.nrows;
             const int e = valid ? __ldg(a.list + J.lbeg + jrow) : 0;
             const __nv_bfloat16 *src = a.q + ((size_t)(e >> kSlotBits) * H + J.h) * D;
@@ -388,6 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      ((uint32_t)((ch % 8) ^ (row & 7)) << 4);
                 cp_async16(dst, valid ? (const void *)(src + ch * 8) : (const void *)a.q, valid);
             }
+            return e;
         };
         auto q_ready = [&]() {
             cp_async_wait_all();
@@ -400,11 +409,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         int job = blockIdx.x;
         Job J;
         while (job < njobs && !get_job<MODE>(a, job, J)) job += gridDim.x;
+        int entry = 0;  // this row's regroup entry (token << 5 | slot), past mode
         if (MODE == kPast && job < njobs) {
-            gather(J);
+            entry = gather(J);
             q_ready();
         }
         while (ok && job < njobs) {
+            // the next job's descriptor, fetched one job ahead
+            int njob = job + gridDim.x;
+            Job NJ;
+            while (njob < njobs && !get_job<MODE>(a, njob, NJ)) njob += gridDim.x;
             // past mode: this job's Q is in place before the next job may be
             // gathered (the softmax warps drive q_full, so it cannot run ahead).
             // Own-block mode: the softmax warps never read Q and do not wait
@@ -417,9 +431,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool row_valid = jrow < J.nrows;
             int row_tok = -1, slot = 0;
             if (MODE == kPast) {
-                const int e = row_valid ? __ldg(a.list + J.lbeg + jrow) : 0;
-                row_tok = e >> kSlotBits;
-                slot = e & ((1 << kSlotBits) - 1);
+                row_tok = entry >> kSlotBits;
+                slot = entry & ((1 << kSlotBits) - 1);
             } else {
                 row_tok = seq0 + J.r0 + jrow;
                 // warm L2 with this row's past partials; the merge reads them only
@@ -539,12 +552,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
             gt += ntile;
-            // the next job; in past mode its Q rows are gathered now (this tile's
+            // in past mode the next job's Q rows are gathered now (this tile's
             // S MMAs are done) and land while this job's epilogue runs
-            int njob = job + gridDim.x;
-            Job NJ;
-            while (njob < njobs && !get_job<MODE>(a, njob, NJ)) njob += gridDim.x;
-            if (MODE == kPast && njob < njobs) gather(NJ);
+            int next_entry = 0;
+            if (MODE == kPast && njob < njobs) next_entry = gather(NJ);
 
             // ---------------- epilogue ----------------
             if (ntile > 0) {
@@ -668,6 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (MODE == kPast && njob < njobs) q_ready();
             job = njob;
             J = NJ;
+            entry = next_entry;
         }
         if (!ok) cp_async_wait_all();  // no copy of ours may land after the exit
     }
@@ -765,6 +777,7 @@ static tc::Args make_tc_args(const Plan &p, const Workspace &ws, const __nv_bflo
     a.list = ws.list;
     a.list_off = ws.list_off;
     a.tile_off = ws.tile_off;
+    a.job_list = ws.job_list;
     a.n_lists = p.NBcap * p.H;
     a.n_rtiles = (p.max_len + tc::kRows - 1) / tc::kRows;
     a.n_jobs = a.n_rtiles * p.num_seqs * p.H;

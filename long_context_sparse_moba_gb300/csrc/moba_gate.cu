@@ -457,12 +457,18 @@ cudaError_t launch_gate(const Plan &p, const Workspace &ws, const __nv_bfloat16 
 // which rows share its attention tile, so outputs stay deterministic.
 // ---------------------------------------------------------------------------
 __global__ void regroup_scan_kernel(const int *__restrict__ counts, int N, int tile_m,
-                                    int *__restrict__ list_off, int *__restrict__ tile_off) {
+                                    int *__restrict__ list_off, int *__restrict__ tile_off,
+                                    int *__restrict__ job_list) {
     cta_exclusive_scan(
         N, [&](int i) { return counts[i]; }, [&](int i, int v) { list_off[i] = v; });
     cta_exclusive_scan(
         N, [&](int i) { return (counts[i] + tile_m - 1) / tile_m; },
-        [&](int i, int v) { tile_off[i] = v; });
+        [&](int i, int v) {
+            tile_off[i] = v;
+            if (i < N)  // the attention jobs of list i
+                for (int t = 0, nt = (counts[i] + tile_m - 1) / tile_m; t < nt; ++t)
+                    job_list[v + t] = i;
+        });
 }
 
 __global__ void regroup_scatter_kernel(Geometry g, const int32_t *__restrict__ idx,
@@ -487,7 +493,7 @@ __global__ void regroup_scatter_kernel(Geometry g, const int32_t *__restrict__ i
 cudaError_t launch_regroup(const Plan &p, const Workspace &ws, cudaStream_t st) {
     const int N = p.NBcap * p.H;
     regroup_scan_kernel<<<1, 1024, 0, st>>>(ws.counts, N, past_tile_rows(), ws.list_off,
-                                            ws.tile_off);
+                                            ws.tile_off, ws.job_list);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const size_t rows = (size_t)p.total * p.H;

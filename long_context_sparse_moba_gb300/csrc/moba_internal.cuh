@@ -50,7 +50,8 @@ struct Workspace {
     int32_t *idx;     // [total][H][topk]
     int *counts;      // [NBcap * H]   queries per (block, head) past list
     int *list_off;    // [NBcap * H + 1]
-    int *tile_off;    // [NBcap * H + 1]
+    int *tile_off;    // [NBcap * H + 1]  first attention job of each list
+    int *job_list;    // [jobs]  list of every past-block attention job
     int *ticket;      // [total * H * km1]  position of a selection inside its list
     __nv_bfloat16 *kbhi, *kblo;  // [NBcap][H][D] bf16 split of kbar (tensor-core gate)
     float *knorm;                // [NBcap][H] L2 norm of each pooled key
