@@ -98,19 +98,26 @@ struct Smem {
     static constexpr uint32_t kK = kQ + kG * NB * kQBox;      // [stage][box]
     static constexpr uint32_t kV = kK + kStages * NB * kKVBox;
     static constexpr uint32_t kTiles = kV + kStages * NB * kKVBox;  // end of the tiles
-    // mbarriers: q_full, q_empty, k_full[2], k_empty[2], v_full[2], v_empty[2],
-    // s_full[g], p_full[g], pv_done[g], drain; then the TMEM address slot and
-    // the abort flag
-    static constexpr int kBarQ = 0, kBarQE = 1, kBarKF = 2, kBarKE = kBarKF + kStages,
+    // 4 KB per softmax warp where its 32 rows are re-laid so that global
+    // reads and writes of whole rows go out as full 128-byte lines
+    static constexpr uint32_t kStageWarp = 4096;
+    static constexpr uint32_t kStage = kTiles;
+    static constexpr uint32_t kEnd = kStage + 4 * kG * kStageWarp;
+    // mbarriers: q_full[g], q_empty[g], k_full[2], k_empty[2], v_full[2],
+    // v_empty[2], s_full[g], p_full[g], pv_done[g], drain; then the TMEM
+    // address slot and the abort flag
+    static constexpr int kBarQ = 0, kBarQE = kBarQ + kG, kBarKF = kBarQE + kG,
+                         kBarKE = kBarKF + kStages,
                          kBarVF = kBarKE + kStages, kBarVE = kBarVF + kStages,
                          kBarS = kBarVE + kStages, kBarP = kBarS + kG, kBarPV = kBarP + kG,
                          kBarDrain = kBarPV + kG, kNumBars = kBarDrain + 1;
     static constexpr uint32_t kMisc = kNumBars * 8 + 8;
     // The tiles need a 1024-byte aligned base; the dynamic window is at least
     // 16-byte aligned, so up to 1008 bytes of slack; the misc words go into
-    // the slack when it is large enough, else right after the tiles.  The
+    // the slack when it is large enough, else right after the staging.  The
     // request keeps a single CTA per SM (it owns all of TMEM).
-    static constexpr uint32_t kNeed = kTiles + 1008 + kMisc;
+    static constexpr uint32_t kNeed = kEnd + 1008 + kMisc;
+    static_assert(kNeed <= 227 * 1024, "shared memory per CTA");
     static constexpr uint32_t kRequest = kNeed > 120 * 1024 ? kNeed : 120 * 1024;
 };
 
@@ -192,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = saddr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t misc = (base - raw >= L::kMisc) ? raw : base + L::kTiles;
+    const uint32_t misc = (base - raw >= L::kMisc) ? raw : base + L::kEnd;
     uint8_t *gmisc = smem_raw + (misc - raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.g.H;
@@ -207,8 +214,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     Ctl ctl{abort_flag, a.status, a.wait_limit};
 
     if (tid == 0) {
-        mbar_init(bar(L::kBarQ), MODE == kPast ? 4 * kG : 1);
-        mbar_init(bar(L::kBarQE), 1);
+        for (int g = 0; g < kG; ++g) {
+            // past mode: one asynchronous arrival per gathering thread
+            mbar_init(bar(L::kBarQ + g), MODE == kPast ? kM : 1);
+            mbar_init(bar(L::kBarQE + g), 1);
+        }
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(L::kBarKF + s), 1);
             mbar_init(bar(L::kBarKE + s), 1);
@@ -246,6 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const CUtensorMap *map = is_k ? &tmap_k : &tmap_v;
             int pend[kStages];  // tile (global count) whose copy is in flight per slot
             for (int s = 0; s < kStages; ++s) pend[s] = -1;
+            int qpend[kG] = {-1, -1};  // own-block mode: Q phase in flight per tile
             int t = 0, qj = 0;  // K/V tiles and Q tiles loaded so far
             bool go = true;
             int job = blockIdx.x;
@@ -257,13 +268,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 Job NJ;
                 while (njob < njobs && !get_job<MODE>(a, njob, NJ)) njob += gridDim.x;
                 if (MODE == kCurrent && is_k) {
-                    // the previous job's S MMAs have read Q before it is replaced
-                    if (qj > 0 && !wait_bar(bar(L::kBarQE), (qj - 1) & 1, ctl)) break;
-                    mbar_expect_tx(bar(L::kBarQ), kG * L::NB * L::kQBox);
-                    for (int g = 0; g < kG; ++g)
+                    for (int g = 0; g < kG && go; ++g) {
+                        // the previous job's S_g MMAs have read Q_g before it is replaced
+                        if (qj > 0 && !wait_bar(bar(L::kBarQE + g), (qj - 1) & 1, ctl)) {
+                            go = false;
+                            break;
+                        }
+                        mbar_expect_tx(bar(L::kBarQ + g), L::NB * L::kQBox);
                         for (int x = 0; x < L::NB; ++x)
-                            tma_load_3d(sQ + (g * L::NB + x) * L::kQBox, &tmap_q, bar(L::kBarQ),
+                            tma_load_3d(sQ + (g * L::NB + x) * L::kQBox, &tmap_q, bar(L::kBarQ + g),
                                         x * kBox, J.h, J.seq0 + J.r0 + g * kM);
+                        qpend[g] = qj;
+                    }
+                    if (!go) break;
                     ++qj;
                 }
                 for (int j = 0; j < J.nkv; ++j, ++t) {
@@ -288,6 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int s = 0; s < kStages; ++s)
                     if (pend[s] >= 0)
                         drain_bar(bar(bfull + s), (pend[s] / kStages) & 1, a.wait_limit);
+                for (int g = 0; g < kG; ++g)
+                    if (qpend[g] >= 0) drain_bar(bar(L::kBarQ + g), qpend[g] & 1, a.wait_limit);
             }
         }
         __syncwarp();  // reconverge before the CTA barrier (bar.sync is per warp)
@@ -306,8 +325,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int njob = job + gridDim.x;  // next descriptor, fetched one job ahead
                 Job NJ;
                 while (njob < njobs && !get_job<MODE>(a, njob, NJ)) njob += gridDim.x;
-                if (!wait_bar(bar(L::kBarQ), qj & 1, ctl)) break;
-                ++qj;
+                // a Q tile without S MMAs in this job is released at once
+#pragma unroll
+                for (int g = 0; g < kG; ++g)
+                    if (ok && J.te[g] <= J.tb[g]) {
+                        ok = wait_bar(bar(L::kBarQ + g), qj & 1, ctl);
+                        if (ok) mbar_arrive(bar(L::kBarQE + g));
+                    }
+                if (!ok) break;
                 for (int j = 0; j <= J.nkv; ++j) {
                     const int tk = t + j, s = tk % kStages;
                     if (j < J.nkv) {
@@ -342,7 +367,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                             if (jp == J.te[g] - 1) tc_commit(bar(L::kBarPV + g));
                         }
-                        if (j < J.nkv && j >= J.tb[g] && j < J.te[g]) {
+                        if (ok && j < J.nkv && j >= J.tb[g] && j < J.te[g]) {
+                            if (j == J.tb[g]) {
+                                // Q_g of this job is in shared memory (TMA, or the
+                                // softmax warps' cp.async gather: generic-proxy
+                                // writes, ordered before the MMA's reads here)
+                                if (!wait_bar(bar(L::kBarQ + g), qj & 1, ctl)) {
+                                    ok = false;
+                                    break;
+                                }
+                                if (MODE == kPast) fence_proxy_async();
+                                tc_fence_after();
+                            }
                             // S_g = Q_g K^T (runs after the PV above: same thread, in order)
                             const uint32_t qb = sQ + g * L::NB * L::kQBox;
 #pragma unroll
@@ -353,17 +389,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 tc_mma(tS, ad, bd, idesc_s, k > 0);
                             }
                             tc_commit(bar(L::kBarS + g));
+                            // the job's last S_g: Q_g may be replaced once it completes
+                            if (j == J.te[g] - 1) tc_commit(bar(L::kBarQE + g));
                         }
                     }
                     if (!ok) break;
-                    if (j < J.nkv) {
-                        // the job's last S: Q may be replaced once it completes
-                        if (MODE == kCurrent && j == J.nkv - 1) tc_commit(bar(L::kBarQE));
-                        tc_commit(bar(L::kBarKE + s));
-                    }
+                    if (j < J.nkv) tc_commit(bar(L::kBarKE + s));
                     if (jp >= 0) tc_commit(bar(L::kBarVE + sp));
                 }
                 t += J.nkv;
+                ++qj;
 #pragma unroll
                 for (int g = 0; g < kG; ++g) gt[g] += J.te[g] - J.tb[g];
                 job = njob;
@@ -384,49 +419,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tSg = tmem + lane_off + g * 256;
         const uint32_t tOg = tSg + 128;
         const uint32_t sQg = sQ + g * L::NB * L::kQBox;
-        // past mode: gather job J's rows of Q for tile g (cp.async, zero rows
-        // past nrows); the arrival on q_full happens later
-        auto gather = [&](const Job &J) -> int {
-            const bool valid = jrow < J.nrows;
-            const int e = valid ? __ldg(a.list + J.lbeg + jrow) : 0;
-            const __nv_bfloat16 *src = a.q + ((size_t)(e >> kSlotBits) * H + J.h) * D;
-#pragma unroll
-            for (int ch = 0; ch < D / 8; ++ch) {
-                const uint32_t dst = sQg + (ch / 8) * L::kQBox + row * 128 +
-                                     ((uint32_t)((ch % 8) ^ (row & 7)) << 4);
-                cp_async16(dst, valid ? (const void *)(src + ch * 8) : (const void *)a.q, valid);
-            }
-            return e;
+        const uint32_t stg = base + L::kStage + (uint32_t)(warp - 2) * L::kStageWarp;
+        // past mode: this row's regroup entry (token << 5 | slot) in job J
+        auto list_entry = [&](const Job &J) -> int {
+            return (jrow < J.nrows) ? __ldg(a.list + J.lbeg + jrow) : 0;
         };
-        auto q_ready = [&]() {
-            cp_async_wait_all();
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::kBarQ));
+        // past mode: gather job J's rows of Q for tile g (cp.async, zero rows
+        // past nrows); q_full[g] completes when every thread's copies landed
+        // Each copy instruction moves 128 bytes of each of four rows: lane ->
+        // (row r = it * 4 + lane / 8 of this warp's 32, 16-byte chunk lane % 8).
+        auto gather = [&](const Job &J, int e) {
+            const int ch = lane & 7;
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                const int r = it * 4 + (lane >> 3);
+                const int er = __shfl_sync(0xffffffffu, e, r);
+                const bool valid = g * kM + quarter * 32 + r < J.nrows;
+                const __nv_bfloat16 *src = a.q + ((size_t)(er >> kSlotBits) * H + J.h) * D + ch * 8;
+                const uint32_t dst = sQg + (uint32_t)(quarter * 32 + r) * 128 +
+                                     ((uint32_t)(ch ^ (r & 7)) << 4);
+#pragma unroll
+                for (int x = 0; x < L::NB; ++x)
+                    cp_async16(dst + x * L::kQBox,
+                               valid ? (const void *)(src + x * kBox) : (const void *)a.q, valid);
+            }
+            cp_async_arrive_noinc(bar(L::kBarQ + g));
         };
         int gt = 0, gj = 0, qj = 0;  // S/P tiles of tile g, jobs with rows in tile g, jobs
         bool ok = true;
         int job = blockIdx.x;
         Job J;
         while (job < njobs && !get_job<MODE>(a, job, J)) job += gridDim.x;
-        int entry = 0;  // this row's regroup entry (token << 5 | slot), past mode
+        int entry = 0;  // this row's regroup entry in the current job, past mode
         if (MODE == kPast && job < njobs) {
-            entry = gather(J);
-            q_ready();
+            entry = list_entry(J);
+            gather(J, entry);
         }
         while (ok && job < njobs) {
-            // the next job's descriptor, fetched one job ahead
+            // the next job's descriptor, fetched one job ahead, and (past mode)
+            // this row's entry in it, loaded now and used after the last tile
             int njob = job + gridDim.x;
             Job NJ;
             while (njob < njobs && !get_job<MODE>(a, njob, NJ)) njob += gridDim.x;
-            // past mode: this job's Q is in place before the next job may be
-            // gathered (the softmax warps drive q_full, so it cannot run ahead).
-            // Own-block mode: the softmax warps never read Q and do not wait
-            // on it -- the producer may already be two phases ahead.
-            if (MODE == kPast) {
-                if (!__all_sync(0xffffffffu, wait_bar(bar(L::kBarQ), qj & 1, ctl))) break;
-                ++qj;
-            }
+            const int next_entry = (MODE == kPast && njob < njobs) ? list_entry(NJ) : 0;
             const int seq0 = J.seq0, h = J.h;
             const bool row_valid = jrow < J.nrows;
             int row_tok = -1, slot = 0;
@@ -438,12 +473,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // warm L2 with this row's past partials; the merge reads them only
                 // after the last tile, so the fetch overlaps the attention loop
                 if (row_valid && !a.dense && a.km1 > 0) {
-                    const int ci = (row_tok - seq0) / a.g.bs;
+                    // every earlier block was a candidate, so the row holds
+                    // min(topk - 1, its block index) partials, slots 0, 1, ...
+                    const int npre = min(a.km1, (row_tok - seq0) / a.g.bs);
                     const size_t rowid = (size_t)row_tok * H + h;
-                    const int32_t *sel = a.idx + rowid * a.topk;
-                    for (int s2 = 0; s2 < a.km1; ++s2) {
-                        const int c = __ldg(sel + s2);
-                        if (c < 0 || c >= ci) break;
+                    for (int s2 = 0; s2 < npre; ++s2) {
                         const char *po = reinterpret_cast<const char *>(a.part_o + (rowid * a.km1 + s2) * D);
 #pragma unroll
                         for (int ln = 0; ln < D * 2; ln += 128)
@@ -552,10 +586,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
             gt += ntile;
-            // in past mode the next job's Q rows are gathered now (this tile's
-            // S MMAs are done) and land while this job's epilogue runs
-            int next_entry = 0;
-            if (MODE == kPast && njob < njobs) next_entry = gather(NJ);
+            // in past mode the next job's Q rows are gathered as soon as the MMA
+            // has released Q_g (this job's S_g MMAs are done): they land while
+            // this job's epilogue runs, and the next job's S_g needs no wait
+            // on the softmax warps
+            if (MODE == kPast && njob < njobs) {
+                if (!__all_sync(0xffffffffu, wait_bar(bar(L::kBarQE + g), qj & 1, ctl))) {
+                    ok = false;
+                    break;
+                }
+                ++qj;
+                gather(NJ, next_entry);
+            }
 
             // ---------------- epilogue ----------------
             if (ntile > 0) {
@@ -569,101 +611,147 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float lse2 = m_run + __log2f(l_run);
                 if (MODE == kPast) {
                     const size_t pslot = ((size_t)row_tok * H + h) * a.km1 + slot;
-                    __nv_bfloat16 *dst = a.part_o + pslot * D;
-#pragma unroll
-                    for (int c0 = 0; c0 < D; c0 += 32) {
-                        uint32_t o[32];
-                        tc_ld32(tOg + c0, o);
-                        tc_wait_ld();
-                        if (row_valid) {
-#pragma unroll
-                            for (int c = 0; c < 32; c += 8) {
-                                uint4 pkd;
-                                uint32_t *pw = reinterpret_cast<uint32_t *>(&pkd);
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    __nv_bfloat162 bb =
-                                        __floats2bfloat162_rn(__uint_as_float(o[c + 2 * e]) * inv,
-                                                              __uint_as_float(o[c + 2 * e + 1]) * inv);
-                                    pw[e] = *reinterpret_cast<uint32_t *>(&bb);
-                                }
-                                *reinterpret_cast<uint4 *>(dst + c0 + c) = pkd;
-                            }
-                        }
-                    }
-                    if (row_valid) a.part_lse[pslot] = lse2;
-                } else {
-                    // log-sum-exp merge with the row's past partials (ascending blocks)
-                    float w_cur = 1.f, wsum = 1.f, mmax = lse2;
-                    int np = 0;
-                    const size_t rowid = (size_t)row_tok * H + h;
-                    if (row_valid && !a.dense && a.km1 > 0) {
-                        const int ci = i_loc / a.g.bs;
-                        const int32_t *sel = a.idx + rowid * a.topk;
-                        for (; np < a.km1; ++np) {
-                            const int c = __ldg(sel + np);
-                            if (c < 0 || c >= ci) break;
-                            mmax = fmaxf(mmax, __ldg(a.part_lse + rowid * a.km1 + np));
-                        }
-                        if (np > 0) {
-                            w_cur = fast_exp2(lse2 - mmax);
-                            wsum = w_cur;
-                            for (int s2 = 0; s2 < np; ++s2)
-                                wsum += fast_exp2(__ldg(a.part_lse + rowid * a.km1 + s2) - mmax);
-                        }
-                    }
-                    const float iw = 1.f / wsum;
-                    const float fcur = w_cur * inv * iw;
-                    __nv_bfloat16 *dst = a.out + rowid * D;
+                    const unsigned long long my_dst =
+                        reinterpret_cast<unsigned long long>(a.part_o + pslot * D);
 #pragma unroll
                     for (int c0 = 0; c0 < D; c0 += 64) {
-                        // 64 columns of O from TMEM in one go, then the partials'
-                        // loads of those columns all in flight together
+                        // 64 columns of my row as bf16 (128 bytes) into the staging rows
                         uint32_t o[2][32];
                         tc_ld32(tOg + c0, o[0]);
                         tc_ld32(tOg + c0 + 32, o[1]);
                         tc_wait_ld();
-                        if (row_valid) {
 #pragma unroll
-                            for (int c = 0; c < 64; ++c)
-                                o[c >> 5][c & 31] = __float_as_uint(__uint_as_float(o[c >> 5][c & 31]) * fcur);
-                            for (int s2 = 0; s2 < np; ++s2) {
-                                const size_t ps = rowid * a.km1 + s2;
-                                const float w = fast_exp2(__ldg(a.part_lse + ps) - mmax) * iw;
-                                const uint4 *src =
-                                    reinterpret_cast<const uint4 *>(a.part_o + ps * D + c0);
-                                uint4 f[8];
+                        for (int ch = 0; ch < 8; ++ch) {
+                            uint32_t w[4];
 #pragma unroll
-                                for (int c = 0; c < 8; ++c) f[c] = __ldg(src + c);
+                            for (int e = 0; e < 4; ++e) {
+                                const int col = ch * 8 + 2 * e;
+                                __nv_bfloat162 bb = __floats2bfloat162_rn(
+                                    __uint_as_float(o[col >> 5][col & 31]) * inv,
+                                    __uint_as_float(o[(col + 1) >> 5][(col + 1) & 31]) * inv);
+                                w[e] = *reinterpret_cast<uint32_t *>(&bb);
+                            }
+                            st_shared_v4(stg + lane * 128 + ((uint32_t)(ch ^ (lane & 7)) << 4), w[0],
+                                         w[1], w[2], w[3]);
+                        }
+                        __syncwarp();
+                        // lane -> (row it * 4 + lane / 8, chunk lane % 8): whole lines out
 #pragma unroll
-                                for (int c = 0; c < 8; ++c) {
-                                    const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&f[c]);
+                        for (int it = 0; it < 8; ++it) {
+                            const int r = it * 4 + (lane >> 3), ch = lane & 7;
+                            const unsigned long long d = __shfl_sync(0xffffffffu, my_dst, r);
+                            const int v = __shfl_sync(0xffffffffu, (int)row_valid, r);
+                            const uint4 val =
+                                ld_shared_v4(stg + r * 128 + ((uint32_t)(ch ^ (r & 7)) << 4));
+                            if (v)
+                                *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(d) + c0 +
+                                                           ch * 8) = val;
+                        }
+                        __syncwarp();
+                    }
+                    if (row_valid) a.part_lse[pslot] = lse2;
+                } else {
+                    // log-sum-exp merge with the row's past partials (slots in
+                    // ascending block order; every earlier block was a candidate,
+                    // so there are min(topk - 1, block index) of them)
+                    const size_t rowid = (size_t)row_tok * H + h;
+                    int np = 0;
+                    float mmax = lse2;
+                    if (row_valid && !a.dense && a.km1 > 0) {
+                        np = min(a.km1, i_loc / a.g.bs);
+                        for (int s2 = 0; s2 < np; ++s2)
+                            mmax = fmaxf(mmax, __ldg(a.part_lse + rowid * a.km1 + s2));
+                    }
+                    float w_cur = 1.f, wsum = 1.f;
+                    if (np > 0) {
+                        w_cur = fast_exp2(lse2 - mmax);
+                        wsum = w_cur;
+                        for (int s2 = 0; s2 < np; ++s2)
+                            wsum += fast_exp2(__ldg(a.part_lse + rowid * a.km1 + s2) - mmax);
+                    }
+                    const float iw = 1.f / wsum;
+                    const float fcur = w_cur * inv * iw;
+                    const int np_warp = __reduce_max_sync(0xffffffffu, np);
+                    // 32 columns per pass; staging [slot pair][32 rows][64 B]; the
+                    // copies map lane -> (row it * 8 + lane / 4, 16-byte chunk lane % 4)
+#pragma unroll 1
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t o[32];
+                        tc_ld32(tOg + c0, o);
+                        tc_wait_ld();
 #pragma unroll
-                                    for (int e = 0; e < 4; ++e) {
-                                        const float2 fv = __bfloat1622float2(b2[e]);
-                                        const int col = 8 * c + 2 * e;
-                                        o[col >> 5][col & 31] = __float_as_uint(
-                                            fmaf(w, fv.x, __uint_as_float(o[col >> 5][col & 31])));
-                                        o[(col + 1) >> 5][(col + 1) & 31] = __float_as_uint(
-                                            fmaf(w, fv.y, __uint_as_float(o[(col + 1) >> 5][(col + 1) & 31])));
+                        for (int c = 0; c < 32; ++c)
+                            o[c] = __float_as_uint(__uint_as_float(o[c]) * fcur);
+                        for (int s0 = 0; s0 < np_warp; s0 += 2) {
+#pragma unroll
+                            for (int it = 0; it < 4; ++it) {
+                                const int r = it * 8 + (lane >> 2), q4 = lane & 3;
+                                const unsigned long long rid =
+                                    __shfl_sync(0xffffffffu, (unsigned long long)rowid, r);
+                                const int npr = __shfl_sync(0xffffffffu, np, r);
+#pragma unroll
+                                for (int ss = 0; ss < 2; ++ss) {
+                                    const bool v = s0 + ss < npr;
+                                    const __nv_bfloat16 *src =
+                                        a.part_o + (rid * a.km1 + s0 + ss) * D + c0 + q4 * 8;
+                                    cp_async16(stg + ss * 2048 + r * 64 +
+                                                   ((uint32_t)(q4 ^ ((r >> 1) & 3)) << 4),
+                                               v ? (const void *)src : (const void *)a.part_o, v);
+                                }
+                            }
+                            cp_async_wait_all();
+                            __syncwarp();
+#pragma unroll
+                            for (int ss = 0; ss < 2; ++ss) {
+                                if (s0 + ss < np) {
+                                    const float w =
+                                        fast_exp2(__ldg(a.part_lse + rowid * a.km1 + s0 + ss) - mmax) * iw;
+#pragma unroll
+                                    for (int q4 = 0; q4 < 4; ++q4) {
+                                        const uint4 f =
+                                            ld_shared_v4(stg + ss * 2048 + lane * 64 +
+                                                         ((uint32_t)(q4 ^ ((lane >> 1) & 3)) << 4));
+                                        const __nv_bfloat162 *b2 =
+                                            reinterpret_cast<const __nv_bfloat162 *>(&f);
+#pragma unroll
+                                        for (int e = 0; e < 4; ++e) {
+                                            const float2 fv = __bfloat1622float2(b2[e]);
+                                            const int col = q4 * 8 + 2 * e;
+                                            o[col] = __float_as_uint(fmaf(w, fv.x, __uint_as_float(o[col])));
+                                            o[col + 1] =
+                                                __float_as_uint(fmaf(w, fv.y, __uint_as_float(o[col + 1])));
+                                        }
                                     }
                                 }
                             }
-#pragma unroll
-                            for (int c = 0; c < 64; c += 8) {
-                                uint4 pkd;
-                                uint32_t *pw = reinterpret_cast<uint32_t *>(&pkd);
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const int col = c + 2 * e;
-                                    __nv_bfloat162 bb = __floats2bfloat162_rn(
-                                        __uint_as_float(o[col >> 5][col & 31]),
-                                        __uint_as_float(o[(col + 1) >> 5][(col + 1) & 31]));
-                                    pw[e] = *reinterpret_cast<uint32_t *>(&bb);
-                                }
-                                *reinterpret_cast<uint4 *>(dst + c0 + c) = pkd;
-                            }
+                            __syncwarp();
                         }
+                        // bf16 result (64 bytes of my row) re-laid, then whole rows out
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int col = q4 * 8 + 2 * e;
+                                __nv_bfloat162 bb = __floats2bfloat162_rn(__uint_as_float(o[col]),
+                                                                          __uint_as_float(o[col + 1]));
+                                w[e] = *reinterpret_cast<uint32_t *>(&bb);
+                            }
+                            st_shared_v4(stg + lane * 64 + ((uint32_t)(q4 ^ ((lane >> 1) & 3)) << 4),
+                                         w[0], w[1], w[2], w[3]);
+                        }
+                        __syncwarp();
+#pragma unroll
+                        for (int it = 0; it < 4; ++it) {
+                            const int r = it * 8 + (lane >> 2), q4 = lane & 3;
+                            const unsigned long long rid =
+                                __shfl_sync(0xffffffffu, (unsigned long long)rowid, r);
+                            const int v = __shfl_sync(0xffffffffu, (int)row_valid, r);
+                            const uint4 val =
+                                ld_shared_v4(stg + r * 64 + ((uint32_t)(q4 ^ ((r >> 1) & 3)) << 4));
+                            if (v) *reinterpret_cast<uint4 *>(a.out + rid * D + c0 + q4 * 8) = val;
+                        }
+                        __syncwarp();
                     }
                     if (row_valid) {
                         const float lse_out = (np > 0) ? mmax + __log2f(wsum) : lse2;
@@ -676,12 +764,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // O_g has been read: the next job's first PV may overwrite it
                 tc_fence_before();
             }
-            if (MODE == kPast && njob < njobs) q_ready();
             job = njob;
             J = NJ;
             entry = next_entry;
         }
-        if (!ok) cp_async_wait_all();  // no copy of ours may land after the exit
+        cp_async_wait_all();  // no copy of ours may land after the exit
     }
     tc_fence_before();
     __syncthreads();
