@@ -76,18 +76,20 @@ size_t workspace_bytes(const Plan &p, Workspace *ws, char *base) {
     std::memset(&w, 0, sizeof w);
     w.cu = static_cast<int *>(take(sizeof(int) * (p.num_seqs + 1)));
     w.blk_base = static_cast<int *>(take(sizeof(int) * (p.num_seqs + 1)));
+    w.gtile = static_cast<int *>(take(sizeof(int) * (p.num_seqs + 1)));
     const bool gate = !p.dense && p.km1 > 0;
     if (gate) {
         const size_t N = (size_t)p.NBcap * p.H;
         const size_t rows = (size_t)p.total * p.H;
         w.kbar = static_cast<float *>(take(sizeof(float) * N * p.D));
         w.idx = static_cast<int32_t *>(take(sizeof(int32_t) * rows * p.topk));
-        w.counts = static_cast<int *>(take(sizeof(int) * N));
+        w.counts = static_cast<int *>(take(sizeof(int) * (N + 1)));
+        w.need_count = w.counts ? w.counts + N : nullptr;
+        w.need_list = static_cast<unsigned long long *>(take(2 * sizeof(long long) * rows));
         w.list_off = static_cast<int *>(take(sizeof(int) * (N + 1)));
         w.tile_off = static_cast<int *>(take(sizeof(int) * (N + 1)));
         w.job_list = static_cast<int *>(
             take(sizeof(int) * (rows * p.km1 / (size_t)past_tile_rows() + N + 1)));
-        w.ticket = static_cast<int *>(take(sizeof(int) * rows * p.km1));
         w.kbhi = static_cast<__nv_bfloat16 *>(take(sizeof(__nv_bfloat16) * N * p.D));
         w.kblo = static_cast<__nv_bfloat16 *>(take(sizeof(__nv_bfloat16) * N * p.D));
         w.knorm = static_cast<float *>(take(sizeof(float) * N));
@@ -160,18 +162,20 @@ static int run_forward(const Plan &p, const int *cu_dev, const void *q, const vo
     const bool gate = !p.dense && p.km1 > 0;
     if (gate) MOBA_TRY(launch_kpool(p, ws, kb, ws.kbar, st));
     prof_mark(call, 2, st);
+    const bool tc_gate = g_gate_kind == 0 && gate_tc_supported(p);
     if (gate) {
-        MOBA_TRY(cudaMemsetAsync(ws.counts, 0, sizeof(int) * (size_t)p.NBcap * p.H, st));
-        if (g_gate_kind == 0 && gate_tc_supported(p)) {
+        // the per-list counts and the exact kernel's row count
+        MOBA_TRY(cudaMemsetAsync(ws.counts, 0, sizeof(int) * ((size_t)p.NBcap * p.H + 1), st));
+        if (tc_gate) {
             MOBA_TRY(launch_kbar_split(p, ws.kbar, ws.kbhi, ws.kblo, ws.knorm, st));
-            MOBA_TRY(launch_gate_tc(p, ws, qb, ws.kbar, ws.kbhi, ws.kblo, ws.knorm, ws.idx, true,
-                                    st));
+            MOBA_TRY(launch_gate_tc(p, ws, qb, ws.kbar, ws.kbhi, ws.kblo, ws.knorm, ws.idx,
+                                    ws.counts, ws.need_list, ws.need_count, st));
         } else {
-            MOBA_TRY(launch_gate(p, ws, qb, ws.kbar, ws.idx, true, st));
+            MOBA_TRY(launch_gate(p, ws, qb, ws.kbar, ws.idx, st));
         }
     }
     prof_mark(call, 3, st);
-    if (gate) MOBA_TRY(launch_regroup(p, ws, st));
+    if (gate) MOBA_TRY(launch_regroup(p, ws, tc_gate, st));
     prof_mark(call, 4, st);
     MOBA_TRY(launch_attn_past(p, ws, qb, kb, vb, st));
     prof_mark(call, 5, st);
@@ -193,11 +197,12 @@ static int with_tables(const Plan &p, const int *cu_dev, cudaStream_t st,
                        int (*body)(const Plan &, Workspace &, void *), void *ctx) {
     Workspace ws;
     std::memset(&ws, 0, sizeof ws);
-    const size_t bytes = align256(sizeof(int) * (p.num_seqs + 1)) * 2;
+    const size_t one = align256(sizeof(int) * (p.num_seqs + 1));
     void *mem = nullptr;
-    if (cudaMallocAsync(&mem, bytes, st) != cudaSuccess) return MOBA_ERR_CUDA;
+    if (cudaMallocAsync(&mem, 3 * one, st) != cudaSuccess) return MOBA_ERR_CUDA;
     ws.cu = static_cast<int *>(mem);
-    ws.blk_base = reinterpret_cast<int *>(static_cast<char *>(mem) + bytes / 2);
+    ws.blk_base = reinterpret_cast<int *>(static_cast<char *>(mem) + one);
+    ws.gtile = reinterpret_cast<int *>(static_cast<char *>(mem) + 2 * one);
     int rc = cuda_status(launch_setup(p, cu_dev, ws, st));
     if (rc == MOBA_OK) rc = body(p, ws, ctx);
     if (cudaFreeAsync(mem, st) != cudaSuccess && rc == MOBA_OK) rc = MOBA_ERR_CUDA;
@@ -225,19 +230,27 @@ static int gate_run(const Plan &p, Workspace &ws, void *c) {
     auto *x = static_cast<GateCtx *>(c);
     const auto *q = static_cast<const __nv_bfloat16 *>(x->q);
     if (g_gate_kind != 0 || !gate_tc_supported(p))
-        return cuda_status(launch_gate(p, ws, q, x->kbar, x->idx, false, x->st));
-    // bf16 split of the caller's kbar in stream-ordered scratch
+        return cuda_status(launch_gate(p, ws, q, x->kbar, x->idx, x->st));
+    // stream-ordered scratch: the bf16 split of the caller's kbar, the norms,
+    // and the rows left to the exact kernel
     const size_t n = (size_t)p.NBcap * p.H * p.D;
+    const size_t rows = (size_t)p.total * p.H;
+    const size_t b_split = align256(2 * n * sizeof(__nv_bfloat16));
+    const size_t b_norm = align256(sizeof(float) * p.NBcap * p.H);
+    const size_t b_list = align256(2 * sizeof(long long) * rows);
     void *mem = nullptr;
-    if (cudaMallocAsync(&mem, 2 * n * sizeof(__nv_bfloat16) + sizeof(float) * p.NBcap * p.H,
-                        x->st) != cudaSuccess)
+    if (cudaMallocAsync(&mem, b_split + b_norm + b_list + 256, x->st) != cudaSuccess)
         return MOBA_ERR_CUDA;
-    auto *hi = static_cast<__nv_bfloat16 *>(mem);
-    auto *nrm = reinterpret_cast<float *>(hi + 2 * n);
-    int rc = cuda_status(launch_kbar_split(p, x->kbar, hi, hi + n, nrm, x->st));
+    char *m = static_cast<char *>(mem);
+    auto *hi = reinterpret_cast<__nv_bfloat16 *>(m);
+    auto *nrm = reinterpret_cast<float *>(m + b_split);
+    auto *list = reinterpret_cast<unsigned long long *>(m + b_split + b_norm);
+    auto *cnt = reinterpret_cast<int *>(m + b_split + b_norm + b_list);
+    int rc = cuda_status(cudaMemsetAsync(cnt, 0, sizeof(int), x->st));
+    if (rc == MOBA_OK) rc = cuda_status(launch_kbar_split(p, x->kbar, hi, hi + n, nrm, x->st));
     if (rc == MOBA_OK)
-        rc = cuda_status(
-            launch_gate_tc(p, ws, q, x->kbar, hi, hi + n, nrm, x->idx, false, x->st));
+        rc = cuda_status(launch_gate_tc(p, ws, q, x->kbar, hi, hi + n, nrm, x->idx, nullptr,
+                                        list, cnt, x->st));
     if (cudaFreeAsync(mem, x->st) != cudaSuccess && rc == MOBA_OK) rc = MOBA_ERR_CUDA;
     return rc;
 }

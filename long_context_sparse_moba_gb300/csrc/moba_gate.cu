@@ -9,6 +9,8 @@
 // will not run" (mhpq.cn/news/582794) section 3.3 (the selected blocks of all
 // queries are batched before attention -- here: a CSR list of query rows per
 // (block, head)).
+#include <algorithm>
+
 #include "moba_internal.cuh"
 
 namespace moba {
@@ -61,17 +63,22 @@ __device__ void cta_exclusive_scan(int N, F f, W write) {
 // S = max_len for every sequence).
 // ---------------------------------------------------------------------------
 __global__ void setup_kernel(const int *__restrict__ cu_in, int num_seqs, int S, int bs,
-                             int *__restrict__ cu, int *__restrict__ blk_base) {
+                             int *__restrict__ cu, int *__restrict__ blk_base,
+                             int *__restrict__ gtile) {
     auto len = [&](int b) { return cu_in ? (cu_in[b + 1] - cu_in[b]) : S; };
     for (int b = threadIdx.x; b <= num_seqs; b += blockDim.x)
         cu[b] = cu_in ? cu_in[b] : b * S;
     cta_exclusive_scan(
         num_seqs, [&](int b) { return (len(b) + bs - 1) / bs; },
         [&](int i, int v) { blk_base[i] = v; });
+    cta_exclusive_scan(
+        num_seqs, [&](int b) { return (len(b) + 127) / 128; },
+        [&](int i, int v) { gtile[i] = v; });
 }
 
 cudaError_t launch_setup(const Plan &p, const int *cu_dev, Workspace &ws, cudaStream_t st) {
-    setup_kernel<<<1, 1024, 0, st>>>(cu_dev, p.num_seqs, p.max_len, p.bs, ws.cu, ws.blk_base);
+    setup_kernel<<<1, 1024, 0, st>>>(cu_dev, p.num_seqs, p.max_len, p.bs, ws.cu, ws.blk_base,
+                                     ws.gtile);
     note_launches(1);
     return cudaGetLastError();
 }
@@ -220,25 +227,20 @@ cudaError_t launch_kpool(const Plan &p, const Workspace &ws, const __nv_bfloat16
 // arrive in ascending order and a strictly greater score is needed to move
 // ahead of an earlier block, which is the lower-index tie-break.  Rows whose
 // own block has at most topk - 1 predecessors take them all without scoring.
-// With COUNT, each past selection also gets a ticket (its position inside the
-// (block, head) query list): ranks come from a shared-memory histogram and one
-// global atomic per non-empty bin reserves the CTA's range.
 // ---------------------------------------------------------------------------
 constexpr int kGateThreads = 128;
 constexpr int kGateRows = 128;
 constexpr int kGateChunk = 64;
-constexpr int kHistBins = 512;
 constexpr int kEmpty = 0x7fffffff;
 
-template <int D, int KCAP, bool COUNT>
+template <int D, int KCAP>
 __global__ __launch_bounds__(kGateThreads) void gate_kernel(
     Geometry g, const __nv_bfloat16 *__restrict__ q, const float *__restrict__ kbar,
-    int32_t *__restrict__ idx, int *__restrict__ ticket, int topk, int *__restrict__ counts) {
+    int32_t *__restrict__ idx, int topk) {
     constexpr int DL = D / 4;  // dims per lane
     constexpr int M = DL / 4;  // float4 chunks per lane
     __shared__ __align__(16) float skb[kGateChunk * D];
-    __shared__ int hist[kHistBins];
-    __shared__ int s_cmax, s_call;
+    __shared__ int s_cmax;
     const int h = blockIdx.y, b = blockIdx.z, H = g.H;
     const int seq0 = __ldg(g.cu + b), L = __ldg(g.cu + b + 1) - seq0;
     const int i0 = blockIdx.x * kGateRows;
@@ -254,15 +256,9 @@ __global__ __launch_bounds__(kGateThreads) void gate_kernel(
     const int my_tok = seq0 + my_i;
     const bool my_scored = my_valid && km1 > 0 && my_ci > km1;
 
-    if (tid == 0) {
-        s_cmax = 0;
-        s_call = 0;
-    }
-    if (COUNT)
-        for (int x = tid; x < kHistBins; x += kGateThreads) hist[x] = 0;
+    if (tid == 0) s_cmax = 0;
     __syncthreads();
     if (my_scored) atomicMax(&s_cmax, my_ci);
-    if (my_valid) atomicMax(&s_call, my_ci);
 
     float qf[4][DL];
 #pragma unroll
@@ -386,44 +382,14 @@ __global__ __launch_bounds__(kGateThreads) void gate_kernel(
         out[npast] = my_ci;
         for (int x = npast + 1; x < topk; ++x) out[x] = -1;
     }
-    if (COUNT) {
-        int rank[KCAP];
-#pragma unroll
-        for (int x = 0; x < KCAP; ++x) {
-            rank[x] = 0;
-            if (x < npast) {
-                const int c = ti[x];
-                rank[x] = (c < kHistBins) ? atomicAdd(&hist[c], 1)
-                                          : atomicAdd(counts + (size_t)(bbase + c) * H + h, 1);
-            }
-        }
-        __syncthreads();
-        const int nbins = min(kHistBins, s_call);
-        for (int x = tid; x < nbins; x += kGateThreads) {
-            const int n = hist[x];
-            hist[x] = n ? atomicAdd(counts + (size_t)(bbase + x) * H + h, n) : 0;
-        }
-        __syncthreads();
-        if (my_valid) {
-            int *tk = ticket + ((size_t)my_tok * H + h) * km1;
-#pragma unroll
-            for (int x = 0; x < KCAP; ++x) {
-                if (x < npast) {
-                    const int c = ti[x];
-                    tk[x] = (c < kHistBins) ? hist[c] + rank[x] : rank[x];
-                }
-            }
-        }
-    }
 }
 
-template <int D, bool COUNT>
+template <int D>
 static void launch_gate_d(dim3 grid, cudaStream_t st, Geometry g, const __nv_bfloat16 *q,
-                          const float *kbar, int32_t *idx, int *ticket, int topk, int *counts) {
+                          const float *kbar, int32_t *idx, int topk) {
     const int km1 = topk - 1;
-#define MOBA_GATE_CASE(KC)                                                               \
-    gate_kernel<D, KC, COUNT><<<grid, kGateThreads, 0, st>>>(g, q, kbar, idx, ticket, topk, \
-                                                              counts);                  \
+#define MOBA_GATE_CASE(KC)                                                        \
+    gate_kernel<D, KC><<<grid, kGateThreads, 0, st>>>(g, q, kbar, idx, topk); \
     return;
     if (km1 <= 1) { MOBA_GATE_CASE(1) }
     if (km1 <= 2) { MOBA_GATE_CASE(2) }
@@ -435,27 +401,70 @@ static void launch_gate_d(dim3 grid, cudaStream_t st, Geometry g, const __nv_bfl
 }
 
 cudaError_t launch_gate(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
-                        const float *kbar, int32_t *idx, bool count, cudaStream_t st) {
+                        const float *kbar, int32_t *idx, cudaStream_t st) {
     dim3 grid((p.max_len + kGateRows - 1) / kGateRows, p.H, p.num_seqs);
     Geometry g = make_geo(p, ws);
-    if (p.D == 64) {
-        if (count) launch_gate_d<64, true>(grid, st, g, q, kbar, idx, ws.ticket, p.topk, ws.counts);
-        else launch_gate_d<64, false>(grid, st, g, q, kbar, idx, nullptr, p.topk, nullptr);
-    } else {
-        if (count) launch_gate_d<128, true>(grid, st, g, q, kbar, idx, ws.ticket, p.topk, ws.counts);
-        else launch_gate_d<128, false>(grid, st, g, q, kbar, idx, nullptr, p.topk, nullptr);
-    }
+    if (p.D == 64) launch_gate_d<64>(grid, st, g, q, kbar, idx, p.topk);
+    else launch_gate_d<128>(grid, st, g, q, kbar, idx, p.topk);
     note_launches(1);
     return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------
-// K3: regroup.  (a) one CTA scans the per-(block, head) counts into list and
-// tile offsets; (b) every past selection is written at its list offset plus
-// the ticket the gate gave it (no atomics).  The order inside a list depends
-// on which CTA reserved its range first; each row's result does not depend on
-// which rows share its attention tile, so outputs stay deterministic.
+// K3: regroup into per-(block, head) lists of the rows that selected that past
+// block.  (a) count: every CTA histograms the selections of a contiguous range
+// of rows in shared memory and adds the histogram into the global counts;
+// (b) one CTA scans the counts into list and tile offsets (and the job table
+// of the past-block attention); (c) scatter: every CTA histograms its rows
+// again, reserves its range inside each list with one atomicSub per non-empty
+// bin (which brings the counts back to zero) and writes each selection at its
+// reserved position.  The order inside a list depends on which CTA reserved
+// first; a row's result does not depend on which rows share its attention
+// tile, so outputs stay deterministic.  With more bins than shared memory
+// holds, every selection goes straight to the global counters.
 // ---------------------------------------------------------------------------
+constexpr int kRgThreads = 512;
+constexpr int kRgSmemBins = 48 * 1024;  // 192 KB of shared-memory histogram at most
+
+// calls f(bin, entry) for every past selection of row r = token * H + head
+template <typename F>
+__device__ __forceinline__ void for_each_selection(const Geometry &g, const int32_t *__restrict__ idx,
+                                                   int topk, size_t r, F f) {
+    const int t = (int)(r / g.H), h = (int)(r % g.H);
+    const int b = upper_index(g.cu, g.num_seqs, t);
+    const int ci = (t - __ldg(g.cu + b)) / g.bs;
+    const int bbase = __ldg(g.blk_base + b);
+    const int32_t *row = idx + r * topk;
+    for (int s = 0; s < topk - 1; ++s) {
+        const int c = __ldg(row + s);
+        if (c < 0 || c >= ci) break;
+        f((bbase + c) * g.H + h, (t << kSlotBits) | s);
+    }
+}
+
+template <bool SMEM>
+__global__ void __launch_bounds__(kRgThreads)
+    regroup_count_kernel(Geometry g, const int32_t *__restrict__ idx, int topk, int rows_per_cta,
+                         int N, int *__restrict__ counts) {
+    extern __shared__ int hist[];
+    const size_t R = (size_t)g.total * g.H;
+    const size_t r0 = (size_t)blockIdx.x * rows_per_cta, r1 = min(R, r0 + rows_per_cta);
+    if (SMEM) {
+        for (int x = threadIdx.x; x < N; x += kRgThreads) hist[x] = 0;
+        __syncthreads();
+    }
+    for (size_t r = r0 + threadIdx.x; r < r1; r += kRgThreads)
+        for_each_selection(g, idx, topk, r, [&](int bin, int) {
+            if (SMEM) atomicAdd(&hist[bin], 1);
+            else atomicAdd(counts + bin, 1);
+        });
+    if (SMEM) {
+        __syncthreads();
+        for (int x = threadIdx.x; x < N; x += kRgThreads)
+            if (hist[x]) atomicAdd(counts + x, hist[x]);
+    }
+}
+
 __global__ void regroup_scan_kernel(const int *__restrict__ counts, int N, int tile_m,
                                     int *__restrict__ list_off, int *__restrict__ tile_off,
                                     int *__restrict__ job_list) {
@@ -471,34 +480,72 @@ __global__ void regroup_scan_kernel(const int *__restrict__ counts, int N, int t
         });
 }
 
-__global__ void regroup_scatter_kernel(Geometry g, const int32_t *__restrict__ idx,
-                                       const int *__restrict__ ticket, int topk,
-                                       const int *__restrict__ list_off, int *__restrict__ list) {
-    const size_t r = (size_t)blockIdx.x * blockDim.x + threadIdx.x;  // token * H + head
-    if (r >= (size_t)g.total * g.H) return;
-    const int t = (int)(r / g.H), h = (int)(r % g.H);
-    const int b = upper_index(g.cu, g.num_seqs, t);
-    const int ci = (t - __ldg(g.cu + b)) / g.bs;
-    const int bbase = __ldg(g.blk_base + b);
-    const int km1 = topk - 1;
-    const int32_t *row = idx + r * topk;
-    const int *tk = ticket + r * km1;
-    for (int s = 0; s < km1; ++s) {
-        const int c = row[s];
-        if (c < 0 || c >= ci) break;
-        list[__ldg(list_off + (size_t)(bbase + c) * g.H + h) + tk[s]] = (t << kSlotBits) | s;
+template <bool SMEM>
+__global__ void __launch_bounds__(kRgThreads)
+    regroup_scatter_kernel(Geometry g, const int32_t *__restrict__ idx, int topk, int rows_per_cta,
+                           int N, int *__restrict__ counts, const int *__restrict__ list_off,
+                           int *__restrict__ list) {
+    extern __shared__ int hist[];
+    const size_t R = (size_t)g.total * g.H;
+    const size_t r0 = (size_t)blockIdx.x * rows_per_cta, r1 = min(R, r0 + rows_per_cta);
+    if (SMEM) {
+        for (int x = threadIdx.x; x < N; x += kRgThreads) hist[x] = 0;
+        __syncthreads();
+        for (size_t r = r0 + threadIdx.x; r < r1; r += kRgThreads)
+            for_each_selection(g, idx, topk, r, [&](int bin, int) { atomicAdd(&hist[bin], 1); });
+        __syncthreads();
+        // this CTA's range in list x: [list_off + remaining - n, list_off + remaining)
+        for (int x = threadIdx.x; x < N; x += kRgThreads) {
+            const int n = hist[x];
+            if (n) hist[x] = __ldg(list_off + x) + atomicSub(counts + x, n) - n;
+        }
+        __syncthreads();
     }
+    for (size_t r = r0 + threadIdx.x; r < r1; r += kRgThreads)
+        for_each_selection(g, idx, topk, r, [&](int bin, int entry) {
+            const int pos = SMEM ? atomicAdd(&hist[bin], 1)
+                                 : __ldg(list_off + bin) + atomicSub(counts + bin, 1) - 1;
+            list[pos] = entry;
+        });
 }
 
-cudaError_t launch_regroup(const Plan &p, const Workspace &ws, cudaStream_t st) {
+cudaError_t launch_regroup(const Plan &p, const Workspace &ws, bool counted, cudaStream_t st) {
     const int N = p.NBcap * p.H;
+    const size_t R = (size_t)p.total * p.H;
+    const bool smem = N <= kRgSmemBins;
+    // enough rows per CTA that clearing and flushing the histogram stays cheap
+    const int rows_per_cta = smem ? (int)std::max<long long>(4096, 4ll * N) : 4096;
+    const unsigned grid = (unsigned)((R + rows_per_cta - 1) / rows_per_cta);
+    const size_t hbytes = smem ? sizeof(int) * (size_t)N : 0;
+    const Geometry g = make_geo(p, ws);
+    cudaError_t e;
+    if (smem) {
+        e = cudaFuncSetAttribute(regroup_count_kernel<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hbytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(regroup_scatter_kernel<true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hbytes);
+        if (e != cudaSuccess) return e;
+    }
+    if (!counted) {
+        if (smem)
+            regroup_count_kernel<true><<<grid, kRgThreads, hbytes, st>>>(g, ws.idx, p.topk,
+                                                                          rows_per_cta, N, ws.counts);
+        else
+            regroup_count_kernel<false><<<grid, kRgThreads, 0, st>>>(g, ws.idx, p.topk,
+                                                                     rows_per_cta, N, ws.counts);
+        note_launches(1);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     regroup_scan_kernel<<<1, 1024, 0, st>>>(ws.counts, N, past_tile_rows(), ws.list_off,
                                             ws.tile_off, ws.job_list);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    const size_t rows = (size_t)p.total * p.H;
-    regroup_scatter_kernel<<<(unsigned)((rows + 255) / 256), 256, 0, st>>>(
-        make_geo(p, ws), ws.idx, ws.ticket, p.topk, ws.list_off, ws.list);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (smem)
+        regroup_scatter_kernel<true><<<grid, kRgThreads, hbytes, st>>>(
+            g, ws.idx, p.topk, rows_per_cta, N, ws.counts, ws.list_off, ws.list);
+    else
+        regroup_scatter_kernel<false><<<grid, kRgThreads, 0, st>>>(
+            g, ws.idx, p.topk, rows_per_cta, N, ws.counts, ws.list_off, ws.list);
     note_launches(2);
     return cudaGetLastError();
 }

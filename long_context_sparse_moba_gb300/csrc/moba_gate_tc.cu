@@ -6,24 +6,33 @@
 // server-side long context" (hncyxsy.com/news/197418) section 3 (current
 // block forced; inner product with the mean-pooled keys).
 //
-// One CTA = 128 consecutive query rows of one (sequence, head), 128 threads;
-// thread r owns row r.
-//   1. TMA loads the rows' q (bf16) and the pooled keys of the sequence's
-//      past blocks split into two bf16 terms, kbar ~= hi + lo (hi = bf16(kbar),
-//      lo = bf16(kbar - hi)); one tcgen05.mma chain per 128 blocks computes
-//      approx[r][c] = q_r . hi_c + q_r . lo_c into TMEM (fp32).
-//   2. Each thread keeps the top (k-1) approximate scores of its row and the
-//      threshold T (the (k-1)-th).  With |approx - exact| <= E, where
-//      E = 2^-13 ||q_r|| max_c ||kbar_c|| (at least 8x the worst case of the
-//      bf16 split, the fp32 MMA accumulation and the fp32 dot product), every
-//      block the exact rule selects has approx >= T - 2E.
-//   3. Only those candidates get the exact fp32 score, with the summation
-//      order of the CUDA-core gate (four lane partials of four interleaved
-//      sums), so the selection -- and its lower-index tie-break -- equals that
-//      kernel's bit for bit.
-// Rows whose own block has at most k-1 predecessors take them all.  With
-// COUNT every past selection also gets its regroup ticket (shared-memory
-// histogram + one global atomic per non-empty bin).
+// Persistent: one CTA per SM walks a contiguous range of units, a unit being
+// 128 consecutive query rows of one (sequence, head).  Units are ordered
+// sequence, head, row tile (the tiles of a head alternate from both ends so a
+// range mixes cheap early rows with costly late ones), so a CTA keeps the
+// pooled keys of one head resident for many units.  320 threads:
+//   warp 0      TMA: a 3-stage ring of q tiles and, whenever the (sequence,
+//               head) changes, the head's pooled keys split into two bf16
+//               terms, kbar ~= hi + lo (hi = bf16(kbar), lo = bf16(kbar - hi));
+//   warp 1      allocates TMEM; lane 0 issues one MMA chain per unit,
+//               approx[r][c] = q_r . hi_c + q_r . lo_c (M128, N = the unit's
+//               scored blocks rounded up to 16, fp32 in TMEM), alternating
+//               between two 256-column TMEM halves;
+//   warps 2..9  two selection warpgroups taking alternate units; thread r
+//               owns row r (its TMEM lane):
+//     1. keeps the top k-1 approximate scores of its row and the k-th.  With
+//        |approx - exact| <= E, E = 2^-13 ||q_r|| max_c ||kbar_c|| (at least
+//        8x the worst case of the bf16 split, the fp32 MMA accumulation and
+//        the fp32 dot product): when the k-th is below T - 2E (T the (k-1)-th)
+//        the approximate top k-1 is the exact one and the row is done;
+//     2. otherwise every block with approx >= T - 2E gets the exact fp32
+//        score, with the summation order of the CUDA-core gate (four lane
+//        partials of four interleaved sums), so the selection -- and its
+//        lower-index tie-break -- equals that kernel's bit for bit.
+// Rows whose own block has at most k-1 predecessors take them all.
+// Every wait is bounded; a wait that runs out records MOBA_ERR_TIMEOUT.
+#include <algorithm>
+
 #include "moba.h"
 #include "moba_internal.cuh"
 #include "moba_ptx.cuh"
@@ -32,37 +41,87 @@ namespace moba {
 namespace gate_tc {
 using namespace ptx;
 
-constexpr int kRows = 128;
-constexpr int kThreads = 128;
-constexpr int kMaxBlocks = 256;  // scored blocks a row may have (TMEM columns)
-constexpr int kHistBins = 512;
+constexpr int kRows = 128;                     // query rows per unit (the MMA's M)
+constexpr int kSelWarps = 8;                   // two selection warpgroups
+constexpr int kThreads = 64 + 32 * kSelWarps;  // TMA warp, MMA warp, selection
+constexpr int kMaxQ = 6;                       // q stages at most
+constexpr int kMaxSlots = 8;                   // TMEM score slots at most
+constexpr int kMaxBlocks = 256;                // blocks per sequence
 constexpr int kEmpty = 0x7fffffff;
 
 struct Args {
     Geometry g;
+    const __nv_bfloat16 *q;  // [total][H][D]
+    int *counts;             // [NB * H] selections per (block, head), or nullptr
+    // rows the score margin cannot settle, for the exact kernel: two words per
+    // row, the row (token * H + head, bit 62 set when every past block is a
+    // candidate) and up to 8 candidate blocks, one byte each, ascending (0xff
+    // = none)
+    unsigned long long *need_list;
+    int *need_count;
+    const int *gtile;    // [num_seqs + 1] 128-row tiles before each sequence
     const float *kbar;   // [NB][H][D] fp32
     const float *knorm;  // [NB][H] L2 norms of the pooled keys
     int32_t *idx;
-    int *ticket;
-    int *counts;
     int topk;
+    // layout chosen by the host from the longest sequence's block count W
+    // (64, 128 or 256): nslots = 512 / W units in flight in TMEM, kb_rows =
+    // pooled-key rows kept resident (W rounded up to 128), nq q stages in
+    // the shared memory left
+    int nq, nslots, kb_rows;
     int *status;
     long long wait_limit;
 };
 
-// CH = blocks per MMA chain (the MMA's N): 64 when every sequence has at most
-// 64 blocks (a smaller footprint, three CTAs per SM), else 128
-template <int D, int CH>
+template <int D>
 struct Smem {
     static constexpr int NB = D / 64;
-    static constexpr uint32_t kQBox = 128 * 128;  // 128 rows x 128 bytes
-    static constexpr uint32_t kBBox = CH * 128;
-    static constexpr uint32_t kQ = 0;
-    static constexpr uint32_t kHi = kQ + NB * kQBox;
-    static constexpr uint32_t kLo = kHi + NB * kBBox;
-    static constexpr uint32_t kTiles = kLo + NB * kBBox;
-    static constexpr uint32_t kRequest = kTiles + 1024;
+    static constexpr uint32_t kQBox = kRows * 128;       // 128 rows x 64 dims
+    static constexpr uint32_t kQStage = NB * kQBox;
+    // tiles from a 1024-byte aligned base: nq q stages, then hi and lo, each
+    // NB boxes of kb_rows x 64 dims
+    // mbarriers: q_full[kMaxQ], q_empty[kMaxQ], kb_full, kb_empty,
+    // s_full[kMaxSlots], s_empty[kMaxSlots], drain; then the TMEM address slot
+    // and the abort flag
+    static constexpr int kBarQF = 0, kBarQE = kBarQF + kMaxQ, kBarKF = kBarQE + kMaxQ,
+                         kBarKE = kBarKF + 1, kBarSF = kBarKE + 1, kBarSE = kBarSF + kMaxSlots,
+                         kBarDrain = kBarSE + kMaxSlots, kNumBars = kBarDrain + 1;
+    static constexpr uint32_t kMisc = kNumBars * 8 + 8;
+    // the misc words go into the alignment slack when it is large enough, else
+    // after the tiles
+    static constexpr uint32_t kTileBudget = 227 * 1024 - 1008 - kMisc;
+    __host__ __device__ static uint32_t kb_bytes(int kb_rows) { return 2u * NB * kb_rows * 128; }
+    __host__ __device__ static uint32_t tiles(int nq, int kb_rows) {
+        return nq * kQStage + kb_bytes(kb_rows);
+    }
 };
+
+struct Unit {
+    int b, h, t, seq0, L, bbase, nb, cmax;
+};
+
+// unit u -> (sequence, head, row tile); cmax = blocks scored by some row of
+// the tile (0 when no row is scored)
+__device__ __forceinline__ void get_unit(const Args &a, long long u, int km1, Unit &U) {
+    const int H = a.g.H;
+    int lo = 0, hi = a.g.num_seqs - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((long long)__ldg(a.gtile + mid) * H <= u) lo = mid; else hi = mid - 1;
+    }
+    U.b = lo;
+    const int tb = __ldg(a.gtile + lo), nt = __ldg(a.gtile + lo + 1) - tb;
+    const long long rem = u - (long long)tb * H;
+    U.h = (int)(rem / nt);
+    const int tz = (int)(rem % nt);
+    U.t = (tz & 1) ? nt - 1 - (tz >> 1) : (tz >> 1);
+    U.seq0 = __ldg(a.g.cu + lo);
+    U.L = __ldg(a.g.cu + lo + 1) - U.seq0;
+    U.bbase = __ldg(a.g.blk_base + lo);
+    U.nb = (U.L + a.g.bs - 1) / a.g.bs;
+    const int cl = (min(U.L, (U.t + 1) * kRows) - 1) / a.g.bs;
+    U.cmax = (km1 > 0 && cl > km1) ? cl : 0;
+}
 
 // bf16 element d of row r of a K-major, 128-byte-swizzled [128][D] tile
 template <int D>
@@ -75,7 +134,8 @@ __device__ __forceinline__ uint32_t q_addr(uint32_t base, int r, int d) {
 // dims [j*D/4, (j+1)*D/4) with four interleaved FMA chains, then
 // (p0 + p1) + (p2 + p3).
 template <int D>
-__device__ __forceinline__ float exact_score(uint32_t sq, int r, const float *__restrict__ kb) {
+__device__ __noinline__ float exact_score(const __nv_bfloat16 *__restrict__ qg,
+                                          const float *__restrict__ kb) {
     constexpr int DL = D / 4, M = DL / 4;
     float p[4];
 #pragma unroll
@@ -84,8 +144,8 @@ __device__ __forceinline__ float exact_score(uint32_t sq, int r, const float *__
 #pragma unroll
         for (int m = 0; m < M; ++m) {
             const int d = j * DL + 4 * m;
-            uint32_t lo, hi;
-            asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(lo), "=r"(hi) : "r"(q_addr<D>(sq, r, d)));
+            const uint2 qw = __ldg(reinterpret_cast<const uint2 *>(qg + d));
+            const uint32_t lo = qw.x, hi = qw.y;
             const float4 k4 = __ldg(reinterpret_cast<const float4 *>(kb + d));
             const float2 q01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&lo));
             const float2 q23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&hi));
@@ -121,277 +181,460 @@ __device__ __forceinline__ void top_insert(float (&ts)[KCAP], int (&ti)[KCAP], i
     }
 }
 
-template <int D, int CH, int KCAP, bool COUNT>
-__global__ void __launch_bounds__(kThreads)
+template <int D, int KCAP>
+__global__ void __launch_bounds__(kThreads, 1)
     gate_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                    const __grid_constant__ CUtensorMap tmap_hi,
                    const __grid_constant__ CUtensorMap tmap_lo, Args a) {
-    using L = Smem<D, CH>;
+    using L = Smem<D>;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t bars[2];  // loads, MMA chain
-    __shared__ uint32_t tmem_slot;
-    __shared__ int s_cmax, s_call, abort_word;
-    __shared__ unsigned s_knmax;
-    __shared__ int hist[kHistBins];
     const uint32_t raw = saddr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t sQ = base + L::kQ, sHi = base + L::kHi, sLo = base + L::kLo;
-    const uint32_t b_load = saddr(&bars[0]), b_mma = saddr(&bars[1]);
-
-    const int h = blockIdx.y, b = blockIdx.z, H = a.g.H;
-    const int seq0 = __ldg(a.g.cu + b), L_len = __ldg(a.g.cu + b + 1) - seq0;
-    const int i0 = blockIdx.x * kRows;
-    if (i0 >= L_len) return;
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int km1 = a.topk - 1;
-    const int bbase = __ldg(a.g.blk_base + b);
-    const int my_i = i0 + tid;
-    const bool my_valid = my_i < L_len;
-    const int my_ci = my_valid ? my_i / a.g.bs : 0;
-    const int my_tok = seq0 + my_i;
-    const bool my_scored = my_valid && km1 > 0 && my_ci > km1;
+    const uint32_t kKBox = (uint32_t)a.kb_rows * 128;  // one 64-dim box of pooled keys
+    const uint32_t misc = (base - raw >= L::kMisc) ? raw : base + L::tiles(a.nq, a.kb_rows);
+    uint8_t *gmisc = smem_raw + (misc - raw);
+    auto bar = [&](int i) -> uint32_t { return misc + 8u * (uint32_t)i; };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gmisc + L::kNumBars * 8);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(gmisc + L::kNumBars * 8 + 4);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = a.g.H, km1 = a.topk - 1;
+    const long long n_units = (long long)H * __ldg(a.gtile + a.g.num_seqs);
+    const long long u0 = n_units * blockIdx.x / gridDim.x;
+    const long long u1 = n_units * (blockIdx.x + 1) / gridDim.x;
+    if (u0 >= u1) return;
+    Ctl ctl{abort_flag, a.status, a.wait_limit};
+    const int nq = a.nq, nslots = a.nslots;
+    const uint32_t slot_cols = 512u / nslots;
+    const uint32_t sQ = base, sHi = base + nq * L::kQStage, sLo = sHi + L::NB * kKBox;
 
     if (tid == 0) {
-        s_cmax = 0;
-        s_call = 0;
-        s_knmax = 0u;
-        abort_word = 0;
-        mbar_init(b_load, 1);
-        mbar_init(b_mma, 1);
+        for (int s = 0; s < kMaxQ; ++s) {
+            mbar_init(bar(L::kBarQF + s), 1);
+            mbar_init(bar(L::kBarQE + s), 4);  // one arrival per selection warp
+        }
+        mbar_init(bar(L::kBarKF), 1);
+        mbar_init(bar(L::kBarKE), 1);
+        for (int w = 0; w < kMaxSlots; ++w) {
+            mbar_init(bar(L::kBarSF + w), 1);
+            mbar_init(bar(L::kBarSE + w), 4);
+        }
+        mbar_init(bar(L::kBarDrain), 1);
+        *abort_flag = 0;
         fence_mbar_init();
     }
-    if (COUNT)
-        for (int x = tid; x < kHistBins; x += kThreads) hist[x] = 0;
-    __syncthreads();
-    if (my_scored) atomicMax(&s_cmax, my_ci);
-    if (my_valid) atomicMax(&s_call, my_ci);
-    __syncthreads();
-    const int cmax = s_cmax;  // blocks 0 .. cmax-1 are scored for some row
-    Ctl ctl{reinterpret_cast<volatile int *>(&abort_word), a.status, a.wait_limit};
-
-    float ts[KCAP];
-    int ti[KCAP];
-#pragma unroll
-    for (int x = 0; x < KCAP; ++x) {
-        ts[x] = -INFINITY;
-        ti[x] = kEmpty;
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         saddr(tmem_slot)),
+                     "r"(512)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    bool ok = true;
-    if (cmax > 0) {
-        // TMEM: one fp32 column per scored block, rounded up to a power of 2
-        const int nchunk = (cmax + CH - 1) / CH;
-        const uint32_t tcols = (nchunk * CH <= 64) ? 64u : (nchunk * CH <= 128) ? 128u : 256u;
-        if (warp == 0) {
-            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                             saddr(&tmem_slot)),
-                         "r"(tcols)
-                         : "memory");
-            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-        }
-        // largest pooled-key norm among the scored blocks (for the margin)
-        for (int c = tid; c < cmax; c += kThreads)
-            atomicMax(&s_knmax, __float_as_uint(__ldg(a.knorm + (size_t)(bbase + c) * H + h)));
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        const uint32_t tmem = tmem_slot;
-        constexpr uint32_t idesc = idesc_bf16(128, CH, 0);
-        for (int ch = 0; ch < nchunk && ok; ++ch) {
-            if (tid == 0) {
-                const uint32_t bytes = (ch == 0 ? L::NB * L::kQBox : 0) + 2 * L::NB * L::kBBox;
-                mbar_expect_tx(b_load, bytes);
-                for (int x = 0; x < L::NB; ++x) {
-                    if (ch == 0)
-                        tma_load_3d(sQ + x * L::kQBox, &tmap_q, b_load, x * 64, h, seq0 + i0);
-                    tma_load_3d(sHi + x * L::kBBox, &tmap_hi, b_load, x * 64, h, bbase + ch * CH);
-                    tma_load_3d(sLo + x * L::kBBox, &tmap_lo, b_load, x * 64, h, bbase + ch * CH);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ================= TMA producer =================
+        if (lane == 0) {
+            long long cur = -1;  // (sequence, head) whose pooled keys are resident
+            int nload = 0, i = 0;
+            int qpend[kMaxQ];
+            for (int s = 0; s < kMaxQ; ++s) qpend[s] = -1;
+            bool go = true;
+            Unit U, NU;  // this unit and the next (fetched one unit ahead)
+            get_unit(a, u0, km1, U);
+            for (long long u = u0; go && u < u1; ++u, ++i, U = NU) {
+                if (u + 1 < u1) get_unit(a, u + 1, km1, NU);
+                const long long pair = (long long)U.b * H + U.h;
+                if (pair != cur) {
+                    // the MMAs that read the previous keys have completed
+                    if (nload > 0 && !wait_bar(bar(L::kBarKE), (nload - 1) & 1, ctl)) {
+                        go = false;
+                        break;
+                    }
+                    const int nch = (U.nb + 127) / 128;  // 128-block chunks, at most 2
+                    mbar_expect_tx(bar(L::kBarKF), 2u * L::NB * nch * 128 * 128);
+                    for (int x = 0; x < L::NB; ++x)
+                        for (int c = 0; c < nch; ++c) {
+                            const uint32_t off = x * kKBox + c * 128 * 128;
+                            tma_load_3d(sHi + off, &tmap_hi, bar(L::kBarKF), x * 64, U.h,
+                                        U.bbase + c * 128);
+                            tma_load_3d(sLo + off, &tmap_lo, bar(L::kBarKF), x * 64, U.h,
+                                        U.bbase + c * 128);
+                        }
+                    ++nload;
+                    cur = pair;
                 }
-                if (wait_bar(b_load, ch & 1, ctl)) {
-                    tc_fence_after();
-                    const uint32_t tS = tmem + ch * CH;
+                const int s = i % nq;
+                if (i >= nq && !wait_bar(bar(L::kBarQE + s), (i / nq - 1) & 1, ctl)) {
+                    go = false;
+                    break;
+                }
+                qpend[s] = -1;
+                mbar_expect_tx(bar(L::kBarQF + s), L::kQStage);
+                for (int x = 0; x < L::NB; ++x)
+                    tma_load_3d(sQ + s * L::kQStage + x * L::kQBox, &tmap_q, bar(L::kBarQF + s),
+                                x * 64, U.h, U.seq0 + U.t * kRows);
+                qpend[s] = i;
+            }
+            if (*abort_flag) {
+                // let the copies still in flight land before the CTA exits
+                for (int s = 0; s < kMaxQ; ++s)
+                    if (qpend[s] >= 0)
+                        drain_bar(bar(L::kBarQF + s), (qpend[s] / nq) & 1, a.wait_limit);
+                if (nload > 0) drain_bar(bar(L::kBarKF), (nload - 1) & 1, a.wait_limit);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ================= MMA issuer =================
+        if (lane == 0) {
+            long long cur = -1;
+            int nload = 0, i = 0;
+            bool ok = true;
+            Unit U, NU;  // this unit and the next (fetched one unit ahead)
+            get_unit(a, u0, km1, U);
+            for (long long u = u0; ok && u < u1; ++u, ++i, U = NU) {
+                if (u + 1 < u1) get_unit(a, u + 1, km1, NU);
+                const long long pair = (long long)U.b * H + U.h;
+                if (pair != cur) {
+                    // the previous keys may be replaced once these MMAs complete
+                    if (nload > 0) tc_commit(bar(L::kBarKE));
+                    if (!wait_bar(bar(L::kBarKF), nload & 1, ctl)) {
+                        ok = false;
+                        break;
+                    }
+                    ++nload;
+                    cur = pair;
+                }
+                const int s = i % nq, w = i % nslots;
+                if (!wait_bar(bar(L::kBarQF + s), (i / nq) & 1, ctl) ||
+                    (i >= nslots && !wait_bar(bar(L::kBarSE + w), (i / nslots - 1) & 1, ctl))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (U.cmax > 0) {
+                    const int n = min((int)slot_cols, (U.cmax + 15) & ~15);
+                    const uint32_t idesc = idesc_bf16(kRows, n, 0);
+                    const uint32_t tS = tmem + w * slot_cols;
+                    const uint32_t qb = sQ + s * L::kQStage;
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k) {
                         const uint32_t off = (uint32_t)(k % 4) * 32;
-                        tc_mma(tS, sdesc(sQ + (k / 4) * L::kQBox + off, 16, 1024),
-                               sdesc(sHi + (k / 4) * L::kBBox + off, 16, 1024), idesc, k > 0);
+                        tc_mma(tS, sdesc(qb + (k / 4) * L::kQBox + off, 16, 1024),
+                               sdesc(sHi + (k / 4) * kKBox + off, 16, 1024), idesc, k > 0);
                     }
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k) {
                         const uint32_t off = (uint32_t)(k % 4) * 32;
-                        tc_mma(tS, sdesc(sQ + (k / 4) * L::kQBox + off, 16, 1024),
-                               sdesc(sLo + (k / 4) * L::kBBox + off, 16, 1024), idesc, 1u);
+                        tc_mma(tS, sdesc(qb + (k / 4) * L::kQBox + off, 16, 1024),
+                               sdesc(sLo + (k / 4) * kKBox + off, 16, 1024), idesc, 1u);
                     }
-                    tc_commit(b_mma);
+                    tc_commit(bar(L::kBarSF + w));
+                } else {
+                    mbar_arrive(bar(L::kBarSF + w));  // no row of the unit is scored
                 }
             }
-            // all threads: the chain finished (its B tiles may be overwritten)
-            ok = __syncthreads_and(wait_bar(b_mma, ch & 1, ctl));
+            // every MMA this thread issued has finished before TMEM is freed
+            tc_commit(bar(L::kBarDrain));
+            drain_bar(bar(L::kBarDrain), 0, a.wait_limit);
+        }
+        __syncwarp();
+    } else {
+        // ================= selection (warps 2..9) =================
+        const int wg = (warp - 2) >> 2, quarter = warp & 3;
+        const int row = quarter * 32 + lane;  // my TMEM lane and q row
+        const uint32_t tlane = tmem + ((uint32_t)(quarter * 32) << 16);
+        Unit U, NU;  // this unit and the warpgroup's next (fetched one unit ahead)
+        if (u0 + wg < u1) get_unit(a, u0 + wg, km1, U);
+        for (long long u = u0 + wg, i = wg; u < u1; u += 2, i += 2, U = NU) {
+            if (u + 2 < u1) get_unit(a, u + 2, km1, NU);
+            const int s = (int)(i % nq), slot = (int)(i % nslots);
+            const uint32_t tS = tlane + slot * slot_cols;
+            const uint32_t sq = sQ + s * L::kQStage;
+            const int my_i = U.t * kRows + row;
+            const bool valid = my_i < U.L;
+            const int ci = valid ? my_i / a.g.bs : 0;
+            const int tok = U.seq0 + my_i;
+            const bool scored = valid && km1 > 0 && ci > km1;
+            // largest pooled-key norm among the unit's scored blocks (the margin)
+            float kn = 0.f;
+            for (int c = lane; c < U.cmax; c += 32)
+                kn = fmaxf(kn, __ldg(a.knorm + (size_t)(U.bbase + c) * H + U.h));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) kn = fmaxf(kn, __shfl_xor_sync(0xffffffffu, kn, o));
+
+            int ti[KCAP];  // selected past blocks, ascending, at the top end
+#pragma unroll
+            for (int x = 0; x < KCAP; ++x) ti[x] = kEmpty;
+            bool need = false;  // the exact kernel writes this row
+            unsigned long long cand = ~0ull;  // its candidate blocks, one byte each
+            int ncand = 0;
+            if (!__all_sync(0xffffffffu, wait_bar(bar(L::kBarSF + slot), (int)(i / nslots) & 1, ctl))) break;
             tc_fence_after();
-        }
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-        if (ok) {
-            // pass 1: top (k-1) of the approximate scores
-            float as[KCAP];
-            int ai[KCAP];
-#pragma unroll
-            for (int x = 0; x < KCAP; ++x) {
-                as[x] = -INFINITY;
-                ai[x] = kEmpty;
-            }
-            for (int c0 = 0; c0 < cmax; c0 += 32) {
-                uint32_t v[32];
-                tc_ld32(tmem + lane_off + c0, v);
-                tc_wait_ld();
-                if (my_scored) {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (c0 + e < my_ci) top_insert<KCAP>(as, ai, km1, __uint_as_float(v[e]), c0 + e);
-                }
-            }
-            float T = -INFINITY;
-#pragma unroll
-            for (int x = 0; x < KCAP; ++x)
-                if (x == km1 - 1) T = as[x];
-            // margin from the norms of q_r and of the pooled keys
+            // ||q_r||^2 for the margin: the last read of the q stage
             float qq = 0.f;
-            if (my_scored)
+            if (scored) {
 #pragma unroll
                 for (int d = 0; d < D; d += 8) {
                     uint32_t w[4];
                     asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                                  : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-                                 : "r"(q_addr<D>(sQ, tid, d)));
+                                 : "r"(q_addr<D>(sq, row, d)));
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[e]));
+                        const float2 f =
+                            __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[e]));
                         qq = fmaf(f.x, f.x, fmaf(f.y, f.y, qq));
                     }
                 }
-            const float E = 0x1p-13f * sqrtf(qq) * __uint_as_float(s_knmax);
-            const float thr = T - 2.f * E;
-            // pass 2: exact fp32 scores of the candidates, in block order
-            const float *kb_head = a.kbar + ((size_t)bbase * H + h) * D;
-            for (int c0 = 0; c0 < cmax; c0 += 32) {
-                uint32_t v[32];
-                tc_ld32(tmem + lane_off + c0, v);
-                tc_wait_ld();
-                if (my_scored) {
-                    uint32_t cand = 0u;  // bit e: block c0 + e is a candidate
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::kBarQE + s));  // the q stage is free
+            if (U.cmax > 0) {
+                // pass 1: the k largest approximate scores of the row (values only:
+                // a min/max insertion network, 2k-1 operations per block)
+                float tv[KCAP + 1];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (c0 + e < my_ci && __uint_as_float(v[e]) >= thr) cand |= 1u << e;
-                    while (cand) {
-                        const int c = c0 + __ffs(cand) - 1;
-                        cand &= cand - 1;
-                        top_insert<KCAP>(ts, ti, km1,
-                                         exact_score<D>(sQ, tid, kb_head + (size_t)c * H * D), c);
+                for (int x = 0; x <= KCAP; ++x) tv[x] = -INFINITY;
+                for (int c0 = 0; c0 < U.cmax; c0 += 32) {
+                    uint32_t v[32];
+                    tc_ld32(tS + c0, v);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const float x = (c0 + e < ci) ? __uint_as_float(v[e]) : -INFINITY;
+#pragma unroll
+                        for (int j = KCAP; j > 0; --j) tv[j] = fmaxf(tv[j], fminf(tv[j - 1], x));
+                        tv[0] = fmaxf(tv[0], x);
+                    }
+                }
+                float T = -INFINITY, Tk = -INFINITY;
+#pragma unroll
+                for (int x = 0; x <= KCAP; ++x) {
+                    if (x == km1 - 1) T = tv[x];
+                    if (x == km1) Tk = tv[x];
+                }
+                const float E = 0x1p-13f * sqrtf(qq) * kn;
+                // When the k-th is below T - 2E the blocks with approx >= T are
+                // the exact top k-1 (exactly k-1 of them).  Otherwise the blocks
+                // with approx >= T - 2E (a superset of the exact top k-1, every
+                // other block scoring below all of them) go to the exact kernel.
+                need = scored && !(Tk < T - 2.f * E);
+                const float cut = need ? T - 2.f * E : T;
+                if (__any_sync(0xffffffffu, scored)) {
+                    for (int c0 = 0; c0 < U.cmax; c0 += 32) {
+                        uint32_t v[32];
+                        tc_ld32(tS + c0, v);
+                        tc_wait_ld();
+                        uint32_t mask = 0u;  // bit e: block c0 + e is selected / a candidate
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (c0 + e < ci && __uint_as_float(v[e]) >= cut) mask |= 1u << e;
+                        if (!scored) mask = 0u;
+                        while (mask) {
+                            const int c = c0 + __ffs(mask) - 1;
+                            mask &= mask - 1;
+                            if (need) {
+                                if (ncand < 8) cand = (cand << 8) | (unsigned long long)c;
+                                ++ncand;
+                            } else {
+                                // ascending arrival: shift in at the top end
+#pragma unroll
+                                for (int x = 0; x + 1 < KCAP; ++x) ti[x] = ti[x + 1];
+                                ti[KCAP - 1] = c;
+                            }
+                        }
                     }
                 }
             }
-        }
-        tc_fence_before();
-        __syncthreads();
-        if (warp == 0) {
-            tc_fence_after();
-            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                         "r"(tcols)
-                         : "memory");
-        }
-    }
-    if (!ok) return;  // MOBA_ERR_TIMEOUT has been recorded
-
-    // selected past blocks of my row, ascending
-    int npast = 0;
-    if (my_valid) {
-        if (my_scored) {
-#pragma unroll
-            for (int x = 0; x < KCAP; ++x)
-                if (x >= km1) ti[x] = kEmpty;
-#pragma unroll
-            for (int pass = 0; pass < KCAP; ++pass) {
-#pragma unroll
-                for (int x = pass & 1; x + 1 < KCAP; x += 2) {
-                    const int lo = min(ti[x], ti[x + 1]), hi = max(ti[x], ti[x + 1]);
-                    ti[x] = lo;
-                    ti[x + 1] = hi;
+            // rows left to the exact kernel: one list reservation per warp
+            const unsigned nmask = __ballot_sync(0xffffffffu, need);
+            if (nmask) {
+                const int leader = __ffs(nmask) - 1;
+                int base = 0;
+                if (lane == leader) base = atomicAdd(a.need_count, __popc(nmask));
+                base = __shfl_sync(0xffffffffu, base, leader);
+                if (need) {
+                    const int slot2 = 2 * (base + __popc(nmask & ((1u << lane) - 1u)));
+                    const unsigned long long row = (unsigned long long)tok * H + U.h;
+                    a.need_list[slot2] = ncand > 8 ? (row | (1ull << 62)) : row;
+                    a.need_list[slot2 + 1] = cand;
                 }
             }
-            npast = km1;
-        } else {
-            npast = (km1 == 0) ? 0 : my_ci;
+            // the TMEM half is free for the unit after next
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::kBarSE + slot));
+
+            // selected past blocks of my row, ascending, then the own block
+            if (valid && !need) {
+                int npast;
+                int32_t *out = a.idx + ((size_t)tok * H + U.h) * a.topk;
+                if (scored) {
 #pragma unroll
-            for (int x = 0; x < KCAP; ++x) ti[x] = x;
-        }
-        int32_t *out = a.idx + ((size_t)my_tok * H + h) * a.topk;
-        if (my_scored) {
+                    for (int pass = 0; pass < KCAP; ++pass) {
 #pragma unroll
-            for (int x = 0; x < KCAP; ++x)
-                if (x < npast) out[x] = ti[x];
-        } else {
-            for (int x = 0; x < npast; ++x) out[x] = x;
+                        for (int x = pass & 1; x + 1 < KCAP; x += 2) {
+                            const int lo = min(ti[x], ti[x + 1]), hi = max(ti[x], ti[x + 1]);
+                            ti[x] = lo;
+                            ti[x + 1] = hi;
+                        }
+                    }
+                    npast = km1;
+#pragma unroll
+                    for (int x = 0; x < KCAP; ++x)
+                        if (x < npast) out[x] = ti[x];
+                } else {
+                    npast = (km1 == 0) ? 0 : ci;  // every past block (ci <= km1)
+                    for (int x = 0; x < npast; ++x) out[x] = x;
+                }
+                out[npast] = ci;
+                for (int x = npast + 1; x < a.topk; ++x) out[x] = -1;
+            }
+            // selections per (block, head): one reduction per distinct block of
+            // the warp and slot
+            if (a.counts && km1 > 0) {
+                const int npast = (!valid || need) ? 0 : scored ? km1 : ci;
+#pragma unroll
+                for (int x = 0; x < KCAP; ++x) {
+                    const int c = (x < npast) ? (scored ? ti[x] : x) : -1;
+                    const unsigned grp = __match_any_sync(0xffffffffu, c);
+                    if (c >= 0 && lane == __ffs(grp) - 1)
+                        atomicAdd(a.counts + (size_t)(U.bbase + c) * H + U.h, __popc(grp));
+                }
+                // unscored rows with more past blocks than KCAP slots
+                for (int x = KCAP; x < npast; ++x)
+                    atomicAdd(a.counts + (size_t)(U.bbase + x) * H + U.h, 1);
+            }
         }
-        out[npast] = my_ci;
-        for (int x = npast + 1; x < a.topk; ++x) out[x] = -1;
     }
-    if (COUNT) {
-        int rank[KCAP];
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(512)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Rows the margin could not settle, one thread each: exact fp32 scores (the
+// CUDA-core gate's summation order) of the row's candidates -- or, when it had
+// more than 8, of every past block -- in ascending block order, the top k-1 of
+// them by (score descending, block ascending), written like the gate's rows.
+// ---------------------------------------------------------------------------
+template <int D, int KCAP>
+__global__ void __launch_bounds__(256)
+    gate_exact_kernel(Geometry g, const __nv_bfloat16 *__restrict__ q,
+                      const float *__restrict__ kbar, int32_t *__restrict__ idx, int topk,
+                      int *__restrict__ counts, const unsigned long long *__restrict__ need_list,
+                      const int *__restrict__ need_count) {
+    const int n = *need_count;
+    const int km1 = topk - 1;
+    for (int w = blockIdx.x * blockDim.x + threadIdx.x; w < n; w += gridDim.x * blockDim.x) {
+        const unsigned long long w0 = need_list[2 * w], cand = need_list[2 * w + 1];
+        const bool all = (w0 >> 62) & 1ull;
+        const long long r = (long long)(w0 & ((1ull << 62) - 1));
+        const int t = (int)(r / g.H), h = (int)(r % g.H);
+        const int b = upper_index(g.cu, g.num_seqs, t);
+        const int ci = (t - __ldg(g.cu + b)) / g.bs;
+        const int bbase = __ldg(g.blk_base + b);
+        const __nv_bfloat16 *qg = q + (size_t)r * D;
+        const float *kb_head = kbar + ((size_t)bbase * g.H + h) * D;
+        float ts[KCAP];
+        int ti[KCAP];
 #pragma unroll
         for (int x = 0; x < KCAP; ++x) {
-            rank[x] = 0;
-            if (x < npast) {
-                const int c = ti[x];
-                rank[x] = (c < kHistBins) ? atomicAdd(&hist[c], 1)
-                                          : atomicAdd(a.counts + (size_t)(bbase + c) * H + h, 1);
+            ts[x] = -INFINITY;
+            ti[x] = kEmpty;
+        }
+        if (all) {
+            for (int c = 0; c < ci; ++c)
+                top_insert<KCAP>(ts, ti, km1, exact_score<D>(qg, kb_head + (size_t)c * g.H * D), c);
+        } else {
+            // candidate bytes were shifted in from the low end: the oldest
+            // (lowest block) sits highest
+            int nc = 0;
+            for (int x = 0; x < 8; ++x) nc += ((cand >> (8 * x)) & 0xffull) != 0xffull;
+            for (int x = nc - 1; x >= 0; --x) {
+                const int c = (int)((cand >> (8 * x)) & 0xffull);
+                top_insert<KCAP>(ts, ti, km1, exact_score<D>(qg, kb_head + (size_t)c * g.H * D), c);
             }
         }
-        __syncthreads();
-        const int nbins = min(kHistBins, s_call);
-        for (int x = tid; x < nbins; x += kThreads) {
-            const int n = hist[x];
-            hist[x] = n ? atomicAdd(a.counts + (size_t)(bbase + x) * H + h, n) : 0;
-        }
-        __syncthreads();
-        if (my_valid) {
-            int *tk = a.ticket + ((size_t)my_tok * H + h) * km1;
 #pragma unroll
-            for (int x = 0; x < KCAP; ++x) {
-                if (x < npast) {
-                    const int c = ti[x];
-                    tk[x] = (c < kHistBins) ? hist[c] + rank[x] : rank[x];
-                }
+        for (int pass = 0; pass < KCAP; ++pass) {
+#pragma unroll
+            for (int x = pass & 1; x + 1 < KCAP; x += 2) {
+                const int lo = min(ti[x], ti[x + 1]), hi = max(ti[x], ti[x + 1]);
+                ti[x] = lo;
+                ti[x + 1] = hi;
             }
         }
+        int32_t *out = idx + (size_t)r * topk;
+#pragma unroll
+        for (int x = 0; x < KCAP; ++x)
+            if (x < km1) {
+                out[x] = ti[x];
+                if (counts) atomicAdd(counts + (size_t)(bbase + ti[x]) * g.H + h, 1);
+            }
+        out[km1] = ci;
+        for (int x = km1 + 1; x < topk; ++x) out[x] = -1;
     }
 }
 
 }  // namespace gate_tc
 
 bool gate_tc_supported(const Plan &p) {
-    // TMEM holds two chunks of 128 block scores; the exact pass keeps the
-    // top list in registers
+    // a warpgroup's TMEM half holds 256 block scores; the selection keeps its
+    // top lists in registers
     const long long nmax = (p.max_len + p.bs - 1) / p.bs;
     return nmax <= gate_tc::kMaxBlocks && p.topk - 1 <= 32 && (p.D == 64 || p.D == 128);
 }
 
-template <int D, int CH, bool COUNT>
+static int sm_count_gate() {
+    static int cached[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (!cached[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = n > 0 ? n : 1;
+    }
+    return cached[dev];
+}
+
+template <int D>
 static cudaError_t launch_gate_tc_d(const Plan &p, const gate_tc::Args &a, const __nv_bfloat16 *q,
                                     const __nv_bfloat16 *khi, const __nv_bfloat16 *klo,
                                     cudaStream_t st) {
     CUtensorMap mq, mh, ml;
-    if (!make_tma_3d(&mq, q, p.total, p.H, D, 128) || !make_tma_3d(&mh, khi, p.NBcap, p.H, D, CH) ||
-        !make_tma_3d(&ml, klo, p.NBcap, p.H, D, CH))
+    if (!make_tma_3d(&mq, q, p.total, p.H, D, gate_tc::kRows) ||
+        !make_tma_3d(&mh, khi, p.NBcap, p.H, D, 128) || !make_tma_3d(&ml, klo, p.NBcap, p.H, D, 128))
         return cudaErrorInvalidValue;
-    dim3 grid((p.max_len + gate_tc::kRows - 1) / gate_tc::kRows, p.H, p.num_seqs);
-    const int smem = gate_tc::Smem<D, CH>::kRequest;
+    // an upper bound of the units; CTAs beyond the real count return at once
+    const long long units_max =
+        (long long)p.H * (((long long)p.total + gate_tc::kRows - 1) / gate_tc::kRows + p.num_seqs);
+    const int grid = (int)std::min<long long>(sm_count_gate(), units_max);
     const int km1 = p.topk - 1;
-#define MOBA_GATE_TC_CASE(KC)                                                                 \
-    {                                                                                         \
-        auto kern = gate_tc::gate_tc_kernel<D, CH, KC, COUNT>;                                    \
+    using L = gate_tc::Smem<D>;
+    const int smem = (int)(L::tiles(a.nq, a.kb_rows) + 1008 + L::kMisc);
+#define MOBA_GATE_TC_CASE(KC)                                                                   \
+    {                                                                                           \
+        auto kern = gate_tc::gate_tc_kernel<D, KC>;                                             \
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                                             smem);                                           \
-        if (e != cudaSuccess) return e;                                                       \
-        kern<<<grid, gate_tc::kThreads, smem, st>>>(mq, mh, ml, a);                           \
-        return cudaGetLastError();                                                            \
+                                             smem);                                             \
+        if (e != cudaSuccess) return e;                                                         \
+        kern<<<grid, gate_tc::kThreads, smem, st>>>(mq, mh, ml, a);                             \
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;                                  \
+        gate_tc::gate_exact_kernel<D, KC><<<4 * sm_count_gate(), 256, 0,                        \
+                                             st>>>(a.g, a.q, a.kbar, a.idx, a.topk, a.counts,  \
+                                                   a.need_list, a.need_count);                 \
+        return cudaGetLastError();                                                              \
     }
     if (km1 <= 1) MOBA_GATE_TC_CASE(1)
     if (km1 <= 2) MOBA_GATE_TC_CASE(2)
@@ -404,7 +647,8 @@ static cudaError_t launch_gate_tc_d(const Plan &p, const gate_tc::Args &a, const
 
 cudaError_t launch_gate_tc(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
                            const float *kbar, const __nv_bfloat16 *khi, const __nv_bfloat16 *klo,
-                           const float *knorm, int32_t *idx, bool count, cudaStream_t st) {
+                           const float *knorm, int32_t *idx, int *counts,
+                           unsigned long long *need_list, int *need_count, cudaStream_t st) {
     gate_tc::Args a;
     a.g.cu = ws.cu;
     a.g.blk_base = ws.blk_base;
@@ -413,26 +657,31 @@ cudaError_t launch_gate_tc(const Plan &p, const Workspace &ws, const __nv_bfloat
     a.g.H = p.H;
     a.g.D = p.D;
     a.g.bs = p.bs;
+    a.q = q;
+    a.counts = counts;
+    a.need_list = need_list;
+    a.need_count = need_count;
+    a.gtile = ws.gtile;
     a.kbar = kbar;
     a.knorm = knorm;
     a.idx = idx;
-    a.ticket = count ? ws.ticket : nullptr;
-    a.counts = count ? ws.counts : nullptr;
     a.topk = p.topk;
     a.status = status_word();
     a.wait_limit = tc_wait_limit();
-    const bool small = (p.max_len + p.bs - 1) / p.bs <= 64;
-    cudaError_t e;
-#define MOBA_GATE_TC_D(DD, CC)                                                  \
-    e = count ? launch_gate_tc_d<DD, CC, true>(p, a, q, khi, klo, st)          \
-              : launch_gate_tc_d<DD, CC, false>(p, a, q, khi, klo, st);
-    if (p.D == 64) {
-        if (small) { MOBA_GATE_TC_D(64, 64) } else { MOBA_GATE_TC_D(64, 128) }
-    } else {
-        if (small) { MOBA_GATE_TC_D(128, 64) } else { MOBA_GATE_TC_D(128, 128) }
-    }
-#undef MOBA_GATE_TC_D
-    note_launches(1);
+    // TMEM slot width W: the longest sequence's blocks rounded up to 64, 128
+    // or 256 columns; as many q stages as the shared memory left holds
+    const int nmax = (p.max_len + p.bs - 1) / p.bs;
+    const int W = nmax <= 64 ? 64 : nmax <= 128 ? 128 : 256;
+    a.nslots = 512 / W;
+    a.kb_rows = W <= 128 ? 128 : 256;
+    const uint32_t budget = p.D == 64 ? gate_tc::Smem<64>::kTileBudget : gate_tc::Smem<128>::kTileBudget;
+    const uint32_t kb = p.D == 64 ? gate_tc::Smem<64>::kb_bytes(a.kb_rows)
+                                  : gate_tc::Smem<128>::kb_bytes(a.kb_rows);
+    const uint32_t qstage = p.D == 64 ? gate_tc::Smem<64>::kQStage : gate_tc::Smem<128>::kQStage;
+    a.nq = std::min<int>(gate_tc::kMaxQ, (int)((budget - kb) / qstage));
+    const cudaError_t e = p.D == 64 ? launch_gate_tc_d<64>(p, a, q, khi, klo, st)
+                                    : launch_gate_tc_d<128>(p, a, q, khi, klo, st);
+    note_launches(2);
     return e;
 }
 

@@ -46,13 +46,16 @@ __device__ __forceinline__ int upper_index(const int *__restrict__ tab, int num_
 struct Workspace {
     int *cu;          // [num_seqs + 1]
     int *blk_base;    // [num_seqs + 1]
+    int *gtile;       // [num_seqs + 1]  128-row gate tiles before each sequence
     float *kbar;      // [NBcap][H][D]
     int32_t *idx;     // [total][H][topk]
-    int *counts;      // [NBcap * H]   queries per (block, head) past list
+    int *counts;      // [NBcap * H]   queries per (block, head) past list (zero
+                      //               again once the scatter has used them)
+    int *need_count;  // [1] rows the tensor-core gate left to its exact kernel
+    unsigned long long *need_list;  // [2 * total * H] those rows and their candidates
     int *list_off;    // [NBcap * H + 1]
     int *tile_off;    // [NBcap * H + 1]  first attention job of each list
     int *job_list;    // [jobs]  list of every past-block attention job
-    int *ticket;      // [total * H * km1]  position of a selection inside its list
     __nv_bfloat16 *kbhi, *kblo;  // [NBcap][H][D] bf16 split of kbar (tensor-core gate)
     float *knorm;                // [NBcap][H] L2 norm of each pooled key
     int *list;        // [total * H * km1]  entries token << 5 | slot
@@ -75,8 +78,10 @@ cudaError_t launch_setup(const Plan &p, const int *cu_dev, Workspace &ws, cudaSt
 cudaError_t launch_kpool(const Plan &p, const Workspace &ws, const __nv_bfloat16 *k,
                          float *kbar, cudaStream_t st);
 cudaError_t launch_gate(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
-                        const float *kbar, int32_t *idx, bool count, cudaStream_t st);
-cudaError_t launch_regroup(const Plan &p, const Workspace &ws, cudaStream_t st);
+                        const float *kbar, int32_t *idx, cudaStream_t st);
+// per-(block, head) lists of the past selections: count (unless the gate has
+// already added its selections into ws.counts), scan, scatter
+cudaError_t launch_regroup(const Plan &p, const Workspace &ws, bool counted, cudaStream_t st);
 // attention over the selected past blocks (skipped on the dense / top-1 paths)
 cudaError_t launch_attn_past(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
                              const __nv_bfloat16 *k, const __nv_bfloat16 *v, cudaStream_t st);
@@ -111,11 +116,16 @@ bool make_tma_3d(CUtensorMap *m, const void *ptr, int total, int H, int D, int r
 // kbar (fp32) -> hi = bf16(kbar), lo = bf16(kbar - hi)
 cudaError_t launch_kbar_split(const Plan &p, const float *kbar, __nv_bfloat16 *hi,
                               __nv_bfloat16 *lo, float *norm, cudaStream_t st);
-// tensor-core gate (scores on tcgen05, exact fp32 re-score of the candidates)
+// tensor-core gate (scores on tcgen05, exact fp32 re-score of the candidates);
+// with counts != nullptr it also adds every past selection into counts.
+// need_list (room for every row) and *need_count (zero on entry) carry the rows
+// whose selection the score margin cannot settle to the exact follow-up kernel
 bool gate_tc_supported(const Plan &p);
 cudaError_t launch_gate_tc(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
                            const float *kbar, const __nv_bfloat16 *khi, const __nv_bfloat16 *klo,
-                           const float *knorm, int32_t *idx, bool count, cudaStream_t st);
+                           const float *knorm, int32_t *idx, int *counts,
+                           unsigned long long *need_list,
+                           int *need_count, cudaStream_t st);
 int mma_tile_rows();
 void tc_debug_set(int flags, long long wait_limit);
 
