@@ -60,6 +60,36 @@ def hbm_bytes(w, topk: int):
     return {"kpool": pool, "gate": gate}
 
 
+# DRAM bytes (read + write) per launch of the dominant kernel, from one ncu
+# capture of the command that produces the default line (the capture and its
+# command are summarised under profiles/).  A figure is reported only while
+# the kernel's sources hash to what was captured.
+TRAFFIC_SOURCES = ("long_context_sparse_moba_gb300/csrc/moba_attn_tc.cu",
+                   "long_context_sparse_moba_gb300/csrc/moba_ptx.cuh",
+                   "long_context_sparse_moba_gb300/csrc/moba_internal.cuh")
+MEASURED_TRAFFIC = {
+    # (workload, topk, phase): (bytes per launch, sha256 of TRAFFIC_SOURCES)
+    ("train32k", 3, "attn_past"): (1037235200 + 538467072,
+                                   "ebd0aa58817bccf6ac8e79c044f55931ab7c362590ead5068e295eea8a48ba64"),
+}
+
+
+def sources_sha256() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload: str, topk: int, phase: str):
+    ent = MEASURED_TRAFFIC.get((workload, topk, phase))
+    if ent is None or ent[1] != sources_sha256():
+        return None
+    return ent[0]
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -395,7 +425,7 @@ def main():
         achieved, peak, unit = (amount / (dms * 1e-3) / 1e12, peaks["bf16_tflops_sustained"],
                                 "TFLOP/s")
     roofline = {"kernel": dom, "bound": kind, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "traffic": None,
+                "frac": achieved / peak, "traffic": measured_traffic(w.name, topk, dom),
                 "peak_source": f"{peak_src} ({'bf16_tflops_sustained' if kind == 'tensor' else 'hbm_gbs'})"}
 
     cpu = None
