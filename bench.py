@@ -90,6 +90,37 @@ def measured_traffic(workload: str, topk: int, phase: str):
     return ent[0]
 
 
+# ---- multi-rank host logic (one process per GPU, weak scaling) ----
+def dist_env():
+    """(world size, rank, local rank) from the launcher's environment."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_workload(w, rank: int):
+    """The workload a rank times: same shapes, its own seed (independent
+    sequences / heads, so the ranks never exchange data)."""
+    from long_context_sparse_moba_gb300 import workloads
+    return workloads.Workload(**{**w.__dict__, "seed": w.seed + 1000 * rank})
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The slowest rank's value (a MAX all-reduce; a no-op on one rank)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(tokens_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Tokens per second of the whole job: every rank's tokens over the slowest
+    rank's step time."""
+    return tokens_per_rank * world / (ms_per_step * 1e-3)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -257,9 +288,7 @@ def main():
     w = workloads.WORKLOADS[args.workload]
     topk = args.topk if args.topk is not None else w.topks[0]
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = dist_env()
 
     if args.impl == "reference":
         if rank == 0:
@@ -281,7 +310,7 @@ def main():
     ops.lib()
 
     dev = torch.device("cuda", local)
-    wr = workloads.Workload(**{**w.__dict__, "seed": w.seed + 1000 * rank})
+    wr = rank_workload(w, rank)
     inp = workloads.make_inputs(wr, device=dev)
     q, k, v = inp.q, inp.k, inp.v
     varlen = w.varlen
@@ -329,10 +358,7 @@ def main():
     launches = ops.launch_count() - launches0
     clk = clocks.stop()
     status = ops.get_status()
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     ms_per_step = elapsed_ms / args.steps
 
     # dense comparison: same kernels with top-k = number of blocks
@@ -380,12 +406,8 @@ def main():
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        ems = e0.elapsed_time(e1) / esteps
-        if world > 1:
-            t = torch.tensor([ems], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": w.total * world / (ems * 1e-3), "unit": "tokens/s",
+        ems = max_over_ranks(e0.elapsed_time(e1) / esteps, world, dev)
+        e2e = {"value": whole_job_rate(w.total, world, ems), "unit": "tokens/s",
                "h2d_bytes_per_step": 3 * q.numel() * 2,
                "d2h_bytes_per_step": out.numel() * 2 + lse.numel() * 4,
                "ms_per_step": ems}
@@ -432,7 +454,7 @@ def main():
     if not args.no_cpu_baseline:
         cpu = cpu_baseline(w, inp, topk)
 
-    line = {"metric": METRIC, "value": w.total * world / (ms_per_step * 1e-3), "unit": "tokens/s",
+    line = {"metric": METRIC, "value": whole_job_rate(w.total, world, ms_per_step), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
