@@ -531,8 +531,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_wait_ld();
                     MOBA_MASK64(sr, 64 * h2)
 #pragma unroll
-                    for (int c = 0; c < 64; ++c)
-                        mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(sr[c >> 5][c & 31]));
+                    for (int c = 0; c < 64; c += 8) {
+                        mx[(c >> 3) & 3] = fmax3(mx[(c >> 3) & 3], __uint_as_float(sr[c >> 5][c & 31]),
+                                                 __uint_as_float(sr[c >> 5][(c & 31) + 1]));
+                        mx[(c >> 3) & 3] = fmax3(mx[(c >> 3) & 3], __uint_as_float(sr[c >> 5][(c & 31) + 2]),
+                                                 __uint_as_float(sr[c >> 5][(c & 31) + 3]));
+                        mx[(c >> 3) & 3] = fmax3(mx[(c >> 3) & 3], __uint_as_float(sr[c >> 5][(c & 31) + 4]),
+                                                 __uint_as_float(sr[c >> 5][(c & 31) + 5]));
+                        mx[(c >> 3) & 3] = fmax3(mx[(c >> 3) & 3], __uint_as_float(sr[c >> 5][(c & 31) + 6]),
+                                                 __uint_as_float(sr[c >> 5][(c & 31) + 7]));
+                    }
                 }
                 const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
                 const float m_new = fmaxf(m_run, mt);
@@ -558,7 +566,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // pass 2: p = 2^(s * scale - mu) as bf16 pairs (keys 2c, 2c+1 in
                 // column c) over the first 64 columns of S; half h2 of the keys goes
                 // to columns 32*h2 .. 32*h2+31, already read when h2 = 1 is written
-                float ls[4] = {0.f, 0.f, 0.f, 0.f};
+                // pairs of keys on the packed fp32 ALU
+                float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+                const float2 nmu2 = make_float2(-mu, -mu);
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2) {
                     uint32_t sr[2][32];
@@ -569,16 +580,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t pk[32];
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
-                        const float p0 = fast_exp2(fmaf(__uint_as_float(sr[(2 * c) >> 5][(2 * c) & 31]), a.scale_log2, -mu));
-                        const float p1 = fast_exp2(fmaf(__uint_as_float(sr[(2 * c + 1) >> 5][(2 * c + 1) & 31]), a.scale_log2, -mu));
-                        ls[c & 3] += p0 + p1;
-                        __nv_bfloat162 bb = __floats2bfloat162_rn(p0, p1);
+                        const float2 x = ffma2(make_float2(__uint_as_float(sr[(2 * c) >> 5][(2 * c) & 31]),
+                                                           __uint_as_float(sr[(2 * c + 1) >> 5][(2 * c + 1) & 31])),
+                                               sc2, nmu2);
+                        float2 pp;
+                        pp.x = fast_exp2(x.x);
+                        pp.y = fast_exp2(x.y);
+                        ls[c & 1] = fadd2(ls[c & 1], pp);
+                        __nv_bfloat162 bb = __floats2bfloat162_rn(pp.x, pp.y);
                         pk[c] = *reinterpret_cast<uint32_t *>(&bb);
                     }
                     tc_st32(tSg + 32 * h2, pk);
                 }
 #undef MOBA_MASK64
-                l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                l_run += (ls[0].x + ls[1].x) + (ls[0].y + ls[1].y);
                 tc_wait_st();
                 tc_fence_before();
                 __syncwarp();
