@@ -521,15 +521,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 SR[c >> 5][c & 31] = 0xff800000u;                                     \
         }                                                                             \
     }
-                // pass 1: row max of the raw scores (the scale is positive)
-                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
+                // One pass per 64-key half: the half's max decides the offset mu
+                // (raised, to a whole number, only when the max exceeds it by more
+                // than 8, so P <= 2^8 and every rescale is by an exact power of 2),
+                // then p = 2^(s * scale - mu) from the same registers, as bf16
+                // pairs (keys 2c, 2c+1 in column c) over the first 64 columns of
+                // S: half h2 goes to columns 32*h2 .. 32*h2+31, already read when
+                // h2 = 1 is written.  When the second half raises mu, the first
+                // half's P in TMEM and the running O and l are rescaled.
+                const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+#pragma unroll 1
                 for (int h2 = 0; h2 < 2; ++h2) {
                     uint32_t sr[2][32];
                     tc_ld32(tSg + 64 * h2, sr[0]);
                     tc_ld32(tSg + 64 * h2 + 32, sr[1]);
                     tc_wait_ld();
                     MOBA_MASK64(sr, 64 * h2)
+                    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
                     for (int c = 0; c < 64; c += 8) {
                         mx[(c >> 3) & 3] = fmax3(mx[(c >> 3) & 3], __uint_as_float(sr[c >> 5][c & 31]),
@@ -541,42 +549,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mx[(c >> 3) & 3] = fmax3(mx[(c >> 3) & 3], __uint_as_float(sr[c >> 5][(c & 31) + 6]),
                                                  __uint_as_float(sr[c >> 5][(c & 31) + 7]));
                     }
-                }
-                const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
-                const float m_new = fmaxf(m_run, mt);
-                // rescale only when the max grew by more than 2^8 (P stays <= 256)
-                const bool need = (jl > 0) && (m_new > m_run + 8.f);
-                const float m_use = (jl == 0 || need) ? m_new : m_run;
-                const float mu = (m_use == -INFINITY) ? 0.f : m_use;
-                if (jl > 0 && __any_sync(0xffffffffu, need)) {
-                    const float alpha = need ? fast_exp2(m_run - m_new) : 1.f;
+                    const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
+                    const bool raise = mt > m_run + 8.f;  // always for the first finite max
+                    const float m_new = raise ? ceilf(mt) : m_run;
+                    if (__any_sync(0xffffffffu, raise && (jl > 0 || h2 > 0))) {
+                        // 2^(old mu - new mu): 0 while nothing was accumulated yet
+                        const float alpha = raise ? pow2_whole(m_run - m_new) : 1.f;
+                        if (jl > 0) {  // O holds earlier tiles (this job's first PV overwrites it)
 #pragma unroll
-                    for (int c0 = 0; c0 < D; c0 += 16) {
-                        uint32_t o[16];
-                        tc_ld16(tOg + c0, o);
-                        tc_wait_ld();
+                            for (int c0 = 0; c0 < D; c0 += 16) {
+                                uint32_t o[16];
+                                tc_ld16(tOg + c0, o);
+                                tc_wait_ld();
 #pragma unroll
-                        for (int c = 0; c < 16; ++c)
-                            o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-                        tc_st16(tOg + c0, o);
+                                for (int c = 0; c < 16; ++c)
+                                    o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                                tc_st16(tOg + c0, o);
+                            }
+                        }
+                        if (h2 > 0) {  // the first half's P was made with the old mu
+                            tc_wait_st();
+#pragma unroll
+                            for (int c0 = 0; c0 < 32; c0 += 16) {
+                                uint32_t pw[16];
+                                tc_ld16(tSg + c0, pw);
+                                tc_wait_ld();
+#pragma unroll
+                                for (int c = 0; c < 16; ++c) {
+                                    float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&pw[c]));
+                                    __nv_bfloat162 bb = __floats2bfloat162_rn(f.x * alpha, f.y * alpha);
+                                    pw[c] = *reinterpret_cast<uint32_t *>(&bb);
+                                }
+                                tc_st16(tSg + c0, pw);
+                            }
+                        }
                     }
-                    if (need) l_run *= alpha;
-                }
-                m_run = m_use;
-                // pass 2: p = 2^(s * scale - mu) as bf16 pairs (keys 2c, 2c+1 in
-                // column c) over the first 64 columns of S; half h2 of the keys goes
-                // to columns 32*h2 .. 32*h2+31, already read when h2 = 1 is written
-                // pairs of keys on the packed fp32 ALU
-                float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-                const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
-                const float2 nmu2 = make_float2(-mu, -mu);
-#pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    uint32_t sr[2][32];
-                    tc_ld32(tSg + 64 * h2, sr[0]);
-                    tc_ld32(tSg + 64 * h2 + 32, sr[1]);
-                    tc_wait_ld();
-                    MOBA_MASK64(sr, 64 * h2)
+                    if (raise) {
+                        l_run *= pow2_whole(m_run - m_new);
+                        m_run = m_new;
+                    }
+                    const float mu = (m_run == -INFINITY) ? 0.f : m_run;
+                    const float2 nmu2 = make_float2(-mu, -mu);
+                    float2 ls[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
                     uint32_t pk[32];
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
@@ -591,9 +605,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         pk[c] = *reinterpret_cast<uint32_t *>(&bb);
                     }
                     tc_st32(tSg + 32 * h2, pk);
+                    l_run += (ls[0].x + ls[1].x) + (ls[0].y + ls[1].y);
                 }
 #undef MOBA_MASK64
-                l_run += (ls[0].x + ls[1].x) + (ls[0].y + ls[1].y);
                 tc_wait_st();
                 tc_fence_before();
                 __syncwarp();

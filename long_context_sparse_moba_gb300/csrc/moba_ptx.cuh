@@ -180,6 +180,10 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_pack(a)), "l"(f2_pack(b)));
     return f2_unpack(d);
 }
+// 2^d for a whole number d <= 0 (or -inf): exact; 0 below the normal range
+__device__ __forceinline__ float pow2_whole(float d) {
+    return d >= -126.f ? __int_as_float((127 + (int)d) << 23) : 0.f;
+}
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
