@@ -42,8 +42,9 @@ namespace gate_tc {
 using namespace ptx;
 
 constexpr int kRows = 128;                     // query rows per unit (the MMA's M)
-constexpr int kSelWarps = 8;                   // two selection warpgroups
-constexpr int kThreads = 64 + 32 * kSelWarps;  // TMA warp, MMA warp, selection
+// TMA warp, MMA warp and NWG selection warpgroups (four when the top lists
+// are short enough to fit the register budget of 20 warps, else two)
+__host__ __device__ constexpr int threads_for(int nwg) { return 64 + 128 * nwg; }
 constexpr int kMaxQ = 6;                       // q stages at most
 constexpr int kMaxSlots = 8;                   // TMEM score slots at most
 constexpr int kMaxBlocks = 256;                // blocks per sequence
@@ -101,27 +102,43 @@ struct Unit {
 };
 
 // unit u -> (sequence, head, row tile); cmax = blocks scored by some row of
-// the tile (0 when no row is scored)
-__device__ __forceinline__ void get_unit(const Args &a, long long u, int km1, Unit &U) {
-    const int H = a.g.H;
-    int lo = 0, hi = a.g.num_seqs - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if ((long long)__ldg(a.gtile + mid) * H <= u) lo = mid; else hi = mid - 1;
+// the tile (0 when no row is scored).  Each role walks increasing units and
+// keeps the current sequence's table entries in registers, so only crossing
+// into another sequence reads memory.
+struct UnitCursor {
+    int b = -1, nt = 0, seq0 = 0, L = 0, bbase = 0;
+    int ub0 = 0, ub1 = 0;  // units of sequence b: [ub0, ub1)
+
+    __device__ __forceinline__ void unit(const Args &a, int u, int km1, Unit &U) {
+        const int H = a.g.H;
+        if (b < 0 || u >= ub1) {
+            int lo = 0, hi = a.g.num_seqs - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (__ldg(a.gtile + mid) * H <= u) lo = mid; else hi = mid - 1;
+            }
+            b = lo;
+            const int tb = __ldg(a.gtile + lo);
+            nt = __ldg(a.gtile + lo + 1) - tb;
+            ub0 = tb * H;
+            ub1 = ub0 + nt * H;
+            seq0 = __ldg(a.g.cu + lo);
+            L = __ldg(a.g.cu + lo + 1) - seq0;
+            bbase = __ldg(a.g.blk_base + lo);
+        }
+        U.b = b;
+        const int rem = u - ub0;
+        U.h = rem / nt;
+        const int tz = rem - U.h * nt;
+        U.t = (tz & 1) ? nt - 1 - (tz >> 1) : (tz >> 1);
+        U.seq0 = seq0;
+        U.L = L;
+        U.bbase = bbase;
+        U.nb = (L + a.g.bs - 1) / a.g.bs;
+        const int cl = (min(L, (U.t + 1) * kRows) - 1) / a.g.bs;
+        U.cmax = (km1 > 0 && cl > km1) ? cl : 0;
     }
-    U.b = lo;
-    const int tb = __ldg(a.gtile + lo), nt = __ldg(a.gtile + lo + 1) - tb;
-    const long long rem = u - (long long)tb * H;
-    U.h = (int)(rem / nt);
-    const int tz = (int)(rem % nt);
-    U.t = (tz & 1) ? nt - 1 - (tz >> 1) : (tz >> 1);
-    U.seq0 = __ldg(a.g.cu + lo);
-    U.L = __ldg(a.g.cu + lo + 1) - U.seq0;
-    U.bbase = __ldg(a.g.blk_base + lo);
-    U.nb = (U.L + a.g.bs - 1) / a.g.bs;
-    const int cl = (min(U.L, (U.t + 1) * kRows) - 1) / a.g.bs;
-    U.cmax = (km1 > 0 && cl > km1) ? cl : 0;
-}
+};
 
 // bf16 element d of row r of a K-major, 128-byte-swizzled [128][D] tile
 template <int D>
@@ -181,8 +198,8 @@ __device__ __forceinline__ void top_insert(float (&ts)[KCAP], int (&ti)[KCAP], i
     }
 }
 
-template <int D, int KCAP>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, int KCAP, int NWG>
+__global__ void __launch_bounds__(threads_for(NWG), 1)
     gate_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                    const __grid_constant__ CUtensorMap tmap_hi,
                    const __grid_constant__ CUtensorMap tmap_lo, Args a) {
@@ -198,9 +215,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gmisc + L::kNumBars * 8 + 4);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.g.H, km1 = a.topk - 1;
-    const long long n_units = (long long)H * __ldg(a.gtile + a.g.num_seqs);
-    const long long u0 = n_units * blockIdx.x / gridDim.x;
-    const long long u1 = n_units * (blockIdx.x + 1) / gridDim.x;
+    // units fit an int (checked on the host)
+    const int n_units = H * __ldg(a.gtile + a.g.num_seqs);
+    const int u0 = (int)((long long)n_units * blockIdx.x / gridDim.x);
+    const int u1 = (int)((long long)n_units * (blockIdx.x + 1) / gridDim.x);
     if (u0 >= u1) return;
     Ctl ctl{abort_flag, a.status, a.wait_limit};
     const int nq = a.nq, nslots = a.nslots;
@@ -237,16 +255,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ================= TMA producer =================
         if (lane == 0) {
-            long long cur = -1;  // (sequence, head) whose pooled keys are resident
+            int cur = -1;  // (sequence, head) whose pooled keys are resident
             int nload = 0, i = 0;
+            int s = 0, qround = 0;  // q stage of unit i and i / nq
             int qpend[kMaxQ];
             for (int s = 0; s < kMaxQ; ++s) qpend[s] = -1;
             bool go = true;
-            Unit U, NU;  // this unit and the next (fetched one unit ahead)
-            get_unit(a, u0, km1, U);
-            for (long long u = u0; go && u < u1; ++u, ++i, U = NU) {
-                if (u + 1 < u1) get_unit(a, u + 1, km1, NU);
-                const long long pair = (long long)U.b * H + U.h;
+            UnitCursor cur_u;
+            Unit U, NU;  // this unit and the next
+            cur_u.unit(a, u0, km1, U);
+            for (int u = u0; go && u < u1; ++u, ++i, U = NU) {
+                if (u + 1 < u1) cur_u.unit(a, u + 1, km1, NU);
+                const int pair = U.b * H + U.h;
                 if (pair != cur) {
                     // the MMAs that read the previous keys have completed
                     if (nload > 0 && !wait_bar(bar(L::kBarKE), (nload - 1) & 1, ctl)) {
@@ -266,8 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++nload;
                     cur = pair;
                 }
-                const int s = i % nq;
-                if (i >= nq && !wait_bar(bar(L::kBarQE + s), (i / nq - 1) & 1, ctl)) {
+                if (i >= nq && !wait_fast(bar(L::kBarQE + s), (qround - 1) & 1, ctl)) {
                     go = false;
                     break;
                 }
@@ -277,6 +296,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_3d(sQ + s * L::kQStage + x * L::kQBox, &tmap_q, bar(L::kBarQF + s),
                                 x * 64, U.h, U.seq0 + U.t * kRows);
                 qpend[s] = i;
+                if (++s == nq) {
+                    s = 0;
+                    ++qround;
+                }
             }
             if (*abort_flag) {
                 // let the copies still in flight land before the CTA exits
@@ -290,14 +313,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ================= MMA issuer =================
         if (lane == 0) {
-            long long cur = -1;
+            int cur = -1;
             int nload = 0, i = 0;
+            int s = 0, qround = 0, w = 0, wround = 0;  // q stage, TMEM slot of unit i
             bool ok = true;
-            Unit U, NU;  // this unit and the next (fetched one unit ahead)
-            get_unit(a, u0, km1, U);
-            for (long long u = u0; ok && u < u1; ++u, ++i, U = NU) {
-                if (u + 1 < u1) get_unit(a, u + 1, km1, NU);
-                const long long pair = (long long)U.b * H + U.h;
+            // shared-memory descriptors: the start-address field (bits 0-13, in
+            // 16-byte units) is advanced by plain addition below
+            const uint64_t dhi = sdesc(sHi, 16, 1024), dlo = sdesc(sLo, 16, 1024);
+            const uint32_t kbox16 = kKBox >> 4;
+            UnitCursor cur_u;
+            Unit U, NU;  // this unit and the next
+            cur_u.unit(a, u0, km1, U);
+            for (int u = u0; ok && u < u1; ++u, ++i, U = NU) {
+                if (u + 1 < u1) cur_u.unit(a, u + 1, km1, NU);
+                const int pair = U.b * H + U.h;
                 if (pair != cur) {
                     // the previous keys may be replaced once these MMAs complete
                     if (nload > 0) tc_commit(bar(L::kBarKE));
@@ -308,9 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++nload;
                     cur = pair;
                 }
-                const int s = i % nq, w = i % nslots;
-                if (!wait_bar(bar(L::kBarQF + s), (i / nq) & 1, ctl) ||
-                    (i >= nslots && !wait_bar(bar(L::kBarSE + w), (i / nslots - 1) & 1, ctl))) {
+                if (!wait_fast(bar(L::kBarQF + s), qround & 1, ctl) ||
+                    (wround > 0 && !wait_fast(bar(L::kBarSE + w), (wround - 1) & 1, ctl))) {
                     ok = false;
                     break;
                 }
@@ -319,22 +347,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int n = min((int)slot_cols, (U.cmax + 15) & ~15);
                     const uint32_t idesc = idesc_bf16(kRows, n, 0);
                     const uint32_t tS = tmem + w * slot_cols;
-                    const uint32_t qb = sQ + s * L::kQStage;
+                    const uint64_t dq = sdesc(sQ + s * L::kQStage, 16, 1024);
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k) {
-                        const uint32_t off = (uint32_t)(k % 4) * 32;
-                        tc_mma(tS, sdesc(qb + (k / 4) * L::kQBox + off, 16, 1024),
-                               sdesc(sHi + (k / 4) * kKBox + off, 16, 1024), idesc, k > 0);
+                        // 16 dims = 32 bytes = 2 units; a 64-dim box further on
+                        const uint64_t aoff = (uint64_t)((k / 4) * (L::kQBox >> 4) + (k % 4) * 2);
+                        const uint64_t boff = (uint64_t)((k / 4) * kbox16 + (k % 4) * 2);
+                        tc_mma(tS, dq + aoff, dhi + boff, idesc, k > 0);
                     }
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k) {
-                        const uint32_t off = (uint32_t)(k % 4) * 32;
-                        tc_mma(tS, sdesc(qb + (k / 4) * L::kQBox + off, 16, 1024),
-                               sdesc(sLo + (k / 4) * kKBox + off, 16, 1024), idesc, 1u);
+                        const uint64_t aoff = (uint64_t)((k / 4) * (L::kQBox >> 4) + (k % 4) * 2);
+                        const uint64_t boff = (uint64_t)((k / 4) * kbox16 + (k % 4) * 2);
+                        tc_mma(tS, dq + aoff, dlo + boff, idesc, 1u);
                     }
                     tc_commit(bar(L::kBarSF + w));
                 } else {
                     mbar_arrive(bar(L::kBarSF + w));  // no row of the unit is scored
+                }
+                if (++s == nq) {
+                    s = 0;
+                    ++qround;
+                }
+                if (++w == nslots) {
+                    w = 0;
+                    ++wround;
                 }
             }
             // every MMA this thread issued has finished before TMEM is freed
@@ -343,15 +380,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else {
-        // ================= selection (warps 2..9) =================
+        // ================= selection (warps 2 ..) =================
+        // warpgroup wg takes units wg, wg + nwg, ...; no more warpgroups than
+        // TMEM slots
         const int wg = (warp - 2) >> 2, quarter = warp & 3;
+        const int nwg = min(NWG, nslots);
         const int row = quarter * 32 + lane;  // my TMEM lane and q row
         const uint32_t tlane = tmem + ((uint32_t)(quarter * 32) << 16);
-        Unit U, NU;  // this unit and the warpgroup's next (fetched one unit ahead)
-        if (u0 + wg < u1) get_unit(a, u0 + wg, km1, U);
-        for (long long u = u0 + wg, i = wg; u < u1; u += 2, i += 2, U = NU) {
-            if (u + 2 < u1) get_unit(a, u + 2, km1, NU);
-            const int s = (int)(i % nq), slot = (int)(i % nslots);
+        UnitCursor cur_u;
+        Unit U, NU;  // this unit and the warpgroup's next
+        int kn_pair = -1;  // (sequence, head) whose key-norm maximum is in kn
+        float kn = 0.f;
+        if (wg < nwg && u0 + wg < u1) cur_u.unit(a, u0 + wg, km1, U);
+        for (int u = u0 + wg, i = wg; wg < nwg && u < u1; u += nwg, i += nwg, U = NU) {
+            if (u + nwg < u1) cur_u.unit(a, u + nwg, km1, NU);
+            const int s = i % nq, slot = i % nslots;
             const uint32_t tS = tlane + slot * slot_cols;
             const uint32_t sq = sQ + s * L::kQStage;
             const int my_i = U.t * kRows + row;
@@ -359,12 +402,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int ci = valid ? my_i / a.g.bs : 0;
             const int tok = U.seq0 + my_i;
             const bool scored = valid && km1 > 0 && ci > km1;
-            // largest pooled-key norm among the unit's scored blocks (the margin)
-            float kn = 0.f;
-            for (int c = lane; c < U.cmax; c += 32)
-                kn = fmaxf(kn, __ldg(a.knorm + (size_t)(U.bbase + c) * H + U.h));
+            // largest pooled-key norm of the head's blocks (the margin), once per
+            // (sequence, head)
+            const int pair = U.b * H + U.h;
+            if (pair != kn_pair) {
+                kn = 0.f;
+                for (int c = lane; c < U.nb; c += 32)
+                    kn = fmaxf(kn, __ldg(a.knorm + (size_t)(U.bbase + c) * H + U.h));
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) kn = fmaxf(kn, __shfl_xor_sync(0xffffffffu, kn, o));
+                for (int o = 16; o > 0; o >>= 1) kn = fmaxf(kn, __shfl_xor_sync(0xffffffffu, kn, o));
+                kn_pair = pair;
+            }
 
             int ti[KCAP];  // selected past blocks, ascending, at the top end
 #pragma unroll
@@ -372,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool need = false;  // the exact kernel writes this row
             unsigned long long cand = ~0ull;  // its candidate blocks, one byte each
             int ncand = 0;
-            if (!__all_sync(0xffffffffu, wait_bar(bar(L::kBarSF + slot), (int)(i / nslots) & 1, ctl))) break;
+            if (!__all_sync(0xffffffffu, wait_fast(bar(L::kBarSF + slot), (i / nslots) & 1, ctl))) break;
             tc_fence_after();
             // ||q_r||^2 for the margin: the last read of the q stage
             float qq = 0.f;
@@ -399,13 +447,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float tv[KCAP + 1];
 #pragma unroll
                 for (int x = 0; x <= KCAP; ++x) tv[x] = -INFINITY;
-                for (int c0 = 0; c0 < U.cmax; c0 += 32) {
-                    uint32_t v[32];
-                    tc_ld32(tS + c0, v);
+                // CW scores per TMEM round trip (64 when the registers allow)
+                constexpr int CW = NWG == 4 ? 32 : 64;
+                uint32_t v[CW / 32][32];
+                for (int c0 = 0; c0 < U.cmax; c0 += CW) {
+#pragma unroll
+                    for (int hh = 0; hh < CW / 32; ++hh) tc_ld32(tS + c0 + 32 * hh, v[hh]);
                     tc_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const float x = (c0 + e < ci) ? __uint_as_float(v[e]) : -INFINITY;
+                    for (int e = 0; e < CW; ++e) {
+                        const float x = (c0 + e < ci) ? __uint_as_float(v[e >> 5][e & 31]) : -INFINITY;
 #pragma unroll
                         for (int j = KCAP; j > 0; --j) tv[j] = fmaxf(tv[j], fminf(tv[j - 1], x));
                         tv[0] = fmaxf(tv[0], x);
@@ -425,17 +476,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 need = scored && !(Tk < T - 2.f * E);
                 const float cut = need ? T - 2.f * E : T;
                 if (__any_sync(0xffffffffu, scored)) {
-                    for (int c0 = 0; c0 < U.cmax; c0 += 32) {
-                        uint32_t v[32];
-                        tc_ld32(tS + c0, v);
-                        tc_wait_ld();
-                        uint32_t mask = 0u;  // bit e: block c0 + e is selected / a candidate
+                    for (int c0 = 0; c0 < U.cmax; c0 += CW) {
+                        if (U.cmax > CW) {  // else pass 1's only chunk is still in registers
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            if (c0 + e < ci && __uint_as_float(v[e]) >= cut) mask |= 1u << e;
-                        if (!scored) mask = 0u;
+                            for (int hh = 0; hh < CW / 32; ++hh) tc_ld32(tS + c0 + 32 * hh, v[hh]);
+                            tc_wait_ld();
+                        }
+                        // bit e: block c0 + e is selected / a candidate
+                        unsigned long long mask = 0ull;
+#pragma unroll
+                        for (int e = 0; e < CW; ++e)
+                            if (c0 + e < ci && __uint_as_float(v[e >> 5][e & 31]) >= cut)
+                                mask |= 1ull << e;
+                        if (!scored) mask = 0ull;
                         while (mask) {
-                            const int c = c0 + __ffs(mask) - 1;
+                            const int c = c0 + __ffsll(mask) - 1;
                             mask &= mask - 1;
                             if (need) {
                                 if (ncand < 8) cand = (cand << 8) | (unsigned long long)c;
@@ -522,20 +577,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Rows the margin could not settle, one thread each: exact fp32 scores (the
+// Rows the margin could not settle, one warp each: exact fp32 scores (the
 // CUDA-core gate's summation order) of the row's candidates -- or, when it had
-// more than 8, of every past block -- in ascending block order, the top k-1 of
-// them by (score descending, block ascending), written like the gate's rows.
+// more than 8, of every past block -- lane l taking candidates l, l + 32, ...
+// in ascending block order; the lanes' top lists are merged with k-1 warp
+// arg-max rounds (score descending, block ascending) and the row is written
+// like the gate's rows.
 // ---------------------------------------------------------------------------
+constexpr int kExactWarps = 8;
+
 template <int D, int KCAP>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(32 * kExactWarps)
     gate_exact_kernel(Geometry g, const __nv_bfloat16 *__restrict__ q,
                       const float *__restrict__ kbar, int32_t *__restrict__ idx, int topk,
                       int *__restrict__ counts, const unsigned long long *__restrict__ need_list,
                       const int *__restrict__ need_count) {
+    const int lane = threadIdx.x & 31;
     const int n = *need_count;
     const int km1 = topk - 1;
-    for (int w = blockIdx.x * blockDim.x + threadIdx.x; w < n; w += gridDim.x * blockDim.x) {
+    for (int w = blockIdx.x * kExactWarps + (threadIdx.x >> 5); w < n;
+         w += gridDim.x * kExactWarps) {
         const unsigned long long w0 = need_list[2 * w], cand = need_list[2 * w + 1];
         const bool all = (w0 >> 62) & 1ull;
         const long long r = (long long)(w0 & ((1ull << 62) - 1));
@@ -545,6 +606,12 @@ __global__ void __launch_bounds__(256)
         const int bbase = __ldg(g.blk_base + b);
         const __nv_bfloat16 *qg = q + (size_t)r * D;
         const float *kb_head = kbar + ((size_t)bbase * g.H + h) * D;
+        // candidate bytes were shifted in from the low end: the oldest (lowest
+        // block) sits highest
+        int nc = 0;
+        if (!all)
+            for (int x = 0; x < 8; ++x) nc += ((cand >> (8 * x)) & 0xffull) != 0xffull;
+        const int ncand = all ? ci : nc;
         float ts[KCAP];
         int ti[KCAP];
 #pragma unroll
@@ -552,37 +619,58 @@ __global__ void __launch_bounds__(256)
             ts[x] = -INFINITY;
             ti[x] = kEmpty;
         }
-        if (all) {
-            for (int c = 0; c < ci; ++c)
-                top_insert<KCAP>(ts, ti, km1, exact_score<D>(qg, kb_head + (size_t)c * g.H * D), c);
-        } else {
-            // candidate bytes were shifted in from the low end: the oldest
-            // (lowest block) sits highest
-            int nc = 0;
-            for (int x = 0; x < 8; ++x) nc += ((cand >> (8 * x)) & 0xffull) != 0xffull;
-            for (int x = nc - 1; x >= 0; --x) {
-                const int c = (int)((cand >> (8 * x)) & 0xffull);
-                top_insert<KCAP>(ts, ti, km1, exact_score<D>(qg, kb_head + (size_t)c * g.H * D), c);
+        for (int j = lane; j < ncand; j += 32) {
+            const int c = all ? j : (int)((cand >> (8 * (nc - 1 - j))) & 0xffull);
+            top_insert<KCAP>(ts, ti, km1, exact_score<D>(qg, kb_head + (size_t)c * g.H * D), c);
+        }
+        int sel[KCAP];
+#pragma unroll
+        for (int x = 0; x < KCAP; ++x) {
+            sel[x] = kEmpty;
+            if (x < km1) {
+                float sv = ts[0];
+                int cv = ti[0];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float s2 = __shfl_xor_sync(0xffffffffu, sv, o);
+                    const int c2 = __shfl_xor_sync(0xffffffffu, cv, o);
+                    if (s2 > sv || (s2 == sv && c2 < cv)) {
+                        sv = s2;
+                        cv = c2;
+                    }
+                }
+                sel[x] = cv;
+                if (ti[0] == cv) {  // the winning lane drops its head
+#pragma unroll
+                    for (int y = 0; y + 1 < KCAP; ++y) {
+                        ts[y] = ts[y + 1];
+                        ti[y] = ti[y + 1];
+                    }
+                    ts[KCAP - 1] = -INFINITY;
+                    ti[KCAP - 1] = kEmpty;
+                }
             }
         }
 #pragma unroll
         for (int pass = 0; pass < KCAP; ++pass) {
 #pragma unroll
             for (int x = pass & 1; x + 1 < KCAP; x += 2) {
-                const int lo = min(ti[x], ti[x + 1]), hi = max(ti[x], ti[x + 1]);
-                ti[x] = lo;
-                ti[x + 1] = hi;
+                const int lo = min(sel[x], sel[x + 1]), hi = max(sel[x], sel[x + 1]);
+                sel[x] = lo;
+                sel[x + 1] = hi;
             }
         }
-        int32_t *out = idx + (size_t)r * topk;
+        if (lane == 0) {
+            int32_t *out = idx + (size_t)r * topk;
 #pragma unroll
-        for (int x = 0; x < KCAP; ++x)
-            if (x < km1) {
-                out[x] = ti[x];
-                if (counts) atomicAdd(counts + (size_t)(bbase + ti[x]) * g.H + h, 1);
-            }
-        out[km1] = ci;
-        for (int x = km1 + 1; x < topk; ++x) out[x] = -1;
+            for (int x = 0; x < KCAP; ++x)
+                if (x < km1) {
+                    out[x] = sel[x];
+                    if (counts) atomicAdd(counts + (size_t)(bbase + sel[x]) * g.H + h, 1);
+                }
+            out[km1] = ci;
+            for (int x = km1 + 1; x < topk; ++x) out[x] = -1;
+        }
     }
 }
 
@@ -592,7 +680,10 @@ bool gate_tc_supported(const Plan &p) {
     // a warpgroup's TMEM half holds 256 block scores; the selection keeps its
     // top lists in registers
     const long long nmax = (p.max_len + p.bs - 1) / p.bs;
-    return nmax <= gate_tc::kMaxBlocks && p.topk - 1 <= 32 && (p.D == 64 || p.D == 128);
+    // the units (head x 128-row tile) are counted in an int
+    const long long units = (long long)p.H * ((long long)p.total / gate_tc::kRows + p.num_seqs + 1);
+    return nmax <= gate_tc::kMaxBlocks && p.topk - 1 <= 32 && (p.D == 64 || p.D == 128) &&
+           units < (1ll << 31);
 }
 
 static int sm_count_gate() {
@@ -625,13 +716,14 @@ static cudaError_t launch_gate_tc_d(const Plan &p, const gate_tc::Args &a, const
     const int smem = (int)(L::tiles(a.nq, a.kb_rows) + 1008 + L::kMisc);
 #define MOBA_GATE_TC_CASE(KC)                                                                   \
     {                                                                                           \
-        auto kern = gate_tc::gate_tc_kernel<D, KC>;                                             \
+        constexpr int nwg = (KC) <= 8 ? 4 : 2;                                                  \
+        auto kern = gate_tc::gate_tc_kernel<D, KC, nwg>;                                        \
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                                              smem);                                             \
         if (e != cudaSuccess) return e;                                                         \
-        kern<<<grid, gate_tc::kThreads, smem, st>>>(mq, mh, ml, a);                             \
+        kern<<<grid, gate_tc::threads_for(nwg), smem, st>>>(mq, mh, ml, a);                    \
         if ((e = cudaGetLastError()) != cudaSuccess) return e;                                  \
-        gate_tc::gate_exact_kernel<D, KC><<<4 * sm_count_gate(), 256, 0,                        \
+        gate_tc::gate_exact_kernel<D, KC><<<4 * sm_count_gate(), 32 * gate_tc::kExactWarps, 0,   \
                                              st>>>(a.g, a.q, a.kbar, a.idx, a.topk, a.counts,  \
                                                    a.need_list, a.need_count);                 \
         return cudaGetLastError();                                                              \

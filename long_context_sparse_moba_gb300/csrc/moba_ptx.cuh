@@ -232,6 +232,10 @@ static __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, cons
         }
     }
 }
+// one inline test first: the bounded wait is a call
+__device__ __forceinline__ bool wait_fast(uint32_t bar, uint32_t parity, const Ctl &c) {
+    return mbar_test(bar, parity) || wait_bar(bar, parity, c);
+}
 // Bounded wait that ignores the abort flag (draining copies / MMAs in flight).
 static __device__ __noinline__ void drain_bar(uint32_t bar, uint32_t parity, long long limit) {
     const long long t0 = clock64();
