@@ -48,6 +48,7 @@ def _load():
         lib.moba_oracle_max_threads.restype = i32
         lib.moba_oracle_kpool.restype = i32
         lib.moba_oracle_kpool.argtypes = [p, p, i32, i32, i32, i32, p]
+        lib.moba_oracle_kpool_max.argtypes = [p, p, i32, i32, i32, i32, p]
         lib.moba_oracle_rows.restype = i32
         lib.moba_oracle_rows.argtypes = [p, p, p, p, i32, i32, i32, i32, i32, p,
                                          i64, p, p, p, p, p, p, p]
@@ -81,20 +82,22 @@ def max_threads() -> int:
     return int(_load().moba_oracle_max_threads())
 
 
-def kpool(k, cu_seqlens, H: int, D: int, block_size: int) -> np.ndarray:
-    """Mean-pooled keys, float64 ``[num_blocks_total, H, D]``."""
+def kpool(k, cu_seqlens, H: int, D: int, block_size: int, pooling: str = "mean") -> np.ndarray:
+    """Pooled keys, float64 ``[num_blocks_total, H, D]``: the mean (default) or
+    the element-wise maximum of each block's keys."""
     kb = _bits(k)
     cu = _cu(cu_seqlens)
     nb = sum(num_blocks(cu[b + 1] - cu[b], block_size) for b in range(len(cu) - 1))
     out = np.zeros((nb, H, D), dtype=np.float64)
-    rc = _load().moba_oracle_kpool(_ptr(kb), _ptr(cu), len(cu) - 1, H, D, block_size, _ptr(out))
+    fn = {"mean": _load().moba_oracle_kpool, "max": _load().moba_oracle_kpool_max}[pooling]
+    rc = fn(_ptr(kb), _ptr(cu), len(cu) - 1, H, D, block_size, _ptr(out))
     if rc != 0:
-        raise ValueError(f"moba_oracle_kpool failed ({rc})")
+        raise ValueError(f"oracle pooling ({pooling}) failed ({rc})")
     return out
 
 
 def moba_rows(q, k, v, cu_seqlens, H: int, D: int, block_size: int, topk: int,
-              row_tok, row_head, given_idx=None, kbar=None) -> dict:
+              row_tok, row_head, given_idx=None, kbar=None, pooling: str = "mean") -> dict:
     """Gate + attention for the listed (token, head) rows.
 
     Returns a dict of numpy arrays: ``idx`` int32 [R, topk] (ascending, -1
@@ -103,7 +106,7 @@ def moba_rows(q, k, v, cu_seqlens, H: int, D: int, block_size: int, topk: int,
     qb, kb, vb = _bits(q), _bits(k), _bits(v)
     cu = _cu(cu_seqlens)
     if kbar is None:
-        kbar = kpool(kb, cu, H, D, block_size)
+        kbar = kpool(kb, cu, H, D, block_size, pooling)
     kbar = np.ascontiguousarray(kbar, dtype=np.float64)
     rt = np.ascontiguousarray(np.asarray(row_tok, dtype=np.int64))
     rh = np.ascontiguousarray(np.asarray(row_head, dtype=np.int32))
@@ -132,12 +135,12 @@ def all_rows(total: int, H: int):
 
 
 def moba_full(q, k, v, cu_seqlens, H: int, D: int, block_size: int, topk: int,
-              given_idx=None) -> dict:
+              given_idx=None, pooling: str = "mean") -> dict:
     """All rows; arrays reshaped to ``[total, H, ...]``."""
     cu = _cu(cu_seqlens)
     total = int(cu[-1])
     tok, head = all_rows(total, H)
     gi = None if given_idx is None else np.asarray(given_idx).reshape(total * H, topk)
-    r = moba_rows(q, k, v, cu, H, D, block_size, topk, tok, head, given_idx=gi)
+    r = moba_rows(q, k, v, cu, H, D, block_size, topk, tok, head, given_idx=gi, pooling=pooling)
     return {"idx": r["idx"].reshape(total, H, topk), "gap": r["gap"].reshape(total, H),
             "out": r["out"].reshape(total, H, D), "lse": r["lse"].reshape(total, H)}

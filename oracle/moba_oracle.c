@@ -31,6 +31,8 @@
  *   R4 attention logits are scaled by 1/sqrt(D); lse is the natural log of
  *      the softmax denominator of the scaled logits.
  *   R5 gating is per (sequence, head): each head pools its own keys.
+ *   R6 max pooling (the variant the server-side page allows) takes the
+ *      element-wise maximum over the block's own tokens.
  *
  * Parity pins for every function here live in tests/test_oracle.py.
  */
@@ -110,6 +112,45 @@ int moba_oracle_kpool(const uint16_t *k, const int64_t *cu, int num_seqs,
                 for (int64_t e = 0; e < HD; ++e) sum[e] += widen_bf16(row[e]);
             }
             for (int64_t e = 0; e < HD; ++e) sum[e] /= (double)(t1 - t0);
+        }
+    }
+    free(base);
+    return 0;
+}
+
+/*
+ * Max-pooled keys: kbar[g][h][d] = max over the tokens t of block g of
+ * k[t][h][d] ([P4] section 3 allows max pooling along the sequence instead of
+ * the mean: it reacts more to blocks dense in key information).  Reading R6:
+ * the maximum is taken per element (per head and dimension), over the block's
+ * own tokens only (a partial tail block included).  Exact in any precision.
+ */
+int moba_oracle_kpool_max(const uint16_t *k, const int64_t *cu, int num_seqs,
+                          int H, int D, int block_size, double *kbar)
+{
+    if (!k || !cu || !kbar || num_seqs < 1 || H < 1 || D < 1 || block_size < 1)
+        return -1;
+    int64_t *base = block_bases(cu, num_seqs, block_size);
+    if (!base) return -2;
+    const int64_t HD = (int64_t)H * D;
+    for (int b = 0; b < num_seqs; ++b) {
+        int64_t t_begin = cu[b], len = cu[b + 1] - cu[b];
+        int64_t n = base[b + 1] - base[b];
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int64_t c = 0; c < n; ++c) {
+            int64_t g = base[b] + c;
+            int64_t t0 = t_begin + c * block_size;
+            int64_t t1 = t0 + block_size;
+            if (t1 > t_begin + len) t1 = t_begin + len;
+            double *mx = kbar + g * HD;
+            for (int64_t e = 0; e < HD; ++e) mx[e] = widen_bf16(k[t0 * HD + e]);
+            for (int64_t t = t0 + 1; t < t1; ++t) {
+                const uint16_t *row = k + t * HD;
+                for (int64_t e = 0; e < HD; ++e) {
+                    const double x = widen_bf16(row[e]);
+                    if (x > mx[e]) mx[e] = x;
+                }
+            }
         }
     }
     free(base);

@@ -111,6 +111,66 @@ def test_kpool_permutation_invariant(oracle_mod):
     np.testing.assert_allclose(a, b, rtol=0, atol=1e-14)
 
 
+def test_kpool_max_matches_numpy_max(oracle_mod):
+    """Max pooling against numpy's element-wise max over each block (two
+    sequences, partial tails, negative and positive keys)."""
+    H, D, bs = 3, 16, 8
+    lens = [37, 16]
+    total = sum(lens)
+    q, k, v = rand_qkv(total, H, D, seed=13)
+    kw = widen(k).numpy()
+    cu = [0, lens[0], total]
+    kbar = oracle_mod.kpool(k, cu, H, D, bs, pooling="max")
+    g = 0
+    for b, L in enumerate(lens):
+        for c in range(oracle_mod.num_blocks(L, bs)):
+            t0, t1 = cu[b] + c * bs, cu[b] + min((c + 1) * bs, L)
+            assert np.array_equal(kbar[g], kw[t0:t1].max(axis=0))
+            g += 1
+    assert g == kbar.shape[0]
+
+
+def test_kpool_max_single_spike(oracle_mod):
+    """One large key in an otherwise negative block: the max sees it, the mean
+    barely moves (worked by hand: keys -1 except one 6, block of 4 -> mean
+    0.75, max 6)."""
+    bs, D = 4, 8
+    k = -torch.ones(8, 1, D)
+    k[5, 0, 0] = 6.0
+    kb = bf16(k)
+    mean = oracle_mod.kpool(kb, [0, 8], 1, D, bs)
+    mx = oracle_mod.kpool(kb, [0, 8], 1, D, bs, pooling="max")
+    assert mean[1, 0, 0] == pytest.approx((6.0 - 3.0) / 4)
+    assert mx[1, 0, 0] == 6.0 and mx[0, 0, 0] == -1.0
+    assert (mx[:, 0, 1:] == -1.0).all()
+
+
+def test_max_pooling_changes_the_selection(oracle_mod):
+    """Block 1 holds one key aligned with the queries (spike 8) among keys of
+    -1; block 2 is uniformly 1.5.  Mean pooling scores block 1 at 1.25 < 1.5,
+    max pooling at 8 > 1.5 (q = e_0), so a row of block 4 with top-k 2 picks
+    block 2 under the mean and block 1 under the max."""
+    bs, D = 4, 8
+    S = 5 * bs
+    q = torch.zeros(S, 1, D)
+    q[:, 0, 0] = 1.0
+    k = torch.zeros(S, 1, D)
+    k[0:4, 0, 0] = -2.0
+    k[4:8, 0, 0] = -1.0
+    k[6, 0, 0] = 8.0
+    k[8:12, 0, 0] = 1.5
+    k[12:16, 0, 0] = -3.0
+    v = torch.randn(S, 1, D, generator=torch.Generator().manual_seed(1))
+    q, k, v = bf16(q), bf16(k), bf16(v)
+    t = 4 * bs + 1
+    mean = oracle_mod.moba_rows(q, k, v, [0, S], 1, D, bs, 2, [t], [0])
+    mx = oracle_mod.moba_rows(q, k, v, [0, S], 1, D, bs, 2, [t], [0], pooling="max")
+    assert mean["idx"][0].tolist() == [2, 4]
+    assert mx["idx"][0].tolist() == [1, 4]
+    assert mean["gap"][0] == pytest.approx(1.5 - 1.25)
+    assert mx["gap"][0] == pytest.approx(8.0 - 1.5)
+
+
 # --------------------------------------------------------------------------
 # gate and top-k selection
 # --------------------------------------------------------------------------
