@@ -216,6 +216,17 @@ int moba_set_attention_kernel(int kind);
  * Both select exactly the same blocks.  MOBA_ERR_INVALID_ARG otherwise. */
 int moba_set_gate_kernel(int kind);
 
+/* Pooling of each block's keys into the representative the gate scores
+ * against (process-wide, not thread-safe; applies to moba_kpool* and to the
+ * forward entry points): MOBA_POOL_MEAN (default) = the mean of the block's
+ * keys ("Moonshot MoBA paper explained" §3.1 mean_pool; "MOBA mixture of block
+ * attention for server-side long context" §3); MOBA_POOL_MAX = their
+ * element-wise maximum, the variant the latter page allows (more sensitive to
+ * blocks holding a few strongly matching keys).  MOBA_ERR_INVALID_ARG for any
+ * other value. */
+enum { MOBA_POOL_MEAN = 0, MOBA_POOL_MAX = 1 };
+int moba_set_pooling(int kind);
+
 /* Test hooks of the bounded waits in the tcgen05 kernels (process-wide):
  * wait_limit_cycles is the clock64 budget of one mbarrier wait (<= 0 restores
  * the default, about 2 s); flags bit 0 makes the K/V producer skip its first

@@ -35,6 +35,9 @@ static std::atomic<unsigned long long> g_launches{0};
 static int g_attn_kind = 0;
 // gate implementation: 0 = tcgen05 scores + exact candidates, 1 = CUDA cores
 static int g_gate_kind = 0;
+// key pooling per block: 0 = mean, 1 = element-wise max
+static int g_pool_kind = 0;
+int pooling_kind() { return g_pool_kind; }
 int past_tile_rows() { return g_attn_kind == 0 ? tc_tile_rows() : mma_tile_rows(); }
 cudaError_t launch_attn_past(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
                              const __nv_bfloat16 *k, const __nv_bfloat16 *v, cudaStream_t st) {
@@ -466,6 +469,12 @@ MOBA_EXPORT int moba_set_attention_kernel(int kind) {
 MOBA_EXPORT int moba_set_gate_kernel(int kind) {
     if (kind != 0 && kind != 1) return MOBA_ERR_INVALID_ARG;
     g_gate_kind = kind;
+    return MOBA_OK;
+}
+
+MOBA_EXPORT int moba_set_pooling(int kind) {
+    if (kind != MOBA_POOL_MEAN && kind != MOBA_POOL_MAX) return MOBA_ERR_INVALID_ARG;
+    g_pool_kind = kind;
     return MOBA_OK;
 }
 

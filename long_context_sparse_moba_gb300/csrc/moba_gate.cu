@@ -84,14 +84,17 @@ cudaError_t launch_setup(const Plan &p, const int *cu_dev, Workspace &ws, cudaSt
 }
 
 // ---------------------------------------------------------------------------
-// K1: mean-pool the keys of every block.  One CTA per (global block, group of
+// K1: pool the keys of every block (mean, or with MAX the element-wise
+// maximum: "MOBA mixture of block attention for server-side long context" §3
+// allows either).  One CTA per (global block, group of
 // 64 16-byte columns of the [H*D] token row).  Threads of a column walk the
 // block's tokens with a stride of TG token groups; the TG partial sums are
-// added in a fixed order, so the result is deterministic.  HBM-bound: every
+// added (or maxed) in a fixed order, so the result is deterministic.  HBM-bound: every
 // key byte is read once with 16-byte loads, coalesced along the token row.
 // ---------------------------------------------------------------------------
 constexpr int kPoolThreads = 256;
 
+template <bool MAX>
 __global__ __launch_bounds__(kPoolThreads) void kpool_kernel(Geometry g,
                                                               const __nv_bfloat16 *__restrict__ k,
                                                               float *__restrict__ kbar) {
@@ -112,7 +115,10 @@ __global__ __launch_bounds__(kPoolThreads) void kpool_kernel(Geometry g,
     // within ~1 ulp, which keeps the gate scores close to exact
     float acc[8], comp[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = comp[e] = 0.f;
+    for (int e = 0; e < 8; ++e) {
+        acc[e] = MAX ? -INFINITY : 0.f;
+        comp[e] = 0.f;
+    }
     auto add8 = [&](const uint4 &u) {
         const __nv_bfloat162 *p = reinterpret_cast<const __nv_bfloat162 *>(&u);
 #pragma unroll
@@ -122,10 +128,14 @@ __global__ __launch_bounds__(kPoolThreads) void kpool_kernel(Geometry g,
 #pragma unroll
             for (int o = 0; o < 2; ++o) {
                 const int k = 2 * e + o;
-                const float y = xs[o] - comp[k];
-                const float t = acc[k] + y;
-                comp[k] = (t - acc[k]) - y;
-                acc[k] = t;
+                if (MAX) {
+                    acc[k] = fmaxf(acc[k], xs[o]);
+                } else {
+                    const float y = xs[o] - comp[k];
+                    const float t = acc[k] + y;
+                    comp[k] = (t - acc[k]) - y;
+                    acc[k] = t;
+                }
             }
         }
     };
@@ -151,8 +161,8 @@ __global__ __launch_bounds__(kPoolThreads) void kpool_kernel(Geometry g,
         for (int e = 0; e < 8; ++e) s[e] = red[colx][e];
         for (int j = 1; j < TG; ++j)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) s[e] += red[j * CW + colx][e];
-        const float cnt = (float)(t1 - t0);
+            for (int e = 0; e < 8; ++e) s[e] = MAX ? fmaxf(s[e], red[j * CW + colx][e]) : s[e] + red[j * CW + colx][e];
+        const float cnt = MAX ? 1.f : (float)(t1 - t0);  // a max needs no division
         float4 *dst = reinterpret_cast<float4 *>(kbar + (size_t)gblk * g.H * g.D) + col * 2;
         dst[0] = make_float4(s[0] / cnt, s[1] / cnt, s[2] / cnt, s[3] / cnt);
         dst[1] = make_float4(s[4] / cnt, s[5] / cnt, s[6] / cnt, s[7] / cnt);
@@ -208,7 +218,10 @@ cudaError_t launch_kpool(const Plan &p, const Workspace &ws, const __nv_bfloat16
     const int HD8 = p.H * p.D / 8;
     const int CW = HD8 < 64 ? HD8 : 64;
     dim3 grid(p.NBcap, (HD8 + CW - 1) / CW);
-    kpool_kernel<<<grid, kPoolThreads, 0, st>>>(make_geo(p, ws), k, kbar);
+    if (pooling_kind() == 1)
+        kpool_kernel<true><<<grid, kPoolThreads, 0, st>>>(make_geo(p, ws), k, kbar);
+    else
+        kpool_kernel<false><<<grid, kPoolThreads, 0, st>>>(make_geo(p, ws), k, kbar);
     note_launches(1);
     return cudaGetLastError();
 }

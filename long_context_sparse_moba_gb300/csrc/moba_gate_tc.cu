@@ -42,8 +42,8 @@ namespace gate_tc {
 using namespace ptx;
 
 constexpr int kRows = 128;                     // query rows per unit (the MMA's M)
-// TMA warp, MMA warp and NWG selection warpgroups (four when the top lists
-// are short enough to fit the register budget of 20 warps, else two)
+// TMA warp, MMA warp and NWG selection warpgroups (three when the top lists
+// are short enough to fit the register budget of 16 warps, else two)
 __host__ __device__ constexpr int threads_for(int nwg) { return 64 + 128 * nwg; }
 constexpr int kMaxQ = 6;                       // q stages at most
 constexpr int kMaxSlots = 8;                   // TMEM score slots at most
@@ -448,7 +448,7 @@ __global__ void __launch_bounds__(threads_for(NWG), 1)
 #pragma unroll
                 for (int x = 0; x <= KCAP; ++x) tv[x] = -INFINITY;
                 // CW scores per TMEM round trip (64 when the registers allow)
-                constexpr int CW = NWG == 4 ? 32 : 64;
+                constexpr int CW = NWG >= 4 ? 32 : 64;
                 uint32_t v[CW / 32][32];
                 for (int c0 = 0; c0 < U.cmax; c0 += CW) {
 #pragma unroll
@@ -716,7 +716,7 @@ static cudaError_t launch_gate_tc_d(const Plan &p, const gate_tc::Args &a, const
     const int smem = (int)(L::tiles(a.nq, a.kb_rows) + 1008 + L::kMisc);
 #define MOBA_GATE_TC_CASE(KC)                                                                   \
     {                                                                                           \
-        constexpr int nwg = (KC) <= 8 ? 4 : 2;                                                  \
+        constexpr int nwg = (KC) <= 8 ? 3 : 2;                                                  \
         auto kern = gate_tc::gate_tc_kernel<D, KC, nwg>;                                        \
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                                              smem);                                             \

@@ -91,6 +91,9 @@ cudaError_t launch_attn_current(const Plan &p, const Workspace &ws, const __nv_b
                                 const __nv_bfloat16 *k, const __nv_bfloat16 *v,
                                 __nv_bfloat16 *out, float *lse, cudaStream_t st);
 
+// pooling of the keys per block: 0 mean, 1 element-wise max
+int pooling_kind();
+
 // count of kernels this library has launched (for the benchmark's launch tally)
 void note_launches(int n);
 

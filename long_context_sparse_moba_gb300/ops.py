@@ -46,6 +46,7 @@ _SIGNATURES = {
     "moba_profile_end": (_I, [_P, _I]),
     "moba_set_attention_kernel": (_I, [_I]),
     "moba_set_gate_kernel": (_I, [_I]),
+    "moba_set_pooling": (_I, [_I]),
     "moba_attn_fwd_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "moba_attn_fwd_noalloc_capacity": (_SZ, []),
     "moba_debug_set": (_I, [_I, ctypes.c_longlong]),
@@ -277,6 +278,16 @@ GATE_CUDA_CORES = 1
 def set_gate_kernel(kind: int):
     """0: tensor-core scores + exact re-score of candidates (default); 1: CUDA cores."""
     _check(lib().moba_set_gate_kernel(int(kind)), "moba_set_gate_kernel")
+
+
+POOL_MEAN = 0
+POOL_MAX = 1
+
+
+def set_pooling(kind: int):
+    """Pooling of each block's keys for the gate (process-wide): POOL_MEAN
+    (default) or POOL_MAX (element-wise maximum over the block's keys)."""
+    _check(lib().moba_set_pooling(int(kind)), "moba_set_pooling")
 
 
 def debug_timeout_info():

@@ -50,6 +50,13 @@ def test_status_strings(lib):
     assert ops.status_string(99) == "MOBA_ERR_UNKNOWN"
 
 
+def test_pooling_switch_validates(lib):
+    assert lib.moba_set_pooling(7) == ops.MOBA_ERR_INVALID_ARG
+    assert lib.moba_set_pooling(-1) == ops.MOBA_ERR_INVALID_ARG
+    assert lib.moba_set_pooling(ops.POOL_MAX) == ops.MOBA_OK
+    assert lib.moba_set_pooling(ops.POOL_MEAN) == ops.MOBA_OK
+
+
 def test_num_blocks(lib):
     assert ops.num_blocks(32768, 512) == 64
     assert ops.num_blocks(131072, 2048) == 64
