@@ -227,6 +227,44 @@ int moba_set_gate_kernel(int kind);
 enum { MOBA_POOL_MEAN = 0, MOBA_POOL_MAX = 1 };
 int moba_set_pooling(int kind);
 
+/*
+ * Decode: one new query token per sequence against its KV cache.  The step
+ * computes exactly what the prefill forward computes for the sequence's last
+ * row i = len - 1 ("Moonshot MoBA paper explained" sections 3.1 and 4.1;
+ * "MOBA mixture of block attention for server-side long context" section 3):
+ * the top (topk - 1) past blocks by <q, kbar> plus the own block, softmax
+ * attention over their keys (the own block up to i).  Selections equal those
+ * of moba_gate_topk for that row.
+ *   q          : [B][H][D] bf16 (device), the new token's queries
+ *   k_cache,
+ *   v_cache    : [B][S_max][H][D] bf16 (device); the new token's k and v are
+ *                already written at position cache_lens[b] - 1
+ *   kbar       : the pooled keys of the caches as written by moba_kpool over
+ *                k_cache with S = S_max (fp32, [B * ceil(S_max/bs)][H][D]);
+ *                only the blocks before each row's own block are read, so a
+ *                caller may keep it current by pooling each block once it is
+ *                complete
+ *   cache_lens : [B] int32 (device), 1 <= len <= S_max; a length outside
+ *                that range gives that sequence zero output and -inf lse and
+ *                MOBA_ERR_INVALID_ARG in the device status word
+ *   out        : [B][H][D] bf16 (device, written); lse: [B][H] fp32 (natural
+ *                log, written); idx: [B][H][topk] int32 or NULL (the
+ *                selection, ascending, -1 padded)
+ * Host-side argument errors return before any launch; topk - 1 above 32
+ * while topk is below ceil(S_max / bs) is MOBA_ERR_UNSUPPORTED.  The plain
+ * form takes its scratch from cudaMallocAsync on the stream; the _ws form
+ * takes it from the caller (256-byte aligned, at least
+ * moba_decode_workspace_size bytes; it allocates nothing).
+ */
+int moba_decode_fwd(const void *q, const void *k_cache, const void *v_cache, const float *kbar,
+                    const int32_t *cache_lens, void *out, float *lse, int32_t *idx, int B, int H,
+                    int S_max, int D, int block_size, int topk, void *stream);
+size_t moba_decode_workspace_size(int B, int H, int D, int topk);
+int moba_decode_fwd_ws(const void *q, const void *k_cache, const void *v_cache,
+                       const float *kbar, const int32_t *cache_lens, void *out, float *lse,
+                       int32_t *idx, int B, int H, int S_max, int D, int block_size, int topk,
+                       void *workspace, size_t workspace_bytes, void *stream);
+
 /* Test hooks of the bounded waits in the tcgen05 kernels (process-wide):
  * wait_limit_cycles is the clock64 budget of one mbarrier wait (<= 0 restores
  * the default, about 2 s); flags bit 0 makes the K/V producer skip its first

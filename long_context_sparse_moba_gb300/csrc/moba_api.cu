@@ -472,6 +472,64 @@ MOBA_EXPORT int moba_set_gate_kernel(int kind) {
     return MOBA_OK;
 }
 
+static int decode_check(const void *q, const void *k, const void *v, const float *kbar,
+                        const int32_t *lens, const void *out, const float *lse, int B, int H,
+                        int S_max, int D, int bs, int topk) {
+    if (!q || !k || !v || !kbar || !lens || !out || !lse) return MOBA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || S_max < 1 || bs < 1 || bs % 64 != 0 || topk < 1)
+        return MOBA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return MOBA_ERR_UNSUPPORTED;
+    if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(out) || misaligned(kbar))
+        return MOBA_ERR_INVALID_ARG;
+    const long long n_max = ((long long)S_max + bs - 1) / bs;
+    // a scored row keeps its top list in registers
+    if (topk - 1 > decode_km1_max() && topk < n_max) return MOBA_ERR_UNSUPPORTED;
+    if ((long long)B * H * topk >= (1ll << 31) || (long long)B * n_max * H >= (1ll << 31))
+        return MOBA_ERR_UNSUPPORTED;
+    return MOBA_OK;
+}
+
+MOBA_EXPORT size_t moba_decode_workspace_size(int B, int H, int D, int topk) {
+    if (B < 1 || H < 1 || (D != 64 && D != 128) || topk < 1) return 0;
+    return decode_scratch(nullptr, B, H, D, topk, nullptr, nullptr, nullptr, nullptr);
+}
+
+MOBA_EXPORT int moba_decode_fwd_ws(const void *q, const void *k_cache, const void *v_cache,
+                                   const float *kbar, const int32_t *cache_lens, void *out,
+                                   float *lse, int32_t *idx, int B, int H, int S_max, int D,
+                                   int block_size, int topk, void *workspace,
+                                   size_t workspace_bytes_, void *stream) {
+    int rc = decode_check(q, k_cache, v_cache, kbar, cache_lens, out, lse, B, H, S_max, D,
+                          block_size, topk);
+    if (rc) return rc;
+    const size_t need = decode_scratch(nullptr, B, H, D, topk, nullptr, nullptr, nullptr, nullptr);
+    if (!workspace || workspace_bytes_ < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
+        return MOBA_ERR_WORKSPACE;
+    auto st = static_cast<cudaStream_t>(stream);
+    const size_t toff = decode_ticket_offset(B, H, D, topk);
+    MOBA_TRY(cudaMemsetAsync(static_cast<char *>(workspace) + toff, 0, sizeof(int) * (size_t)B * H,
+                             st));
+    return cuda_status(launch_decode(q, k_cache, v_cache, kbar, cache_lens, out, lse, idx, B, H,
+                                     S_max, D, block_size, topk, workspace, st));
+}
+
+MOBA_EXPORT int moba_decode_fwd(const void *q, const void *k_cache, const void *v_cache,
+                                const float *kbar, const int32_t *cache_lens, void *out,
+                                float *lse, int32_t *idx, int B, int H, int S_max, int D,
+                                int block_size, int topk, void *stream) {
+    int rc = decode_check(q, k_cache, v_cache, kbar, cache_lens, out, lse, B, H, S_max, D,
+                          block_size, topk);
+    if (rc) return rc;
+    auto st = static_cast<cudaStream_t>(stream);
+    const size_t bytes = decode_scratch(nullptr, B, H, D, topk, nullptr, nullptr, nullptr, nullptr);
+    void *mem = nullptr;
+    if (cudaMallocAsync(&mem, bytes, st) != cudaSuccess) return MOBA_ERR_CUDA;
+    rc = moba_decode_fwd_ws(q, k_cache, v_cache, kbar, cache_lens, out, lse, idx, B, H, S_max, D,
+                            block_size, topk, mem, bytes, stream);
+    if (cudaFreeAsync(mem, st) != cudaSuccess && rc == MOBA_OK) rc = MOBA_ERR_CUDA;
+    return rc;
+}
+
 MOBA_EXPORT int moba_set_pooling(int kind) {
     if (kind != MOBA_POOL_MEAN && kind != MOBA_POOL_MAX) return MOBA_ERR_INVALID_ARG;
     g_pool_kind = kind;

@@ -130,6 +130,14 @@ cudaError_t launch_gate_tc(const Plan &p, const Workspace &ws, const __nv_bfloat
                            unsigned long long *need_list,
                            int *need_count, cudaStream_t st);
 int mma_tile_rows();
+// decode: one query row per (sequence, head) against its KV cache
+int decode_km1_max();
+size_t decode_scratch(void *base, int B, int H, int D, int topk, int32_t **sel, float **ml,
+                      float **po, int **ticket);
+size_t decode_ticket_offset(int B, int H, int D, int topk);
+cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *kbar,
+                          const int32_t *lens, void *out, float *lse, int32_t *idx, int B, int H,
+                          int S_max, int D, int bs, int topk, void *scratch, cudaStream_t st);
 void tc_debug_set(int flags, long long wait_limit);
 
 }  // namespace moba

@@ -47,6 +47,10 @@ _SIGNATURES = {
     "moba_set_attention_kernel": (_I, [_I]),
     "moba_set_gate_kernel": (_I, [_I]),
     "moba_set_pooling": (_I, [_I]),
+    "moba_decode_fwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "moba_decode_workspace_size": (_SZ, [_I, _I, _I, _I]),
+    "moba_decode_fwd_ws": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _SZ,
+                                _P]),
     "moba_attn_fwd_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "moba_attn_fwd_noalloc_capacity": (_SZ, []),
     "moba_debug_set": (_I, [_I, ctypes.c_longlong]),
@@ -187,6 +191,42 @@ def attn_fwd(q, k, v, block_size: int, topk: int, out=None, lse=None, workspace=
                                     block_size, topk, _ptr(workspace), workspace.numel(), st)
     _check(rc, "moba_attn_fwd")
     return out, lse
+
+
+def decode_workspace_size(B: int, H: int, D: int, topk: int) -> int:
+    return int(lib().moba_decode_workspace_size(B, H, D, topk))
+
+
+def decode_fwd(q, k_cache, v_cache, kbar, cache_lens, block_size: int, topk: int, out=None,
+               lse=None, idx=None, workspace=None, stream=None):
+    """One decode step: q [B, H, D] bf16 against k_cache, v_cache [B, S_max, H,
+    D] bf16 (the new token already at position cache_lens[b] - 1), kbar the
+    caches' pooled keys (:func:`kpool` of k_cache), cache_lens int32 [B] on the
+    device -> (out [B, H, D] bf16, lse [B, H] fp32, idx [B, H, topk] int32)."""
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, n)
+    _need(kbar, torch.float32, "kbar")
+    _need(cache_lens, torch.int32, "cache_lens")
+    B, H, D = q.shape
+    if k_cache.dim() != 4 or k_cache.shape[0] != B or k_cache.shape[2:] != (H, D) or \
+            v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache, v_cache must be [B, S_max, H, D] matching q")
+    S_max = k_cache.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, H, dtype=torch.float32, device=q.device)
+    if idx is None:
+        idx = torch.empty(B, H, topk, dtype=torch.int32, device=q.device)
+    st = _stream(stream)
+    args = (_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kbar), _ptr(cache_lens), _ptr(out),
+            _ptr(lse), _ptr(idx), B, H, S_max, D, block_size, topk)
+    if workspace is None:
+        rc = lib().moba_decode_fwd(*args, st)
+    else:
+        rc = lib().moba_decode_fwd_ws(*args, _ptr(workspace), workspace.numel(), st)
+    _check(rc, "moba_decode_fwd")
+    return out, lse, idx
 
 
 def attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, block_size: int, topk: int, out=None,

@@ -57,6 +57,22 @@ def test_pooling_switch_validates(lib):
     assert lib.moba_set_pooling(ops.POOL_MEAN) == ops.MOBA_OK
 
 
+def test_decode_validates_on_the_host(lib):
+    args = lambda **kw: [kw.get(n, FAKE) for n in ("q", "k", "v", "kbar", "lens", "out", "lse")]
+    # B, H, S_max, D, bs, topk
+    assert lib.moba_decode_fwd(*args(q=None), None, 1, 1, 64, 64, 64, 1, None) == 1
+    assert lib.moba_decode_fwd(*args(), None, 0, 1, 64, 64, 64, 1, None) == 1
+    assert lib.moba_decode_fwd(*args(), None, 1, 1, 64, 96, 64, 1, None) == 2      # head dim
+    assert lib.moba_decode_fwd(*args(), None, 1, 1, 64, 64, 96, 1, None) == 1      # block size
+    assert lib.moba_decode_fwd(*args(), None, 1, 1, 64 * 64, 64, 64, 40, None) == 2  # wide top-k
+    assert lib.moba_decode_fwd(*args(q=ctypes.c_void_p(0x10002)), None, 1, 1, 64, 64, 64, 1,
+                               None) == 1                                           # misaligned
+    need = lib.moba_decode_workspace_size(2, 4, 128, 3)
+    assert need > 0 and lib.moba_decode_workspace_size(2, 4, 96, 3) == 0
+    assert lib.moba_decode_fwd_ws(*args(), None, 2, 4, 1024, 128, 256, 3, FAKE, need - 1,
+                                  None) == ops.MOBA_ERR_WORKSPACE
+
+
 def test_num_blocks(lib):
     assert ops.num_blocks(32768, 512) == 64
     assert ops.num_blocks(131072, 2048) == 64
