@@ -69,8 +69,8 @@ TRAFFIC_SOURCES = ("long_context_sparse_moba_gb300/csrc/moba_attn_tc.cu",
                    "long_context_sparse_moba_gb300/csrc/moba_internal.cuh")
 MEASURED_TRAFFIC = {
     # (workload, topk, phase): (bytes per launch, sha256 of TRAFFIC_SOURCES)
-    ("train32k", 3, "attn_past"): (1037235200 + 538467072,
-                                   "ebd0aa58817bccf6ac8e79c044f55931ab7c362590ead5068e295eea8a48ba64"),
+    ("train32k", 3, "attn_past"): (1031735808 + 538555904,
+                                   "795ee3f8a9b21ea879a0c47fca26508a53e3658cba58b62f7772c4334fdb698e"),
 }
 
 
@@ -119,6 +119,42 @@ def whole_job_rate(tokens_per_rank: int, world: int, ms_per_step: float) -> floa
     """Tokens per second of the whole job: every rank's tokens over the slowest
     rank's step time."""
     return tokens_per_rank * world / (ms_per_step * 1e-3)
+
+
+def decode_bench(ops, torch, dev, H, D, bs, topk, B=8, S=32768, steps=50):
+    """One decode step of B sequences with S-token caches (the workload's heads,
+    head size, block size and top-k): time per step, tokens/s and the
+    algorithmic bytes (q, the pooled keys of the past blocks, the selected
+    blocks' K and V, out, lse) over the time, against HBM."""
+    g = torch.Generator(device=dev).manual_seed(77)
+    kc = torch.randn(B, S, H, D, generator=g, device=dev, dtype=torch.bfloat16)
+    vc = torch.randn(B, S, H, D, generator=g, device=dev, dtype=torch.bfloat16)
+    q = torch.randn(B, H, D, generator=g, device=dev, dtype=torch.bfloat16)
+    kbar = ops.kpool(kc, bs)
+    lens = torch.full((B,), S, dtype=torch.int32, device=dev)
+    ws = torch.empty(ops.decode_workspace_size(B, H, D, topk), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty(B, H, dtype=torch.float32, device=dev)
+    idx = torch.empty(B, H, topk, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(5):
+        ops.decode_fwd(q, kc, vc, kbar, lens, bs, topk, out=out, lse=lse, idx=idx, workspace=ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        ops.decode_fwd(q, kc, vc, kbar, lens, bs, topk, out=out, lse=lse, idx=idx, workspace=ws)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    assert ops.get_status() == ops.MOBA_OK
+    ci = (S - 1) // bs
+    kv_keys = min(topk - 1, ci) * bs + (S - ci * bs)
+    nbytes = B * H * (D * 2 + ci * D * 4 + kv_keys * D * 2 * 2 + D * 2 + 4)
+    del kc, vc
+    return {"B": B, "cache_len": S, "topk": topk, "ms_per_step": ms,
+            "tokens_per_s": B / (ms * 1e-3), "gbs": nbytes / (ms * 1e-3) / 1e9,
+            "bytes_per_step": nbytes}
 
 
 def load_peaks():
@@ -281,6 +317,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -380,6 +417,10 @@ def main():
                  "effective_tflops": 4 * D * (dcur + dpast) * H / (dms * 1e-3) / 1e12,
                  "sparse_speedup": dms / ms_per_step}
 
+    decode = None
+    if not args.no_decode and rank == 0 and not varlen:
+        decode = decode_bench(ops, torch, dev, H, D, bs, topk)
+
     # end to end through the public API with pinned host buffers
     e2e = None
     if not args.no_e2e:
@@ -418,6 +459,8 @@ def main():
         return
 
     peaks, peak_src = load_peaks()
+    if decode is not None:
+        decode["frac_hbm"] = decode["gbs"] / peaks["hbm_gbs"]
     cur, past = issued_pairs(w.seqlens, bs, topk)
     flops = 4 * D * (cur + past) * H
     tflops = flops / (ms_per_step * 1e-3) / 1e12
@@ -463,7 +506,7 @@ def main():
             "frac_of_bf16_peak": tflops / peaks["bf16_tflops_sustained"],
             "issued_flops_per_step": flops,
             "sparsity_vs_dense_causal": None,
-            "roofline": roofline, "phases": phases, "dense": dense, "e2e": e2e,
+            "roofline": roofline, "phases": phases, "dense": dense, "decode": decode, "e2e": e2e,
             "cpu_baseline": cpu, "gpu_launches": launches, "clocks": clk,
             "device_status": ops.status_string(status)}
     dcur, dpast = issued_pairs(w.seqlens, bs, n_max)
