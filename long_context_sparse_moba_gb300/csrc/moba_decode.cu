@@ -180,49 +180,59 @@ __global__ void __launch_bounds__(32 * kAttnWarps) decode_attn_kernel(Args a) {
         const size_t tok_stride = (size_t)a.H * D;
         const __nv_bfloat16 *kbase = a.k + ((size_t)b * a.S_max * a.H + h) * D + q4 * DQ;
         const __nv_bfloat16 *vbase = a.v + ((size_t)b * a.S_max * a.H + h) * D + q4 * DQ;
-        // the loop bound is the same for the whole warp (the shuffles below
-        // need every lane); a quad past the block's end computes nothing
-        for (int t_base = t0; t_base < t1; t_base += kQuads) {
-            const int t = t_base + quad;
-            const bool live = t < t1;
-            uint4 ku[DQ / 8], vu[DQ / 8];
+        // Two keys per quad and iteration, their K and V loads all issued
+        // before use.  The loop bound is the same for the whole warp (the
+        // shuffles below need every lane); a quad past the block's end
+        // computes nothing for that key.
+        for (int t_base = t0; t_base < t1; t_base += 2 * kQuads) {
+            int t[2];
+            bool live[2];
+            uint4 ku[2][DQ / 8], vu[2][DQ / 8];
 #pragma unroll
-            for (int x = 0; x < DQ / 8; ++x) {
-                ku[x] = live ? __ldcs(reinterpret_cast<const uint4 *>(kbase + (size_t)t * tok_stride) + x)
-                             : make_uint4(0, 0, 0, 0);
-                vu[x] = live ? __ldcs(reinterpret_cast<const uint4 *>(vbase + (size_t)t * tok_stride) + x)
-                             : make_uint4(0, 0, 0, 0);
-            }
-            float s = 0.f;
+            for (int u = 0; u < 2; ++u) {
+                t[u] = t_base + u * kQuads + quad;
+                live[u] = t[u] < t1;
 #pragma unroll
-            for (int x = 0; x < DQ / 8; ++x) {
-                const __nv_bfloat162 *p2 = reinterpret_cast<const __nv_bfloat162 *>(&ku[x]);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = __bfloat1622float2(p2[e]);
-                    s = fmaf(qf[8 * x + 2 * e], f.x, s);
-                    s = fmaf(qf[8 * x + 2 * e + 1], f.y, s);
+                for (int x = 0; x < DQ / 8; ++x) {
+                    ku[u][x] = live[u] ? __ldcs(reinterpret_cast<const uint4 *>(kbase + (size_t)t[u] * tok_stride) + x)
+                                       : make_uint4(0, 0, 0, 0);
+                    vu[u][x] = live[u] ? __ldcs(reinterpret_cast<const uint4 *>(vbase + (size_t)t[u] * tok_stride) + x)
+                                       : make_uint4(0, 0, 0, 0);
                 }
             }
-            s += __shfl_xor_sync(0xffffffffu, s, 1);
-            s += __shfl_xor_sync(0xffffffffu, s, 2);
-            if (!live) continue;
-            const float xl = s * a.scale_log2;
-            const float m_new = fmaxf(m, xl);
-            const float corr = ptx::fast_exp2(m - m_new);
-            const float p = ptx::fast_exp2(xl - m_new);
-            l = l * corr + p;
 #pragma unroll
-            for (int x = 0; x < DQ / 8; ++x) {
-                const __nv_bfloat162 *p2 = reinterpret_cast<const __nv_bfloat162 *>(&vu[x]);
+            for (int u = 0; u < 2; ++u) {
+                float s = 0.f;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = __bfloat1622float2(p2[e]);
-                    o[8 * x + 2 * e] = fmaf(p, f.x, o[8 * x + 2 * e] * corr);
-                    o[8 * x + 2 * e + 1] = fmaf(p, f.y, o[8 * x + 2 * e + 1] * corr);
+                for (int x = 0; x < DQ / 8; ++x) {
+                    const __nv_bfloat162 *p2 = reinterpret_cast<const __nv_bfloat162 *>(&ku[u][x]);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __bfloat1622float2(p2[e]);
+                        s = fmaf(qf[8 * x + 2 * e], f.x, s);
+                        s = fmaf(qf[8 * x + 2 * e + 1], f.y, s);
+                    }
                 }
+                s += __shfl_xor_sync(0xffffffffu, s, 1);
+                s += __shfl_xor_sync(0xffffffffu, s, 2);
+                if (!live[u]) continue;
+                const float xl = s * a.scale_log2;
+                const float m_new = fmaxf(m, xl);
+                const float corr = ptx::fast_exp2(m - m_new);
+                const float p = ptx::fast_exp2(xl - m_new);
+                l = l * corr + p;
+#pragma unroll
+                for (int x = 0; x < DQ / 8; ++x) {
+                    const __nv_bfloat162 *p2 = reinterpret_cast<const __nv_bfloat162 *>(&vu[u][x]);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __bfloat1622float2(p2[e]);
+                        o[8 * x + 2 * e] = fmaf(p, f.x, o[8 * x + 2 * e] * corr);
+                        o[8 * x + 2 * e + 1] = fmaf(p, f.y, o[8 * x + 2 * e + 1] * corr);
+                    }
+                }
+                m = m_new;
             }
-            m = m_new;
         }
     }
     // combine the quads: common max, rescaled sums and O
