@@ -6,12 +6,13 @@
 // the current block) and "MOBA mixture of block attention for server-side long
 // context" (hncyxsy.com/news/197418) section 3 (force_current_block).
 //
-// One CTA = one job of up to 256 query rows held as two 128-row tiles (g = 0,
-// 1) that share every 128-key K/V tile, 352 threads in five roles:
-//   warp 0      TMA producers: lane 0 loads the Q tiles (contiguous rows) and a
+// Persistent: one CTA per SM walks jobs blockIdx.x, + gridDim.x, ...; a job is
+// up to 256 query rows held as two 128-row tiles (g = 0, 1) that share every
+// 128-key K/V tile.  320 threads in four roles:
+//   warp 0      TMA producers: lane 0 loads the Q tiles (own-block mode) and a
 //               2-stage ring of K tiles, lane 1 a 2-stage ring of V tiles (one
 //               TMA stream per thread tops out well below what the tensor core
-//               consumes);
+//               consumes); the rings run ahead into the next job;
 //   warp 1      allocates all 512 TMEM columns; lane 0 issues the MMAs
 //                 S_g = Q_g K_j^T   (M128 N128 K=D, A and B from shared memory)
 //                 O_g += P_g V_j    (M128 N=D K128, A = P_g from TMEM)
@@ -21,20 +22,24 @@
 //               order, S_g(j) may overwrite the TMEM columns that P_g(j-1)
 //               occupies;
 //   warps 2..9  softmax of tile 0 (warps 2..5) and tile 1 (6..9): thread r owns
-//               row r (its TMEM lane); it reads its 128 scores, updates the
-//               running max / sum, rescales its O row in TMEM when the max grew
-//               by more than 2^8, and writes P (bf16 pairs) back over the first
-//               64 columns of its S.  Epilogue per tile.
+//               row r (its TMEM lane).  Per 64-key half of S it reads the half
+//               once, takes its max, raises the offset (to a whole number) only
+//               when the max exceeds it by more than 8 (then O, the running sum
+//               and, for the second half, the first half's P are rescaled by an
+//               exact power of two), and writes P = 2^(s * scale - offset) as
+//               bf16 pairs over the first 64 columns of S; the arithmetic runs
+//               on packed fp32 pairs.  Epilogue per tile, rows re-laid through
+//               4 KB of shared memory per warp for full-line global access.
 // TMEM: S_g at columns 256g .. 256g+127 (P_g in the first 64), O_g at
-// 256g+128 .. 256g+128+D.  One CTA per SM (192 KB of shared memory).
-// Per 128 keys the shared-memory traffic is Q + K for each S MMA and V for
-// each PV MMA, which balances the tensor core and the exponential unit.
+// 256g+128 .. 256g+128+D.  One CTA per SM (192 KB of tiles + 32 KB of staging).
 //
 // Modes:
 //   kPast     gathered rows: up to 256 rows of one regroup list (rows that
-//             selected the same past block of the same head); the softmax warps
-//             gather Q with cp.async; output = normalised fp32 partial O and
-//             its log2-sum-exp per (row, slot);
+//             selected the same past block of the same head), jobs looked up in
+//             the table the regroup scan writes; the softmax warps gather the
+//             next job's Q rows with cp.async as soon as the MMA has released
+//             Q_g, arriving on its barrier asynchronously; output = normalised
+//             bf16 partial O and its log2-sum-exp per (row, slot);
 //   kCurrent  rows [r0, r0 + 256) of a sequence: causal attention over the own
 //             block (every key up to the row on the dense path), then the
 //             log-sum-exp merge with the row's past partials -> bf16 out, lse.

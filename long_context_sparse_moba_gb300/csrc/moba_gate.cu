@@ -227,7 +227,9 @@ cudaError_t launch_kpool(const Plan &p, const Workspace &ws, const __nv_bfloat16
 }
 
 // ---------------------------------------------------------------------------
-// K2: gate + top-k.  A CTA scores 128 consecutive query rows of one (sequence,
+// K2 on the CUDA cores (selectable with moba_set_gate_kernel, and used when a
+// sequence has more blocks than the tensor-core gate's TMEM holds): gate +
+// top-k.  A CTA scores 128 consecutive query rows of one (sequence,
 // head) against the pooled keys of that sequence's past blocks.  Four lanes
 // share a row: lane j of a quad holds dims [j*D/4, (j+1)*D/4) of the quad's 4
 // rows in fp32 registers, so every pooled-key load from shared memory feeds 16

@@ -10,25 +10,29 @@
 // 128 consecutive query rows of one (sequence, head).  Units are ordered
 // sequence, head, row tile (the tiles of a head alternate from both ends so a
 // range mixes cheap early rows with costly late ones), so a CTA keeps the
-// pooled keys of one head resident for many units.  320 threads:
-//   warp 0      TMA: a 3-stage ring of q tiles and, whenever the (sequence,
-//               head) changes, the head's pooled keys split into two bf16
-//               terms, kbar ~= hi + lo (hi = bf16(kbar), lo = bf16(kbar - hi));
+// pooled keys of one head resident for many units.  Roles:
+//   warp 0      TMA: a ring of q tiles (as many stages as the shared memory
+//               left beside the keys holds) and, whenever the (sequence, head)
+//               changes, the head's pooled keys split into two bf16 terms,
+//               kbar ~= hi + lo (hi = bf16(kbar), lo = bf16(kbar - hi));
 //   warp 1      allocates TMEM; lane 0 issues one MMA chain per unit,
 //               approx[r][c] = q_r . hi_c + q_r . lo_c (M128, N = the unit's
-//               scored blocks rounded up to 16, fp32 in TMEM), alternating
-//               between two 256-column TMEM halves;
-//   warps 2..9  two selection warpgroups taking alternate units; thread r
-//               owns row r (its TMEM lane):
-//     1. keeps the top k-1 approximate scores of its row and the k-th.  With
+//               scored blocks rounded up to 16, fp32 in TMEM), into as many
+//               TMEM slots as the longest sequence's block count allows;
+//   warps 2 ..  NWG selection warpgroups taking units in turn; thread r owns
+//               row r (its TMEM lane):
+//     1. keeps the k largest approximate scores of its row.  With
 //        |approx - exact| <= E, E = 2^-13 ||q_r|| max_c ||kbar_c|| (at least
 //        8x the worst case of the bf16 split, the fp32 MMA accumulation and
 //        the fp32 dot product): when the k-th is below T - 2E (T the (k-1)-th)
-//        the approximate top k-1 is the exact one and the row is done;
-//     2. otherwise every block with approx >= T - 2E gets the exact fp32
-//        score, with the summation order of the CUDA-core gate (four lane
-//        partials of four interleaved sums), so the selection -- and its
-//        lower-index tie-break -- equals that kernel's bit for bit.
+//        the blocks with approx >= T are the exact top k-1 and the row is
+//        written here, with its selections added into the per-list counts;
+//     2. otherwise the row and its candidates (approx >= T - 2E: they hold
+//        the exact top k-1, and every other block scores below all of them)
+//        go to gate_exact_kernel, which scores them exactly with the summation
+//        order of the CUDA-core gate (four lane partials of four interleaved
+//        sums), so the selection -- and its lower-index tie-break -- equals
+//        that kernel's bit for bit.
 // Rows whose own block has at most k-1 predecessors take them all.
 // Every wait is bounded; a wait that runs out records MOBA_ERR_TIMEOUT.
 #include <algorithm>
