@@ -19,6 +19,7 @@ import argparse
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -68,18 +69,27 @@ TRAFFIC_SOURCES = ("long_context_sparse_moba_gb300/csrc/moba_attn_tc.cu",
                    "long_context_sparse_moba_gb300/csrc/moba_ptx.cuh",
                    "long_context_sparse_moba_gb300/csrc/moba_internal.cuh")
 MEASURED_TRAFFIC = {
-    # (workload, topk, phase): (bytes per launch, sha256 of TRAFFIC_SOURCES)
+    # (workload, topk, phase): (bytes per launch, sources_sha256() of the code measured)
     ("train32k", 3, "attn_past"): (1031735808 + 538555904,
-                                   "795ee3f8a9b21ea879a0c47fca26508a53e3658cba58b62f7772c4334fdb698e"),
+                                   "1626be6acd205fe85b08cdd692056e099e23ccea68a7c42eddb115c8b59386fe"),
 }
 
 
+def code_only(text: str) -> str:
+    """Source text without comments and blank lines: what the compiler sees."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*", "", ln).rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def sources_sha256() -> str:
+    """Hash of the kernel sources' code (comments excluded), so that measured
+    counters stay attached to the code they were taken on."""
     import hashlib
     h = hashlib.sha256()
     for rel in TRAFFIC_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(code_only(f.read()).encode())
     return h.hexdigest()
 
 
