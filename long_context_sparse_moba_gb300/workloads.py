@@ -171,3 +171,14 @@ def sample_rows(w: Workload, count: int, seed: int = 1234, needle_queries=()):
     toks += [int(x) for x in torch.randint(0, w.total, (rest,), generator=g)]
     heads += [int(x) for x in torch.randint(0, w.H, (rest,), generator=g)]
     return toks[:count], heads[:count]
+
+
+def make_grad(w: Workload, device="cpu", scale: float = 1.0) -> torch.Tensor:
+    """Upstream gradient dL/d(out) for the backward pass: N(0, scale^2) in the
+    layout of q, from its own generator (seeded with the workload's seed + 7919)
+    so that drawing it leaves q, k, v unchanged."""
+    device = torch.device(device)
+    g = torch.Generator(device=device).manual_seed(w.seed + 7919)
+    d = torch.randn(w.total, w.H, w.D, generator=g, device=device, dtype=torch.float32)
+    d = d.mul_(scale).to(torch.bfloat16)
+    return d if w.varlen else d.view(w.B, w.S, w.H, w.D)

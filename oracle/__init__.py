@@ -1,4 +1,4 @@
-"""CPU oracle of the MoBA forward pass -- test infrastructure only.
+"""CPU oracle of the MoBA forward and backward passes -- test infrastructure only.
 
 Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  The CUDA library never calls it and
@@ -50,6 +50,11 @@ def _load():
         lib.moba_oracle_kpool.argtypes = [p, p, i32, i32, i32, i32, p]
         lib.moba_oracle_kpool_max.argtypes = [p, p, i32, i32, i32, i32, p]
         lib.moba_oracle_rows.restype = i32
+        lib.moba_oracle_bwd.restype = i32
+        lib.moba_oracle_bwd.argtypes = [p, p, p, p, p, i32, i32, i32, i32, i32, p, p, p, p]
+        lib.moba_oracle_bwd_dq_rows.restype = i32
+        lib.moba_oracle_bwd_dq_rows.argtypes = [p, p, p, p, p, i32, i32, i32, i32, i32, i64,
+                                                p, p, p, p]
         lib.moba_oracle_rows.argtypes = [p, p, p, p, i32, i32, i32, i32, i32, p,
                                          i64, p, p, p, p, p, p, p]
         _lib = lib
@@ -144,3 +149,42 @@ def moba_full(q, k, v, cu_seqlens, H: int, D: int, block_size: int, topk: int,
     r = moba_rows(q, k, v, cu, H, D, block_size, topk, tok, head, given_idx=gi, pooling=pooling)
     return {"idx": r["idx"].reshape(total, H, topk), "gap": r["gap"].reshape(total, H),
             "out": r["out"].reshape(total, H, D), "lse": r["lse"].reshape(total, H)}
+
+
+def moba_bwd(q, k, v, dout, cu_seqlens, H: int, D: int, block_size: int, topk: int,
+             idx=None, pooling: str = "mean") -> dict:
+    """Backward pass with the gate's selection held fixed: ``dq``, ``dk``,
+    ``dv`` float64 ``[total, H, D]`` for the upstream gradient ``dout``.
+    ``idx`` ([total, H, topk]) defaults to the oracle's own selection."""
+    qb, kb, vb, gb = _bits(q), _bits(k), _bits(v), _bits(dout)
+    cu = _cu(cu_seqlens)
+    total = int(cu[-1])
+    if idx is None:
+        idx = moba_full(qb, kb, vb, cu, H, D, block_size, topk, pooling=pooling)["idx"]
+    idx = np.ascontiguousarray(np.asarray(idx, dtype=np.int32).reshape(total, H, topk))
+    dq = np.empty((total, H, D), dtype=np.float64)
+    dk = np.empty((total, H, D), dtype=np.float64)
+    dv = np.empty((total, H, D), dtype=np.float64)
+    rc = _load().moba_oracle_bwd(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(gb), _ptr(cu), len(cu) - 1,
+                                 H, D, block_size, topk, _ptr(idx), _ptr(dq), _ptr(dk), _ptr(dv))
+    if rc != 0:
+        raise ValueError(f"moba_oracle_bwd failed ({rc})")
+    return {"dq": dq, "dk": dk, "dv": dv, "idx": idx}
+
+
+def moba_bwd_dq_rows(q, k, v, dout, cu_seqlens, H: int, D: int, block_size: int, topk: int,
+                     row_tok, row_head, idx) -> np.ndarray:
+    """dq float64 [R, D] of the listed rows, for their selections idx [R, topk]."""
+    qb, kb, vb, gb = _bits(q), _bits(k), _bits(v), _bits(dout)
+    cu = _cu(cu_seqlens)
+    rt = np.ascontiguousarray(np.asarray(row_tok, dtype=np.int64))
+    rh = np.ascontiguousarray(np.asarray(row_head, dtype=np.int32))
+    R = rt.shape[0]
+    gi = np.ascontiguousarray(np.asarray(idx, dtype=np.int32).reshape(R, topk))
+    dq = np.empty((R, D), dtype=np.float64)
+    rc = _load().moba_oracle_bwd_dq_rows(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(gb), _ptr(cu),
+                                         len(cu) - 1, H, D, block_size, topk, R, _ptr(rt),
+                                         _ptr(rh), _ptr(gi), _ptr(dq))
+    if rc != 0:
+        raise ValueError(f"moba_oracle_bwd_dq_rows failed ({rc})")
+    return dq

@@ -1,8 +1,8 @@
 /*
  * moba_oracle.c -- plain, slow CPU oracle of the Mixture of Block Attention
- * (MoBA) forward pass.  TEST INFRASTRUCTURE ONLY: the tests, the smoke check
- * and the CPU-baseline leg of the benchmark call it; the CUDA library never
- * does, and the two share no code.
+ * (MoBA) forward and backward passes.  TEST INFRASTRUCTURE ONLY: the tests,
+ * the smoke check and the CPU-baseline leg of the benchmark call it; the CUDA
+ * library never does, and the two share no code.
  *
  * Pages this follows (cited by page title and section):
  *   [P2] "Moonshot MoBA paper explained: sparse-attention config skeleton"
@@ -33,6 +33,11 @@
  *   R5 gating is per (sequence, head): each head pools its own keys.
  *   R6 max pooling (the variant the server-side page allows) takes the
  *      element-wise maximum over the block's own tokens.
+ *   R7 the backward pass holds the gate's selection fixed (top-k is piecewise
+ *      constant, so it passes no gradient; none reaches the pooled keys):
+ *      gradients flow through the softmax attention over the selected keys
+ *      only.  [P4] section 3 trains MoBA layers end to end (it blames the
+ *      sparse gradient path for a higher SFT loss).
  *
  * Parity pins for every function here live in tests/test_oracle.py.
  */
@@ -316,5 +321,162 @@ int moba_oracle_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
         free(sel);
     }
     free(base);
+    return failed ? -3 : 0;
+}
+
+/*
+ * Backward pass of one row (reading R7): the softmax attention of row i of
+ * sequence b, head h over the keys of its selected blocks, differentiated.
+ * With z_j = (q . k_j) / sqrt(D), P_j = exp(z_j - lse), o = sum_j P_j v_j and
+ * the upstream gradient g = dL/do:
+ *   dP_j = g . v_j,  delta = g . o,  dz_j = P_j (dP_j - delta)
+ *   dL/dq   = sum_j dz_j k_j / sqrt(D)
+ *   dL/dk_j += dz_j q / sqrt(D),   dL/dv_j += P_j g
+ * dq_row receives dL/dq; dk, dv (whole [total][H][D] arrays) are accumulated
+ * into when not NULL.  sel holds the nsel selected local blocks.
+ */
+static void row_backward(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                         const uint16_t *dout, int64_t t_begin, int64_t i, int h,
+                         int H, int D, int block_size, const int64_t *sel,
+                         int64_t nsel, double *dq_row, double *dk, double *dv)
+{
+    const double scale = 1.0 / sqrt((double)D);
+    const int64_t t = t_begin + i;
+    int64_t nkeys = 0;
+    for (int64_t j = 0; j < nsel; ++j) {
+        int64_t k0 = sel[j] * block_size, k1 = k0 + block_size;
+        if (k1 > i + 1) k1 = i + 1;
+        if (k1 > k0) nkeys += k1 - k0;
+    }
+    double *z = (double *)malloc(sizeof(double) * (size_t)(nkeys > 0 ? nkeys : 1));
+    int64_t *kt = (int64_t *)malloc(sizeof(int64_t) * (size_t)(nkeys > 0 ? nkeys : 1));
+    double *o = (double *)calloc((size_t)D, sizeof(double));
+    const uint16_t *qrow = q + (t * H + h) * D;
+    const uint16_t *grow = dout + (t * H + h) * D;
+    int64_t n = 0;
+    for (int64_t j = 0; j < nsel; ++j) {
+        int64_t k0 = sel[j] * block_size, k1 = k0 + block_size;
+        if (k1 > i + 1) k1 = i + 1;
+        for (int64_t p = k0; p < k1; ++p) {
+            const uint16_t *krow = k + ((t_begin + p) * H + h) * D;
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d) dot += widen_bf16(qrow[d]) * widen_bf16(krow[d]);
+            z[n] = dot * scale;
+            kt[n] = t_begin + p;
+            ++n;
+        }
+    }
+    double m = -INFINITY;
+    for (int64_t j = 0; j < nkeys; ++j) if (z[j] > m) m = z[j];
+    double l = 0.0;
+    for (int64_t j = 0; j < nkeys; ++j) l += exp(z[j] - m);
+    /* z now holds P_j */
+    for (int64_t j = 0; j < nkeys; ++j) z[j] = exp(z[j] - m) / l;
+    for (int64_t j = 0; j < nkeys; ++j) {
+        const uint16_t *vrow = v + (kt[j] * H + h) * D;
+        for (int d = 0; d < D; ++d) o[d] += z[j] * widen_bf16(vrow[d]);
+    }
+    double delta = 0.0;
+    for (int d = 0; d < D; ++d) delta += widen_bf16(grow[d]) * o[d];
+    for (int d = 0; d < D; ++d) dq_row[d] = 0.0;
+    for (int64_t j = 0; j < nkeys; ++j) {
+        const uint16_t *krow = k + (kt[j] * H + h) * D;
+        const uint16_t *vrow = v + (kt[j] * H + h) * D;
+        double dp = 0.0;
+        for (int d = 0; d < D; ++d) dp += widen_bf16(grow[d]) * widen_bf16(vrow[d]);
+        const double dz = z[j] * (dp - delta);
+        for (int d = 0; d < D; ++d) dq_row[d] += dz * widen_bf16(krow[d]) * scale;
+        if (dk) {
+            double *dkr = dk + (kt[j] * H + h) * D;
+            for (int d = 0; d < D; ++d) dkr[d] += dz * widen_bf16(qrow[d]) * scale;
+        }
+        if (dv) {
+            double *dvr = dv + (kt[j] * H + h) * D;
+            for (int d = 0; d < D; ++d) dvr[d] += z[j] * widen_bf16(grow[d]);
+        }
+    }
+    free(o);
+    free(kt);
+    free(z);
+}
+
+/* The selected local blocks of one row, from a [.][topk] selection table
+ * (entries < 0 or after the row's own block ignored). */
+static int64_t row_selection(const int32_t *idx_row, int topk, int64_t ci, int64_t *sel)
+{
+    int64_t nsel = 0;
+    for (int j = 0; j < topk; ++j) {
+        int32_t c = idx_row[j];
+        if (c >= 0 && c <= ci) sel[nsel++] = c;
+    }
+    return nsel;
+}
+
+/*
+ * Gradients dq, dk, dv ([total][H][D], double) of the MoBA attention for the
+ * upstream gradient dout ([total][H][D] bf16 bits), with the selection idx
+ * ([total][H][topk], as the forward's gate returns it) held fixed.  Each
+ * (sequence, head) pair is independent; its rows run in order.
+ */
+int moba_oracle_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                    const uint16_t *dout, const int64_t *cu, int num_seqs, int H, int D,
+                    int block_size, int topk, const int32_t *idx, double *dq,
+                    double *dk, double *dv)
+{
+    if (!q || !k || !v || !dout || !cu || !idx || !dq || !dk || !dv) return -1;
+    if (num_seqs < 1 || H < 1 || D < 1 || block_size < 1 || topk < 1) return -1;
+    const int64_t total = cu[num_seqs];
+    memset(dk, 0, sizeof(double) * (size_t)(total * H * D));
+    memset(dv, 0, sizeof(double) * (size_t)(total * H * D));
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t bh = 0; bh < (int64_t)num_seqs * H; ++bh) {
+        const int b = (int)(bh / H), h = (int)(bh % H);
+        const int64_t t_begin = cu[b], len = cu[b + 1] - cu[b];
+        int64_t *sel = (int64_t *)malloc(sizeof(int64_t) * (size_t)topk);
+        for (int64_t i = 0; i < len; ++i) {
+            const int64_t t = t_begin + i;
+            const int64_t nsel = row_selection(idx + (t * H + h) * topk, topk,
+                                               i / block_size, sel);
+            row_backward(q, k, v, dout, t_begin, i, h, H, D, block_size, sel, nsel,
+                         dq + (t * H + h) * D, dk, dv);
+        }
+        free(sel);
+    }
+    return 0;
+}
+
+/* dq alone for a list of (token, head) rows -- the part of the backward that
+ * a single row determines, for sampled checks at sizes the whole pass would
+ * take too long on.  idx holds the listed rows' selections ([nrows][topk]). */
+int moba_oracle_bwd_dq_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                            const uint16_t *dout, const int64_t *cu, int num_seqs, int H,
+                            int D, int block_size, int topk, int64_t nrows,
+                            const int64_t *row_tok, const int32_t *row_head,
+                            const int32_t *idx, double *dq)
+{
+    if (!q || !k || !v || !dout || !cu || !row_tok || !row_head || !idx || !dq) return -1;
+    if (num_seqs < 1 || H < 1 || D < 1 || block_size < 1 || topk < 1) return -1;
+    int failed = 0;
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t t = row_tok[r];
+        const int h = row_head[r];
+        int lo = 0, hi = num_seqs - 1;
+        while (lo < hi) {
+            int mid = (lo + hi + 1) / 2;
+            if (cu[mid] <= t) lo = mid; else hi = mid - 1;
+        }
+        if (t < cu[lo] || t >= cu[lo + 1] || h < 0 || h >= H) {
+#pragma omp atomic write
+            failed = 1;
+            continue;
+        }
+        const int64_t i = t - cu[lo];
+        int64_t *sel = (int64_t *)malloc(sizeof(int64_t) * (size_t)topk);
+        const int64_t nsel = row_selection(idx + r * topk, topk, i / block_size, sel);
+        row_backward(q, k, v, dout, cu[lo], i, h, H, D, block_size, sel, nsel, dq + r * D,
+                     NULL, NULL);
+        free(sel);
+    }
     return failed ? -3 : 0;
 }
