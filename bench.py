@@ -167,6 +167,47 @@ def decode_bench(ops, torch, dev, H, D, bs, topk, B=8, S=32768, steps=50):
             "bytes_per_step": nbytes}
 
 
+def backward_bench(ops, torch, w, inp, topk, out, lse, flops_fwd, steps=10):
+    """The backward pass (dq, dk, dv for a seeded upstream gradient) after the
+    timed forward: time per call and its issued tensor-core work, five
+    products per (query, key) pair against the forward's two, over the time."""
+    from long_context_sparse_moba_gb300 import workloads
+    dev = inp.q.device
+    dout = workloads.make_grad(w, device=dev)
+    dq, dk, dv = (torch.empty_like(inp.q) for _ in range(3))
+    ws = None
+    if not w.varlen:
+        ws = torch.empty(ops.bwd_workspace_size(w.B, w.H, w.S, w.D, w.block_size, topk),
+                         dtype=torch.uint8, device=dev)
+        cu = None
+    else:
+        cu = torch.tensor(inp.cu_seqlens, dtype=torch.int32, device=dev)
+
+    def call():
+        if w.varlen:
+            ops.attn_bwd_varlen(inp.q, inp.k, inp.v, out, lse, dout, cu, w.S, w.block_size, topk)
+        else:
+            ops.attn_bwd(inp.q, inp.k, inp.v, out, lse, dout, w.block_size, topk, dq=dq, dk=dk,
+                         dv=dv, workspace=ws)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert ops.get_status() == ops.MOBA_OK
+    ms = e0.elapsed_time(e1) / steps
+    flops = 2.5 * flops_fwd
+    return {"topk": topk, "ms_per_step": ms, "tokens_per_s": w.total / (ms * 1e-3),
+            "issued_flops": flops, "effective_tflops": flops / (ms * 1e-3) / 1e12,
+            "steps": steps}
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -328,6 +369,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-backward", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -474,6 +516,11 @@ def main():
     cur, past = issued_pairs(w.seqlens, bs, topk)
     flops = 4 * D * (cur + past) * H
     tflops = flops / (ms_per_step * 1e-3) / 1e12
+    backward = None
+    if not args.no_backward:
+        rc_, rp_ = issued_pairs(wr.seqlens, bs, topk)
+        backward = backward_bench(ops, torch, wr, inp, topk, out, lse, 4 * D * (rc_ + rp_) * H)
+        backward["frac_bf16"] = backward["effective_tflops"] / peaks["bf16_tflops_sustained"]
     per_call = {kk: vv / max(ncalls, 1) for kk, vv in phase_ms.items()}
     total_phase = sum(per_call.values())
     hbm = hbm_bytes(w, topk)
@@ -516,7 +563,8 @@ def main():
             "frac_of_bf16_peak": tflops / peaks["bf16_tflops_sustained"],
             "issued_flops_per_step": flops,
             "sparsity_vs_dense_causal": None,
-            "roofline": roofline, "phases": phases, "dense": dense, "decode": decode, "e2e": e2e,
+            "roofline": roofline, "phases": phases, "dense": dense, "decode": decode,
+            "backward": backward, "e2e": e2e,
             "cpu_baseline": cpu, "gpu_launches": launches, "clocks": clk,
             "device_status": ops.status_string(status)}
     dcur, dpast = issued_pairs(w.seqlens, bs, n_max)

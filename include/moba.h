@@ -146,6 +146,45 @@ int moba_attn_fwd_varlen_ws(const void *q, const void *k, const void *v, void *o
                             void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Backward pass of moba_attn_fwd: the gradients of the MoBA attention with
+ * the gate's selection held fixed (top-k is piecewise constant and passes no
+ * gradient; none reaches the pooled keys).  "MOBA ... server-side long
+ * context" section 3 trains MoBA layers end to end; the selection is the
+ * forward's ("Moonshot MoBA paper explained" sections 3.1 and 4.1), recomputed
+ * here with the same kernels.
+ *   q, k, v   : [B][S][H][D] bf16 (device), the forward's inputs
+ *   out, lse  : the forward's results ([B][S][H][D] bf16, [B][H][S] fp32)
+ *   dout      : [B][S][H][D] bf16 (device), dL/d(out)
+ *   dq, dk, dv: [B][S][H][D] bf16 (device, written)
+ * The summation order follows the GPU's scheduling (the per-block query lists
+ * fill in any order; dq adds fp32 atomics), so results may differ between
+ * calls in their last bits.
+ * Host-side argument errors (null or 16-byte-misaligned tensors, the sizes
+ * moba_attn_fwd rejects) return before any launch.  Scratch (the forward's
+ * selection tables and lists, an fp32 dq accumulator of B*S*H*D floats and
+ * B*S*H floats of dO . O) comes from cudaMallocAsync on `stream`; the _ws form
+ * takes it from the caller (256-byte aligned, at least
+ * moba_attn_bwd_workspace_size bytes, else MOBA_ERR_WORKSPACE).
+ */
+int moba_attn_bwd(const void *q, const void *k, const void *v, const void *out,
+                  const float *lse, const void *dout, void *dq, void *dk, void *dv, int B, int H,
+                  int S, int D, int block_size, int topk, void *stream);
+size_t moba_attn_bwd_workspace_size(int B, int H, int S, int D, int block_size, int topk);
+int moba_attn_bwd_ws(const void *q, const void *k, const void *v, const void *out,
+                     const float *lse, const void *dout, void *dq, void *dk, void *dv, int B,
+                     int H, int S, int D, int block_size, int topk, void *workspace,
+                     size_t workspace_bytes, void *stream);
+
+/* Varlen backward: every tensor [total_tokens][H][D] bf16, lse [H][total_tokens]
+ * fp32 as moba_attn_fwd_varlen wrote it; cu_seqlens DEVICE int32. */
+int moba_attn_bwd_varlen(const void *q, const void *k, const void *v, const void *out,
+                         const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                         const int32_t *cu_seqlens, int num_seqs, int total_tokens,
+                         int max_seqlen, int H, int D, int block_size, int topk, void *stream);
+size_t moba_attn_bwd_varlen_workspace_size(int num_seqs, int total_tokens, int max_seqlen, int H,
+                                           int D, int block_size, int topk);
+
+/*
  * moba_attn_fwd for callers that cannot allocate device memory: for example
  * code running under a memory manager that owns the whole device (where an
  * extra cudaMalloc can fail or fragment its pool), or a serving loop that must

@@ -68,7 +68,7 @@ static void prof_mark(int call, int phase, cudaStream_t st) {
 
 static inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-size_t workspace_bytes(const Plan &p, Workspace *ws, char *base) {
+size_t workspace_bytes(const Plan &p, Workspace *ws, char *base, bool backward) {
     size_t off = 0;
     auto take = [&](size_t bytes) -> void * {
         void *r = base ? static_cast<void *>(base + off) : nullptr;
@@ -97,8 +97,16 @@ size_t workspace_bytes(const Plan &p, Workspace *ws, char *base) {
         w.kblo = static_cast<__nv_bfloat16 *>(take(sizeof(__nv_bfloat16) * N * p.D));
         w.knorm = static_cast<float *>(take(sizeof(float) * N));
         w.list = static_cast<int *>(take(sizeof(int) * rows * p.km1));
-        w.part_o = static_cast<__nv_bfloat16 *>(take(sizeof(__nv_bfloat16) * rows * p.km1 * p.D));
-        w.part_lse = static_cast<float *>(take(sizeof(float) * rows * p.km1));
+        if (!backward) {
+            w.part_o =
+                static_cast<__nv_bfloat16 *>(take(sizeof(__nv_bfloat16) * rows * p.km1 * p.D));
+            w.part_lse = static_cast<float *>(take(sizeof(float) * rows * p.km1));
+        }
+    }
+    if (backward) {
+        const size_t rows = (size_t)p.total * p.H;
+        w.dq_acc = static_cast<float *>(take(sizeof(float) * rows * p.D));
+        w.delta = static_cast<float *>(take(sizeof(float) * rows));
     }
     if (ws) *ws = w;
     return off;
@@ -184,6 +192,42 @@ static int run_forward(const Plan &p, const int *cu_dev, const void *q, const vo
     prof_mark(call, 5, st);
     MOBA_TRY(launch_attn_current(p, ws, qb, kb, vb, static_cast<__nv_bfloat16 *>(out), lse, st));
     prof_mark(call, 6, st);
+    return MOBA_OK;
+}
+
+// Backward: the forward's selection recomputed (same kernels, so the same
+// selection), then the gradient kernels.
+static int run_backward(const Plan &p, const int *cu_dev, const void *q, const void *k,
+                        const void *v, const void *out, const float *lse, const void *dout,
+                        void *dq, void *dk, void *dv, void *workspace, size_t ws_bytes,
+                        cudaStream_t st) {
+    Workspace ws;
+    const size_t need = workspace_bytes(p, &ws, static_cast<char *>(workspace), true);
+    if (!workspace || ws_bytes < need) return MOBA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255) return MOBA_ERR_WORKSPACE;
+    const auto *qb = static_cast<const __nv_bfloat16 *>(q);
+    const auto *kb = static_cast<const __nv_bfloat16 *>(k);
+    MOBA_TRY(launch_setup(p, cu_dev, ws, st));
+    const bool gate = !p.dense && p.km1 > 0;
+    const bool tc_gate = g_gate_kind == 0 && gate_tc_supported(p);
+    if (gate) {
+        MOBA_TRY(launch_kpool(p, ws, kb, ws.kbar, st));
+        MOBA_TRY(cudaMemsetAsync(ws.counts, 0, sizeof(int) * ((size_t)p.NBcap * p.H + 1), st));
+        if (tc_gate) {
+            MOBA_TRY(launch_kbar_split(p, ws.kbar, ws.kbhi, ws.kblo, ws.knorm, st));
+            MOBA_TRY(launch_gate_tc(p, ws, qb, ws.kbar, ws.kbhi, ws.kblo, ws.knorm, ws.idx,
+                                    ws.counts, ws.need_list, ws.need_count, st));
+        } else {
+            MOBA_TRY(launch_gate(p, ws, qb, ws.kbar, ws.idx, st));
+        }
+        MOBA_TRY(launch_regroup(p, ws, tc_gate, st));
+    }
+    MOBA_TRY(cudaMemsetAsync(ws.dq_acc, 0, sizeof(float) * (size_t)p.total * p.H * p.D, st));
+    MOBA_TRY(launch_attn_bwd(p, ws, qb, kb, static_cast<const __nv_bfloat16 *>(v),
+                             static_cast<const __nv_bfloat16 *>(out), lse,
+                             static_cast<const __nv_bfloat16 *>(dout),
+                             static_cast<__nv_bfloat16 *>(dq), static_cast<__nv_bfloat16 *>(dk),
+                             static_cast<__nv_bfloat16 *>(dv), st));
     return MOBA_OK;
 }
 
@@ -409,6 +453,83 @@ MOBA_EXPORT int moba_attn_fwd_varlen(const void *q, const void *k, const void *v
     rc = run_forward(p, cu_seqlens, q, k, v, out, lse, ws, bytes, st);
     if (cudaFreeAsync(ws, st) != cudaSuccess && rc == MOBA_OK) rc = MOBA_ERR_CUDA;
     return rc;
+}
+
+static int check_bwd_tensors(const void *q, const void *k, const void *v, const void *out,
+                             const float *lse, const void *dout, const void *dq, const void *dk,
+                             const void *dv) {
+    int rc = check_tensors(q, k, v, out, lse);
+    if (rc) return rc;
+    if (!dout || !dq || !dk || !dv) return MOBA_ERR_INVALID_ARG;
+    if (misaligned(dout) || misaligned(dq) || misaligned(dk) || misaligned(dv))
+        return MOBA_ERR_INVALID_ARG;
+    return MOBA_OK;
+}
+
+MOBA_EXPORT size_t moba_attn_bwd_workspace_size(int B, int H, int S, int D, int block_size,
+                                                int topk) {
+    Plan p;
+    if (make_plan(B, (long long)B * S, S, H, D, block_size, topk, true, &p)) return 0;
+    return workspace_bytes(p, nullptr, nullptr, true);
+}
+
+MOBA_EXPORT size_t moba_attn_bwd_varlen_workspace_size(int num_seqs, int total_tokens,
+                                                       int max_seqlen, int H, int D,
+                                                       int block_size, int topk) {
+    Plan p;
+    if (make_plan(num_seqs, total_tokens, max_seqlen, H, D, block_size, topk, false, &p)) return 0;
+    return workspace_bytes(p, nullptr, nullptr, true);
+}
+
+MOBA_EXPORT int moba_attn_bwd_ws(const void *q, const void *k, const void *v, const void *out,
+                                 const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                                 int B, int H, int S, int D, int block_size, int topk,
+                                 void *workspace, size_t workspace_bytes_, void *stream) {
+    int rc = check_bwd_tensors(q, k, v, out, lse, dout, dq, dk, dv);
+    if (rc) return rc;
+    Plan p;
+    rc = make_plan(B, (long long)B * S, S, H, D, block_size, topk, true, &p);
+    if (rc) return rc;
+    return run_backward(p, nullptr, q, k, v, out, lse, dout, dq, dk, dv, workspace,
+                        workspace_bytes_, static_cast<cudaStream_t>(stream));
+}
+
+static int bwd_alloc_run(const Plan &p, const int *cu, const void *q, const void *k, const void *v,
+                         const void *out, const float *lse, const void *dout, void *dq, void *dk,
+                         void *dv, cudaStream_t st) {
+    const size_t bytes = workspace_bytes(p, nullptr, nullptr, true);
+    void *ws = nullptr;
+    if (cudaMallocAsync(&ws, bytes, st) != cudaSuccess) return MOBA_ERR_CUDA;
+    int rc = run_backward(p, cu, q, k, v, out, lse, dout, dq, dk, dv, ws, bytes, st);
+    if (cudaFreeAsync(ws, st) != cudaSuccess && rc == MOBA_OK) rc = MOBA_ERR_CUDA;
+    return rc;
+}
+
+MOBA_EXPORT int moba_attn_bwd(const void *q, const void *k, const void *v, const void *out,
+                              const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                              int B, int H, int S, int D, int block_size, int topk, void *stream) {
+    int rc = check_bwd_tensors(q, k, v, out, lse, dout, dq, dk, dv);
+    if (rc) return rc;
+    Plan p;
+    rc = make_plan(B, (long long)B * S, S, H, D, block_size, topk, true, &p);
+    if (rc) return rc;
+    return bwd_alloc_run(p, nullptr, q, k, v, out, lse, dout, dq, dk, dv,
+                         static_cast<cudaStream_t>(stream));
+}
+
+MOBA_EXPORT int moba_attn_bwd_varlen(const void *q, const void *k, const void *v, const void *out,
+                                     const float *lse, const void *dout, void *dq, void *dk,
+                                     void *dv, const int32_t *cu_seqlens, int num_seqs,
+                                     int total_tokens, int max_seqlen, int H, int D,
+                                     int block_size, int topk, void *stream) {
+    int rc = check_bwd_tensors(q, k, v, out, lse, dout, dq, dk, dv);
+    if (rc) return rc;
+    if (!cu_seqlens) return MOBA_ERR_INVALID_ARG;
+    Plan p;
+    rc = make_plan(num_seqs, total_tokens, max_seqlen, H, D, block_size, topk, false, &p);
+    if (rc) return rc;
+    return bwd_alloc_run(p, cu_seqlens, q, k, v, out, lse, dout, dq, dk, dv,
+                         static_cast<cudaStream_t>(stream));
 }
 
 static int g_last_timeout[4] = {0, 0, 0, 0};

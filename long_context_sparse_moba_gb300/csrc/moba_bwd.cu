@@ -1,0 +1,408 @@
+// moba_bwd.cu -- backward pass of MoBA attention: dq, dk, dv through the
+// selected blocks, with the gate's selection held fixed (top-k is piecewise
+// constant and passes no gradient; none reaches the pooled keys).
+//
+// Page: "MOBA mixture of block attention for server-side long context"
+// (hncyxsy.com/news/197418) section 3 trains MoBA layers end to end and
+// attributes a higher SFT loss to the sparse gradient path; the selection and
+// the attention being differentiated are those of the forward pass
+// ("Moonshot MoBA paper explained", gsyq.cn/news/227272, sections 3.1, 4.1).
+//
+// For row i with selected keys J_i (its own block up to i, and every key of
+// its selected past blocks), P_ij = exp(s_ij / sqrt(D) - lse_i),
+// delta_i = dO_i . O_i and dS_ij = P_ij (dO_i . v_j - delta_i):
+//   dq_i = sum_j dS_ij k_j / sqrt(D),  dk_j = sum_i dS_ij q_i / sqrt(D),
+//   dv_j = sum_i P_ij dO_i.
+//
+// Three kernels:
+//   bwd_delta_kernel  -- delta = rowwise dO . O (a warp per (token, head));
+//   bwd_kv_kernel     -- key-major: one work unit = 64 keys of one block of
+//                        one head.  It walks every query row that attends to
+//                        those keys -- the rows of the block itself from the
+//                        unit's first key on (causal mask on the diagonal;
+//                        on the dense path every later row of the sequence)
+//                        and the rows of later blocks that selected the block
+//                        (the regroup list of the forward pass) -- in tiles
+//                        of 64, and per tile forms S^T = K Q^T and
+//                        dP^T = V dO^T on the tensor cores (mma.sync bf16,
+//                        fp32 accumulate), P and dS in fp32, then
+//                        dV += P^T dO, dK += dS^T Q (registers, written once
+//                        per unit: every key belongs to exactly one unit) and
+//                        dQ += dS K added into an fp32 accumulator with
+//                        vector atomics;
+//   bwd_dq_kernel     -- dq = bf16(accumulator / sqrt(D)).
+// 8 warps: warp w owns keys 16 (w % 4) .. +15; for S^T and dP^T it takes
+// query rows 32 (w / 4) .. +31, for dV, dK and dQ the column half w / 4 of D.
+// P^T, dS^T and dS pass between the two phases through shared memory (bf16).
+#include "moba_internal.cuh"
+#include "moba_mma.cuh"
+
+namespace moba {
+
+namespace bwd {
+
+using namespace mma;
+
+constexpr int kM = 64;          // query rows per tile
+constexpr int kN = 64;          // keys per work unit
+constexpr int kThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct Args {
+    Geometry g;
+    const __nv_bfloat16 *q, *k, *v, *dout;
+    const float *lse;           // forward lse, natural log, forward layout
+    const float *delta;         // [total][H]
+    float *dq_acc;              // [total][H][D], zero on entry
+    __nv_bfloat16 *dq_out, *dk, *dv;  // [total][H][D]
+    int fixed, S_fixed, dense, km1;
+    const int *list, *list_off; // regroup lists (past selections)
+    int tiles_per_block;        // bs / kN
+    long long n_units;          // NBcap * H * tiles_per_block
+    float scale, scale_log2;
+};
+
+template <int D>
+constexpr int smem_bytes() {
+    return 2 * kN * D * 2 + 2 * kM * D * 2 + 3 * kN * kM * 2 + 3 * kM * 4;
+}
+
+// 64 rows x D of a token-gathered bf16 matrix into a swizzled tile; rows with
+// token < 0 are zero-filled (source size 0; the address stays valid).
+template <int D, typename TokOf>
+__device__ __forceinline__ void load_rows(uint32_t s_base, const __nv_bfloat16 *base,
+                                          size_t rstride, TokOf tok_of) {
+    constexpr int CH = D / 8;
+#pragma unroll
+    for (int j = 0; j < (64 * CH) / kThreads; ++j) {
+        const int id = threadIdx.x + j * kThreads;
+        const int r = id / CH, ch = id % CH;
+        const int tok = tok_of(r);
+        const __nv_bfloat16 *src = tok >= 0 ? base + (size_t)tok * rstride + ch * 8 : base;
+        cp_async16(s_base + swz<D>(r, ch), src, tok >= 0);
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16 *__restrict__ out,
+                                                        const __nv_bfloat16 *__restrict__ dout,
+                                                        float *__restrict__ delta,
+                                                        long long rows) {
+    const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (r >= rows) return;  // whole warps leave together
+    const int lane = threadIdx.x & 31;
+    constexpr int PER = D / 32;
+    const __nv_bfloat16 *o = out + r * D + lane * PER;
+    const __nv_bfloat16 *g = dout + r * D + lane * PER;
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < PER; i += 2) {
+        const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(o + i));
+        const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(g + i));
+        acc = fmaf(x.x, y.x, acc);
+        acc = fmaf(x.y, y.y, acc);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) delta[r] = acc;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 2) bwd_kv_kernel(Args a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int KS = D / 16;   // k-steps over the head dimension
+    constexpr int NH = D / 16;   // 8-column tiles in a warp's half of D
+    uint8_t *pK = smem;
+    uint8_t *pV = pK + kN * D * 2;
+    uint8_t *pQ = pV + kN * D * 2;
+    uint8_t *pO = pQ + kM * D * 2;
+    uint8_t *pP = pO + kM * D * 2;   // P^T  [key][row]
+    uint8_t *pS = pP + kN * kM * 2;  // dS^T [key][row]
+    uint8_t *pR = pS + kN * kM * 2;  // dS   [row][key]
+    int *r_tok = reinterpret_cast<int *>(pR + kM * kN * 2);
+    float *r_lse = reinterpret_cast<float *>(r_tok + kM);  // log2 domain
+    float *r_del = r_lse + kM;
+    const uint32_t sK = smem_u32(pK), sV = smem_u32(pV), sQ = smem_u32(pQ), sO = smem_u32(pO);
+    const uint32_t sP = smem_u32(pP), sS = smem_u32(pS), sR = smem_u32(pR);
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int wm = warp & 3, wn = warp >> 2;
+    const int g = lane >> 2, t = lane & 3;
+    const int H = a.g.H;
+    const size_t rstride = (size_t)H * D;
+    const int NB = __ldg(a.g.blk_base + a.g.num_seqs);
+
+    for (long long u = blockIdx.x; u < a.n_units; u += gridDim.x) {
+        const int kt = (int)(u % a.tiles_per_block);
+        const long long L = u / a.tiles_per_block;
+        const int gblk = (int)(L / H), h = (int)(L % H);
+        if (gblk >= NB) break;  // units run in block order: the rest are past the end too
+        const int b = upper_index(a.g.blk_base, a.g.num_seqs, gblk);
+        const int c = gblk - __ldg(a.g.blk_base + b);
+        const int seq0 = __ldg(a.g.cu + b), seq_end = __ldg(a.g.cu + b + 1);
+        const int kv0 = seq0 + c * a.g.bs;
+        const int kv_end = min(kv0 + a.g.bs, seq_end);
+        const int key0 = kv0 + kt * kN;
+        if (key0 >= kv_end) continue;
+        const int nkeys = min(kN, kv_end - key0);
+        const int own_end = a.dense ? seq_end : kv_end;
+        const int n_own = (own_end - key0 + kM - 1) / kM;
+        int lbeg = 0, lcnt = 0;
+        if (!a.dense && a.km1 > 0) {
+            lbeg = __ldg(a.list_off + L);
+            lcnt = __ldg(a.list_off + L + 1) - lbeg;
+        }
+        const int n_tiles = n_own + (lcnt + kM - 1) / kM;
+
+        load_rows<D>(sK, a.k + (size_t)h * D, rstride,
+                     [&](int r) { return r < nkeys ? key0 + r : -1; });
+        load_rows<D>(sV, a.v + (size_t)h * D, rstride,
+                     [&](int r) { return r < nkeys ? key0 + r : -1; });
+        cp_async_commit();
+
+        float dk[NH][4], dv[NH][4];
+#pragma unroll
+        for (int j = 0; j < NH; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dk[j][e] = dv[j][e] = 0.f;
+
+        for (int qt = 0; qt < n_tiles; ++qt) {
+            const bool own = qt < n_own;
+            if (threadIdx.x < kM) {
+                const int r = threadIdx.x;
+                int tok = -1;
+                if (own) {
+                    const int x = key0 + qt * kM + r;
+                    if (x < own_end) tok = x;
+                } else {
+                    const int pr = (qt - n_own) * kM + r;
+                    if (pr < lcnt) tok = __ldg(a.list + lbeg + pr) >> kSlotBits;
+                }
+                r_tok[r] = tok;
+                float l2 = 0.f, dl = 0.f;
+                if (tok >= 0) {
+                    const size_t li = a.fixed ? ((size_t)b * H + h) * a.S_fixed + (tok - seq0)
+                                              : (size_t)h * a.g.total + tok;
+                    l2 = __ldg(a.lse + li) * kLog2e;
+                    dl = __ldg(a.delta + (size_t)tok * H + h);
+                }
+                r_lse[r] = l2;
+                r_del[r] = dl;
+            }
+            __syncthreads();
+            load_rows<D>(sQ, a.q + (size_t)h * D, rstride, [&](int r) { return r_tok[r]; });
+            load_rows<D>(sO, a.dout + (size_t)h * D, rstride, [&](int r) { return r_tok[r]; });
+            cp_async_commit();
+            cp_async_wait<0>();
+            __syncthreads();
+
+            // S^T and dP^T: keys 16 wm .. +15 x rows 32 wn .. +31
+            float s[4][4], dp[4][4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s[j][e] = dp[j][e] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                uint32_t ka[4], va[4];
+                const uint32_t aoff = swz<D>(wm * 16 + (lane & 15), ks * 2 + (lane >> 4));
+                ldsm_x4(ka[0], ka[1], ka[2], ka[3], sK + aoff);
+                ldsm_x4(va[0], va[1], va[2], va[3], sV + aoff);
+#pragma unroll
+                for (int np = 0; np < 2; ++np) {
+                    const uint32_t boff = swz<D>(wn * 32 + np * 16 + (lane & 7) + ((lane >> 4) << 3),
+                                                 ks * 2 + ((lane >> 3) & 1));
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(b0, b1, b2, b3, sQ + boff);
+                    mma16816(s[2 * np], ka, b0, b1);
+                    mma16816(s[2 * np + 1], ka, b2, b3);
+                    ldsm_x4(b0, b1, b2, b3, sO + boff);
+                    mma16816(dp[2 * np], va, b0, b1);
+                    mma16816(dp[2 * np + 1], va, b2, b3);
+                }
+            }
+            // P, dS (fp32) -> bf16 tiles in shared memory
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int kl = wm * 16 + g + 8 * hh;
+                    const int rl = wn * 32 + 8 * j + 2 * t;
+                    float pv[2], dsv[2];
+#pragma unroll
+                    for (int e1 = 0; e1 < 2; ++e1) {
+                        const int e = hh * 2 + e1;
+                        const int r = rl + e1;
+                        const int tok = r_tok[r];
+                        const bool ok = tok >= 0 && kl < nkeys && (!own || key0 + kl <= tok);
+                        const float p = ok ? fast_exp2(s[j][e] * a.scale_log2 - r_lse[r]) : 0.f;
+                        pv[e1] = p;
+                        dsv[e1] = p * (dp[j][e] - r_del[r]);
+                    }
+                    const uint32_t o_kr = swz<64>(kl, rl >> 3) + (rl & 7) * 2;
+                    *reinterpret_cast<uint32_t *>(pP + o_kr) = pack_bf16(pv[0], pv[1]);
+                    *reinterpret_cast<uint32_t *>(pS + o_kr) = pack_bf16(dsv[0], dsv[1]);
+                    *reinterpret_cast<__nv_bfloat16 *>(pR + swz<64>(rl, kl >> 3) + (kl & 7) * 2) =
+                        __float2bfloat16_rn(dsv[0]);
+                    *reinterpret_cast<__nv_bfloat16 *>(pR + swz<64>(rl + 1, kl >> 3) + (kl & 7) * 2) =
+                        __float2bfloat16_rn(dsv[1]);
+                }
+            }
+            __syncthreads();
+
+            // dV += P^T dO, dK += dS^T Q: keys 16 wm .. +15 x column half wn
+#pragma unroll
+            for (int ks = 0; ks < kM / 16; ++ks) {
+                uint32_t pa[4], sa[4];
+                const uint32_t aoff = swz<64>(wm * 16 + (lane & 15), ks * 2 + (lane >> 4));
+                ldsm_x4(pa[0], pa[1], pa[2], pa[3], sP + aoff);
+                ldsm_x4(sa[0], sa[1], sa[2], sa[3], sS + aoff);
+#pragma unroll
+                for (int d2 = 0; d2 < NH / 2; ++d2) {
+                    const uint32_t boff = swz<D>(ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3),
+                                                 wn * (D / 16) + d2 * 2 + (lane >> 4));
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(b0, b1, b2, b3, sO + boff);
+                    mma16816(dv[2 * d2], pa, b0, b1);
+                    mma16816(dv[2 * d2 + 1], pa, b2, b3);
+                    ldsm_x4_t(b0, b1, b2, b3, sQ + boff);
+                    mma16816(dk[2 * d2], sa, b0, b1);
+                    mma16816(dk[2 * d2 + 1], sa, b2, b3);
+                }
+            }
+
+            // dQ (unscaled) += dS K: rows 16 wm .. +15 x column half wn
+            float dq[NH][4];
+#pragma unroll
+            for (int j = 0; j < NH; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) dq[j][e] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < kN / 16; ++ks) {
+                uint32_t ra[4];
+                ldsm_x4(ra[0], ra[1], ra[2], ra[3],
+                        sR + swz<64>(wm * 16 + (lane & 15), ks * 2 + (lane >> 4)));
+#pragma unroll
+                for (int d2 = 0; d2 < NH / 2; ++d2) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(b0, b1, b2, b3,
+                              sK + swz<D>(ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3),
+                                          wn * (D / 16) + d2 * 2 + (lane >> 4)));
+                    mma16816(dq[2 * d2], ra, b0, b1);
+                    mma16816(dq[2 * d2 + 1], ra, b2, b3);
+                }
+            }
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int tok = r_tok[wm * 16 + g + 8 * hh];
+                if (tok < 0) continue;
+                float *dst = a.dq_acc + ((size_t)tok * H + h) * D + wn * (D / 2) + 2 * t;
+#pragma unroll
+                for (int nt = 0; nt < NH; ++nt)
+                    atomicAdd(reinterpret_cast<float2 *>(dst + nt * 8),
+                              make_float2(dq[nt][2 * hh], dq[nt][2 * hh + 1]));
+            }
+            __syncthreads();
+        }
+
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int kl = wm * 16 + g + 8 * hh;
+            if (kl >= nkeys) continue;
+            const size_t o = ((size_t)(key0 + kl) * H + h) * D + wn * (D / 2) + 2 * t;
+#pragma unroll
+            for (int nt = 0; nt < NH; ++nt) {
+                *reinterpret_cast<__nv_bfloat162 *>(a.dk + o + nt * 8) =
+                    __floats2bfloat162_rn(dk[nt][2 * hh] * a.scale, dk[nt][2 * hh + 1] * a.scale);
+                *reinterpret_cast<__nv_bfloat162 *>(a.dv + o + nt * 8) =
+                    __floats2bfloat162_rn(dv[nt][2 * hh], dv[nt][2 * hh + 1]);
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256) bwd_dq_kernel(const float4 *__restrict__ acc,
+                                                     uint2 *__restrict__ dq, long long n4,
+                                                     float scale) {
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+         i += (long long)gridDim.x * blockDim.x) {
+        const float4 x = acc[i];
+        __nv_bfloat162 lo = __floats2bfloat162_rn(x.x * scale, x.y * scale);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(x.z * scale, x.w * scale);
+        uint2 w;
+        w.x = *reinterpret_cast<uint32_t *>(&lo);
+        w.y = *reinterpret_cast<uint32_t *>(&hi);
+        dq[i] = w;
+    }
+}
+
+}  // namespace bwd
+
+static int sm_count_bwd() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
+}
+
+template <int D>
+static cudaError_t launch_bwd_d(const Plan &p, const Workspace &ws, const bwd::Args &a,
+                                const __nv_bfloat16 *out, cudaStream_t st) {
+    using namespace bwd;
+    const long long rows = (long long)p.total * p.H;
+    bwd_delta_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(out, a.dout, ws.delta, rows);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    constexpr int smem = smem_bytes<D>();
+    cudaFuncSetAttribute(bwd_kv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const long long grid = a.n_units < (1ll << 30) ? a.n_units : (1ll << 30);
+    bwd_kv_kernel<D><<<(unsigned)grid, kThreads, smem, st>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const long long n4 = rows * D / 4;
+    const long long blocks = (n4 + 255) / 256;
+    const int cap = sm_count_bwd() * 8;
+    bwd_dq_kernel<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, st>>>(
+        reinterpret_cast<const float4 *>(ws.dq_acc), reinterpret_cast<uint2 *>(a.dq_out), n4,
+        a.scale);
+    note_launches(3);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_attn_bwd(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
+                            const __nv_bfloat16 *k, const __nv_bfloat16 *v,
+                            const __nv_bfloat16 *out, const float *lse,
+                            const __nv_bfloat16 *dout, __nv_bfloat16 *dq, __nv_bfloat16 *dk,
+                            __nv_bfloat16 *dv, cudaStream_t st) {
+    bwd::Args a;
+    a.g.cu = ws.cu;
+    a.g.blk_base = ws.blk_base;
+    a.g.num_seqs = p.num_seqs;
+    a.g.total = p.total;
+    a.g.H = p.H;
+    a.g.D = p.D;
+    a.g.bs = p.bs;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.dout = dout;
+    a.lse = lse;
+    a.delta = ws.delta;
+    a.dq_acc = ws.dq_acc;
+    a.dq_out = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.fixed = p.fixed ? 1 : 0;
+    a.S_fixed = p.max_len;
+    a.dense = p.dense ? 1 : 0;
+    a.km1 = p.km1;
+    a.list = ws.list;
+    a.list_off = ws.list_off;
+    a.tiles_per_block = p.bs / bwd::kN;
+    a.n_units = (long long)p.NBcap * p.H * a.tiles_per_block;
+    a.scale = (float)(1.0 / __builtin_sqrt((double)p.D));
+    a.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)p.D));
+    return p.D == 64 ? launch_bwd_d<64>(p, ws, a, out, st) : launch_bwd_d<128>(p, ws, a, out, st);
+}
+
+}  // namespace moba

@@ -61,6 +61,9 @@ struct Workspace {
     int *list;        // [total * H * km1]  entries token << 5 | slot
     __nv_bfloat16 *part_o;  // [total * H * km1][D]  normalised partial outputs (bf16)
     float *part_lse;  // [total * H * km1]     partial log2-sum-exp
+    // backward pass only (part_o / part_lse are not carved then)
+    float *dq_acc;    // [total][H][D]  fp32 dq accumulator
+    float *delta;     // [total][H]     dO . O per row
 };
 
 struct Plan {
@@ -71,7 +74,9 @@ struct Plan {
     bool fixed;       // [B][S] layout (lse [B][H][S]) rather than varlen
 };
 
-size_t workspace_bytes(const Plan &p, Workspace *ws, char *base);
+// backward = true: the backward pass's scratch (no partial outputs; the dq
+// accumulator and the per-row dO . O instead)
+size_t workspace_bytes(const Plan &p, Workspace *ws, char *base, bool backward = false);
 
 // ---- launchers (each returns cudaGetLastError() of its launch) ----
 cudaError_t launch_setup(const Plan &p, const int *cu_dev, Workspace &ws, cudaStream_t st);
@@ -139,5 +144,12 @@ cudaError_t launch_decode(const void *q, const void *k, const void *v, const flo
                           const int32_t *lens, void *out, float *lse, int32_t *idx, int B, int H,
                           int S_max, int D, int bs, int topk, void *scratch, cudaStream_t st);
 void tc_debug_set(int flags, long long wait_limit);
+// backward: delta, then dk / dv (and the dq accumulator, which must be zero on
+// entry) over the regroup lists, then dq
+cudaError_t launch_attn_bwd(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
+                            const __nv_bfloat16 *k, const __nv_bfloat16 *v,
+                            const __nv_bfloat16 *out, const float *lse,
+                            const __nv_bfloat16 *dout, __nv_bfloat16 *dq, __nv_bfloat16 *dk,
+                            __nv_bfloat16 *dv, cudaStream_t st);
 
 }  // namespace moba

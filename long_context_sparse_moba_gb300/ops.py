@@ -55,6 +55,13 @@ _SIGNATURES = {
     "moba_attn_fwd_noalloc_capacity": (_SZ, []),
     "moba_debug_set": (_I, [_I, ctypes.c_longlong]),
     "moba_debug_timeout_info": (None, [_P]),
+    "moba_attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "moba_attn_bwd_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "moba_attn_bwd_ws": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P,
+                              _SZ, _P]),
+    "moba_attn_bwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                                  _I, _I, _P]),
+    "moba_attn_bwd_varlen_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
 }
 
 PHASES = ("tables", "kpool", "gate", "regroup", "attn_past", "attn_current")
@@ -254,6 +261,57 @@ def attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, block_size: int, topk:
                                            st)
     _check(rc, "moba_attn_fwd_varlen")
     return out, lse
+
+
+def bwd_workspace_size(B, H, S, D, block_size, topk) -> int:
+    return int(lib().moba_attn_bwd_workspace_size(B, H, S, D, block_size, topk))
+
+
+def attn_bwd(q, k, v, out, lse, dout, block_size: int, topk: int, dq=None, dk=None, dv=None,
+             workspace=None, stream=None):
+    """MoBA backward for the forward ``attn_fwd(q, k, v, block_size, topk)``:
+    q, k, v, out, dout [B, S, H, D] bf16 and lse [B, H, S] fp32 (as the forward
+    returned them) -> (dq, dk, dv) [B, S, H, D] bf16.  The gate's selection is
+    recomputed and held fixed."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
+        _need(t, torch.bfloat16, n)
+    _need(lse, torch.float32, "lse")
+    B, S, H, D = q.shape
+    for t, n in ((k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
+        if t.shape != q.shape:
+            raise ValueError(f"{n} must have the shape of q")
+    if tuple(lse.shape) != (B, H, S):
+        raise ValueError("lse must be [B, H, S]")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    st = _stream(stream)
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+            _ptr(dv), B, H, S, D, block_size, topk)
+    if workspace is None:
+        rc = lib().moba_attn_bwd(*args, st)
+    else:
+        rc = lib().moba_attn_bwd_ws(*args, _ptr(workspace), workspace.numel(), st)
+    _check(rc, "moba_attn_bwd")
+    return dq, dk, dv
+
+
+def attn_bwd_varlen(q, k, v, out, lse, dout, cu_seqlens, max_seqlen: int, block_size: int,
+                    topk: int, stream=None):
+    """Varlen backward: q, k, v, out, dout [total, H, D] bf16, lse [H, total]
+    fp32, cu_seqlens int32 CUDA [num_seqs + 1] -> (dq, dk, dv) [total, H, D]."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
+        _need(t, torch.bfloat16, n)
+    _need(lse, torch.float32, "lse")
+    _need(cu_seqlens, torch.int32, "cu_seqlens")
+    total, H, D = q.shape
+    ns = cu_seqlens.numel() - 1
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    rc = lib().moba_attn_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                                    _ptr(dq), _ptr(dk), _ptr(dv), _ptr(cu_seqlens), ns, total,
+                                    max_seqlen, H, D, block_size, topk, _stream(stream))
+    _check(rc, "moba_attn_bwd_varlen")
+    return dq, dk, dv
 
 
 def get_status(stream=None) -> int:

@@ -127,3 +127,30 @@ def test_workspace_grows_with_topk_and_dense_needs_little(lib):
     assert wider > sparse > dense > 0
     # the partial outputs dominate: tokens * heads * (topk - 1) * D bf16 values
     assert sparse >= 32768 * 32 * 2 * 128 * 2
+
+
+def test_backward_validates_on_the_host(lib):
+    F = FAKE
+    args = (1, 2, 4096, 128, 512, 3)
+    # null and misaligned tensors
+    assert lib.moba_attn_bwd(F, F, F, F, F, None, F, F, F, *args, None) == ops.MOBA_ERR_INVALID_ARG
+    assert lib.moba_attn_bwd(F, F, F, F, F, F, F, None, F, *args, None) == ops.MOBA_ERR_INVALID_ARG
+    odd = ctypes.c_void_p(0x10002)
+    assert lib.moba_attn_bwd(F, F, F, F, F, F, odd, F, F, *args, None) == ops.MOBA_ERR_INVALID_ARG
+    # the forward's size rules
+    assert lib.moba_attn_bwd(F, F, F, F, F, F, F, F, F, 1, 2, 4096, 96, 512, 3,
+                             None) == ops.MOBA_ERR_UNSUPPORTED
+    assert lib.moba_attn_bwd(F, F, F, F, F, F, F, F, F, 1, 2, 4096, 128, 500, 3,
+                             None) == ops.MOBA_ERR_INVALID_ARG
+    assert lib.moba_attn_bwd_varlen(F, F, F, F, F, F, F, F, F, None, 1, 64, 64, 1, 64, 64, 1,
+                                    None) == ops.MOBA_ERR_INVALID_ARG
+    # caller scratch: too small is refused before any launch
+    need = lib.moba_attn_bwd_workspace_size(*args)
+    assert need > 0
+    assert lib.moba_attn_bwd_ws(F, F, F, F, F, F, F, F, F, *args, ctypes.c_void_p(0x100000),
+                                need - 1, None) == ops.MOBA_ERR_WORKSPACE
+    # no partial outputs, but the fp32 dq accumulator and dO . O per row
+    rows = 4096 * 2
+    assert need >= rows * 128 * 4 + rows * 4
+    # (varlen bounds the block count by total / bs + sequences: at least as much)
+    assert lib.moba_attn_bwd_varlen_workspace_size(1, 4096, 4096, 2, 128, 512, 3) >= need
