@@ -29,7 +29,8 @@
 //                        dV += P^T dO, dK += dS^T Q (registers, written once
 //                        per unit: every key belongs to exactly one unit) and
 //                        dQ += dS K added into an fp32 accumulator with
-//                        vector atomics;
+//                        16-byte vector atomics; the next tile's rows load
+//                        while the dQ products run;
 //   bwd_dq_kernel     -- dq = bf16(accumulator / sqrt(D)).
 // 8 warps: warp w owns keys 16 (w % 4) .. +15; for S^T and dP^T it takes
 // query rows 32 (w / 4) .. +31, for dV, dK and dQ the column half w / 4 of D.
@@ -64,7 +65,7 @@ struct Args {
 
 template <int D>
 constexpr int smem_bytes() {
-    return 2 * kN * D * 2 + 2 * kM * D * 2 + 3 * kN * kM * 2 + 3 * kM * 4;
+    return 2 * kN * D * 2 + 2 * kM * D * 2 + 3 * kN * kM * 2 + 2 * 3 * kM * 4;
 }
 
 // 64 rows x D of a token-gathered bf16 matrix into a swizzled tile; rows with
@@ -119,9 +120,10 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_kv_kernel(Args a) {
     uint8_t *pP = pO + kM * D * 2;   // P^T  [key][row]
     uint8_t *pS = pP + kN * kM * 2;  // dS^T [key][row]
     uint8_t *pR = pS + kN * kM * 2;  // dS   [row][key]
+    // per-row metadata of two query tiles (the current and the next)
     int *r_tok = reinterpret_cast<int *>(pR + kM * kN * 2);
-    float *r_lse = reinterpret_cast<float *>(r_tok + kM);  // log2 domain
-    float *r_del = r_lse + kM;
+    float *r_lse = reinterpret_cast<float *>(r_tok + 2 * kM);  // log2 domain
+    float *r_del = r_lse + 2 * kM;
     const uint32_t sK = smem_u32(pK), sV = smem_u32(pV), sQ = smem_u32(pQ), sO = smem_u32(pO);
     const uint32_t sP = smem_u32(pP), sS = smem_u32(pS), sR = smem_u32(pR);
 
@@ -154,31 +156,20 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_kv_kernel(Args a) {
         }
         const int n_tiles = n_own + (lcnt + kM - 1) / kM;
 
-        load_rows<D>(sK, a.k + (size_t)h * D, rstride,
-                     [&](int r) { return r < nkeys ? key0 + r : -1; });
-        load_rows<D>(sV, a.v + (size_t)h * D, rstride,
-                     [&](int r) { return r < nkeys ? key0 + r : -1; });
-        cp_async_commit();
-
-        float dk[NH][4], dv[NH][4];
-#pragma unroll
-        for (int j = 0; j < NH; ++j)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) dk[j][e] = dv[j][e] = 0.f;
-
-        for (int qt = 0; qt < n_tiles; ++qt) {
-            const bool own = qt < n_own;
+        // token of row r of query tile qt (-1: no row)
+        auto tok_of = [&](int qt, int r) -> int {
+            if (qt < n_own) {
+                const int x = key0 + qt * kM + r;
+                return x < own_end ? x : -1;
+            }
+            const int pr = (qt - n_own) * kM + r;
+            return pr < lcnt ? (__ldg(a.list + lbeg + pr) >> kSlotBits) : -1;
+        };
+        // row token, lse (log2) and delta of tile qt into metadata buffer mb
+        auto fill_meta = [&](int qt, int mb) {
             if (threadIdx.x < kM) {
                 const int r = threadIdx.x;
-                int tok = -1;
-                if (own) {
-                    const int x = key0 + qt * kM + r;
-                    if (x < own_end) tok = x;
-                } else {
-                    const int pr = (qt - n_own) * kM + r;
-                    if (pr < lcnt) tok = __ldg(a.list + lbeg + pr) >> kSlotBits;
-                }
-                r_tok[r] = tok;
+                const int tok = tok_of(qt, r);
                 float l2 = 0.f, dl = 0.f;
                 if (tok >= 0) {
                     const size_t li = a.fixed ? ((size_t)b * H + h) * a.S_fixed + (tok - seq0)
@@ -186,13 +177,34 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_kv_kernel(Args a) {
                     l2 = __ldg(a.lse + li) * kLog2e;
                     dl = __ldg(a.delta + (size_t)tok * H + h);
                 }
-                r_lse[r] = l2;
-                r_del[r] = dl;
+                r_tok[mb * kM + r] = tok;
+                r_lse[mb * kM + r] = l2;
+                r_del[mb * kM + r] = dl;
             }
-            __syncthreads();
-            load_rows<D>(sQ, a.q + (size_t)h * D, rstride, [&](int r) { return r_tok[r]; });
-            load_rows<D>(sO, a.dout + (size_t)h * D, rstride, [&](int r) { return r_tok[r]; });
-            cp_async_commit();
+        };
+
+        load_rows<D>(sK, a.k + (size_t)h * D, rstride,
+                     [&](int r) { return r < nkeys ? key0 + r : -1; });
+        load_rows<D>(sV, a.v + (size_t)h * D, rstride,
+                     [&](int r) { return r < nkeys ? key0 + r : -1; });
+        load_rows<D>(sQ, a.q + (size_t)h * D, rstride, [&](int r) { return tok_of(0, r); });
+        load_rows<D>(sO, a.dout + (size_t)h * D, rstride, [&](int r) { return tok_of(0, r); });
+        cp_async_commit();
+        fill_meta(0, 0);
+
+        float dk[NH][4], dv[NH][4];
+#pragma unroll
+        for (int j = 0; j < NH; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dk[j][e] = dv[j][e] = 0.f;
+
+        // Per tile: [wait for Q, dO] S^T, dP^T -> P, dS [sync] dV, dK [sync]
+        // start loading the next tile's Q, dO, then dQ and its atomics.
+        for (int qt = 0; qt < n_tiles; ++qt) {
+            const bool own = qt < n_own;
+            const int *m_tok = r_tok + (qt & 1) * kM;
+            const float *m_lse = r_lse + (qt & 1) * kM;
+            const float *m_del = r_del + (qt & 1) * kM;
             cp_async_wait<0>();
             __syncthreads();
 
@@ -233,11 +245,11 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_kv_kernel(Args a) {
                     for (int e1 = 0; e1 < 2; ++e1) {
                         const int e = hh * 2 + e1;
                         const int r = rl + e1;
-                        const int tok = r_tok[r];
+                        const int tok = m_tok[r];
                         const bool ok = tok >= 0 && kl < nkeys && (!own || key0 + kl <= tok);
-                        const float p = ok ? fast_exp2(s[j][e] * a.scale_log2 - r_lse[r]) : 0.f;
+                        const float p = ok ? fast_exp2(s[j][e] * a.scale_log2 - m_lse[r]) : 0.f;
                         pv[e1] = p;
-                        dsv[e1] = p * (dp[j][e] - r_del[r]);
+                        dsv[e1] = p * (dp[j][e] - m_del[r]);
                     }
                     const uint32_t o_kr = swz<64>(kl, rl >> 3) + (rl & 7) * 2;
                     *reinterpret_cast<uint32_t *>(pP + o_kr) = pack_bf16(pv[0], pv[1]);
@@ -270,6 +282,16 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_kv_kernel(Args a) {
                     mma16816(dk[2 * d2 + 1], sa, b2, b3);
                 }
             }
+            __syncthreads();  // Q and dO of this tile are no longer read
+
+            if (qt + 1 < n_tiles) {
+                load_rows<D>(sQ, a.q + (size_t)h * D, rstride,
+                             [&](int r) { return tok_of(qt + 1, r); });
+                load_rows<D>(sO, a.dout + (size_t)h * D, rstride,
+                             [&](int r) { return tok_of(qt + 1, r); });
+                cp_async_commit();
+                fill_meta(qt + 1, (qt + 1) & 1);
+            }
 
             // dQ (unscaled) += dS K: rows 16 wm .. +15 x column half wn
             float dq[NH][4];
@@ -292,18 +314,25 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_kv_kernel(Args a) {
                     mma16816(dq[2 * d2 + 1], ra, b2, b3);
                 }
             }
+            // lane pairs (t, t ^ 1) swap halves: the even lane adds columns
+            // 2t .. 2t+3 of row g, the odd lane columns 2t-2 .. 2t+1 of row g+8
+            const bool odd = t & 1;
+            const int row_l = wm * 16 + g + (odd ? 8 : 0);
+            const int tok = m_tok[row_l];
+            float *dst = a.dq_acc + ((size_t)(tok < 0 ? 0 : tok) * H + h) * D + wn * (D / 2) +
+                         2 * (t & ~1);
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int tok = r_tok[wm * 16 + g + 8 * hh];
-                if (tok < 0) continue;
-                float *dst = a.dq_acc + ((size_t)tok * H + h) * D + wn * (D / 2) + 2 * t;
-#pragma unroll
-                for (int nt = 0; nt < NH; ++nt)
-                    atomicAdd(reinterpret_cast<float2 *>(dst + nt * 8),
-                              make_float2(dq[nt][2 * hh], dq[nt][2 * hh + 1]));
+            for (int nt = 0; nt < NH; ++nt) {
+                const float x = odd ? dq[nt][0] : dq[nt][2];
+                const float y = odd ? dq[nt][1] : dq[nt][3];
+                const float rx = __shfl_xor_sync(0xffffffffu, x, 1);
+                const float ry = __shfl_xor_sync(0xffffffffu, y, 1);
+                const float4 v4 = odd ? make_float4(rx, ry, dq[nt][2], dq[nt][3])
+                                      : make_float4(dq[nt][0], dq[nt][1], rx, ry);
+                if (tok >= 0) atomicAdd(reinterpret_cast<float4 *>(dst + nt * 8), v4);
             }
-            __syncthreads();
         }
+        __syncthreads();  // K and dS are no longer read: the next unit may load
 
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {

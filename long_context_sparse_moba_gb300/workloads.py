@@ -72,6 +72,10 @@ WORKLOADS = {
     "train32k": Workload("train32k", (32768,), H=32, D=128, block_size=512, topks=(3, 64),
                          seed=1, qkv_scale=1.0 / math.sqrt(128.0), offset_std=0.5,
                          notes="B1 H32 S32768 D128 bs512 (64 blocks) top-k 3; top-k 64 = dense"),
+    "train8k": Workload("train8k", (8192,), H=32, D=128, block_size=512, topks=(3,),
+                        seed=6, qkv_scale=1.0 / math.sqrt(128.0), offset_std=0.5,
+                        notes="the 32K training shape cut to 8192 tokens (16 blocks), for "
+                              "kernel profiles that must stay small"),
     "long128k": Workload("long128k", (131072,), H=32, D=128, block_size=2048, topks=(3,),
                          seed=2, offset_std=0.5, needle_block_frac=0.05,
                          needle_query_frac=0.01,
