@@ -52,6 +52,19 @@ cudaError_t launch_attn_current(const Plan &p, const Workspace &ws, const __nv_b
 }
 void note_launches(int n) { g_launches.fetch_add((unsigned long long)n); }
 
+int sm_count() {
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 1;
+        cached[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
 // Optional phase timing: CUDA events recorded on the caller's stream between
 // the phases of each forward call (setup, kpool, gate, regroup, attention
 // over past blocks, attention over the own block + merge).

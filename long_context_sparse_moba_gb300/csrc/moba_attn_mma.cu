@@ -340,12 +340,6 @@ __global__ __launch_bounds__(kThreads, 2) void current_kernel(Args a) {
 
 int mma_tile_rows() { return mma_path::kM; }
 
-static int sm_count() {
-    int dev = 0, n = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    return n > 0 ? n : 1;
-}
 
 static mma_path::Args make_args(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
                                 const __nv_bfloat16 *k, const __nv_bfloat16 *v,

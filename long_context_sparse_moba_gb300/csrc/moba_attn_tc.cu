@@ -854,18 +854,6 @@ bool make_tma_3d(CUtensorMap *m, const void *ptr, int total, int H, int D, int r
 
 static long long g_wait_limit = 4000000000ll;  // ~2 s at 2 GHz
 
-static int sm_count_tc() {
-    static int cached[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) dev = 0;
-    if (!cached[dev]) {
-        int n = 0;
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        cached[dev] = n > 0 ? n : 1;
-    }
-    return cached[dev];
-}
 static int g_debug_flags = 0;
 
 void tc_debug_set(int flags, long long wait_limit) {
@@ -935,7 +923,7 @@ static cudaError_t launch_tc(const Plan &p, const tc::Args &a, const __nv_bfloat
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // persistent: one CTA per SM (fewer when there are fewer own-block jobs)
-    int ctas = sm_count_tc();
+    int ctas = sm_count();
     if (MODE == tc::kCurrent && a.n_jobs < ctas) ctas = a.n_jobs;
     const dim3 grid(ctas > 0 ? ctas : 1);
     kern<<<grid, tc::kThreads, smem, st>>>(mq, mk, mv, a);

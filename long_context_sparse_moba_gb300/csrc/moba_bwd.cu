@@ -367,12 +367,6 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float4 *__restrict__ 
 
 }  // namespace bwd
 
-static int sm_count_bwd() {
-    int dev = 0, n = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    return n > 0 ? n : 1;
-}
 
 template <int D>
 static cudaError_t launch_bwd_d(const Plan &p, const Workspace &ws, const bwd::Args &a,
@@ -390,7 +384,7 @@ static cudaError_t launch_bwd_d(const Plan &p, const Workspace &ws, const bwd::A
     if (e != cudaSuccess) return e;
     const long long n4 = rows * D / 4;
     const long long blocks = (n4 + 255) / 256;
-    const int cap = sm_count_bwd() * 8;
+    const int cap = sm_count() * 8;
     bwd_dq_kernel<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, st>>>(
         reinterpret_cast<const float4 *>(ws.dq_acc), reinterpret_cast<uint2 *>(a.dq_out), n4,
         a.scale);

@@ -642,18 +642,6 @@ bool gate_tc_supported(const Plan &p) {
            units < (1ll << 31);
 }
 
-static int sm_count_gate() {
-    static int cached[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) dev = 0;
-    if (!cached[dev]) {
-        int n = 0;
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        cached[dev] = n > 0 ? n : 1;
-    }
-    return cached[dev];
-}
 
 template <int D>
 static cudaError_t launch_gate_tc_d(const Plan &p, const gate_tc::Args &a, const __nv_bfloat16 *q,
@@ -666,7 +654,7 @@ static cudaError_t launch_gate_tc_d(const Plan &p, const gate_tc::Args &a, const
     // an upper bound of the units; CTAs beyond the real count return at once
     const long long units_max =
         (long long)p.H * (((long long)p.total + gate_tc::kRows - 1) / gate_tc::kRows + p.num_seqs);
-    const int grid = (int)std::min<long long>(sm_count_gate(), units_max);
+    const int grid = (int)std::min<long long>(sm_count(), units_max);
     const int km1 = p.topk - 1;
     using L = gate_tc::Smem<D>;
     const int smem = (int)(L::tiles(a.nq, a.kb_rows) + 1008 + L::kMisc);
@@ -679,7 +667,7 @@ static cudaError_t launch_gate_tc_d(const Plan &p, const gate_tc::Args &a, const
         if (e != cudaSuccess) return e;                                                         \
         kern<<<grid, gate_tc::threads_for(nwg), smem, st>>>(mq, mh, ml, a);                    \
         if ((e = cudaGetLastError()) != cudaSuccess) return e;                                  \
-        gate_tc::gate_exact_kernel<D, KC><<<4 * sm_count_gate(), 32 * gate_tc::kExactWarps, 0,   \
+        gate_tc::gate_exact_kernel<D, KC><<<4 * sm_count(), 32 * gate_tc::kExactWarps, 0,   \
                                              st>>>(a.g, a.q, a.kbar, a.idx, a.topk, a.counts,  \
                                                    a.need_list, a.need_count);                 \
         return cudaGetLastError();                                                              \

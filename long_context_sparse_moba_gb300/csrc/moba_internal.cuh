@@ -102,6 +102,9 @@ int pooling_kind();
 // count of kernels this library has launched (for the benchmark's launch tally)
 void note_launches(int n);
 
+// streaming multiprocessors of the current device (cached per device)
+int sm_count();
+
 // rows per tile of the past-block attention kernel in use (regroup tiling)
 int past_tile_rows();
 
