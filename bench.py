@@ -71,7 +71,7 @@ TRAFFIC_SOURCES = ("long_context_sparse_moba_gb300/csrc/moba_attn_tc.cu",
 MEASURED_TRAFFIC = {
     # (workload, topk, phase): (bytes per launch, sources_sha256() of the code measured)
     ("train32k", 3, "attn_past"): (1031735808 + 538555904,
-                                   "1626be6acd205fe85b08cdd692056e099e23ccea68a7c42eddb115c8b59386fe"),
+                                   "b3849337b3be598e6afa581d8c98fb9c0bea5bf54ecee09c4948743f726e599e"),
 }
 
 
