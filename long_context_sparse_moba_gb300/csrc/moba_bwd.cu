@@ -32,9 +32,10 @@
 //                        16-byte vector atomics; the next tile's rows load
 //                        while the dQ products run;
 //   bwd_dq_kernel     -- dq = bf16(accumulator / sqrt(D)).
-// 8 warps: warp w owns keys 16 (w % 4) .. +15; for S^T and dP^T it takes
-// query rows 32 (w / 4) .. +31, for dV, dK and dQ the column half w / 4 of D.
-// P^T, dS^T and dS pass between the two phases through shared memory (bf16).
+// 8 warps: for S^T and dP^T warp w takes keys 16 (w % 4) .. +15 x query rows
+// 32 (w / 4) .. +31; for dV and dK keys 16 (w % 4) .. +15 x the column half
+// w / 4 of D; for dQ query rows 16 (w % 4) .. +15 x the same column half.
+// P^T, dS^T and dS pass between the phases through shared memory (bf16).
 #include "moba_internal.cuh"
 #include "moba_mma.cuh"
 
