@@ -111,6 +111,24 @@ def _need(t, dtype, name):
         raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
 
 
+def _out(t, shape, dtype, like, name):
+    """A result buffer: a new tensor on like's device, or the caller's one
+    after checking its dtype, layout, shape and device."""
+    shape = tuple(int(x) for x in shape)
+    if t is None:
+        return torch.empty(shape, dtype=dtype, device=like.device)
+    _need(t, dtype, name)
+    if tuple(t.shape) != shape or t.device != like.device:
+        raise ValueError(f"{name} must have shape {shape} on {like.device}")
+    return t
+
+
+def _ws(workspace):
+    if workspace is not None:
+        _need(workspace, torch.uint8, "workspace")
+    return workspace
+
+
 def num_blocks(length: int, block_size: int) -> int:
     return int(lib().moba_num_blocks(int(length), int(block_size)))
 
@@ -146,6 +164,8 @@ def gate_topk(q, kbar, block_size: int, topk: int, stream=None):
     _need(q, torch.bfloat16, "q")
     _need(kbar, torch.float32, "kbar")
     B, S, H, D = q.shape
+    if block_size > 0 and tuple(kbar.shape) != (B * num_blocks(S, block_size), H, D):
+        raise ValueError("kbar must be [B * ceil(S / block_size), H, D] (as kpool returns it)")
     idx = torch.empty(B, S, H, topk, dtype=torch.int32, device=q.device)
     _check(lib().moba_gate_topk(_ptr(q), _ptr(kbar), _ptr(idx), B, H, S, D, block_size, topk,
                                 _stream(stream)), "moba_gate_topk")
@@ -185,10 +205,9 @@ def attn_fwd(q, k, v, block_size: int, topk: int, out=None, lse=None, workspace=
     B, S, H, D = q.shape
     if k.shape != q.shape or v.shape != q.shape:
         raise ValueError("q, k, v must have the same shape")
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None:
-        lse = torch.empty(B, H, S, dtype=torch.float32, device=q.device)
+    out = _out(out, q.shape, torch.bfloat16, q, "out")
+    lse = _out(lse, (B, H, S), torch.float32, q, "lse")
+    workspace = _ws(workspace)
     st = _stream(stream)
     if workspace is None:
         rc = lib().moba_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, S, D,
@@ -219,12 +238,12 @@ def decode_fwd(q, k_cache, v_cache, kbar, cache_lens, block_size: int, topk: int
             v_cache.shape != k_cache.shape:
         raise ValueError("k_cache, v_cache must be [B, S_max, H, D] matching q")
     S_max = k_cache.shape[1]
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None:
-        lse = torch.empty(B, H, dtype=torch.float32, device=q.device)
-    if idx is None:
-        idx = torch.empty(B, H, topk, dtype=torch.int32, device=q.device)
+    if block_size > 0 and tuple(kbar.shape) != (B * num_blocks(S_max, block_size), H, D):
+        raise ValueError("kbar must be [B * ceil(S_max / block_size), H, D] (kpool of k_cache)")
+    out = _out(out, q.shape, torch.bfloat16, q, "out")
+    lse = _out(lse, (B, H), torch.float32, q, "lse")
+    idx = _out(idx, (B, H, topk), torch.int32, q, "idx")
+    workspace = _ws(workspace)
     st = _stream(stream)
     args = (_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kbar), _ptr(cache_lens), _ptr(out),
             _ptr(lse), _ptr(idx), B, H, S_max, D, block_size, topk)
@@ -245,10 +264,12 @@ def attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, block_size: int, topk:
     _need(cu_seqlens, torch.int32, "cu_seqlens")
     total, H, D = q.shape
     ns = cu_seqlens.numel() - 1
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None:
-        lse = torch.empty(H, total, dtype=torch.float32, device=q.device)
+    for t, n in ((k, "k"), (v, "v")):
+        if t.shape != q.shape:
+            raise ValueError(f"{n} must have the shape of q")
+    out = _out(out, q.shape, torch.bfloat16, q, "out")
+    lse = _out(lse, (H, total), torch.float32, q, "lse")
+    workspace = _ws(workspace)
     st = _stream(stream)
     if workspace is None:
         rc = lib().moba_attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
@@ -282,9 +303,10 @@ def attn_bwd(q, k, v, out, lse, dout, block_size: int, topk: int, dq=None, dk=No
             raise ValueError(f"{n} must have the shape of q")
     if tuple(lse.shape) != (B, H, S):
         raise ValueError("lse must be [B, H, S]")
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(q) if dk is None else dk
-    dv = torch.empty_like(q) if dv is None else dv
+    dq = _out(dq, q.shape, torch.bfloat16, q, "dq")
+    dk = _out(dk, q.shape, torch.bfloat16, q, "dk")
+    dv = _out(dv, q.shape, torch.bfloat16, q, "dv")
+    workspace = _ws(workspace)
     st = _stream(stream)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
             _ptr(dv), B, H, S, D, block_size, topk)
@@ -306,6 +328,11 @@ def attn_bwd_varlen(q, k, v, out, lse, dout, cu_seqlens, max_seqlen: int, block_
     _need(cu_seqlens, torch.int32, "cu_seqlens")
     total, H, D = q.shape
     ns = cu_seqlens.numel() - 1
+    for t, n in ((k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
+        if t.shape != q.shape:
+            raise ValueError(f"{n} must have the shape of q")
+    if tuple(lse.shape) != (H, total):
+        raise ValueError("lse must be [H, total]")
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
     rc = lib().moba_attn_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
                                     _ptr(dq), _ptr(dk), _ptr(dv), _ptr(cu_seqlens), ns, total,
@@ -359,6 +386,11 @@ def attn_fwd_noalloc(q, k, v, block_size: int, topk: int, out, lse, stream=None)
         _need(t, torch.bfloat16, n)
     _need(lse, torch.float32, "lse")
     B, S, H, D = q.shape
+    for t, n in ((k, "k"), (v, "v"), (out, "out")):
+        if t.shape != q.shape:
+            raise ValueError(f"{n} must have the shape of q")
+    if tuple(lse.shape) != (B, H, S):
+        raise ValueError("lse must be [B, H, S]")
     _check(lib().moba_attn_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, S,
                                        D, block_size, topk, _stream(stream)),
            "moba_attn_fwd_noalloc")
