@@ -39,7 +39,8 @@
  *      only.  [P4] section 3 trains MoBA layers end to end (it blames the
  *      sparse gradient path for a higher SFT loss).
  *
- * Parity pins for every function here live in tests/test_oracle.py.
+ * Parity pins for every function here live in tests/test_oracle.py (forward)
+ * and tests/test_oracle_bwd.py (backward).
  */
 #include <math.h>
 #include <stdint.h>
