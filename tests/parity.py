@@ -104,3 +104,19 @@ def compare(w: workloads.Workload, inp, topk: int, out, lse, idx_gpu=None, rows=
     assert stats["out_mean"] <= OUT_MEAN, stats
     assert stats["lse_max"] <= LSE_MAX, stats
     return stats
+
+
+def tie_masks(w, idx_gpu, ref_idx, gap):
+    """Rows (token, head) and keys (token, head) excluded because of near ties."""
+    differ = (idx_gpu != ref_idx).any(axis=-1)                       # [total, H]
+    assert not (differ & (gap >= TIE_GAP)).any(), "selection differs away from a tie"
+    row_ok = ~differ
+    key_ok = np.ones((w.total, w.H), dtype=bool)
+    cu = w.cu_seqlens()
+    bs = w.block_size
+    for t, h in zip(*np.nonzero(differ)):
+        b = int(np.searchsorted(cu, t, side="right") - 1)
+        for c in set(idx_gpu[t, h].tolist()) ^ set(ref_idx[t, h].tolist()):
+            if c >= 0:
+                key_ok[cu[b] + c * bs: min(cu[b] + (c + 1) * bs, cu[b + 1]), h] = False
+    return row_ok, key_ok

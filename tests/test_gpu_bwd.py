@@ -25,7 +25,7 @@ import torch
 import oracle
 from long_context_sparse_moba_gb300 import ops, workloads
 
-from .parity import TIE_GAP, flat, gpu_forward
+from .parity import TIE_GAP, flat, gpu_forward, tie_masks
 
 pytestmark = pytest.mark.gpu
 
@@ -59,22 +59,6 @@ def check(name, got, ref, keep=None):
     mx, mn = err.max() / np.abs(ref).max(), err.mean() / np.abs(ref).mean()
     assert mx <= TOL[name][0] and mn <= TOL[name][1], (name, mx, mn)
     return mx, mn
-
-
-def tie_masks(w, idx_gpu, ref_idx, gap):
-    """Rows (token, head) and keys (token, head) excluded because of near ties."""
-    differ = (idx_gpu != ref_idx).any(axis=-1)                       # [total, H]
-    assert not (differ & (gap >= TIE_GAP)).any(), "selection differs away from a tie"
-    row_ok = ~differ
-    key_ok = np.ones((w.total, w.H), dtype=bool)
-    cu = w.cu_seqlens()
-    bs = w.block_size
-    for t, h in zip(*np.nonzero(differ)):
-        b = int(np.searchsorted(cu, t, side="right") - 1)
-        for c in set(idx_gpu[t, h].tolist()) ^ set(ref_idx[t, h].tolist()):
-            if c >= 0:
-                key_ok[cu[b] + c * bs: min(cu[b] + (c + 1) * bs, cu[b + 1]), h] = False
-    return row_ok, key_ok
 
 
 def run_case(w, topk, dout_scale=1.0):
