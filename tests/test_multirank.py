@@ -54,7 +54,7 @@ def _worker(rank, world, port, out):
 
 def test_two_ranks_weak_scaling_and_max_time():
     world = 2
-    manager = mp.Manager()
+    manager = mp.get_context("spawn").Manager()  # no fork of a threaded process
     out = manager.dict()
     mp.spawn(_worker, args=(world, free_port(), out), nprocs=world, join=True)
     r0, r1 = out[0], out[1]
