@@ -357,6 +357,165 @@ def config_of(w, topk):
 # our arm
 # ---------------------------------------------------------------------------
 
+def phase_work(w, topk):
+    """Algorithmic work of each timed phase: (bound, amount) -- HBM bytes for
+    pooling and gate, issued tensor FLOPs for the two attention kernels."""
+    cur, past = issued_pairs(w.seqlens, w.block_size, topk)
+    hbm = hbm_bytes(w, topk)
+    return {"kpool": ("hbm", hbm["kpool"]), "gate": ("hbm", hbm["gate"]),
+            "attn_past": ("tensor", 4 * w.D * past * w.H),
+            "attn_current": ("tensor", 4 * w.D * cur * w.H)}
+
+
+def roofline_of(w, topk, per_call, peaks, peak_src):
+    """Per-phase rates and the dominant kernel's roofline entry.  Tensor work
+    is divided by the burst bf16 peak: every timed loop here lasts well under a
+    second."""
+    work = phase_work(w, topk)
+    total_phase = sum(per_call.values())
+    phases = {}
+    for name, ms in per_call.items():
+        ent = {"ms": ms, "share": ms / total_phase if total_phase > 0 else None}
+        if name in work and ms > 0:
+            kind, amount = work[name]
+            if kind == "hbm":
+                ent["gbs"] = amount / (ms * 1e-3) / 1e9
+                ent["frac_hbm"] = ent["gbs"] / peaks["hbm_gbs"]
+            else:
+                ent["tflops"] = amount / (ms * 1e-3) / 1e12
+                ent["frac_bf16"] = ent["tflops"] / peaks["bf16_tflops"]
+        phases[name] = ent
+    dom = max((n for n in per_call if n in work and per_call[n] > 0), key=lambda n: per_call[n])
+    kind, amount = work[dom]
+    dms = per_call[dom]
+    if kind == "hbm":
+        achieved, peak, unit, key = amount / (dms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s", "hbm_gbs"
+    else:
+        achieved, peak, unit, key = (amount / (dms * 1e-3) / 1e12, peaks["bf16_tflops"], "TFLOP/s",
+                                     "bf16_tflops")
+    roofline = {"kernel": dom, "bound": kind, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "traffic": measured_traffic(w.name, topk, dom),
+                "peak_source": f"{peak_src} ({key}, burst)"}
+    return phases, roofline
+
+
+class Forward:
+    """One workload's inputs resident on the GPU and a forward step through
+    the C ABI (caller workspace, so the timed step allocates nothing)."""
+
+    def __init__(self, ops, torch, w, dev):
+        from long_context_sparse_moba_gb300 import workloads
+        self.ops, self.torch, self.w, self.dev = ops, torch, w, dev
+        self.inp = workloads.make_inputs(w, device=dev)
+        H, D = w.H, w.D
+        if w.varlen:
+            self.cu = torch.tensor(self.inp.cu_seqlens, dtype=torch.int32, device=dev)
+            self.lse = torch.empty(H, w.total, dtype=torch.float32, device=dev)
+        else:
+            self.cu = None
+            self.lse = torch.empty(w.B, H, w.S, dtype=torch.float32, device=dev)
+        self.out = torch.empty_like(self.inp.q)
+        self.ws = None
+        self.ws_topk = None
+
+    def workspace(self, topk):
+        w, ops = self.w, self.ops
+        if self.ws_topk != topk:
+            if w.varlen:
+                nb = ops.varlen_workspace_size(w.B, w.total, w.S, w.H, w.D, w.block_size, topk)
+            else:
+                nb = ops.workspace_size(w.B, w.H, w.S, w.D, w.block_size, topk)
+            self.ws = None
+            self.ws = self.torch.empty(max(nb, 256), dtype=self.torch.uint8, device=self.dev)
+            self.ws_topk = topk
+        return self.ws
+
+    def step(self, topk, **kw):
+        w, inp = self.w, self.inp
+        ws = self.workspace(topk)
+        if w.varlen:
+            self.ops.attn_fwd_varlen(inp.q, inp.k, inp.v, self.cu, w.S, w.block_size, topk,
+                                     out=self.out, lse=self.lse, workspace=ws, **kw)
+        else:
+            self.ops.attn_fwd(inp.q, inp.k, inp.v, w.block_size, topk, out=self.out,
+                              lse=self.lse, workspace=ws, **kw)
+
+    def time(self, topk, steps, warmup, phases=True, barrier=None):
+        """(ms per step over `steps` forward calls timed with CUDA events on the
+        launch stream, {phase: mean ms}, kernels launched in the timed loop)."""
+        torch, ops = self.torch, self.ops
+        for _ in range(warmup):
+            self.step(topk)
+        torch.cuda.synchronize()
+        assert ops.get_status() == ops.MOBA_OK
+        stream = torch.cuda.current_stream()
+        evs = [ops.phase_events(stream) for _ in range(steps)] if phases else None
+        torch.cuda.synchronize()
+        if barrier:
+            barrier()
+        launches0 = ops.launch_count()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for s in range(steps):
+            self.step(topk, phase_events=evs[s] if phases else None)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if barrier:
+            barrier()
+        launches = ops.launch_count() - launches0
+        ms = e0.elapsed_time(e1) / steps
+        per_call = None
+        if phases:
+            per_call = {n: 0.0 for n in ops.PHASES}
+            for ev in evs:
+                for n, v in ops.phase_ms(ev).items():
+                    per_call[n] += v / steps
+        assert ops.get_status() == ops.MOBA_OK
+        return ms, per_call, launches
+
+
+def workload_entry(fw, topk, steps, warmup, peaks, peak_src):
+    """Measured sub-object of the bench line for one (workload, top-k)."""
+    w = fw.w
+    ms, per_call, launches = fw.time(topk, steps, warmup)
+    cur, past = issued_pairs(w.seqlens, w.block_size, topk)
+    flops = 4 * w.D * (cur + past) * w.H
+    tfl = flops / (ms * 1e-3) / 1e12
+    phases, roofline = roofline_of(w, topk, per_call, peaks, peak_src)
+    n_max = (w.S + w.block_size - 1) // w.block_size
+    dcur, dpast = issued_pairs(w.seqlens, w.block_size, n_max)
+    return {"config": config_of(w, topk), "steps": steps, "warmup": warmup,
+            "ms_per_step": ms, "tokens_per_s": w.total / (ms * 1e-3),
+            "issued_flops_per_step": flops, "effective_tflops": tfl,
+            "frac_of_bf16_peak": tfl / peaks["bf16_tflops"],
+            "sparsity_vs_dense_causal": 1.0 - (cur + past) / (dcur + dpast),
+            "phases": phases, "roofline": roofline, "gpu_launches": launches}
+
+
+def near_tie_report(w, fw, topk, n_rows=4096, seed=4242):
+    """Selections the forward used (its idx_out), checked against the oracle's
+    on a seeded row sample: rows whose last kept and first dropped past blocks
+    score within 1e-5 are counted as near ties; any other difference is a
+    mismatch.  Part of the CPU-baseline leg (the oracle runs on the host)."""
+    import oracle
+    from long_context_sparse_moba_gb300 import workloads
+    torch, ops = fw.torch, fw.ops
+    shape = (w.total, w.H, topk) if w.varlen else (w.B, w.S, w.H, topk)
+    idx = torch.empty(shape, dtype=torch.int32, device=fw.dev)
+    fw.step(topk, idx_out=idx)
+    torch.cuda.synchronize()
+    tok, head = workloads.sample_rows(w, n_rows, seed=seed)
+    gi = idx.reshape(w.total, w.H, topk).cpu().numpy()[tok, head]
+    host = tuple(x.reshape(-1, w.H, w.D).cpu() for x in (fw.inp.q, fw.inp.k, fw.inp.v))
+    ref = oracle.moba_rows(*host, w.cu_seqlens(), w.H, w.D, w.block_size, topk, tok, head)
+    near = ref["gap"] < 1e-5
+    differ = (gi != ref["idx"]).any(axis=1)
+    return {"workload": w.name, "topk": topk, "sampled_rows": int(len(tok)),
+            "near_tie_rows": int(near.sum()), "near_tie_rows_selected_differently":
+            int((near & differ).sum()), "mismatches_outside_near_ties": int((differ & ~near).sum()),
+            "tie_gap": 1e-5}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -370,6 +529,8 @@ def main():
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--no-range", action="store_true",
+                    help="skip the other workloads of the metric's range (128K, 1M, varlen)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -397,95 +558,61 @@ def main():
     if world > 1:
         dist.barrier()
     ops.lib()
+    barrier = dist.barrier if world > 1 else None
 
     dev = torch.device("cuda", local)
     wr = rank_workload(w, rank)
-    inp = workloads.make_inputs(wr, device=dev)
+    fw = Forward(ops, torch, wr, dev)
+    inp = fw.inp
     q, k, v = inp.q, inp.k, inp.v
-    varlen = w.varlen
-    H, D, bs = w.H, w.D, w.block_size
-    if varlen:
-        cu = torch.tensor(inp.cu_seqlens, dtype=torch.int32, device=dev)
-        ws_bytes = ops.varlen_workspace_size(w.B, w.total, w.S, H, D, bs, topk)
-        lse = torch.empty(H, w.total, dtype=torch.float32, device=dev)
-    else:
-        ws_bytes = ops.workspace_size(w.B, H, w.S, D, bs, topk)
-        lse = torch.empty(w.B, H, w.S, dtype=torch.float32, device=dev)
-    out = torch.empty_like(q)
-    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
+    bs, H, D = w.block_size, w.H, w.D
+    peaks, peak_src = load_peaks()
 
-    def step(topk_=topk, ws_=ws):
-        if varlen:
-            ops.attn_fwd_varlen(q, k, v, cu, w.S, bs, topk_, out=out, lse=lse, workspace=ws_)
-        else:
-            ops.attn_fwd(q, k, v, bs, topk_, out=out, lse=lse, workspace=ws_)
-
+    # ---------------- the headline: timed steps of the workload ----------------
     for _ in range(args.warmup):
-        step()
+        fw.step(topk)
     torch.cuda.synchronize()
-    assert ops.get_status() == ops.MOBA_OK
-
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    launches0 = ops.launch_count()
-    ops.profile_begin(args.steps)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    elapsed_ms = ev0.elapsed_time(ev1)
-    ncalls, phase_ms = ops.profile_end()
-    launches = ops.launch_count() - launches0
+    ms_per_step, per_call, launches = fw.time(topk, args.steps, 0, barrier=barrier)
     clk = clocks.stop()
     status = ops.get_status()
-    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
-    ms_per_step = elapsed_ms / args.steps
+    ms_per_step = max_over_ranks(ms_per_step, world, dev)
 
     # dense comparison: same kernels with top-k = number of blocks
     dense = None
     n_max = (w.S + bs - 1) // bs
     if not args.no_dense and topk < n_max:
-        dsteps = 3
-        step(n_max, ws)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(dsteps):
-            step(n_max, ws)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        dms = e0.elapsed_time(e1) / dsteps
+        dms, _, _ = fw.time(n_max, 3, 1, phases=False)
         dcur, dpast = issued_pairs(w.seqlens, bs, n_max)
+        dfl = 4 * D * (dcur + dpast) * H
         dense = {"topk": n_max, "ms_per_step": dms,
-                 "effective_tflops": 4 * D * (dcur + dpast) * H / (dms * 1e-3) / 1e12,
+                 "effective_tflops": dfl / (dms * 1e-3) / 1e12,
+                 "frac_of_bf16_peak": dfl / (dms * 1e-3) / 1e12 / peaks["bf16_tflops"],
                  "sparse_speedup": dms / ms_per_step}
+        fw.workspace(topk)
 
     decode = None
-    if not args.no_decode and rank == 0 and not varlen:
+    if not args.no_decode and rank == 0 and not w.varlen:
         decode = decode_bench(ops, torch, dev, H, D, bs, topk)
+        decode["frac_hbm"] = decode["gbs"] / peaks["hbm_gbs"]
 
     # end to end through the public API with pinned host buffers
     e2e = None
     if not args.no_e2e:
+        out, lse = fw.out, fw.lse
         hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
         hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
         esteps = max(3, min(args.steps, 20))
+        stream = torch.cuda.current_stream()
 
         def e2e_step():
             q.copy_(hq, non_blocking=True)
             k.copy_(hk, non_blocking=True)
             v.copy_(hv, non_blocking=True)
-            step()
+            fw.step(topk)
             hout.copy_(out, non_blocking=True)
             hlse.copy_(lse, non_blocking=True)
 
@@ -504,55 +631,53 @@ def main():
                "h2d_bytes_per_step": 3 * q.numel() * 2,
                "d2h_bytes_per_step": out.numel() * 2 + lse.numel() * 4,
                "ms_per_step": ems}
+        del hq, hk, hv, hout, hlse
 
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
 
-    peaks, peak_src = load_peaks()
-    if decode is not None:
-        decode["frac_hbm"] = decode["gbs"] / peaks["hbm_gbs"]
     cur, past = issued_pairs(w.seqlens, bs, topk)
     flops = 4 * D * (cur + past) * H
     tflops = flops / (ms_per_step * 1e-3) / 1e12
     backward = None
     if not args.no_backward:
         rc_, rp_ = issued_pairs(wr.seqlens, bs, topk)
-        backward = backward_bench(ops, torch, wr, inp, topk, out, lse, 4 * D * (rc_ + rp_) * H)
-        backward["frac_bf16"] = backward["effective_tflops"] / peaks["bf16_tflops_sustained"]
-    per_call = {kk: vv / max(ncalls, 1) for kk, vv in phase_ms.items()}
-    total_phase = sum(per_call.values())
-    hbm = hbm_bytes(w, topk)
-    work = {"kpool": ("hbm", hbm["kpool"]), "gate": ("hbm", hbm["gate"]),
-            "attn_past": ("tensor", 4 * D * past * H), "attn_current": ("tensor", 4 * D * cur * H)}
-    phases = {}
-    for name, ms in per_call.items():
-        ent = {"ms": ms, "share": ms / total_phase if total_phase > 0 else None}
-        if name in work and ms > 0:
-            kind, amount = work[name]
-            if kind == "hbm":
-                ent["gbs"] = amount / (ms * 1e-3) / 1e9
-                ent["frac_hbm"] = ent["gbs"] / peaks["hbm_gbs"]
-            else:
-                ent["tflops"] = amount / (ms * 1e-3) / 1e12
-                ent["frac_bf16"] = ent["tflops"] / peaks["bf16_tflops_sustained"]
-        phases[name] = ent
-    dom = max((n for n in per_call if n in work), key=lambda n: per_call[n])
-    kind, amount = work[dom]
-    dms = per_call[dom]
-    if kind == "hbm":
-        achieved, peak, unit = amount / (dms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
-    else:
-        achieved, peak, unit = (amount / (dms * 1e-3) / 1e12, peaks["bf16_tflops_sustained"],
-                                "TFLOP/s")
-    roofline = {"kernel": dom, "bound": kind, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "traffic": measured_traffic(w.name, topk, dom),
-                "peak_source": f"{peak_src} ({'bf16_tflops_sustained' if kind == 'tensor' else 'hbm_gbs'})"}
+        backward = backward_bench(ops, torch, wr, inp, topk, fw.out, fw.lse,
+                                  4 * D * (rc_ + rp_) * H)
+        backward["frac_bf16"] = backward["effective_tflops"] / peaks["bf16_tflops"]
+    phases, roofline = roofline_of(w, topk, per_call, peaks, peak_src)
 
-    cpu = None
+    cpu = near = None
     if not args.no_cpu_baseline:
         cpu = cpu_baseline(w, inp, topk)
+        near = [near_tie_report(w, fw, topk)]
+
+    # ---------------- the rest of the metric's range (32K to 1M) ----------------
+    rng = {}
+    if not args.no_range and world == 1:
+        fw_keep = fw
+        for name, steps in (("long128k", 20), ("prefill1m", 10)):
+            if name == w.name:
+                continue
+            fw = None
+            torch.cuda.empty_cache()
+            fo = Forward(ops, torch, workloads.WORKLOADS[name], dev)
+            t = workloads.WORKLOADS[name].topks[0]
+            rng[name] = workload_entry(fo, t, steps, 3, peaks, peak_src)
+            if not args.no_cpu_baseline:
+                near.append(near_tie_report(fo.w, fo, t))
+            del fo
+        if w.name != "varlen":
+            torch.cuda.empty_cache()
+            fo = Forward(ops, torch, workloads.WORKLOADS["varlen"], dev)
+            rng["varlen"] = {str(t): workload_entry(fo, t, 20, 3, peaks, peak_src)
+                             for t in fo.w.topks}
+            if not args.no_cpu_baseline:
+                near.append(near_tie_report(fo.w, fo, 3))
+            del fo
+        fw = fw_keep
 
     line = {"metric": METRIC, "value": whole_job_rate(w.total, world, ms_per_step), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -560,11 +685,11 @@ def main():
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": config_of(w, topk),
             "effective_tflops": tflops * world,
-            "frac_of_bf16_peak": tflops / peaks["bf16_tflops_sustained"],
+            "frac_of_bf16_peak": tflops / peaks["bf16_tflops"],
             "issued_flops_per_step": flops,
             "sparsity_vs_dense_causal": None,
             "roofline": roofline, "phases": phases, "dense": dense, "decode": decode,
-            "backward": backward, "e2e": e2e,
+            "backward": backward, "range": rng or None, "near_ties": near, "e2e": e2e,
             "cpu_baseline": cpu, "gpu_launches": launches, "clocks": clk,
             "device_status": ops.status_string(status)}
     dcur, dpast = issued_pairs(w.seqlens, bs, n_max)

@@ -64,6 +64,65 @@ typedef enum {
     MOBA_ERR_TIMEOUT = 5       /* a kernel gave up a bounded wait (device status word) */
 } moba_status_t;
 
+/*
+ * Per-call options of the _ex entry points.  Passing NULL, or a structure
+ * whose fields are all zero, selects the defaults.  The library keeps no
+ * process-wide setting: two threads may call with different options on
+ * different streams at the same time.
+ *
+ *   pooling      how each block's keys are pooled into the representative the
+ *                gate scores: MOBA_POOL_MEAN (default) = their mean ("Moonshot
+ *                MoBA paper explained" section 3.1 mean_pool; "MOBA mixture of
+ *                block attention for server-side long context" section 3);
+ *                MOBA_POOL_MAX = their element-wise maximum, the variant the
+ *                latter page also allows.
+ *   gate_kernel  MOBA_GATE_TENSOR_CORES (default): block scores on the tensor
+ *                cores (q times the pooled keys split into two bf16 terms,
+ *                fp32 accumulation) and an exact fp32 re-score of the blocks
+ *                inside a proven error margin of the top-(k-1) boundary; used
+ *                while the longest sequence has at most 256 blocks, the CUDA
+ *                cores above that.  MOBA_GATE_CUDA_CORES: every score on the
+ *                CUDA cores.  Both select exactly the same blocks.
+ *   attn_kernel  MOBA_ATTN_TCGEN05 (default): tcgen05 MMAs with TMEM
+ *                accumulators and TMA-staged K/V; MOBA_ATTN_MMA_SYNC: the
+ *                warp-level mma.sync kernels kept as the measured baseline.
+ *                Same selection; results within the stated tolerances.
+ *   debug_flags  test hook of the bounded waits: bit 0 makes the tcgen05
+ *                attention's K/V producer skip its first load, so that the
+ *                consumer's wait runs out and MOBA_ERR_TIMEOUT is recorded in
+ *                the device status word instead of the GPU hanging.  0 in use.
+ *   wait_limit_cycles  clock64 budget of one bounded wait; <= 0 keeps the
+ *                default (about 2 s).
+ *   idx_out      forward only, optional DEVICE int32 [tokens][H][topk]: the
+ *                selection the call used (as moba_gate_topk writes it: the
+ *                selected blocks ascending, -1 padded), written also on the
+ *                paths that run no gate (top-1, and top-k covering every
+ *                block).  4-byte aligned.
+ *   phase_events forward only, optional: an array of 7 cudaEvent_t (passed as
+ *                void *) owned by the caller; the call records event i on its
+ *                stream before phase i and event 6 after the last one.  Phases:
+ *                0 sequence tables, 1 key pooling, 2 gate + top-k, 3 regroup,
+ *                4 attention over past blocks, 5 attention over the own block
+ *                + merge (a phase a path skips is empty).  A NULL entry is
+ *                skipped.
+ * An option value outside its set returns MOBA_ERR_INVALID_ARG before any
+ * launch.
+ */
+enum { MOBA_POOL_MEAN = 0, MOBA_POOL_MAX = 1 };
+enum { MOBA_GATE_TENSOR_CORES = 0, MOBA_GATE_CUDA_CORES = 1 };
+enum { MOBA_ATTN_TCGEN05 = 0, MOBA_ATTN_MMA_SYNC = 1 };
+enum { MOBA_NUM_PHASES = 6 };
+
+typedef struct moba_options {
+    int pooling;
+    int gate_kernel;
+    int attn_kernel;
+    int debug_flags;
+    long long wait_limit_cycles;
+    int32_t *idx_out;
+    void *const *phase_events;
+} moba_options_t;
+
 /* Number of blocks of a sequence: ceil(len / block_size) (the tail block may
  * be partial).  "Moonshot MoBA paper explained" section 4.1 divides the
  * context length by the block size (32768 / 512 = 64). */
@@ -75,15 +134,23 @@ int moba_num_blocks(int len, int block_size);
  *   kbar : [B * n][H][D] fp32 (device, written), n = moba_num_blocks(S, bs);
  *          kbar[b*n + c][h][:] = mean of k[b][t][h][:] over the tokens t of
  *          block c (the tail block averages only the tokens it holds).
+ *          Blocks are the outer index (not heads) so that the pooled keys of
+ *          packed variable-length sequences concatenate like their tokens do.
+ * moba_kpool_ex takes the per-call options (only `pooling` applies).
  */
 int moba_kpool(const void *k, float *kbar, int B, int H, int S, int D, int block_size,
                void *stream);
+int moba_kpool_ex(const void *k, float *kbar, int B, int H, int S, int D, int block_size,
+                  const moba_options_t *options, void *stream);
 
 /* Varlen form: k [total_tokens][H][D]; cu_seqlens is a DEVICE int32 array of
  * num_seqs + 1 prefix offsets (cu_seqlens[num_seqs] == total_tokens).
  * kbar: [sum over sequences of n_b][H][D], sequence 0's blocks first. */
 int moba_kpool_varlen(const void *k, float *kbar, const int32_t *cu_seqlens, int num_seqs,
                       int total_tokens, int H, int D, int block_size, void *stream);
+int moba_kpool_varlen_ex(const void *k, float *kbar, const int32_t *cu_seqlens, int num_seqs,
+                         int total_tokens, int H, int D, int block_size,
+                         const moba_options_t *options, void *stream);
 
 /*
  * Gate and top-k selection ("Moonshot MoBA paper explained" sections 3.1 and
@@ -97,12 +164,19 @@ int moba_kpool_varlen(const void *k, float *kbar, const int32_t *cu_seqlens, int
  */
 int moba_gate_topk(const void *q, const float *kbar, int32_t *idx, int B, int H, int S, int D,
                    int block_size, int topk, void *stream);
+/* with per-call options (only `gate_kernel` applies) */
+int moba_gate_topk_ex(const void *q, const float *kbar, int32_t *idx, int B, int H, int S, int D,
+                      int block_size, int topk, const moba_options_t *options, void *stream);
 
 /* Varlen form of moba_gate_topk: q [total_tokens][H][D], idx
  * [total_tokens][H][topk]; cu_seqlens as for moba_kpool_varlen. */
 int moba_gate_topk_varlen(const void *q, const float *kbar, int32_t *idx,
                           const int32_t *cu_seqlens, int num_seqs, int total_tokens, int H,
                           int D, int block_size, int topk, void *stream);
+int moba_gate_topk_varlen_ex(const void *q, const float *kbar, int32_t *idx,
+                             const int32_t *cu_seqlens, int num_seqs, int total_tokens, int H,
+                             int D, int block_size, int topk, const moba_options_t *options,
+                             void *stream);
 
 /*
  * Full MoBA forward: pool, gate, regroup of the queries by selected block,
@@ -116,8 +190,10 @@ int moba_gate_topk_varlen(const void *q, const float *kbar, int32_t *idx,
 int moba_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse, int B,
                   int H, int S, int D, int block_size, int topk, void *stream);
 
-/* Bytes of device scratch moba_attn_fwd_ws needs for these sizes. */
+/* Bytes of device scratch moba_attn_fwd_ws / _ex need for these sizes (the
+ * same for every option); moba_workspace_size is the same function. */
 size_t moba_attn_fwd_workspace_size(int B, int H, int S, int D, int block_size, int topk);
+size_t moba_workspace_size(int B, int H, int S, int D, int block_size, int topk);
 
 /* moba_attn_fwd with caller-provided device scratch (256-byte aligned,
  * at least moba_attn_fwd_workspace_size bytes; MOBA_ERR_WORKSPACE if
@@ -127,11 +203,25 @@ int moba_attn_fwd_ws(const void *q, const void *k, const void *v, void *out, flo
                      int H, int S, int D, int block_size, int topk, void *workspace,
                      size_t workspace_bytes, void *stream);
 
+/* moba_attn_fwd with per-call options (NULL = defaults).  workspace may be
+ * NULL (scratch from cudaMallocAsync on the stream, as moba_attn_fwd) or the
+ * caller's scratch (as moba_attn_fwd_ws). */
+int moba_attn_fwd_ex(const void *q, const void *k, const void *v, void *out, float *lse, int B,
+                     int H, int S, int D, int block_size, int topk, const moba_options_t *options,
+                     void *workspace, size_t workspace_bytes, void *stream);
+
 /*
  * Varlen forward: q, k, v, out [total_tokens][H][D] bf16; lse
  * [H][total_tokens] fp32; cu_seqlens DEVICE int32 [num_seqs + 1];
  * max_seqlen >= every sequence length.  Each sequence is partitioned into
  * its own blocks starting at its first token.
+ * cu_seqlens lives on the device, so its consistency is checked there, by the
+ * first kernel of the call: it must start at 0, never decrease, give no
+ * sequence more than max_seqlen tokens and end at total_tokens.  When it does
+ * not, no later kernel of the call reads or writes anything through it, out
+ * and lse are left unwritten, and MOBA_ERR_INVALID_ARG is recorded in the
+ * device status word (read it with moba_get_status).  The same check guards
+ * every varlen entry point.
  */
 int moba_attn_fwd_varlen(const void *q, const void *k, const void *v, void *out, float *lse,
                          const int32_t *cu_seqlens, int num_seqs, int total_tokens,
@@ -139,6 +229,12 @@ int moba_attn_fwd_varlen(const void *q, const void *k, const void *v, void *out,
 
 size_t moba_attn_fwd_varlen_workspace_size(int num_seqs, int total_tokens, int max_seqlen, int H,
                                            int D, int block_size, int topk);
+
+int moba_attn_fwd_varlen_ex(const void *q, const void *k, const void *v, void *out, float *lse,
+                            const int32_t *cu_seqlens, int num_seqs, int total_tokens,
+                            int max_seqlen, int H, int D, int block_size, int topk,
+                            const moba_options_t *options, void *workspace,
+                            size_t workspace_bytes, void *stream);
 
 int moba_attn_fwd_varlen_ws(const void *q, const void *k, const void *v, void *out, float *lse,
                             const int32_t *cu_seqlens, int num_seqs, int total_tokens,
@@ -174,6 +270,12 @@ int moba_attn_bwd_ws(const void *q, const void *k, const void *v, const void *ou
                      const float *lse, const void *dout, void *dq, void *dk, void *dv, int B,
                      int H, int S, int D, int block_size, int topk, void *workspace,
                      size_t workspace_bytes, void *stream);
+/* with per-call options (pooling and gate_kernel decide the recomputed
+ * selection and must match the forward's); workspace may be NULL */
+int moba_attn_bwd_ex(const void *q, const void *k, const void *v, const void *out,
+                     const float *lse, const void *dout, void *dq, void *dk, void *dv, int B,
+                     int H, int S, int D, int block_size, int topk, const moba_options_t *options,
+                     void *workspace, size_t workspace_bytes, void *stream);
 
 /* Varlen backward: every tensor [total_tokens][H][D] bf16, lse [H][total_tokens]
  * fp32 as moba_attn_fwd_varlen wrote it; cu_seqlens DEVICE int32. */
@@ -183,6 +285,12 @@ int moba_attn_bwd_varlen(const void *q, const void *k, const void *v, const void
                          int max_seqlen, int H, int D, int block_size, int topk, void *stream);
 size_t moba_attn_bwd_varlen_workspace_size(int num_seqs, int total_tokens, int max_seqlen, int H,
                                            int D, int block_size, int topk);
+int moba_attn_bwd_varlen_ex(const void *q, const void *k, const void *v, const void *out,
+                            const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                            const int32_t *cu_seqlens, int num_seqs, int total_tokens,
+                            int max_seqlen, int H, int D, int block_size, int topk,
+                            const moba_options_t *options, void *workspace,
+                            size_t workspace_bytes, void *stream);
 
 /*
  * moba_attn_fwd for callers that cannot allocate device memory: for example
@@ -211,9 +319,11 @@ int moba_attn_fwd_noalloc(const void *q, const void *k, const void *v, void *out
 /* Bytes of the static scratch array used by moba_attn_fwd_noalloc. */
 size_t moba_attn_fwd_noalloc_capacity(void);
 
-/* Synchronises `stream`, returns the device status word (MOBA_OK or
- * MOBA_ERR_TIMEOUT) of the current device and clears it; MOBA_ERR_CUDA if
- * the synchronisation itself failed. */
+/* Synchronises `stream`, returns the device status word of the current device
+ * (MOBA_OK, MOBA_ERR_TIMEOUT from a bounded wait, or MOBA_ERR_INVALID_ARG from
+ * inconsistent device-side lengths) and clears it; MOBA_ERR_CUDA if the
+ * synchronisation itself failed.  The word is per device, shared by all
+ * streams: a call reports what any earlier work on the device recorded. */
 int moba_get_status(void *stream);
 
 /* Static, human-readable name of a status code. */
@@ -224,47 +334,8 @@ const char *moba_status_string(int code);
 const char *moba_last_cuda_error(void);
 
 /* Number of kernels this library has launched since it was loaded (a
- * process-wide tally; host only). */
+ * process-wide tally, counted atomically; host only). */
 unsigned long long moba_launch_count(void);
-
-/*
- * Phase timing of the forward entry points (tracing aid; not thread-safe).
- * moba_profile_begin(max_calls) starts recording CUDA events on each call's
- * stream between its phases, for at most max_calls calls; moba_profile_end
- * stops, waits for the recorded events and writes into phase_ms[0..5] the
- * milliseconds summed over the recorded calls for: 0 sequence tables,
- * 1 key pooling, 2 gate + top-k, 3 regroup, 4 attention over past blocks,
- * 5 attention over the own block + merge.  Returns the number of calls
- * recorded, or a negated status code.  Phases a call skips read as ~0.
- */
-int moba_profile_begin(int max_calls);
-int moba_profile_end(float *phase_ms, int n_phases);
-
-/* Attention implementation used by the forward entry points (process-wide,
- * not thread-safe): 0 = tcgen05 MMA with TMEM accumulators and TMA-staged
- * K/V (default); 1 = the warp-level mma.sync kernels, kept as the measured
- * baseline.  Both give the same selection and results within the stated
- * tolerances.  MOBA_ERR_INVALID_ARG for any other value. */
-int moba_set_attention_kernel(int kind);
-
-/* Gate implementation (process-wide, not thread-safe): 0 = block scores on
- * the tensor cores (q times the pooled keys split into two bf16 terms, fp32
- * accumulation) followed by an exact fp32 re-score of the blocks within a
- * proven error margin of the top-(k-1) boundary (default; used when the
- * longest sequence has at most 256 blocks); 1 = all scores on the CUDA cores.
- * Both select exactly the same blocks.  MOBA_ERR_INVALID_ARG otherwise. */
-int moba_set_gate_kernel(int kind);
-
-/* Pooling of each block's keys into the representative the gate scores
- * against (process-wide, not thread-safe; applies to moba_kpool* and to the
- * forward entry points): MOBA_POOL_MEAN (default) = the mean of the block's
- * keys ("Moonshot MoBA paper explained" §3.1 mean_pool; "MOBA mixture of block
- * attention for server-side long context" §3); MOBA_POOL_MAX = their
- * element-wise maximum, the variant the latter page allows (more sensitive to
- * blocks holding a few strongly matching keys).  MOBA_ERR_INVALID_ARG for any
- * other value. */
-enum { MOBA_POOL_MEAN = 0, MOBA_POOL_MAX = 1 };
-int moba_set_pooling(int kind);
 
 /*
  * Decode: one new query token per sequence against its KV cache.  The step
@@ -304,15 +375,9 @@ int moba_decode_fwd_ws(const void *q, const void *k_cache, const void *v_cache,
                        int32_t *idx, int B, int H, int S_max, int D, int block_size, int topk,
                        void *workspace, size_t workspace_bytes, void *stream);
 
-/* Test hooks of the bounded waits in the tcgen05 kernels (process-wide):
- * wait_limit_cycles is the clock64 budget of one mbarrier wait (<= 0 restores
- * the default, about 2 s); flags bit 0 makes the K/V producer skip its first
- * load so that the consumer's wait runs out and MOBA_ERR_TIMEOUT is recorded
- * (read it with moba_get_status) instead of hanging the GPU. */
-int moba_debug_set(int flags, long long wait_limit_cycles);
-
-/* Where the timeout reported by the last moba_get_status happened: out4 =
- * {barrier shared-memory address, parity, block index, thread index}. */
+/* Where the timeout reported by the calling thread's last moba_get_status
+ * happened: out4 = {barrier shared-memory address, parity, block index, thread
+ * index}. */
 void moba_debug_timeout_info(int *out4);
 
 #ifdef __cplusplus

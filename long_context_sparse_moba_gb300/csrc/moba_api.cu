@@ -18,36 +18,31 @@ namespace moba {
 __device__ int g_moba_status[8];
 
 int *status_word() {
-    static int *addr[64] = {nullptr};
+    static std::atomic<int *> addr[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    if (!addr[dev]) {
+    int *a = addr[dev].load(std::memory_order_relaxed);
+    if (!a) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_moba_status) != cudaSuccess) return nullptr;
-        addr[dev] = static_cast<int *>(p);
+        a = static_cast<int *>(p);
+        addr[dev].store(a, std::memory_order_relaxed);
     }
-    return addr[dev];
+    return a;
 }
 
 static std::atomic<unsigned long long> g_launches{0};
 
-// attention implementation: 0 = tcgen05 / TMEM / TMA, 1 = warp-level mma.sync
-static int g_attn_kind = 0;
-// gate implementation: 0 = tcgen05 scores + exact candidates, 1 = CUDA cores
-static int g_gate_kind = 0;
-// key pooling per block: 0 = mean, 1 = element-wise max
-static int g_pool_kind = 0;
-int pooling_kind() { return g_pool_kind; }
-int past_tile_rows() { return g_attn_kind == 0 ? tc_tile_rows() : mma_tile_rows(); }
+int past_tile_rows(const Plan &p) { return p.attn_kind == 0 ? tc_tile_rows() : mma_tile_rows(); }
 cudaError_t launch_attn_past(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
                              const __nv_bfloat16 *k, const __nv_bfloat16 *v, cudaStream_t st) {
-    return g_attn_kind == 0 ? launch_attn_past_tc(p, ws, q, k, v, st)
+    return p.attn_kind == 0 ? launch_attn_past_tc(p, ws, q, k, v, st)
                             : launch_attn_past_mma(p, ws, q, k, v, st);
 }
 cudaError_t launch_attn_current(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
                                 const __nv_bfloat16 *k, const __nv_bfloat16 *v,
                                 __nv_bfloat16 *out, float *lse, cudaStream_t st) {
-    return g_attn_kind == 0 ? launch_attn_current_tc(p, ws, q, k, v, out, lse, st)
+    return p.attn_kind == 0 ? launch_attn_current_tc(p, ws, q, k, v, out, lse, st)
                             : launch_attn_current_mma(p, ws, q, k, v, out, lse, st);
 }
 void note_launches(int n) { g_launches.fetch_add((unsigned long long)n); }
@@ -65,21 +60,23 @@ int sm_count() {
     return n;
 }
 
-// Optional phase timing: CUDA events recorded on the caller's stream between
-// the phases of each forward call (setup, kpool, gate, regroup, attention
-// over past blocks, attention over the own block + merge).
+// Optional phase timing: the caller's CUDA events, recorded on the call's
+// stream between the phases of a forward call (set-up, kpool, gate, regroup,
+// attention over past blocks, attention over the own block + merge).
 constexpr int kPhases = 6;
-struct Profiler {
-    bool on = false;
-    int used = 0;
-    std::vector<cudaEvent_t> ev;  // (kPhases + 1) per recorded call
-} g_prof;
 
-static void prof_mark(int call, int phase, cudaStream_t st) {
-    if (call >= 0) cudaEventRecord(g_prof.ev[(size_t)call * (kPhases + 1) + phase], st);
+static void prof_mark(void *const *events, int phase, cudaStream_t st) {
+    if (events && events[phase]) cudaEventRecord(static_cast<cudaEvent_t>(events[phase]), st);
 }
 
 static inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// The job table is sized for the smaller tile of the two attention kernels, so
+// that the workspace size does not depend on the per-call kernel choice.
+static size_t job_rows_min() {
+    const int a = tc_tile_rows(), b = mma_tile_rows();
+    return (size_t)(a < b ? a : b);
+}
 
 size_t workspace_bytes(const Plan &p, Workspace *ws, char *base, bool backward) {
     size_t off = 0;
@@ -93,6 +90,7 @@ size_t workspace_bytes(const Plan &p, Workspace *ws, char *base, bool backward) 
     w.cu = static_cast<int *>(take(sizeof(int) * (p.num_seqs + 1)));
     w.blk_base = static_cast<int *>(take(sizeof(int) * (p.num_seqs + 1)));
     w.gtile = static_cast<int *>(take(sizeof(int) * (p.num_seqs + 1)));
+    w.bad = static_cast<int *>(take(sizeof(int)));
     const bool gate = !p.dense && p.km1 > 0;
     if (gate) {
         const size_t N = (size_t)p.NBcap * p.H;
@@ -105,7 +103,7 @@ size_t workspace_bytes(const Plan &p, Workspace *ws, char *base, bool backward) 
         w.list_off = static_cast<int *>(take(sizeof(int) * (N + 1)));
         w.tile_off = static_cast<int *>(take(sizeof(int) * (N + 1)));
         w.job_list = static_cast<int *>(
-            take(sizeof(int) * (rows * p.km1 / (size_t)past_tile_rows() + N + 1)));
+            take(sizeof(int) * (rows * p.km1 / (size_t)job_rows_min() + N + 1)));
         w.kbhi = static_cast<__nv_bfloat16 *>(take(sizeof(__nv_bfloat16) * N * p.D));
         w.kblo = static_cast<__nv_bfloat16 *>(take(sizeof(__nv_bfloat16) * N * p.D));
         w.knorm = static_cast<float *>(take(sizeof(float) * N));
@@ -144,6 +142,11 @@ static int make_plan(int num_seqs, long long total, int max_len, int H, int D, i
     p->bs = bs;
     p->topk = topk;
     p->fixed = fixed;
+    p->pool = MOBA_POOL_MEAN;
+    p->gate_kind = MOBA_GATE_TENSOR_CORES;
+    p->attn_kind = MOBA_ATTN_TCGEN05;
+    p->debug_flags = 0;
+    p->wait_limit = kDefaultWaitLimit;
     p->dense = topk >= n_max;
     p->km1 = p->dense ? 0 : topk - 1;
     const long long nbcap = fixed ? (long long)num_seqs * n_max : total / bs + num_seqs;
@@ -151,6 +154,23 @@ static int make_plan(int num_seqs, long long total, int max_len, int H, int D, i
     p->NBcap = (int)nbcap;
     if (!p->dense && p->km1 > kMaxPastSlots) return MOBA_ERR_UNSUPPORTED;
     if (total * H * (long long)(p->km1 > 0 ? p->km1 : 1) >= (1ll << 31)) return MOBA_ERR_UNSUPPORTED;
+    return MOBA_OK;
+}
+
+// Copies the caller's per-call options into the plan (NULL = defaults).
+static int apply_options(const moba_options_t *o, Plan *p) {
+    if (!o) return MOBA_OK;
+    if (o->pooling != MOBA_POOL_MEAN && o->pooling != MOBA_POOL_MAX) return MOBA_ERR_INVALID_ARG;
+    if (o->gate_kernel != MOBA_GATE_TENSOR_CORES && o->gate_kernel != MOBA_GATE_CUDA_CORES)
+        return MOBA_ERR_INVALID_ARG;
+    if (o->attn_kernel != MOBA_ATTN_TCGEN05 && o->attn_kernel != MOBA_ATTN_MMA_SYNC)
+        return MOBA_ERR_INVALID_ARG;
+    if (o->debug_flags < 0) return MOBA_ERR_INVALID_ARG;
+    p->pool = o->pooling;
+    p->gate_kind = o->gate_kernel;
+    p->attn_kind = o->attn_kernel;
+    p->debug_flags = o->debug_flags;
+    p->wait_limit = o->wait_limit_cycles > 0 ? o->wait_limit_cycles : kDefaultWaitLimit;
     return MOBA_OK;
 }
 
@@ -169,7 +189,7 @@ static thread_local cudaError_t g_last_cuda_error = cudaSuccess;
 
 static int run_forward(const Plan &p, const int *cu_dev, const void *q, const void *k,
                        const void *v, void *out, float *lse, void *workspace, size_t ws_bytes,
-                       cudaStream_t st) {
+                       const moba_options_t *opt, cudaStream_t st) {
     Workspace ws;
     const size_t need = workspace_bytes(p, &ws, static_cast<char *>(workspace));
     if (!workspace || ws_bytes < need) return MOBA_ERR_WORKSPACE;
@@ -177,16 +197,17 @@ static int run_forward(const Plan &p, const int *cu_dev, const void *q, const vo
     const auto *qb = static_cast<const __nv_bfloat16 *>(q);
     const auto *kb = static_cast<const __nv_bfloat16 *>(k);
     const auto *vb = static_cast<const __nv_bfloat16 *>(v);
-    int call = -1;
-    if (g_prof.on && (size_t)(g_prof.used + 1) * (kPhases + 1) <= g_prof.ev.size())
-        call = g_prof.used++;
-    prof_mark(call, 0, st);
+    void *const *ev = opt ? opt->phase_events : nullptr;
+    int32_t *idx_out = opt ? opt->idx_out : nullptr;
+    prof_mark(ev, 0, st);
     MOBA_TRY(launch_setup(p, cu_dev, ws, st));
-    prof_mark(call, 1, st);
+    prof_mark(ev, 1, st);
     const bool gate = !p.dense && p.km1 > 0;
+    // the selection goes straight to the caller's buffer when one is given
+    if (gate && idx_out) ws.idx = idx_out;
     if (gate) MOBA_TRY(launch_kpool(p, ws, kb, ws.kbar, st));
-    prof_mark(call, 2, st);
-    const bool tc_gate = g_gate_kind == 0 && gate_tc_supported(p);
+    prof_mark(ev, 2, st);
+    const bool tc_gate = p.gate_kind == MOBA_GATE_TENSOR_CORES && gate_tc_supported(p);
     if (gate) {
         // the per-list counts and the exact kernel's row count
         MOBA_TRY(cudaMemsetAsync(ws.counts, 0, sizeof(int) * ((size_t)p.NBcap * p.H + 1), st));
@@ -197,14 +218,16 @@ static int run_forward(const Plan &p, const int *cu_dev, const void *q, const vo
         } else {
             MOBA_TRY(launch_gate(p, ws, qb, ws.kbar, ws.idx, st));
         }
+    } else if (idx_out) {
+        MOBA_TRY(launch_fill_idx(p, ws, idx_out, st));
     }
-    prof_mark(call, 3, st);
+    prof_mark(ev, 3, st);
     if (gate) MOBA_TRY(launch_regroup(p, ws, tc_gate, st));
-    prof_mark(call, 4, st);
+    prof_mark(ev, 4, st);
     MOBA_TRY(launch_attn_past(p, ws, qb, kb, vb, st));
-    prof_mark(call, 5, st);
+    prof_mark(ev, 5, st);
     MOBA_TRY(launch_attn_current(p, ws, qb, kb, vb, static_cast<__nv_bfloat16 *>(out), lse, st));
-    prof_mark(call, 6, st);
+    prof_mark(ev, 6, st);
     return MOBA_OK;
 }
 
@@ -222,7 +245,7 @@ static int run_backward(const Plan &p, const int *cu_dev, const void *q, const v
     const auto *kb = static_cast<const __nv_bfloat16 *>(k);
     MOBA_TRY(launch_setup(p, cu_dev, ws, st));
     const bool gate = !p.dense && p.km1 > 0;
-    const bool tc_gate = g_gate_kind == 0 && gate_tc_supported(p);
+    const bool tc_gate = p.gate_kind == MOBA_GATE_TENSOR_CORES && gate_tc_supported(p);
     if (gate) {
         MOBA_TRY(launch_kpool(p, ws, kb, ws.kbar, st));
         MOBA_TRY(cudaMemsetAsync(ws.counts, 0, sizeof(int) * ((size_t)p.NBcap * p.H + 1), st));
@@ -259,10 +282,11 @@ static int with_tables(const Plan &p, const int *cu_dev, cudaStream_t st,
     std::memset(&ws, 0, sizeof ws);
     const size_t one = align256(sizeof(int) * (p.num_seqs + 1));
     void *mem = nullptr;
-    if (cudaMallocAsync(&mem, 3 * one, st) != cudaSuccess) return MOBA_ERR_CUDA;
+    if (cudaMallocAsync(&mem, 3 * one + 256, st) != cudaSuccess) return MOBA_ERR_CUDA;
     ws.cu = static_cast<int *>(mem);
     ws.blk_base = reinterpret_cast<int *>(static_cast<char *>(mem) + one);
     ws.gtile = reinterpret_cast<int *>(static_cast<char *>(mem) + 2 * one);
+    ws.bad = reinterpret_cast<int *>(static_cast<char *>(mem) + 3 * one);
     int rc = cuda_status(launch_setup(p, cu_dev, ws, st));
     if (rc == MOBA_OK) rc = body(p, ws, ctx);
     if (cudaFreeAsync(mem, st) != cudaSuccess && rc == MOBA_OK) rc = MOBA_ERR_CUDA;
@@ -289,7 +313,7 @@ static int pool_run(const Plan &p, Workspace &ws, void *c) {
 static int gate_run(const Plan &p, Workspace &ws, void *c) {
     auto *x = static_cast<GateCtx *>(c);
     const auto *q = static_cast<const __nv_bfloat16 *>(x->q);
-    if (g_gate_kind != 0 || !gate_tc_supported(p))
+    if (p.gate_kind != MOBA_GATE_TENSOR_CORES || !gate_tc_supported(p))
         return cuda_status(launch_gate(p, ws, q, x->kbar, x->idx, x->st));
     // stream-ordered scratch: the bf16 split of the caller's kbar, the norms,
     // and the rows left to the exact kernel
@@ -336,58 +360,95 @@ MOBA_EXPORT const char *moba_status_string(int code) {
     }
 }
 
-MOBA_EXPORT int moba_kpool(const void *k, float *kbar, int B, int H, int S, int D, int block_size,
-                           void *stream) {
+
+// ---------------------------------------------------------------------------
+// pooling and gate entry points
+// ---------------------------------------------------------------------------
+MOBA_EXPORT int moba_kpool_ex(const void *k, float *kbar, int B, int H, int S, int D,
+                              int block_size, const moba_options_t *opt, void *stream) {
     if (!k || !kbar) return MOBA_ERR_INVALID_ARG;
     Plan p;
     int rc = make_plan(B, (long long)B * S, S, H, D, block_size, 1, true, &p);
-    if (rc) return rc;
+    if (rc || (rc = apply_options(opt, &p))) return rc;
     if (misaligned(k) || misaligned(kbar)) return MOBA_ERR_INVALID_ARG;
     PoolCtx c{k, kbar, static_cast<cudaStream_t>(stream)};
     return with_tables(p, nullptr, c.st, pool_run, &c);
 }
 
-MOBA_EXPORT int moba_kpool_varlen(const void *k, float *kbar, const int32_t *cu_seqlens,
-                                  int num_seqs, int total_tokens, int H, int D, int block_size,
-                                  void *stream) {
+MOBA_EXPORT int moba_kpool(const void *k, float *kbar, int B, int H, int S, int D, int block_size,
+                           void *stream) {
+    return moba_kpool_ex(k, kbar, B, H, S, D, block_size, nullptr, stream);
+}
+
+MOBA_EXPORT int moba_kpool_varlen_ex(const void *k, float *kbar, const int32_t *cu_seqlens,
+                                     int num_seqs, int total_tokens, int H, int D, int block_size,
+                                     const moba_options_t *opt, void *stream) {
     if (!k || !kbar || !cu_seqlens) return MOBA_ERR_INVALID_ARG;
     Plan p;
     int rc = make_plan(num_seqs, total_tokens, total_tokens, H, D, block_size, 1, false, &p);
-    if (rc) return rc;
+    if (rc || (rc = apply_options(opt, &p))) return rc;
     if (misaligned(k) || misaligned(kbar)) return MOBA_ERR_INVALID_ARG;
     PoolCtx c{k, kbar, static_cast<cudaStream_t>(stream)};
     return with_tables(p, cu_seqlens, c.st, pool_run, &c);
 }
 
-MOBA_EXPORT int moba_gate_topk(const void *q, const float *kbar, int32_t *idx, int B, int H, int S,
-                               int D, int block_size, int topk, void *stream) {
+MOBA_EXPORT int moba_kpool_varlen(const void *k, float *kbar, const int32_t *cu_seqlens,
+                                  int num_seqs, int total_tokens, int H, int D, int block_size,
+                                  void *stream) {
+    return moba_kpool_varlen_ex(k, kbar, cu_seqlens, num_seqs, total_tokens, H, D, block_size,
+                                nullptr, stream);
+}
+
+MOBA_EXPORT int moba_gate_topk_ex(const void *q, const float *kbar, int32_t *idx, int B, int H,
+                                  int S, int D, int block_size, int topk,
+                                  const moba_options_t *opt, void *stream) {
     if (!q || !kbar || !idx) return MOBA_ERR_INVALID_ARG;
     Plan p;
     int rc = make_plan(B, (long long)B * S, S, H, D, block_size, topk, true, &p);
-    if (rc) return rc;
+    if (rc || (rc = apply_options(opt, &p))) return rc;
     if (topk - 1 > kMaxPastSlots && !p.dense) return MOBA_ERR_UNSUPPORTED;
     if (misaligned(q) || misaligned(kbar)) return MOBA_ERR_INVALID_ARG;
     GateCtx c{q, kbar, idx, static_cast<cudaStream_t>(stream)};
     return with_tables(p, nullptr, c.st, gate_run, &c);
 }
 
-MOBA_EXPORT int moba_gate_topk_varlen(const void *q, const float *kbar, int32_t *idx,
-                                      const int32_t *cu_seqlens, int num_seqs, int total_tokens,
-                                      int H, int D, int block_size, int topk, void *stream) {
+MOBA_EXPORT int moba_gate_topk(const void *q, const float *kbar, int32_t *idx, int B, int H, int S,
+                               int D, int block_size, int topk, void *stream) {
+    return moba_gate_topk_ex(q, kbar, idx, B, H, S, D, block_size, topk, nullptr, stream);
+}
+
+MOBA_EXPORT int moba_gate_topk_varlen_ex(const void *q, const float *kbar, int32_t *idx,
+                                         const int32_t *cu_seqlens, int num_seqs,
+                                         int total_tokens, int H, int D, int block_size, int topk,
+                                         const moba_options_t *opt, void *stream) {
     if (!q || !kbar || !idx || !cu_seqlens) return MOBA_ERR_INVALID_ARG;
     Plan p;
     int rc = make_plan(num_seqs, total_tokens, total_tokens, H, D, block_size, topk, false, &p);
-    if (rc) return rc;
+    if (rc || (rc = apply_options(opt, &p))) return rc;
     if (misaligned(q) || misaligned(kbar)) return MOBA_ERR_INVALID_ARG;
     GateCtx c{q, kbar, idx, static_cast<cudaStream_t>(stream)};
     return with_tables(p, cu_seqlens, c.st, gate_run, &c);
 }
 
+MOBA_EXPORT int moba_gate_topk_varlen(const void *q, const float *kbar, int32_t *idx,
+                                      const int32_t *cu_seqlens, int num_seqs, int total_tokens,
+                                      int H, int D, int block_size, int topk, void *stream) {
+    return moba_gate_topk_varlen_ex(q, kbar, idx, cu_seqlens, num_seqs, total_tokens, H, D,
+                                    block_size, topk, nullptr, stream);
+}
+
+// ---------------------------------------------------------------------------
+// forward entry points
+// ---------------------------------------------------------------------------
 MOBA_EXPORT size_t moba_attn_fwd_workspace_size(int B, int H, int S, int D, int block_size,
                                                 int topk) {
     Plan p;
     if (make_plan(B, (long long)B * S, S, H, D, block_size, topk, true, &p)) return 0;
     return workspace_bytes(p, nullptr, nullptr);
+}
+
+MOBA_EXPORT size_t moba_workspace_size(int B, int H, int S, int D, int block_size, int topk) {
+    return moba_attn_fwd_workspace_size(B, H, S, D, block_size, topk);
 }
 
 MOBA_EXPORT size_t moba_attn_fwd_varlen_workspace_size(int num_seqs, int total_tokens,
@@ -406,32 +467,66 @@ static int check_tensors(const void *q, const void *k, const void *v, const void
     return MOBA_OK;
 }
 
+static int check_options_buffers(const moba_options_t *opt) {
+    if (opt && opt->idx_out && (reinterpret_cast<uintptr_t>(opt->idx_out) & 3))
+        return MOBA_ERR_INVALID_ARG;
+    return MOBA_OK;
+}
+
+// Runs the forward in the caller's workspace, or in scratch taken from
+// cudaMallocAsync on the stream and released on it afterwards.
+static int forward_any(const Plan &p, const int *cu, const void *q, const void *k, const void *v,
+                       void *out, float *lse, const moba_options_t *opt, void *workspace,
+                       size_t ws_bytes, cudaStream_t st) {
+    if (workspace) return run_forward(p, cu, q, k, v, out, lse, workspace, ws_bytes, opt, st);
+    const size_t bytes = workspace_bytes(p, nullptr, nullptr);
+    void *ws = nullptr;
+    if (cudaMallocAsync(&ws, bytes, st) != cudaSuccess) return MOBA_ERR_CUDA;
+    int rc = run_forward(p, cu, q, k, v, out, lse, ws, bytes, opt, st);
+    if (cudaFreeAsync(ws, st) != cudaSuccess && rc == MOBA_OK) rc = MOBA_ERR_CUDA;
+    return rc;
+}
+
+MOBA_EXPORT int moba_attn_fwd_ex(const void *q, const void *k, const void *v, void *out,
+                                 float *lse, int B, int H, int S, int D, int block_size, int topk,
+                                 const moba_options_t *opt, void *workspace,
+                                 size_t workspace_bytes_, void *stream) {
+    int rc = check_tensors(q, k, v, out, lse);
+    if (rc || (rc = check_options_buffers(opt))) return rc;
+    Plan p;
+    rc = make_plan(B, (long long)B * S, S, H, D, block_size, topk, true, &p);
+    if (rc || (rc = apply_options(opt, &p))) return rc;
+    return forward_any(p, nullptr, q, k, v, out, lse, opt, workspace, workspace_bytes_,
+                       static_cast<cudaStream_t>(stream));
+}
+
 MOBA_EXPORT int moba_attn_fwd_ws(const void *q, const void *k, const void *v, void *out,
                                  float *lse, int B, int H, int S, int D, int block_size, int topk,
                                  void *workspace, size_t workspace_bytes_, void *stream) {
-    int rc = check_tensors(q, k, v, out, lse);
-    if (rc) return rc;
-    Plan p;
-    rc = make_plan(B, (long long)B * S, S, H, D, block_size, topk, true, &p);
-    if (rc) return rc;
-    return run_forward(p, nullptr, q, k, v, out, lse, workspace, workspace_bytes_,
-                       static_cast<cudaStream_t>(stream));
+    if (!workspace) return MOBA_ERR_WORKSPACE;
+    return moba_attn_fwd_ex(q, k, v, out, lse, B, H, S, D, block_size, topk, nullptr, workspace,
+                            workspace_bytes_, stream);
 }
 
 MOBA_EXPORT int moba_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse,
                               int B, int H, int S, int D, int block_size, int topk, void *stream) {
+    return moba_attn_fwd_ex(q, k, v, out, lse, B, H, S, D, block_size, topk, nullptr, nullptr, 0,
+                            stream);
+}
+
+MOBA_EXPORT int moba_attn_fwd_varlen_ex(const void *q, const void *k, const void *v, void *out,
+                                        float *lse, const int32_t *cu_seqlens, int num_seqs,
+                                        int total_tokens, int max_seqlen, int H, int D,
+                                        int block_size, int topk, const moba_options_t *opt,
+                                        void *workspace, size_t workspace_bytes_, void *stream) {
     int rc = check_tensors(q, k, v, out, lse);
-    if (rc) return rc;
+    if (rc || (rc = check_options_buffers(opt))) return rc;
+    if (!cu_seqlens) return MOBA_ERR_INVALID_ARG;
     Plan p;
-    rc = make_plan(B, (long long)B * S, S, H, D, block_size, topk, true, &p);
-    if (rc) return rc;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const size_t bytes = workspace_bytes(p, nullptr, nullptr);
-    void *ws = nullptr;
-    if (cudaMallocAsync(&ws, bytes, st) != cudaSuccess) return MOBA_ERR_CUDA;
-    rc = run_forward(p, nullptr, q, k, v, out, lse, ws, bytes, st);
-    if (cudaFreeAsync(ws, st) != cudaSuccess && rc == MOBA_OK) rc = MOBA_ERR_CUDA;
-    return rc;
+    rc = make_plan(num_seqs, total_tokens, max_seqlen, H, D, block_size, topk, false, &p);
+    if (rc || (rc = apply_options(opt, &p))) return rc;
+    return forward_any(p, cu_seqlens, q, k, v, out, lse, opt, workspace, workspace_bytes_,
+                       static_cast<cudaStream_t>(stream));
 }
 
 MOBA_EXPORT int moba_attn_fwd_varlen_ws(const void *q, const void *k, const void *v, void *out,
@@ -439,35 +534,23 @@ MOBA_EXPORT int moba_attn_fwd_varlen_ws(const void *q, const void *k, const void
                                         int total_tokens, int max_seqlen, int H, int D,
                                         int block_size, int topk, void *workspace,
                                         size_t workspace_bytes_, void *stream) {
-    int rc = check_tensors(q, k, v, out, lse);
-    if (rc) return rc;
-    if (!cu_seqlens) return MOBA_ERR_INVALID_ARG;
-    Plan p;
-    rc = make_plan(num_seqs, total_tokens, max_seqlen, H, D, block_size, topk, false, &p);
-    if (rc) return rc;
-    return run_forward(p, cu_seqlens, q, k, v, out, lse, workspace, workspace_bytes_,
-                       static_cast<cudaStream_t>(stream));
+    if (!workspace) return MOBA_ERR_WORKSPACE;
+    return moba_attn_fwd_varlen_ex(q, k, v, out, lse, cu_seqlens, num_seqs, total_tokens,
+                                   max_seqlen, H, D, block_size, topk, nullptr, workspace,
+                                   workspace_bytes_, stream);
 }
 
 MOBA_EXPORT int moba_attn_fwd_varlen(const void *q, const void *k, const void *v, void *out,
                                      float *lse, const int32_t *cu_seqlens, int num_seqs,
                                      int total_tokens, int max_seqlen, int H, int D,
                                      int block_size, int topk, void *stream) {
-    int rc = check_tensors(q, k, v, out, lse);
-    if (rc) return rc;
-    if (!cu_seqlens) return MOBA_ERR_INVALID_ARG;
-    Plan p;
-    rc = make_plan(num_seqs, total_tokens, max_seqlen, H, D, block_size, topk, false, &p);
-    if (rc) return rc;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const size_t bytes = workspace_bytes(p, nullptr, nullptr);
-    void *ws = nullptr;
-    if (cudaMallocAsync(&ws, bytes, st) != cudaSuccess) return MOBA_ERR_CUDA;
-    rc = run_forward(p, cu_seqlens, q, k, v, out, lse, ws, bytes, st);
-    if (cudaFreeAsync(ws, st) != cudaSuccess && rc == MOBA_OK) rc = MOBA_ERR_CUDA;
-    return rc;
+    return moba_attn_fwd_varlen_ex(q, k, v, out, lse, cu_seqlens, num_seqs, total_tokens,
+                                   max_seqlen, H, D, block_size, topk, nullptr, nullptr, 0, stream);
 }
 
+// ---------------------------------------------------------------------------
+// backward entry points
+// ---------------------------------------------------------------------------
 static int check_bwd_tensors(const void *q, const void *k, const void *v, const void *out,
                              const float *lse, const void *dout, const void *dq, const void *dk,
                              const void *dv) {
@@ -494,22 +577,11 @@ MOBA_EXPORT size_t moba_attn_bwd_varlen_workspace_size(int num_seqs, int total_t
     return workspace_bytes(p, nullptr, nullptr, true);
 }
 
-MOBA_EXPORT int moba_attn_bwd_ws(const void *q, const void *k, const void *v, const void *out,
-                                 const float *lse, const void *dout, void *dq, void *dk, void *dv,
-                                 int B, int H, int S, int D, int block_size, int topk,
-                                 void *workspace, size_t workspace_bytes_, void *stream) {
-    int rc = check_bwd_tensors(q, k, v, out, lse, dout, dq, dk, dv);
-    if (rc) return rc;
-    Plan p;
-    rc = make_plan(B, (long long)B * S, S, H, D, block_size, topk, true, &p);
-    if (rc) return rc;
-    return run_backward(p, nullptr, q, k, v, out, lse, dout, dq, dk, dv, workspace,
-                        workspace_bytes_, static_cast<cudaStream_t>(stream));
-}
-
-static int bwd_alloc_run(const Plan &p, const int *cu, const void *q, const void *k, const void *v,
-                         const void *out, const float *lse, const void *dout, void *dq, void *dk,
-                         void *dv, cudaStream_t st) {
+static int backward_any(const Plan &p, const int *cu, const void *q, const void *k, const void *v,
+                        const void *out, const float *lse, const void *dout, void *dq, void *dk,
+                        void *dv, void *workspace, size_t ws_bytes, cudaStream_t st) {
+    if (workspace)
+        return run_backward(p, cu, q, k, v, out, lse, dout, dq, dk, dv, workspace, ws_bytes, st);
     const size_t bytes = workspace_bytes(p, nullptr, nullptr, true);
     void *ws = nullptr;
     if (cudaMallocAsync(&ws, bytes, st) != cudaSuccess) return MOBA_ERR_CUDA;
@@ -518,16 +590,51 @@ static int bwd_alloc_run(const Plan &p, const int *cu, const void *q, const void
     return rc;
 }
 
-MOBA_EXPORT int moba_attn_bwd(const void *q, const void *k, const void *v, const void *out,
-                              const float *lse, const void *dout, void *dq, void *dk, void *dv,
-                              int B, int H, int S, int D, int block_size, int topk, void *stream) {
+MOBA_EXPORT int moba_attn_bwd_ex(const void *q, const void *k, const void *v, const void *out,
+                                 const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                                 int B, int H, int S, int D, int block_size, int topk,
+                                 const moba_options_t *opt, void *workspace,
+                                 size_t workspace_bytes_, void *stream) {
     int rc = check_bwd_tensors(q, k, v, out, lse, dout, dq, dk, dv);
     if (rc) return rc;
     Plan p;
     rc = make_plan(B, (long long)B * S, S, H, D, block_size, topk, true, &p);
+    if (rc || (rc = apply_options(opt, &p))) return rc;
+    return backward_any(p, nullptr, q, k, v, out, lse, dout, dq, dk, dv, workspace,
+                        workspace_bytes_, static_cast<cudaStream_t>(stream));
+}
+
+MOBA_EXPORT int moba_attn_bwd_ws(const void *q, const void *k, const void *v, const void *out,
+                                 const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                                 int B, int H, int S, int D, int block_size, int topk,
+                                 void *workspace, size_t workspace_bytes_, void *stream) {
+    if (!workspace) return MOBA_ERR_WORKSPACE;
+    return moba_attn_bwd_ex(q, k, v, out, lse, dout, dq, dk, dv, B, H, S, D, block_size, topk,
+                            nullptr, workspace, workspace_bytes_, stream);
+}
+
+MOBA_EXPORT int moba_attn_bwd(const void *q, const void *k, const void *v, const void *out,
+                              const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                              int B, int H, int S, int D, int block_size, int topk, void *stream) {
+    return moba_attn_bwd_ex(q, k, v, out, lse, dout, dq, dk, dv, B, H, S, D, block_size, topk,
+                            nullptr, nullptr, 0, stream);
+}
+
+MOBA_EXPORT int moba_attn_bwd_varlen_ex(const void *q, const void *k, const void *v,
+                                        const void *out, const float *lse, const void *dout,
+                                        void *dq, void *dk, void *dv, const int32_t *cu_seqlens,
+                                        int num_seqs, int total_tokens, int max_seqlen, int H,
+                                        int D, int block_size, int topk,
+                                        const moba_options_t *opt, void *workspace,
+                                        size_t workspace_bytes_, void *stream) {
+    int rc = check_bwd_tensors(q, k, v, out, lse, dout, dq, dk, dv);
     if (rc) return rc;
-    return bwd_alloc_run(p, nullptr, q, k, v, out, lse, dout, dq, dk, dv,
-                         static_cast<cudaStream_t>(stream));
+    if (!cu_seqlens) return MOBA_ERR_INVALID_ARG;
+    Plan p;
+    rc = make_plan(num_seqs, total_tokens, max_seqlen, H, D, block_size, topk, false, &p);
+    if (rc || (rc = apply_options(opt, &p))) return rc;
+    return backward_any(p, cu_seqlens, q, k, v, out, lse, dout, dq, dk, dv, workspace,
+                        workspace_bytes_, static_cast<cudaStream_t>(stream));
 }
 
 MOBA_EXPORT int moba_attn_bwd_varlen(const void *q, const void *k, const void *v, const void *out,
@@ -535,17 +642,15 @@ MOBA_EXPORT int moba_attn_bwd_varlen(const void *q, const void *k, const void *v
                                      void *dv, const int32_t *cu_seqlens, int num_seqs,
                                      int total_tokens, int max_seqlen, int H, int D,
                                      int block_size, int topk, void *stream) {
-    int rc = check_bwd_tensors(q, k, v, out, lse, dout, dq, dk, dv);
-    if (rc) return rc;
-    if (!cu_seqlens) return MOBA_ERR_INVALID_ARG;
-    Plan p;
-    rc = make_plan(num_seqs, total_tokens, max_seqlen, H, D, block_size, topk, false, &p);
-    if (rc) return rc;
-    return bwd_alloc_run(p, cu_seqlens, q, k, v, out, lse, dout, dq, dk, dv,
-                         static_cast<cudaStream_t>(stream));
+    return moba_attn_bwd_varlen_ex(q, k, v, out, lse, dout, dq, dk, dv, cu_seqlens, num_seqs,
+                                   total_tokens, max_seqlen, H, D, block_size, topk, nullptr,
+                                   nullptr, 0, stream);
 }
 
-static int g_last_timeout[4] = {0, 0, 0, 0};
+// ---------------------------------------------------------------------------
+// status, tally
+// ---------------------------------------------------------------------------
+static thread_local int g_last_timeout[4] = {0, 0, 0, 0};
 
 MOBA_EXPORT void moba_debug_timeout_info(int *out4) {
     if (out4)
@@ -565,47 +670,9 @@ MOBA_EXPORT int moba_get_status(void *stream) {
 
 MOBA_EXPORT unsigned long long moba_launch_count(void) { return g_launches.load(); }
 
-MOBA_EXPORT int moba_profile_begin(int max_calls) {
-    if (max_calls < 1) return MOBA_ERR_INVALID_ARG;
-    const size_t need = (size_t)max_calls * (kPhases + 1);
-    while (g_prof.ev.size() < need) {
-        cudaEvent_t e;
-        if (cudaEventCreate(&e) != cudaSuccess) return MOBA_ERR_CUDA;
-        g_prof.ev.push_back(e);
-    }
-    g_prof.used = 0;
-    g_prof.on = true;
-    return MOBA_OK;
-}
-
-MOBA_EXPORT int moba_profile_end(float *phase_ms, int n_phases) {
-    g_prof.on = false;
-    if (!phase_ms || n_phases < kPhases) return -MOBA_ERR_INVALID_ARG;
-    for (int i = 0; i < kPhases; ++i) phase_ms[i] = 0.f;
-    for (int c = 0; c < g_prof.used; ++c) {
-        cudaEvent_t *e = &g_prof.ev[(size_t)c * (kPhases + 1)];
-        if (cudaEventSynchronize(e[kPhases]) != cudaSuccess) return -MOBA_ERR_CUDA;
-        for (int i = 0; i < kPhases; ++i) {
-            float ms = 0.f;
-            if (cudaEventElapsedTime(&ms, e[i], e[i + 1]) != cudaSuccess) return -MOBA_ERR_CUDA;
-            phase_ms[i] += ms;
-        }
-    }
-    return g_prof.used;
-}
-
-MOBA_EXPORT int moba_set_attention_kernel(int kind) {
-    if (kind != 0 && kind != 1) return MOBA_ERR_INVALID_ARG;
-    g_attn_kind = kind;
-    return MOBA_OK;
-}
-
-MOBA_EXPORT int moba_set_gate_kernel(int kind) {
-    if (kind != 0 && kind != 1) return MOBA_ERR_INVALID_ARG;
-    g_gate_kind = kind;
-    return MOBA_OK;
-}
-
+// ---------------------------------------------------------------------------
+// decode
+// ---------------------------------------------------------------------------
 static int decode_check(const void *q, const void *k, const void *v, const float *kbar,
                         const int32_t *lens, const void *out, const float *lse, int B, int H,
                         int S_max, int D, int bs, int topk) {
@@ -664,18 +731,6 @@ MOBA_EXPORT int moba_decode_fwd(const void *q, const void *k_cache, const void *
     return rc;
 }
 
-MOBA_EXPORT int moba_set_pooling(int kind) {
-    if (kind != MOBA_POOL_MEAN && kind != MOBA_POOL_MAX) return MOBA_ERR_INVALID_ARG;
-    g_pool_kind = kind;
-    return MOBA_OK;
-}
-
-MOBA_EXPORT int moba_debug_set(int flags, long long wait_limit_cycles) {
-    if (flags < 0) return MOBA_ERR_INVALID_ARG;
-    tc_debug_set(flags, wait_limit_cycles);
-    return MOBA_OK;
-}
-
 // ---------------------------------------------------------------------------
 // Forward pass that allocates nothing.  Its scratch lives in one file-scope
 // device array that every device loading this library keeps until the process
@@ -686,15 +741,15 @@ static constexpr size_t kStaticScratchBytes = 64ull << 20;  // 64 MiB
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 static void *static_scratch() {
-    static void *addr[64] = {nullptr};
+    static std::atomic<void *> addr[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    if (!addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) return nullptr;
-        addr[dev] = p;
+    void *a = addr[dev].load(std::memory_order_relaxed);
+    if (!a) {
+        if (cudaGetSymbolAddress(&a, g_static_scratch) != cudaSuccess) return nullptr;
+        addr[dev].store(a, std::memory_order_relaxed);
     }
-    return addr[dev];
+    return a;
 }
 
 MOBA_EXPORT size_t moba_attn_fwd_noalloc_capacity(void) { return kStaticScratchBytes; }
@@ -712,7 +767,7 @@ MOBA_EXPORT int moba_attn_fwd_noalloc(const void *q, const void *k, const void *
     if (!scratch) return MOBA_ERR_CUDA;
     // run_forward clears the per-(block, head) counters itself (a memset, not
     // an allocation); every other scratch area is written before it is read
-    return run_forward(p, nullptr, q, k, v, out, lse, scratch, kStaticScratchBytes,
+    return run_forward(p, nullptr, q, k, v, out, lse, scratch, kStaticScratchBytes, nullptr,
                        static_cast<cudaStream_t>(stream));
 }
 

@@ -205,6 +205,7 @@ __global__ __launch_bounds__(kThreads, 2) void past_kernel(Args a) {
     const uint32_t sK = sQ + kM * D * 2;
     const uint32_t sV = sK + kN * D * 2;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    MOBA_RETURN_IF_BAD(a.g);
     const int total_tiles = __ldg(a.tile_off + a.n_lists);
     const int H = a.g.H;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
@@ -257,6 +258,7 @@ __global__ __launch_bounds__(kThreads, 2) void current_kernel(Args a) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int h = blockIdx.y, b = blockIdx.z;
     const int H = a.g.H;
+    MOBA_RETURN_IF_BAD(a.g);
     const int seq0 = __ldg(a.g.cu + b), len = __ldg(a.g.cu + b + 1) - seq0;
     const int r0 = blockIdx.x * kM;
     if (r0 >= len) return;
@@ -347,6 +349,7 @@ static mma_path::Args make_args(const Plan &p, const Workspace &ws, const __nv_b
     mma_path::Args a;
     a.g.cu = ws.cu;
     a.g.blk_base = ws.blk_base;
+    a.g.bad = ws.bad;
     a.g.num_seqs = p.num_seqs;
     a.g.total = p.total;
     a.g.H = p.H;

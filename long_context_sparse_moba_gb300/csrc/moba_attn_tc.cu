@@ -208,6 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *gmisc = smem_raw + (misc - raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.g.H;
+    MOBA_RETURN_IF_BAD(a.g);
     const int njobs = (MODE == kPast) ? __ldg(a.tile_off + a.n_lists) : a.n_jobs;
     if ((int)blockIdx.x >= njobs) return;
 
@@ -852,23 +853,14 @@ bool make_tma_3d(CUtensorMap *m, const void *ptr, int total, int H, int D, int r
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-static long long g_wait_limit = 4000000000ll;  // ~2 s at 2 GHz
-
-static int g_debug_flags = 0;
-
-void tc_debug_set(int flags, long long wait_limit) {
-    g_debug_flags = flags;
-    g_wait_limit = wait_limit > 0 ? wait_limit : 4000000000ll;
-}
-
 int tc_tile_rows() { return tc::kRows; }
-long long tc_wait_limit() { return g_wait_limit; }
 
 static tc::Args make_tc_args(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
                              __nv_bfloat16 *out, float *lse) {
     tc::Args a;
     a.g.cu = ws.cu;
     a.g.blk_base = ws.blk_base;
+    a.g.bad = ws.bad;
     a.g.num_seqs = p.num_seqs;
     a.g.total = p.total;
     a.g.H = p.H;
@@ -894,8 +886,8 @@ static tc::Args make_tc_args(const Plan &p, const Workspace &ws, const __nv_bflo
     a.part_lse = ws.part_lse;
     a.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)p.D));
     a.status = status_word();
-    a.wait_limit = g_wait_limit;
-    a.debug_flags = g_debug_flags;
+    a.wait_limit = p.wait_limit;
+    a.debug_flags = p.debug_flags;
     return a;
 }
 

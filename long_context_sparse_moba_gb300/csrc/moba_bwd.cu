@@ -132,6 +132,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_kv_kernel(Args a) {
     const int wm = warp & 3, wn = warp >> 2;
     const int g = lane >> 2, t = lane & 3;
     const int H = a.g.H;
+    MOBA_RETURN_IF_BAD(a.g);
     const size_t rstride = (size_t)H * D;
     const int NB = __ldg(a.g.blk_base + a.g.num_seqs);
 
@@ -401,6 +402,7 @@ cudaError_t launch_attn_bwd(const Plan &p, const Workspace &ws, const __nv_bfloa
     bwd::Args a;
     a.g.cu = ws.cu;
     a.g.blk_base = ws.blk_base;
+    a.g.bad = ws.bad;
     a.g.num_seqs = p.num_seqs;
     a.g.total = p.total;
     a.g.H = p.H;

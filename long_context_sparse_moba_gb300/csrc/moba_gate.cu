@@ -60,14 +60,39 @@ __device__ void cta_exclusive_scan(int N, F f, W write) {
 
 // ---------------------------------------------------------------------------
 // Sequence tables.  cu_in: device int32 [num_seqs+1] or nullptr (fixed length
-// S = max_len for every sequence).
+// S = max_len for every sequence).  Caller-provided offsets are checked first:
+// they must start at 0, never decrease, give no sequence more than max_len
+// tokens and end at `total`.  Offsets that fail leave every sequence empty,
+// raise the `bad` flag that the later kernels test at entry, and record
+// MOBA_ERR_INVALID_ARG in the device status word (moba_get_status): nothing
+// is read or written through them.
 // ---------------------------------------------------------------------------
-__global__ void setup_kernel(const int *__restrict__ cu_in, int num_seqs, int S, int bs,
+__global__ void setup_kernel(const int *__restrict__ cu_in, int num_seqs, int S, int total, int bs,
                              int *__restrict__ cu, int *__restrict__ blk_base,
-                             int *__restrict__ gtile) {
-    auto len = [&](int b) { return cu_in ? (cu_in[b + 1] - cu_in[b]) : S; };
+                             int *__restrict__ gtile, int *__restrict__ bad, int *status) {
+    __shared__ int s_bad;
+    if (threadIdx.x == 0) s_bad = 0;
+    __syncthreads();
+    if (cu_in) {
+        for (int b = threadIdx.x; b <= num_seqs; b += blockDim.x) {
+            const int x = cu_in[b];
+            bool ok = (b > 0 || x == 0) && (b < num_seqs || x == total);
+            if (b < num_seqs) {
+                const int len = cu_in[b + 1] - x;
+                ok = ok && len >= 0 && len <= S;
+            }
+            if (!ok) s_bad = 1;
+        }
+    }
+    __syncthreads();
+    const bool invalid = s_bad != 0;
+    if (threadIdx.x == 0) {
+        *bad = invalid ? 1 : 0;
+        if (invalid && status) atomicCAS(status, 0, 1 /* MOBA_ERR_INVALID_ARG */);
+    }
+    auto len = [&](int b) { return invalid ? 0 : cu_in ? (cu_in[b + 1] - cu_in[b]) : S; };
     for (int b = threadIdx.x; b <= num_seqs; b += blockDim.x)
-        cu[b] = cu_in ? cu_in[b] : b * S;
+        cu[b] = invalid ? 0 : cu_in ? cu_in[b] : b * S;
     cta_exclusive_scan(
         num_seqs, [&](int b) { return (len(b) + bs - 1) / bs; },
         [&](int i, int v) { blk_base[i] = v; });
@@ -77,10 +102,26 @@ __global__ void setup_kernel(const int *__restrict__ cu_in, int num_seqs, int S,
 }
 
 cudaError_t launch_setup(const Plan &p, const int *cu_dev, Workspace &ws, cudaStream_t st) {
-    setup_kernel<<<1, 1024, 0, st>>>(cu_dev, p.num_seqs, p.max_len, p.bs, ws.cu, ws.blk_base,
-                                     ws.gtile);
+    setup_kernel<<<1, 1024, 0, st>>>(cu_dev, p.num_seqs, p.max_len, p.total, p.bs, ws.cu,
+                                     ws.blk_base, ws.gtile, ws.bad, status_word());
     note_launches(1);
     return cudaGetLastError();
+}
+
+// idx rows of the paths that run no gate: the own block and every earlier
+// block, ascending (top-1 keeps the own block alone), -1 padded
+__global__ void fill_idx_kernel(Geometry g, int32_t *__restrict__ idx, int topk, int km1) {
+    MOBA_RETURN_IF_BAD(g);
+    const size_t R = (size_t)g.total * g.H;
+    for (size_t r = (size_t)blockIdx.x * blockDim.x + threadIdx.x; r < R;
+         r += (size_t)gridDim.x * blockDim.x) {
+        const int t = (int)(r / g.H);
+        const int b = upper_index(g.cu, g.num_seqs, t);
+        const int ci = (t - __ldg(g.cu + b)) / g.bs;
+        const int npast = min(ci, km1);  // km1 = 0 for top-1, topk - 1 >= ci when dense
+        int32_t *out = idx + r * topk;
+        for (int x = 0; x < topk; ++x) out[x] = x < npast ? x : x == npast ? ci : -1;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -99,6 +140,7 @@ __global__ __launch_bounds__(kPoolThreads) void kpool_kernel(Geometry g,
                                                               const __nv_bfloat16 *__restrict__ k,
                                                               float *__restrict__ kbar) {
     __shared__ float red[kPoolThreads][9];
+    MOBA_RETURN_IF_BAD(g);
     const int gblk = blockIdx.x;
     if (gblk >= __ldg(g.blk_base + g.num_seqs)) return;
     const int b = upper_index(g.blk_base, g.num_seqs, gblk);
@@ -205,6 +247,7 @@ static Geometry make_geo(const Plan &p, const Workspace &ws) {
     Geometry g;
     g.cu = ws.cu;
     g.blk_base = ws.blk_base;
+    g.bad = ws.bad;
     g.num_seqs = p.num_seqs;
     g.total = p.total;
     g.H = p.H;
@@ -218,7 +261,7 @@ cudaError_t launch_kpool(const Plan &p, const Workspace &ws, const __nv_bfloat16
     const int HD8 = p.H * p.D / 8;
     const int CW = HD8 < 64 ? HD8 : 64;
     dim3 grid(p.NBcap, (HD8 + CW - 1) / CW);
-    if (pooling_kind() == 1)
+    if (p.pool == 1)
         kpool_kernel<true><<<grid, kPoolThreads, 0, st>>>(make_geo(p, ws), k, kbar);
     else
         kpool_kernel<false><<<grid, kPoolThreads, 0, st>>>(make_geo(p, ws), k, kbar);
@@ -227,7 +270,7 @@ cudaError_t launch_kpool(const Plan &p, const Workspace &ws, const __nv_bfloat16
 }
 
 // ---------------------------------------------------------------------------
-// K2 on the CUDA cores (selectable with moba_set_gate_kernel, and used when a
+// K2 on the CUDA cores (selectable per call, and used when a
 // sequence has more blocks than the tensor-core gate's TMEM holds): gate +
 // top-k.  A CTA scores 128 consecutive query rows of one (sequence,
 // head) against the pooled keys of that sequence's past blocks.  Four lanes
@@ -256,6 +299,7 @@ __global__ __launch_bounds__(kGateThreads) void gate_kernel(
     constexpr int M = DL / 4;  // float4 chunks per lane
     __shared__ __align__(16) float skb[kGateChunk * D];
     __shared__ int s_cmax;
+    MOBA_RETURN_IF_BAD(g);
     const int h = blockIdx.y, b = blockIdx.z, H = g.H;
     const int seq0 = __ldg(g.cu + b), L = __ldg(g.cu + b + 1) - seq0;
     const int i0 = blockIdx.x * kGateRows;
@@ -462,6 +506,7 @@ __global__ void __launch_bounds__(kRgThreads)
     regroup_count_kernel(Geometry g, const int32_t *__restrict__ idx, int topk, int rows_per_cta,
                          int N, int *__restrict__ counts) {
     extern __shared__ int hist[];
+    MOBA_RETURN_IF_BAD(g);
     const size_t R = (size_t)g.total * g.H;
     const size_t r0 = (size_t)blockIdx.x * rows_per_cta, r1 = min(R, r0 + rows_per_cta);
     if (SMEM) {
@@ -501,6 +546,7 @@ __global__ void __launch_bounds__(kRgThreads)
                            int N, int *__restrict__ counts, const int *__restrict__ list_off,
                            int *__restrict__ list) {
     extern __shared__ int hist[];
+    MOBA_RETURN_IF_BAD(g);
     const size_t R = (size_t)g.total * g.H;
     const size_t r0 = (size_t)blockIdx.x * rows_per_cta, r1 = min(R, r0 + rows_per_cta);
     if (SMEM) {
@@ -552,7 +598,7 @@ cudaError_t launch_regroup(const Plan &p, const Workspace &ws, bool counted, cud
         note_launches(1);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    regroup_scan_kernel<<<1, 1024, 0, st>>>(ws.counts, N, past_tile_rows(), ws.list_off,
+    regroup_scan_kernel<<<1, 1024, 0, st>>>(ws.counts, N, past_tile_rows(p), ws.list_off,
                                             ws.tile_off, ws.job_list);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (smem)
@@ -562,6 +608,14 @@ cudaError_t launch_regroup(const Plan &p, const Workspace &ws, bool counted, cud
         regroup_scatter_kernel<false><<<grid, kRgThreads, 0, st>>>(
             g, ws.idx, p.topk, rows_per_cta, N, ws.counts, ws.list_off, ws.list);
     note_launches(2);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fill_idx(const Plan &p, const Workspace &ws, int32_t *idx, cudaStream_t st) {
+    const size_t R = (size_t)p.total * p.H;
+    const unsigned blocks = (unsigned)std::min<size_t>((R + 255) / 256, 8192);
+    fill_idx_kernel<<<blocks, 256, 0, st>>>(make_geo(p, ws), idx, p.topk, p.dense ? p.topk - 1 : p.km1);
+    note_launches(1);
     return cudaGetLastError();
 }
 

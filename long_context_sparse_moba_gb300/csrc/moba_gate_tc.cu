@@ -56,6 +56,11 @@ __host__ __device__ constexpr int threads_for(int nwg) { return 64 + 128 * nwg; 
 constexpr int kMaxQ = 6;                       // q stages at most
 constexpr int kMaxSlots = 8;                   // TMEM score slots at most
 constexpr int kMaxBlocks = 256;                // blocks per sequence
+// Rows left to the exact kernel carry up to 8 candidate blocks packed one byte
+// each with 0xff as the empty marker: past candidates are below the own block,
+// so at most kMaxBlocks - 2 = 254, and a candidate id of 255 -- which would
+// read as empty -- cannot occur while the cap holds.
+static_assert(kMaxBlocks <= 256, "candidate block ids are packed into one byte each");
 
 struct Args {
     Geometry g;
@@ -170,6 +175,7 @@ __global__ void __launch_bounds__(threads_for(NWG), 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gmisc + L::kNumBars * 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gmisc + L::kNumBars * 8 + 4);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    MOBA_RETURN_IF_BAD(a.g);
     const int H = a.g.H, km1 = a.topk - 1;
     // units fit an int (checked on the host)
     const int n_units = H * __ldg(a.gtile + a.g.num_seqs);
@@ -548,6 +554,7 @@ __global__ void __launch_bounds__(32 * kExactWarps)
                       const float *__restrict__ kbar, int32_t *__restrict__ idx, int topk,
                       int *__restrict__ counts, const unsigned long long *__restrict__ need_list,
                       const int *__restrict__ need_count) {
+    MOBA_RETURN_IF_BAD(g);
     const int lane = threadIdx.x & 31;
     const int n = *need_count;
     const int km1 = topk - 1;
@@ -688,6 +695,7 @@ cudaError_t launch_gate_tc(const Plan &p, const Workspace &ws, const __nv_bfloat
     gate_tc::Args a;
     a.g.cu = ws.cu;
     a.g.blk_base = ws.blk_base;
+    a.g.bad = ws.bad;
     a.g.num_seqs = p.num_seqs;
     a.g.total = p.total;
     a.g.H = p.H;
@@ -703,7 +711,7 @@ cudaError_t launch_gate_tc(const Plan &p, const Workspace &ws, const __nv_bfloat
     a.idx = idx;
     a.topk = p.topk;
     a.status = status_word();
-    a.wait_limit = tc_wait_limit();
+    a.wait_limit = p.wait_limit;
     // TMEM slot width W: the longest sequence's blocks rounded up to 64, 128
     // or 256 columns; as many q stages as the shared memory left holds
     const int nmax = (p.max_len + p.bs - 1) / p.bs;

@@ -27,6 +27,10 @@ int *status_word();
 struct Geometry {
     const int *cu;        // [num_seqs + 1]
     const int *blk_base;  // [num_seqs + 1]
+    // set by the table set-up when caller-provided sequence offsets are
+    // inconsistent (not starting at 0, decreasing, longer than max_seqlen, or
+    // not ending at total); every kernel that reads the tables returns at once
+    const int *bad;
     int num_seqs;
     int total;            // tokens
     int H, D, bs;
@@ -47,6 +51,7 @@ struct Workspace {
     int *cu;          // [num_seqs + 1]
     int *blk_base;    // [num_seqs + 1]
     int *gtile;       // [num_seqs + 1]  128-row gate tiles before each sequence
+    int *bad;         // [1] inconsistent sequence offsets (see Geometry::bad)
     float *kbar;      // [NBcap][H][D]
     int32_t *idx;     // [total][H][topk]
     int *counts;      // [NBcap * H]   queries per (block, head) past list (zero
@@ -72,7 +77,24 @@ struct Plan {
     int km1;          // past slots per row (topk - 1), 0 on the dense path
     bool dense;       // topk covers every block of every sequence
     bool fixed;       // [B][S] layout (lse [B][H][S]) rather than varlen
+    // per-call options (moba_options_t); defaults are all zero except the wait
+    int pool;               // key pooling: 0 mean, 1 element-wise max
+    int gate_kind;          // 0 tensor-core scores + exact candidates, 1 CUDA cores
+    int attn_kind;          // 0 tcgen05 / TMEM / TMA, 1 warp-level mma.sync
+    int debug_flags;        // bit 0: the K/V producer skips its first load
+    long long wait_limit;   // clock64 budget of one bounded wait
 };
+
+// clock64 budget of one bounded wait when the caller gives none (~2 s at 2 GHz)
+constexpr long long kDefaultWaitLimit = 4000000000ll;
+
+// Returns from a kernel when the table set-up flagged the caller's sequence
+// offsets; every thread of the kernel reads the same word, so the whole grid
+// leaves before any barrier.
+#define MOBA_RETURN_IF_BAD(g)                 \
+    do {                                      \
+        if ((g).bad && *(g).bad) return;      \
+    } while (0)
 
 // backward = true: the backward pass's scratch (no partial outputs; the dq
 // accumulator and the per-row dO . O instead)
@@ -96,17 +118,14 @@ cudaError_t launch_attn_current(const Plan &p, const Workspace &ws, const __nv_b
                                 const __nv_bfloat16 *k, const __nv_bfloat16 *v,
                                 __nv_bfloat16 *out, float *lse, cudaStream_t st);
 
-// pooling of the keys per block: 0 mean, 1 element-wise max
-int pooling_kind();
-
 // count of kernels this library has launched (for the benchmark's launch tally)
 void note_launches(int n);
 
 // streaming multiprocessors of the current device (cached per device)
 int sm_count();
 
-// rows per tile of the past-block attention kernel in use (regroup tiling)
-int past_tile_rows();
+// rows per tile of the past-block attention kernel the plan uses (regroup tiling)
+int past_tile_rows(const Plan &p);
 
 // the two attention implementations: tcgen05 / TMEM / TMA (default) and the
 // warp-level mma.sync baseline
@@ -121,7 +140,6 @@ cudaError_t launch_attn_current_mma(const Plan &p, const Workspace &ws, const __
                                     const __nv_bfloat16 *k, const __nv_bfloat16 *v,
                                     __nv_bfloat16 *out, float *lse, cudaStream_t st);
 int tc_tile_rows();
-long long tc_wait_limit();
 // [total][H][D] bf16 as a 3-D TMA tensor (D, H, total), box 64 x 1 x rows, 128B swizzle
 bool make_tma_3d(CUtensorMap *m, const void *ptr, int total, int H, int D, int rows);
 // kbar (fp32) -> hi = bf16(kbar), lo = bf16(kbar - hi)
@@ -146,7 +164,9 @@ size_t decode_ticket_offset(int B, int H, int D, int topk);
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *kbar,
                           const int32_t *lens, void *out, float *lse, int32_t *idx, int B, int H,
                           int S_max, int D, int bs, int topk, void *scratch, cudaStream_t st);
-void tc_debug_set(int flags, long long wait_limit);
+// idx of the rows the gate does not run for (top-1, or top-k covering every
+// block): the own block and every earlier one, ascending, -1 padded
+cudaError_t launch_fill_idx(const Plan &p, const Workspace &ws, int32_t *idx, cudaStream_t st);
 // backward: delta, then dk / dv (and the dq accumulator, which must be zero on
 // entry) over the regroup lists, then dq
 cudaError_t launch_attn_bwd(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,

@@ -42,18 +42,12 @@ _SIGNATURES = {
                                      _P, _SZ, _P]),
     "moba_get_status": (_I, [_P]),
     "moba_launch_count": (ctypes.c_ulonglong, []),
-    "moba_profile_begin": (_I, [_I]),
-    "moba_profile_end": (_I, [_P, _I]),
-    "moba_set_attention_kernel": (_I, [_I]),
-    "moba_set_gate_kernel": (_I, [_I]),
-    "moba_set_pooling": (_I, [_I]),
     "moba_decode_fwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "moba_decode_workspace_size": (_SZ, [_I, _I, _I, _I]),
     "moba_decode_fwd_ws": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _SZ,
                                 _P]),
     "moba_attn_fwd_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "moba_attn_fwd_noalloc_capacity": (_SZ, []),
-    "moba_debug_set": (_I, [_I, ctypes.c_longlong]),
     "moba_debug_timeout_info": (None, [_P]),
     "moba_attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "moba_attn_bwd_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
@@ -62,9 +56,71 @@ _SIGNATURES = {
     "moba_attn_bwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                                   _I, _I, _P]),
     "moba_attn_bwd_varlen_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "moba_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "moba_kpool_ex": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "moba_kpool_varlen_ex": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "moba_gate_topk_ex": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "moba_gate_topk_varlen_ex": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "moba_attn_fwd_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "moba_attn_fwd_varlen_ex": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P,
+                                     _P, _SZ, _P]),
+    "moba_attn_bwd_ex": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P,
+                              _P, _SZ, _P]),
+    "moba_attn_bwd_varlen_ex": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
+                                     _I, _I, _I, _P, _P, _SZ, _P]),
 }
 
+POOL_MEAN = 0
+POOL_MAX = 1
+GATE_TCGEN05 = 0
+GATE_CUDA_CORES = 1
+ATTN_TCGEN05 = 0
+ATTN_MMA_SYNC = 1
+
+
+class Options(ctypes.Structure):
+    """``moba_options_t``: per-call options (all zero = the defaults)."""
+    _fields_ = [("pooling", ctypes.c_int), ("gate_kernel", ctypes.c_int),
+                ("attn_kernel", ctypes.c_int), ("debug_flags", ctypes.c_int),
+                ("wait_limit_cycles", ctypes.c_longlong), ("idx_out", ctypes.c_void_p),
+                ("phase_events", ctypes.c_void_p)]
+
+
+def _options(pooling=POOL_MEAN, gate_kernel=GATE_TCGEN05, attn_kernel=ATTN_TCGEN05,
+             debug_flags=0, wait_limit_cycles=0, idx_out=None, phase_events=None):
+    """An Options structure and the objects that must outlive the call."""
+    o = Options(int(pooling), int(gate_kernel), int(attn_kernel), int(debug_flags),
+                int(wait_limit_cycles), None, None)
+    keep = []
+    if idx_out is not None:
+        o.idx_out = idx_out.data_ptr()
+    if phase_events is not None:
+        if len(phase_events) != len(PHASES) + 1:
+            raise ValueError(f"phase_events needs {len(PHASES) + 1} events")
+        arr = (ctypes.c_void_p * len(phase_events))()
+        for i, ev in enumerate(phase_events):
+            arr[i] = ev.cuda_event
+        o.phase_events = ctypes.cast(arr, ctypes.c_void_p)
+        keep.append(arr)
+    return o, keep
+
 PHASES = ("tables", "kpool", "gate", "regroup", "attn_past", "attn_current")
+
+
+def phase_events(stream=None):
+    """Seven timing events for the forward's ``phase_events`` option, created on
+    the stream (torch creates an event's CUDA handle at its first record)."""
+    st = stream if stream is not None else torch.cuda.current_stream()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(PHASES) + 1)]
+    for e in evs:
+        e.record(st)
+    return evs
+
+
+def phase_ms(events) -> dict:
+    """{phase: ms} between the recorded events (synchronises the last one)."""
+    events[-1].synchronize()
+    return {name: events[i].elapsed_time(events[i + 1]) for i, name in enumerate(PHASES)}
 
 
 def lib():
@@ -137,29 +193,33 @@ def _nb_total(cu_host, block_size):
     return sum(num_blocks(cu_host[b + 1] - cu_host[b], block_size) for b in range(len(cu_host) - 1))
 
 
-def kpool(k, block_size: int, stream=None):
-    """Mean-pooled keys of k [B, S, H, D] -> kbar [B * n, H, D] fp32."""
+def kpool(k, block_size: int, stream=None, pooling=POOL_MEAN):
+    """Pooled keys of k [B, S, H, D] -> kbar [B * n, H, D] fp32 (mean, or the
+    element-wise maximum with ``pooling=POOL_MAX``)."""
     _need(k, torch.bfloat16, "k")
     B, S, H, D = k.shape
     kbar = torch.empty(B * num_blocks(S, block_size), H, D, dtype=torch.float32, device=k.device)
-    _check(lib().moba_kpool(_ptr(k), _ptr(kbar), B, H, S, D, block_size, _stream(stream)),
-           "moba_kpool")
+    o, _keep = _options(pooling=pooling)
+    _check(lib().moba_kpool_ex(_ptr(k), _ptr(kbar), B, H, S, D, block_size, ctypes.byref(o),
+                               _stream(stream)), "moba_kpool")
     return kbar
 
 
-def kpool_varlen(k, cu_seqlens, block_size: int, stream=None):
+def kpool_varlen(k, cu_seqlens, block_size: int, stream=None, pooling=POOL_MEAN):
     """Varlen k [total, H, D], cu_seqlens int32 CUDA [num_seqs + 1]."""
     _need(k, torch.bfloat16, "k")
     _need(cu_seqlens, torch.int32, "cu_seqlens")
     total, H, D = k.shape
     nb = _nb_total(cu_seqlens.tolist(), block_size)
     kbar = torch.empty(nb, H, D, dtype=torch.float32, device=k.device)
-    _check(lib().moba_kpool_varlen(_ptr(k), _ptr(kbar), _ptr(cu_seqlens), cu_seqlens.numel() - 1,
-                                   total, H, D, block_size, _stream(stream)), "moba_kpool_varlen")
+    o, _keep = _options(pooling=pooling)
+    _check(lib().moba_kpool_varlen_ex(_ptr(k), _ptr(kbar), _ptr(cu_seqlens),
+                                      cu_seqlens.numel() - 1, total, H, D, block_size,
+                                      ctypes.byref(o), _stream(stream)), "moba_kpool_varlen")
     return kbar
 
 
-def gate_topk(q, kbar, block_size: int, topk: int, stream=None):
+def gate_topk(q, kbar, block_size: int, topk: int, stream=None, gate_kernel=GATE_TCGEN05):
     """Selected blocks idx [B, S, H, topk] int32 (ascending, -1 padded)."""
     _need(q, torch.bfloat16, "q")
     _need(kbar, torch.float32, "kbar")
@@ -167,20 +227,24 @@ def gate_topk(q, kbar, block_size: int, topk: int, stream=None):
     if block_size > 0 and tuple(kbar.shape) != (B * num_blocks(S, block_size), H, D):
         raise ValueError("kbar must be [B * ceil(S / block_size), H, D] (as kpool returns it)")
     idx = torch.empty(B, S, H, topk, dtype=torch.int32, device=q.device)
-    _check(lib().moba_gate_topk(_ptr(q), _ptr(kbar), _ptr(idx), B, H, S, D, block_size, topk,
-                                _stream(stream)), "moba_gate_topk")
+    o, _keep = _options(gate_kernel=gate_kernel)
+    _check(lib().moba_gate_topk_ex(_ptr(q), _ptr(kbar), _ptr(idx), B, H, S, D, block_size, topk,
+                                   ctypes.byref(o), _stream(stream)), "moba_gate_topk")
     return idx
 
 
-def gate_topk_varlen(q, kbar, cu_seqlens, block_size: int, topk: int, stream=None):
+def gate_topk_varlen(q, kbar, cu_seqlens, block_size: int, topk: int, stream=None,
+                     gate_kernel=GATE_TCGEN05):
     _need(q, torch.bfloat16, "q")
     _need(kbar, torch.float32, "kbar")
     _need(cu_seqlens, torch.int32, "cu_seqlens")
     total, H, D = q.shape
     idx = torch.empty(total, H, topk, dtype=torch.int32, device=q.device)
-    _check(lib().moba_gate_topk_varlen(_ptr(q), _ptr(kbar), _ptr(idx), _ptr(cu_seqlens),
-                                       cu_seqlens.numel() - 1, total, H, D, block_size, topk,
-                                       _stream(stream)), "moba_gate_topk_varlen")
+    o, _keep = _options(gate_kernel=gate_kernel)
+    _check(lib().moba_gate_topk_varlen_ex(_ptr(q), _ptr(kbar), _ptr(idx), _ptr(cu_seqlens),
+                                          cu_seqlens.numel() - 1, total, H, D, block_size, topk,
+                                          ctypes.byref(o), _stream(stream)),
+           "moba_gate_topk_varlen")
     return idx
 
 
@@ -193,13 +257,22 @@ def varlen_workspace_size(num_seqs, total, max_seqlen, H, D, block_size, topk) -
                                                          block_size, topk))
 
 
+def _idx_buffer(idx_out, rows_shape, topk, like):
+    if idx_out is None:
+        return None
+    return _out(idx_out, (*rows_shape, topk), torch.int32, like, "idx_out")
+
+
 def attn_fwd(q, k, v, block_size: int, topk: int, out=None, lse=None, workspace=None,
-             stream=None):
+             stream=None, idx_out=None, phase_events=None, **options):
     """MoBA forward for q, k, v [B, S, H, D] bf16 -> (out [B, S, H, D] bf16, lse [B, H, S] fp32).
 
     With ``workspace`` (a uint8 CUDA tensor of at least :func:`workspace_size`
     bytes) the call allocates nothing; otherwise the library allocates its
-    scratch stream-ordered."""
+    scratch stream-ordered.  ``idx_out`` ([B, S, H, topk] int32) receives the
+    selection the call used; ``phase_events`` (see :func:`phase_events`) are
+    recorded between its phases; further keyword ``options`` (pooling,
+    gate_kernel, attn_kernel, debug_flags, wait_limit_cycles) are per call."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, torch.bfloat16, n)
     B, S, H, D = q.shape
@@ -208,13 +281,12 @@ def attn_fwd(q, k, v, block_size: int, topk: int, out=None, lse=None, workspace=
     out = _out(out, q.shape, torch.bfloat16, q, "out")
     lse = _out(lse, (B, H, S), torch.float32, q, "lse")
     workspace = _ws(workspace)
-    st = _stream(stream)
-    if workspace is None:
-        rc = lib().moba_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, S, D,
-                                 block_size, topk, st)
-    else:
-        rc = lib().moba_attn_fwd_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, S, D,
-                                    block_size, topk, _ptr(workspace), workspace.numel(), st)
+    idx_out = _idx_buffer(idx_out, (B, S, H), topk, q)
+    o, _keep = _options(idx_out=idx_out, phase_events=phase_events, **options)
+    rc = lib().moba_attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, S, D,
+                                block_size, topk, ctypes.byref(o), _ptr(workspace),
+                                workspace.numel() if workspace is not None else 0,
+                                _stream(stream))
     _check(rc, "moba_attn_fwd")
     return out, lse
 
@@ -256,9 +328,11 @@ def decode_fwd(q, k_cache, v_cache, kbar, cache_lens, block_size: int, topk: int
 
 
 def attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, block_size: int, topk: int, out=None,
-                    lse=None, workspace=None, stream=None):
+                    lse=None, workspace=None, stream=None, idx_out=None, phase_events=None,
+                    **options):
     """Varlen MoBA forward: q, k, v [total, H, D] bf16, cu_seqlens int32 CUDA
-    [num_seqs + 1] -> (out [total, H, D] bf16, lse [H, total] fp32)."""
+    [num_seqs + 1] -> (out [total, H, D] bf16, lse [H, total] fp32).  Options
+    as for :func:`attn_fwd` (``idx_out`` is [total, H, topk])."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, torch.bfloat16, n)
     _need(cu_seqlens, torch.int32, "cu_seqlens")
@@ -270,16 +344,13 @@ def attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, block_size: int, topk:
     out = _out(out, q.shape, torch.bfloat16, q, "out")
     lse = _out(lse, (H, total), torch.float32, q, "lse")
     workspace = _ws(workspace)
-    st = _stream(stream)
-    if workspace is None:
-        rc = lib().moba_attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
-                                        _ptr(cu_seqlens), ns, total, max_seqlen, H, D,
-                                        block_size, topk, st)
-    else:
-        rc = lib().moba_attn_fwd_varlen_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
-                                           _ptr(cu_seqlens), ns, total, max_seqlen, H, D,
-                                           block_size, topk, _ptr(workspace), workspace.numel(),
-                                           st)
+    idx_out = _idx_buffer(idx_out, (total, H), topk, q)
+    o, _keep = _options(idx_out=idx_out, phase_events=phase_events, **options)
+    rc = lib().moba_attn_fwd_varlen_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                       _ptr(cu_seqlens), ns, total, max_seqlen, H, D,
+                                       block_size, topk, ctypes.byref(o), _ptr(workspace),
+                                       workspace.numel() if workspace is not None else 0,
+                                       _stream(stream))
     _check(rc, "moba_attn_fwd_varlen")
     return out, lse
 
@@ -289,11 +360,11 @@ def bwd_workspace_size(B, H, S, D, block_size, topk) -> int:
 
 
 def attn_bwd(q, k, v, out, lse, dout, block_size: int, topk: int, dq=None, dk=None, dv=None,
-             workspace=None, stream=None):
+             workspace=None, stream=None, **options):
     """MoBA backward for the forward ``attn_fwd(q, k, v, block_size, topk)``:
     q, k, v, out, dout [B, S, H, D] bf16 and lse [B, H, S] fp32 (as the forward
     returned them) -> (dq, dk, dv) [B, S, H, D] bf16.  The gate's selection is
-    recomputed and held fixed."""
+    recomputed (with the same ``options`` as the forward) and held fixed."""
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
         _need(t, torch.bfloat16, n)
     _need(lse, torch.float32, "lse")
@@ -307,19 +378,18 @@ def attn_bwd(q, k, v, out, lse, dout, block_size: int, topk: int, dq=None, dk=No
     dk = _out(dk, q.shape, torch.bfloat16, q, "dk")
     dv = _out(dv, q.shape, torch.bfloat16, q, "dv")
     workspace = _ws(workspace)
-    st = _stream(stream)
-    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
-            _ptr(dv), B, H, S, D, block_size, topk)
-    if workspace is None:
-        rc = lib().moba_attn_bwd(*args, st)
-    else:
-        rc = lib().moba_attn_bwd_ws(*args, _ptr(workspace), workspace.numel(), st)
+    o, _keep = _options(**options)
+    rc = lib().moba_attn_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                                _ptr(dq), _ptr(dk), _ptr(dv), B, H, S, D, block_size, topk,
+                                ctypes.byref(o), _ptr(workspace),
+                                workspace.numel() if workspace is not None else 0,
+                                _stream(stream))
     _check(rc, "moba_attn_bwd")
     return dq, dk, dv
 
 
 def attn_bwd_varlen(q, k, v, out, lse, dout, cu_seqlens, max_seqlen: int, block_size: int,
-                    topk: int, stream=None):
+                    topk: int, stream=None, **options):
     """Varlen backward: q, k, v, out, dout [total, H, D] bf16, lse [H, total]
     fp32, cu_seqlens int32 CUDA [num_seqs + 1] -> (dq, dk, dv) [total, H, D]."""
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
@@ -334,9 +404,11 @@ def attn_bwd_varlen(q, k, v, out, lse, dout, cu_seqlens, max_seqlen: int, block_
     if tuple(lse.shape) != (H, total):
         raise ValueError("lse must be [H, total]")
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
-    rc = lib().moba_attn_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
-                                    _ptr(dq), _ptr(dk), _ptr(dv), _ptr(cu_seqlens), ns, total,
-                                    max_seqlen, H, D, block_size, topk, _stream(stream))
+    o, _keep = _options(**options)
+    rc = lib().moba_attn_bwd_varlen_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                       _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(cu_seqlens),
+                                       ns, total, max_seqlen, H, D, block_size, topk,
+                                       ctypes.byref(o), None, 0, _stream(stream))
     _check(rc, "moba_attn_bwd_varlen")
     return dq, dk, dv
 
@@ -349,33 +421,6 @@ def get_status(stream=None) -> int:
 def launch_count() -> int:
     """Kernels launched by the library so far in this process."""
     return int(lib().moba_launch_count())
-
-
-def profile_begin(max_calls: int):
-    _check(lib().moba_profile_begin(int(max_calls)), "moba_profile_begin")
-
-
-def profile_end() -> tuple:
-    """(calls recorded, {phase: total ms}) of the forward calls since profile_begin."""
-    buf = (ctypes.c_float * len(PHASES))()
-    n = lib().moba_profile_end(ctypes.cast(buf, ctypes.c_void_p), len(PHASES))
-    if n < 0:
-        raise RuntimeError(f"moba_profile_end failed: {status_string(-n)}")
-    return n, dict(zip(PHASES, (float(x) for x in buf)))
-
-
-ATTN_TCGEN05 = 0
-ATTN_MMA_SYNC = 1
-
-
-def set_attention_kernel(kind: int):
-    """0: tcgen05 / TMEM / TMA kernels (default); 1: warp-level mma.sync baseline."""
-    _check(lib().moba_set_attention_kernel(int(kind)), "moba_set_attention_kernel")
-
-
-def debug_set(flags: int = 0, wait_limit_cycles: int = 0):
-    """Fault-injection hooks of the bounded waits (flags bit 0: skip a K/V load)."""
-    _check(lib().moba_debug_set(int(flags), int(wait_limit_cycles)), "moba_debug_set")
 
 
 def attn_fwd_noalloc(q, k, v, block_size: int, topk: int, out, lse, stream=None):
@@ -399,25 +444,6 @@ def attn_fwd_noalloc(q, k, v, block_size: int, topk: int, out, lse, stream=None)
 
 def noalloc_capacity() -> int:
     return int(lib().moba_attn_fwd_noalloc_capacity())
-
-
-GATE_TCGEN05 = 0
-GATE_CUDA_CORES = 1
-
-
-def set_gate_kernel(kind: int):
-    """0: tensor-core scores + exact re-score of candidates (default); 1: CUDA cores."""
-    _check(lib().moba_set_gate_kernel(int(kind)), "moba_set_gate_kernel")
-
-
-POOL_MEAN = 0
-POOL_MAX = 1
-
-
-def set_pooling(kind: int):
-    """Pooling of each block's keys for the gate (process-wide): POOL_MEAN
-    (default) or POOL_MAX (element-wise maximum over the block's keys)."""
-    _check(lib().moba_set_pooling(int(kind)), "moba_set_pooling")
 
 
 def debug_timeout_info():

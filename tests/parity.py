@@ -27,24 +27,37 @@ def flat(x):
     return x.reshape(-1, *x.shape[2:]) if x.dim() == 4 else x
 
 
-def gpu_select(inp, w: workloads.Workload, topk: int):
+def gpu_select(inp, w: workloads.Workload, topk: int, pooling=ops.POOL_MEAN,
+               gate_kernel=ops.GATE_TCGEN05):
     """kbar and idx from the library's pooling and gate entry points."""
     if w.varlen:
         cu = torch.tensor(inp.cu_seqlens, dtype=torch.int32, device=inp.q.device)
-        kbar = ops.kpool_varlen(inp.k, cu, w.block_size)
-        idx = ops.gate_topk_varlen(inp.q, kbar, cu, w.block_size, topk)
+        kbar = ops.kpool_varlen(inp.k, cu, w.block_size, pooling=pooling)
+        idx = ops.gate_topk_varlen(inp.q, kbar, cu, w.block_size, topk, gate_kernel=gate_kernel)
     else:
-        kbar = ops.kpool(inp.k, w.block_size)
-        idx = ops.gate_topk(inp.q, kbar, w.block_size, topk)
+        kbar = ops.kpool(inp.k, w.block_size, pooling=pooling)
+        idx = ops.gate_topk(inp.q, kbar, w.block_size, topk, gate_kernel=gate_kernel)
     return kbar, flat(idx)
 
 
-def gpu_forward(inp, w: workloads.Workload, topk: int):
+def gpu_forward(inp, w: workloads.Workload, topk: int, with_idx=False, stream=None, **options):
+    """The forward through the C ABI; with ``with_idx`` also the selection the
+    forward itself used (its idx_out option), as [total, H, topk]."""
+    dev = inp.q.device
+    idx = None
     if w.varlen:
-        cu = torch.tensor(inp.cu_seqlens, dtype=torch.int32, device=inp.q.device)
-        out, lse = ops.attn_fwd_varlen(inp.q, inp.k, inp.v, cu, w.S, w.block_size, topk)
+        cu = torch.tensor(inp.cu_seqlens, dtype=torch.int32, device=dev)
+        if with_idx:
+            idx = torch.empty(w.total, w.H, topk, dtype=torch.int32, device=dev)
+        out, lse = ops.attn_fwd_varlen(inp.q, inp.k, inp.v, cu, w.S, w.block_size, topk,
+                                       idx_out=idx, stream=stream, **options)
     else:
-        out, lse = ops.attn_fwd(inp.q, inp.k, inp.v, w.block_size, topk)
+        if with_idx:
+            idx = torch.empty(w.B, w.S, w.H, topk, dtype=torch.int32, device=dev)
+        out, lse = ops.attn_fwd(inp.q, inp.k, inp.v, w.block_size, topk, idx_out=idx,
+                                stream=stream, **options)
+    if with_idx:
+        return out, lse, flat(idx)
     return out, lse
 
 

@@ -50,11 +50,46 @@ def test_status_strings(lib):
     assert ops.status_string(99) == "MOBA_ERR_UNKNOWN"
 
 
-def test_pooling_switch_validates(lib):
-    assert lib.moba_set_pooling(7) == ops.MOBA_ERR_INVALID_ARG
-    assert lib.moba_set_pooling(-1) == ops.MOBA_ERR_INVALID_ARG
-    assert lib.moba_set_pooling(ops.POOL_MAX) == ops.MOBA_OK
-    assert lib.moba_set_pooling(ops.POOL_MEAN) == ops.MOBA_OK
+def test_options_validate_on_the_host(lib):
+    """Out-of-set option values are rejected before any launch (the fake
+    pointers are never dereferenced)."""
+    fake = ctypes.c_void_p(0x10000)
+    for field, bad in (("pooling", 7), ("pooling", -1), ("gate_kernel", 2), ("attn_kernel", 5),
+                       ("debug_flags", -1)):
+        o = ops.Options()
+        setattr(o, field, bad)
+        assert lib.moba_kpool_ex(fake, fake, 1, 1, 64, 64, 64, ctypes.byref(o),
+                                 None) == ops.MOBA_ERR_INVALID_ARG, field
+        assert lib.moba_attn_fwd_ex(fake, fake, fake, fake, fake, 1, 1, 64, 64, 64, 3,
+                                    ctypes.byref(o), None, 0, None) == ops.MOBA_ERR_INVALID_ARG
+        assert lib.moba_attn_bwd_ex(fake, fake, fake, fake, fake, fake, fake, fake, fake, 1, 1,
+                                    64, 64, 64, 3, ctypes.byref(o), None, 0,
+                                    None) == ops.MOBA_ERR_INVALID_ARG
+    o = ops.Options()
+    o.idx_out = 0x10002  # not 4-byte aligned
+    assert lib.moba_attn_fwd_ex(fake, fake, fake, fake, fake, 1, 1, 64, 64, 64, 3,
+                                ctypes.byref(o), None, 0, None) == ops.MOBA_ERR_INVALID_ARG
+
+
+def test_options_struct_layout():
+    """The ctypes mirror of moba_options_t has the C layout (LP64: int x4,
+    long long, two pointers = 40 bytes)."""
+    assert ctypes.sizeof(ops.Options) == 40
+    assert ops.Options.wait_limit_cycles.offset == 16
+    assert ops.Options.idx_out.offset == 24 and ops.Options.phase_events.offset == 32
+
+
+def test_no_process_wide_switches(lib):
+    """Kernel choice, pooling, fault injection and phase timing are per call:
+    the library exports no setter for them."""
+    for name in ("moba_set_pooling", "moba_set_gate_kernel", "moba_set_attention_kernel",
+                 "moba_debug_set", "moba_profile_begin", "moba_profile_end"):
+        assert not hasattr(lib, name), name
+
+
+def test_workspace_size_alias(lib):
+    assert lib.moba_workspace_size(1, 32, 32768, 128, 512, 3) == \
+        lib.moba_attn_fwd_workspace_size(1, 32, 32768, 128, 512, 3) > 0
 
 
 def test_decode_validates_on_the_host(lib):

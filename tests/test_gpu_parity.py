@@ -21,11 +21,15 @@ def built():
     ops.lib()
 
 
-def run_case(w, topk, rows=None, device="cuda"):
+def run_case(w, topk, rows=None, device="cuda", **options):
+    """The forward on one workload, its selection read back through idx_out and
+    checked (with the outputs) against the oracle; the standalone gate entry
+    point must select the same blocks."""
     inp = workloads.make_inputs(w, device=device)
-    kbar_g, idx = gpu_select(inp, w, topk)
-    out, lse = gpu_forward(inp, w, topk)
+    kbar_g, idx_gate = gpu_select(inp, w, topk)
+    out, lse, idx = gpu_forward(inp, w, topk, with_idx=True, **options)
     assert ops.get_status() == ops.MOBA_OK
+    assert torch.equal(idx, idx_gate)
     return inp, kbar_g, idx, out, lse, compare(w, inp, topk, out, lse, idx_gpu=idx, rows=rows)
 
 
@@ -84,8 +88,7 @@ def test_long128k_sampled_with_needles():
     w = workloads.WORKLOADS["long128k"]
     inp = workloads.make_inputs(w, device="cuda")
     rows = workloads.sample_rows(w, 4096, needle_queries=inp.needle_queries)
-    _, idx = gpu_select(inp, w, 3)
-    out, lse = gpu_forward(inp, w, 3)
+    out, lse, idx = gpu_forward(inp, w, 3, with_idx=True)
     st = compare(w, inp, 3, out, lse, idx_gpu=idx, rows=rows)
     print("long128k", st)
 
@@ -174,12 +177,8 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     recorded, and the next call on the same context is correct."""
     w = workloads.custom((2048,), 1, 128, 256, topk=3, seed=6)
     inp = workloads.make_inputs(w, device="cuda")
-    try:
-        ops.debug_set(1, 20_000_000)  # ~10 ms per wait
-        gpu_forward(inp, w, 3)
-        assert ops.get_status() == ops.MOBA_ERR_TIMEOUT
-    finally:
-        ops.debug_set(0, 0)
+    gpu_forward(inp, w, 3, debug_flags=1, wait_limit_cycles=20_000_000)  # ~10 ms per wait
+    assert ops.get_status() == ops.MOBA_ERR_TIMEOUT
     out, lse = gpu_forward(inp, w, 3)
     assert ops.get_status() == ops.MOBA_OK
     compare(w, inp, 3, out, lse)
@@ -190,11 +189,7 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     ((512,), 2, 128, 128, 4), ((200, 1, 64, 129), 2, 128, 64, 3)])
 def test_mma_sync_baseline_path(seqlens, H, D, bs, topk):
     w = workloads.custom(seqlens, H, D, bs, topk=topk, seed=17)
-    try:
-        ops.set_attention_kernel(ops.ATTN_MMA_SYNC)
-        *_, st = run_case(w, topk)
-    finally:
-        ops.set_attention_kernel(ops.ATTN_TCGEN05)
+    *_, st = run_case(w, topk, attn_kernel=ops.ATTN_MMA_SYNC)
     print("mma.sync", seqlens, st)
 
 
@@ -210,12 +205,48 @@ def test_tensor_core_gate_equals_cuda_core_gate(seqlens, H, D, bs, topk):
     the very same blocks as the all-CUDA-core gate."""
     w = workloads.custom(seqlens, H, D, bs, topk=topk, seed=31)
     inp = workloads.make_inputs(w, device="cuda")
-    try:
-        ops.set_gate_kernel(ops.GATE_CUDA_CORES)
-        _, ref = gpu_select(inp, w, topk)
-        ops.set_gate_kernel(ops.GATE_TCGEN05)
-        _, got = gpu_select(inp, w, topk)
-    finally:
-        ops.set_gate_kernel(ops.GATE_TCGEN05)
+    _, ref = gpu_select(inp, w, topk, gate_kernel=ops.GATE_CUDA_CORES)
+    _, got = gpu_select(inp, w, topk)
     assert ops.get_status() == ops.MOBA_OK
     assert torch.equal(ref, got)
+    # and the forward on the CUDA-core gate uses that same selection
+    _, _, fidx = gpu_forward(inp, w, topk, with_idx=True, gate_kernel=ops.GATE_CUDA_CORES)
+    assert ops.get_status() == ops.MOBA_OK
+    assert torch.equal(ref, fidx)
+
+
+# ---------------------------------------------------------------------------
+# device-side lengths that contradict the host arguments
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("cu,max_seqlen", [
+    ((0, 2048, 4096), 1024),        # max_seqlen below a sequence's length
+    ((0, 3000, 2000, 4096), 4096),  # offsets decrease
+    ((0, 2048, 4000), 2048),        # last offset is not the token count
+    ((16, 2048, 4096), 4096),       # first offset is not 0
+])
+def test_inconsistent_cu_seqlens_are_reported_not_used(cu, max_seqlen):
+    """cu_seqlens lives on the device, so the first kernel of each varlen call
+    checks it; when it contradicts the host arguments every later kernel returns
+    without touching memory through it and the status word reports
+    MOBA_ERR_INVALID_ARG.  The context stays usable: a correct call follows."""
+    total, H, D, bs = 4096, 2, 128, 256
+    g = torch.Generator(device="cuda").manual_seed(3)
+    q, k, v = (torch.randn(total, H, D, generator=g, device="cuda").to(torch.bfloat16)
+               for _ in range(3))
+    dcu = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    assert ops.get_status() == ops.MOBA_OK
+    ops.attn_fwd_varlen(q, k, v, dcu, max_seqlen, bs, 3)
+    assert ops.get_status() == ops.MOBA_ERR_INVALID_ARG
+    kbar = ops.kpool_varlen(k, dcu, bs)
+    assert ops.get_status() == ops.MOBA_ERR_INVALID_ARG
+    ops.gate_topk_varlen(q, torch.zeros_like(kbar), dcu, bs, 3)
+    assert ops.get_status() == ops.MOBA_ERR_INVALID_ARG
+    out = torch.zeros_like(q)
+    lse = torch.zeros(H, total, dtype=torch.float32, device="cuda")
+    ops.attn_bwd_varlen(q, k, v, out, lse, q, dcu, max_seqlen, bs, 3)
+    assert ops.get_status() == ops.MOBA_ERR_INVALID_ARG
+    # a consistent call on the same context
+    w = workloads.custom((2048, 2048), H, D, bs, topk=3, seed=44)
+    *_, st = run_case(w, 3)
+    print("after invalid offsets", st)

@@ -1,18 +1,16 @@
 """The no-allocation forward (moba_attn_fwd_noalloc) against moba_attn_fwd.
 
-Some callers cannot allocate device memory (a memory manager owns the whole
-device, or the serving loop must not allocate); this entry point runs the same
-forward with its scratch in the library's static device array.  This file is
-collected last on purpose."""
+Some callers cannot allocate device memory: a memory manager that owns the
+whole device, or a serving loop that must not allocate on its latency path.
+This entry point runs the same forward with its scratch in the library's static
+device array.  The file is collected last on purpose, so that a run stopping at
+the first failure has run every other test before this one."""
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
 from long_context_sparse_moba_gb300 import ops, workloads
-
-from .parity import LSE_MAX, OUT_MAX, OUT_MEAN
 
 
 @pytest.fixture(scope="module")
@@ -32,19 +30,24 @@ def test_noalloc_rejects_sizes_beyond_its_array(lib):
 
 @pytest.mark.gpu
 def test_noalloc_matches_allocating_entry_point(lib):
+    """Two calls in a row share the static array, which keeps the previous
+    call's contents.  The first call is the larger problem (more selections,
+    longer lists), so a later call that read a scratch area it never rewrote
+    would see the first call's values; the second call uses other inputs and
+    another top-k.  Both must equal moba_attn_fwd bit for bit (the same kernels
+    run in the same order, and the forward is deterministic)."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    w = workloads.custom((4096, 4096), 4, 128, 512, topk=3, seed=21)
-    assert ops.workspace_size(2, 4, 4096, 128, 512, 3) <= ops.noalloc_capacity()
-    inp = workloads.make_inputs(w, device="cuda")
-    ref_out, ref_lse = ops.attn_fwd(inp.q, inp.k, inp.v, 512, 3)
-    for call in range(2):  # two calls in a row share (and reuse) the static scratch
+    cases = [(workloads.custom((4096, 4096), 4, 128, 256, topk=6, seed=21), 6),
+             (workloads.custom((4096, 4096), 4, 128, 512, topk=3, seed=22), 3)]
+    for w, topk in cases:
+        assert ops.workspace_size(w.B, w.H, w.S, w.D, w.block_size, topk) <= ops.noalloc_capacity()
+    for call, (w, topk) in enumerate(cases):
+        inp = workloads.make_inputs(w, device="cuda")
+        ref_out, ref_lse = ops.attn_fwd(inp.q, inp.k, inp.v, w.block_size, topk)
         out = torch.full_like(inp.q, float("nan"))
-        lse = torch.full((2, 4, 4096), float("nan"), dtype=torch.float32, device="cuda")
-        ops.attn_fwd_noalloc(inp.q, inp.k, inp.v, 512, 3, out, lse)
+        lse = torch.full((w.B, w.H, w.S), float("nan"), dtype=torch.float32, device="cuda")
+        ops.attn_fwd_noalloc(inp.q, inp.k, inp.v, w.block_size, topk, out, lse)
         assert ops.get_status() == ops.MOBA_OK
-        err = (out.float() - ref_out.float()).abs()
-        lerr = (lse - ref_lse).abs()
-        assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all(), call
-        assert err.max().item() <= OUT_MAX and err.mean().item() <= OUT_MEAN, call
-        assert lerr.max().item() <= LSE_MAX, call
+        assert torch.equal(out, ref_out), call
+        assert torch.equal(lse, ref_lse), call
