@@ -362,9 +362,14 @@ def phase_work(w, topk):
     pooling and gate, issued tensor FLOPs for the two attention kernels."""
     cur, past = issued_pairs(w.seqlens, w.block_size, topk)
     hbm = hbm_bytes(w, topk)
-    return {"kpool": ("hbm", hbm["kpool"]), "gate": ("hbm", hbm["gate"]),
-            "attn_past": ("tensor", 4 * w.D * past * w.H),
+    work = {"attn_past": ("tensor", 4 * w.D * past * w.H),
             "attn_current": ("tensor", 4 * w.D * cur * w.H)}
+    n_max = (w.S + w.block_size - 1) // w.block_size
+    if 1 < topk < n_max:  # pooling and gate run only when some row is scored
+        work.update(kpool=("hbm", hbm["kpool"]), gate=("hbm", hbm["gate"]))
+    if past == 0:
+        del work["attn_past"]
+    return work
 
 
 def roofline_of(w, topk, per_call, peaks, peak_src):
