@@ -71,6 +71,12 @@ static void prof_mark(void *const *events, int phase, cudaStream_t st) {
 
 static inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Rows of the tensor-core gate's list of rows left to its exact kernel: every
+// gate CTA owns the rows of its 128-row units (padded tiles included).
+static size_t need_list_rows(const Plan &p) {
+    return (size_t)p.H * ((size_t)p.total + 128 * (size_t)p.num_seqs);
+}
+
 // The job table is sized for the smaller tile of the two attention kernels, so
 // that the workspace size does not depend on the per-call kernel choice.
 static size_t job_rows_min() {
@@ -98,8 +104,9 @@ size_t workspace_bytes(const Plan &p, Workspace *ws, char *base, bool backward) 
         w.kbar = static_cast<float *>(take(sizeof(float) * N * p.D));
         w.idx = static_cast<int32_t *>(take(sizeof(int32_t) * rows * p.topk));
         w.counts = static_cast<int *>(take(sizeof(int) * (N + 1)));
-        w.need_count = w.counts ? w.counts + N : nullptr;
-        w.need_list = static_cast<unsigned long long *>(take(2 * sizeof(long long) * rows));
+        w.need_count = static_cast<int *>(take(sizeof(int) * kMaxGateCtas));
+        w.need_list = static_cast<unsigned long long *>(
+            take(2 * sizeof(long long) * need_list_rows(p)));
         w.list_off = static_cast<int *>(take(sizeof(int) * (N + 1)));
         w.tile_off = static_cast<int *>(take(sizeof(int) * (N + 1)));
         w.job_list = static_cast<int *>(
@@ -209,7 +216,7 @@ static int run_forward(const Plan &p, const int *cu_dev, const void *q, const vo
     prof_mark(ev, 2, st);
     const bool tc_gate = p.gate_kind == MOBA_GATE_TENSOR_CORES && gate_tc_supported(p);
     if (gate) {
-        // the per-list counts and the exact kernel's row count
+        // the per-list counts
         MOBA_TRY(cudaMemsetAsync(ws.counts, 0, sizeof(int) * ((size_t)p.NBcap * p.H + 1), st));
         if (tc_gate) {
             MOBA_TRY(launch_kbar_split(p, ws.kbar, ws.kbhi, ws.kblo, ws.knorm, st));
@@ -318,20 +325,19 @@ static int gate_run(const Plan &p, Workspace &ws, void *c) {
     // stream-ordered scratch: the bf16 split of the caller's kbar, the norms,
     // and the rows left to the exact kernel
     const size_t n = (size_t)p.NBcap * p.H * p.D;
-    const size_t rows = (size_t)p.total * p.H;
     const size_t b_split = align256(2 * n * sizeof(__nv_bfloat16));
     const size_t b_norm = align256(sizeof(float) * p.NBcap * p.H);
-    const size_t b_list = align256(2 * sizeof(long long) * rows);
+    const size_t b_list = align256(2 * sizeof(long long) * need_list_rows(p));
     void *mem = nullptr;
-    if (cudaMallocAsync(&mem, b_split + b_norm + b_list + 256, x->st) != cudaSuccess)
+    if (cudaMallocAsync(&mem, b_split + b_norm + b_list + sizeof(int) * kMaxGateCtas, x->st) !=
+        cudaSuccess)
         return MOBA_ERR_CUDA;
     char *m = static_cast<char *>(mem);
     auto *hi = reinterpret_cast<__nv_bfloat16 *>(m);
     auto *nrm = reinterpret_cast<float *>(m + b_split);
     auto *list = reinterpret_cast<unsigned long long *>(m + b_split + b_norm);
     auto *cnt = reinterpret_cast<int *>(m + b_split + b_norm + b_list);
-    int rc = cuda_status(cudaMemsetAsync(cnt, 0, sizeof(int), x->st));
-    if (rc == MOBA_OK) rc = cuda_status(launch_kbar_split(p, x->kbar, hi, hi + n, nrm, x->st));
+    int rc = cuda_status(launch_kbar_split(p, x->kbar, hi, hi + n, nrm, x->st));
     if (rc == MOBA_OK)
         rc = cuda_status(launch_gate_tc(p, ws, q, x->kbar, hi, hi + n, nrm, x->idx, nullptr,
                                         list, cnt, x->st));

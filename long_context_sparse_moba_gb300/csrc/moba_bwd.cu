@@ -378,11 +378,17 @@ static cudaError_t launch_bwd_d(const Plan &p, const Workspace &ws, const bwd::A
     bwd_delta_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(out, a.dout, ws.delta, rows);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    constexpr int smem = smem_bytes<D>();
-    cudaFuncSetAttribute(bwd_kv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    const long long grid = a.n_units < (1ll << 30) ? a.n_units : (1ll << 30);
-    bwd_kv_kernel<D><<<(unsigned)grid, kThreads, smem, st>>>(a);
-    e = cudaGetLastError();
+    if (bwd_tc_supported(p)) {
+        // dk, dv and the dq accumulator on the tcgen05 tensor cores
+        e = launch_bwd_kv_tc(p, ws, a.q, a.k, a.v, a.lse, a.dout, a.dk, a.dv, st);
+    } else {
+        constexpr int smem = smem_bytes<D>();
+        cudaFuncSetAttribute(bwd_kv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        const long long grid = a.n_units < (1ll << 30) ? a.n_units : (1ll << 30);
+        bwd_kv_kernel<D><<<(unsigned)grid, kThreads, smem, st>>>(a);
+        note_launches(1);
+        e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return e;
     const long long n4 = rows * D / 4;
     const long long blocks = (n4 + 255) / 256;
@@ -390,7 +396,7 @@ static cudaError_t launch_bwd_d(const Plan &p, const Workspace &ws, const bwd::A
     bwd_dq_kernel<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, st>>>(
         reinterpret_cast<const float4 *>(ws.dq_acc), reinterpret_cast<uint2 *>(a.dq_out), n4,
         a.scale);
-    note_launches(3);
+    note_launches(2);
     return cudaGetLastError();
 }
 

@@ -54,6 +54,11 @@ constexpr int kRows = 128;                     // query rows per unit (the MMA's
 // are short enough to fit the register budget of 16 warps, else two)
 __host__ __device__ constexpr int threads_for(int nwg) { return 64 + 128 * nwg; }
 constexpr int kMaxQ = 6;                       // q stages at most
+#ifndef MOBA_GATE_NWG_SHORT
+#define MOBA_GATE_NWG_SHORT 4
+#endif
+// selection warpgroups when the top lists hold at most two blocks
+constexpr int kNwgShort = MOBA_GATE_NWG_SHORT;
 constexpr int kMaxSlots = 8;                   // TMEM score slots at most
 constexpr int kMaxBlocks = 256;                // blocks per sequence
 // Rows left to the exact kernel carry up to 8 candidate blocks packed one byte
@@ -69,7 +74,8 @@ struct Args {
     // rows the score margin cannot settle, for the exact kernel: two words per
     // row, the row (token * H + head, bit 62 set when every past block is a
     // candidate) and up to 8 candidate blocks, one byte each, ascending (0xff
-    // = none)
+    // = none).  CTA b writes its rows from row u0_b * 128 on (u0_b its first
+    // unit: room for all of its rows) and their number into need_count[b].
     unsigned long long *need_list;
     int *need_count;
     const int *gtile;    // [num_seqs + 1] 128-row tiles before each sequence
@@ -78,10 +84,13 @@ struct Args {
     int32_t *idx;
     int topk;
     // layout chosen by the host from the longest sequence's block count W
-    // (64, 128 or 256): nslots = 512 / W units in flight in TMEM, kb_rows =
-    // pooled-key rows kept resident (W rounded up to 128), nq q stages in
-    // the shared memory left
-    int nq, nslots, kb_rows;
+    // (64, 128 or 256): nslots units in flight in TMEM, kb_rows = pooled-key
+    // rows kept resident per term, nq q stages in the shared memory left.
+    // cat (W = 64): each 64-dim box holds the 64 hi rows followed by the 64
+    // lo rows, so one MMA chain with N = 128 scores q against both terms
+    // (columns c and 64 + c of a slot hold q.hi_c and q.lo_c); otherwise two
+    // chains accumulate q.hi and q.lo into the same columns.
+    int nq, nslots, kb_rows, cat;
     int *status;
     long long wait_limit;
 };
@@ -94,12 +103,12 @@ struct Smem {
     // tiles from a 1024-byte aligned base: nq q stages, then hi and lo, each
     // NB boxes of kb_rows x 64 dims
     // mbarriers: q_full[kMaxQ], q_empty[kMaxQ], kb_full, kb_empty,
-    // s_full[kMaxSlots], s_empty[kMaxSlots], drain; then the TMEM address slot
-    // and the abort flag
+    // s_full[kMaxSlots], s_empty[kMaxSlots], drain; then the TMEM address slot,
+    // the abort flag and the count of rows left to the exact kernel
     static constexpr int kBarQF = 0, kBarQE = kBarQF + kMaxQ, kBarKF = kBarQE + kMaxQ,
                          kBarKE = kBarKF + 1, kBarSF = kBarKE + 1, kBarSE = kBarSF + kMaxSlots,
                          kBarDrain = kBarSE + kMaxSlots, kNumBars = kBarDrain + 1;
-    static constexpr uint32_t kMisc = kNumBars * 8 + 8;
+    static constexpr uint32_t kMisc = kNumBars * 8 + 16;
     // the misc words go into the alignment slack when it is large enough, else
     // after the tiles
     static constexpr uint32_t kTileBudget = 227 * 1024 - 1008 - kMisc;
@@ -168,12 +177,15 @@ __global__ void __launch_bounds__(threads_for(NWG), 1)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = saddr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t kKBox = (uint32_t)a.kb_rows * 128;  // one 64-dim box of pooled keys
+    // stride between the 64-dim boxes of pooled keys; in cat mode a box holds
+    // both terms
+    const uint32_t kKBox = (uint32_t)a.kb_rows * 128 * (a.cat ? 2u : 1u);
     const uint32_t misc = (base - raw >= L::kMisc) ? raw : base + L::tiles(a.nq, a.kb_rows);
     uint8_t *gmisc = smem_raw + (misc - raw);
     auto bar = [&](int i) -> uint32_t { return misc + 8u * (uint32_t)i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gmisc + L::kNumBars * 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gmisc + L::kNumBars * 8 + 4);
+    int *need_cnt = reinterpret_cast<int *>(gmisc + L::kNumBars * 8 + 8);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     MOBA_RETURN_IF_BAD(a.g);
     const int H = a.g.H, km1 = a.topk - 1;
@@ -181,11 +193,15 @@ __global__ void __launch_bounds__(threads_for(NWG), 1)
     const int n_units = H * __ldg(a.gtile + a.g.num_seqs);
     const int u0 = (int)((long long)n_units * blockIdx.x / gridDim.x);
     const int u1 = (int)((long long)n_units * (blockIdx.x + 1) / gridDim.x);
-    if (u0 >= u1) return;
+    if (u0 >= u1) {
+        if (tid == 0) a.need_count[blockIdx.x] = 0;
+        return;
+    }
     Ctl ctl{abort_flag, a.status, a.wait_limit};
     const int nq = a.nq, nslots = a.nslots;
     const uint32_t slot_cols = 512u / nslots;
-    const uint32_t sQ = base, sHi = base + nq * L::kQStage, sLo = sHi + L::NB * kKBox;
+    const uint32_t sQ = base, sHi = base + nq * L::kQStage;
+    const uint32_t sLo = a.cat ? sHi + (uint32_t)a.kb_rows * 128 : sHi + L::NB * kKBox;
 
     if (tid == 0) {
         for (int s = 0; s < kMaxQ; ++s) {
@@ -200,6 +216,7 @@ __global__ void __launch_bounds__(threads_for(NWG), 1)
         }
         mbar_init(bar(L::kBarDrain), 1);
         *abort_flag = 0;
+        *need_cnt = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -235,11 +252,14 @@ __global__ void __launch_bounds__(threads_for(NWG), 1)
                         go = false;
                         break;
                     }
-                    const int nch = (U.nb + 127) / 128;  // 128-block chunks, at most 2
-                    mbar_expect_tx(bar(L::kBarKF), 2u * L::NB * nch * 128 * 128);
+                    // chunks of kb_rows blocks (one in cat mode, else at most 2
+                    // of 128)
+                    const int rows = a.cat ? a.kb_rows : 128;
+                    const int nch = (U.nb + rows - 1) / rows;
+                    mbar_expect_tx(bar(L::kBarKF), 2u * L::NB * nch * rows * 128);
                     for (int x = 0; x < L::NB; ++x)
                         for (int c = 0; c < nch; ++c) {
-                            const uint32_t off = x * kKBox + c * 128 * 128;
+                            const uint32_t off = x * kKBox + c * rows * 128;
                             tma_load_3d(sHi + off, &tmap_hi, bar(L::kBarKF), x * 64, U.h,
                                         U.bbase + c * 128);
                             tma_load_3d(sLo + off, &tmap_lo, bar(L::kBarKF), x * 64, U.h,
@@ -305,7 +325,19 @@ __global__ void __launch_bounds__(threads_for(NWG), 1)
                     break;
                 }
                 tc_fence_after();
-                if (U.cmax > 0) {
+                if (U.cmax > 0 && a.cat) {
+                    // one chain: N = 128 rows of [hi; lo]
+                    const uint32_t idesc = idesc_bf16(kRows, 128, 0);
+                    const uint32_t tS = tmem + w * slot_cols;
+                    const uint64_t dq = sdesc(sQ + s * L::kQStage, 16, 1024);
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint64_t aoff = (uint64_t)((k / 4) * (L::kQBox >> 4) + (k % 4) * 2);
+                        const uint64_t boff = (uint64_t)((k / 4) * kbox16 + (k % 4) * 2);
+                        tc_mma(tS, dq + aoff, dhi + boff, idesc, k > 0);
+                    }
+                    tc_commit(bar(L::kBarSF + w));
+                } else if (U.cmax > 0) {
                     const int n = min((int)slot_cols, (U.cmax + 15) & ~15);
                     const uint32_t idesc = idesc_bf16(kRows, n, 0);
                     const uint32_t tS = tmem + w * slot_cols;
@@ -382,9 +414,9 @@ __global__ void __launch_bounds__(threads_for(NWG), 1)
             bool need = false;  // the exact kernel writes this row
             unsigned long long cand = ~0ull;  // its candidate blocks, one byte each
             int ncand = 0;
-            if (!__all_sync(0xffffffffu, wait_fast(bar(L::kBarSF + slot), (i / nslots) & 1, ctl))) break;
-            tc_fence_after();
-            // ||q_r||^2 for the margin: the last read of the q stage
+            // ||q_r||^2 for the margin, read from the q stage as soon as it has
+            // landed, so that it overlaps the unit's MMAs
+            if (!__all_sync(0xffffffffu, wait_fast(bar(L::kBarQF + s), (i / nq) & 1, ctl))) break;
             float qq = 0.f;
             if (scored) {
 #pragma unroll
@@ -401,21 +433,53 @@ __global__ void __launch_bounds__(threads_for(NWG), 1)
                     }
                 }
             }
+            if (!__all_sync(0xffffffffu, wait_fast(bar(L::kBarSF + slot), (i / nslots) & 1, ctl))) break;
+            tc_fence_after();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::kBarQE + s));  // the q stage is free
+            if (lane == 0) mbar_arrive(bar(L::kBarQE + s));  // the MMAs have read the q stage
+            // the TMEM slot is handed back right after its last read
+            bool slot_held = true;
+            auto release_slot = [&]() {
+                if (slot_held) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(L::kBarSE + slot));
+                    slot_held = false;
+                }
+            };
             if (U.cmax > 0) {
                 // pass 1: the k largest approximate scores of the row (values only:
                 // a min/max insertion network, 2k-1 operations per block)
                 float tv[KCAP + 1];
 #pragma unroll
                 for (int x = 0; x <= KCAP; ++x) tv[x] = -INFINITY;
-                // CW scores per TMEM round trip (64 when the registers allow)
+                // CW scores per TMEM round trip (64 when the registers allow);
+                // in cat mode a score is the sum of its hi and lo columns
                 constexpr int CW = NWG >= 4 ? 32 : 64;
                 uint32_t v[CW / 32][32];
-                for (int c0 = 0; c0 < U.cmax; c0 += CW) {
+                auto load_chunk = [&](int c0) {
 #pragma unroll
-                    for (int hh = 0; hh < CW / 32; ++hh) tc_ld32(tS + c0 + 32 * hh, v[hh]);
+                    for (int hh = 0; hh < CW / 32; ++hh) {
+                        tc_ld32(tS + c0 + 32 * hh, v[hh]);
+                        if (a.cat) {  // the lo columns, 16 at a time (register budget)
+#pragma unroll
+                            for (int q16 = 0; q16 < 2; ++q16) {
+                                uint32_t lo[16];
+                                tc_ld16(tS + 64 + c0 + 32 * hh + 16 * q16, lo);
+                                tc_wait_ld();
+#pragma unroll
+                                for (int e = 0; e < 16; ++e)
+                                    v[hh][16 * q16 + e] = __float_as_uint(
+                                        __uint_as_float(v[hh][16 * q16 + e]) + __uint_as_float(lo[e]));
+                            }
+                        }
+                    }
                     tc_wait_ld();
+                };
+                const bool one_chunk = U.cmax <= CW;
+                for (int c0 = 0; c0 < U.cmax; c0 += CW) {
+                    load_chunk(c0);
+                    if (one_chunk) release_slot();
 #pragma unroll
                     for (int e = 0; e < CW; ++e) {
                         const float x = (c0 + e < ci) ? __uint_as_float(v[e >> 5][e & 31]) : -INFINITY;
@@ -439,11 +503,8 @@ __global__ void __launch_bounds__(threads_for(NWG), 1)
                 const float cut = need ? T - 2.f * E : T;
                 if (__any_sync(0xffffffffu, scored)) {
                     for (int c0 = 0; c0 < U.cmax; c0 += CW) {
-                        if (U.cmax > CW) {  // else pass 1's only chunk is still in registers
-#pragma unroll
-                            for (int hh = 0; hh < CW / 32; ++hh) tc_ld32(tS + c0 + 32 * hh, v[hh]);
-                            tc_wait_ld();
-                        }
+                        // else pass 1's only chunk is still in registers
+                        if (!one_chunk) load_chunk(c0);
                         // bit e: block c0 + e is selected / a candidate
                         unsigned long long mask = 0ull;
 #pragma unroll
@@ -467,24 +528,23 @@ __global__ void __launch_bounds__(threads_for(NWG), 1)
                     }
                 }
             }
-            // rows left to the exact kernel: one list reservation per warp
+            release_slot();  // the slot is free for the unit after next
+            // rows left to the exact kernel go to this CTA's own region of the
+            // list (room for all of its rows), reserved with a shared-memory count
             const unsigned nmask = __ballot_sync(0xffffffffu, need);
             if (nmask) {
                 const int leader = __ffs(nmask) - 1;
                 int base = 0;
-                if (lane == leader) base = atomicAdd(a.need_count, __popc(nmask));
+                if (lane == leader) base = atomicAdd(need_cnt, __popc(nmask));
                 base = __shfl_sync(0xffffffffu, base, leader);
                 if (need) {
-                    const int slot2 = 2 * (base + __popc(nmask & ((1u << lane) - 1u)));
-                    const unsigned long long row = (unsigned long long)tok * H + U.h;
-                    a.need_list[slot2] = ncand > 8 ? (row | (1ull << 62)) : row;
+                    const size_t slot2 =
+                        2 * ((size_t)u0 * kRows + base + __popc(nmask & ((1u << lane) - 1u)));
+                    const unsigned long long rowid = (unsigned long long)tok * H + U.h;
+                    a.need_list[slot2] = ncand > 8 ? (rowid | (1ull << 62)) : rowid;
                     a.need_list[slot2 + 1] = cand;
                 }
             }
-            // the TMEM half is free for the unit after next
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::kBarSE + slot));
 
             // selected past blocks of my row, ascending, then the own block
             if (valid && !need) {
@@ -530,6 +590,7 @@ __global__ void __launch_bounds__(threads_for(NWG), 1)
     }
     tc_fence_before();
     __syncthreads();
+    if (tid == 0) a.need_count[blockIdx.x] = *need_cnt;
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
@@ -547,20 +608,28 @@ __global__ void __launch_bounds__(threads_for(NWG), 1)
 // like the gate's rows.
 // ---------------------------------------------------------------------------
 constexpr int kExactWarps = 8;
+constexpr int kExactSplit = 4;  // CTAs of the exact kernel per gate CTA
 
 template <int D, int KCAP>
 __global__ void __launch_bounds__(32 * kExactWarps)
     gate_exact_kernel(Geometry g, const __nv_bfloat16 *__restrict__ q,
                       const float *__restrict__ kbar, int32_t *__restrict__ idx, int topk,
                       int *__restrict__ counts, const unsigned long long *__restrict__ need_list,
-                      const int *__restrict__ need_count) {
+                      const int *__restrict__ need_count, const int *__restrict__ gtile,
+                      int gate_ctas) {
     MOBA_RETURN_IF_BAD(g);
     const int lane = threadIdx.x & 31;
-    const int n = *need_count;
     const int km1 = topk - 1;
-    for (int w = blockIdx.x * kExactWarps + (threadIdx.x >> 5); w < n;
-         w += gridDim.x * kExactWarps) {
-        const unsigned long long w0 = need_list[2 * w], cand = need_list[2 * w + 1];
+    // the gate's CTA cb left need_count[cb] rows from row u0_cb * 128 of the
+    // list; kExactSplit CTAs share a region, warp by warp
+    const int n_units = g.H * __ldg(gtile + g.num_seqs);
+    const int part = blockIdx.x % kExactSplit;
+    for (int cb = blockIdx.x / kExactSplit; cb < gate_ctas; cb += gridDim.x / kExactSplit) {
+    const size_t region = (size_t)((long long)n_units * cb / gate_ctas) * kRows;
+    const int n = need_count[cb];
+    for (int w = part * kExactWarps + (threadIdx.x >> 5); w < n; w += kExactSplit * kExactWarps) {
+        const size_t e = region + w;
+        const unsigned long long w0 = need_list[2 * e], cand = need_list[2 * e + 1];
         const bool all = (w0 >> 62) & 1ull;
         const long long r = (long long)(w0 & ((1ull << 62) - 1));
         const int t = (int)(r / g.H), h = (int)(r % g.H);
@@ -635,6 +704,7 @@ __global__ void __launch_bounds__(32 * kExactWarps)
             for (int x = km1 + 1; x < topk; ++x) out[x] = -1;
         }
     }
+    }
 }
 
 }  // namespace gate_tc
@@ -655,28 +725,31 @@ static cudaError_t launch_gate_tc_d(const Plan &p, const gate_tc::Args &a, const
                                     const __nv_bfloat16 *khi, const __nv_bfloat16 *klo,
                                     cudaStream_t st) {
     CUtensorMap mq, mh, ml;
+    const int kb_box = a.cat ? a.kb_rows : 128;  // pooled-key rows per TMA box
     if (!make_tma_3d(&mq, q, p.total, p.H, D, gate_tc::kRows) ||
-        !make_tma_3d(&mh, khi, p.NBcap, p.H, D, 128) || !make_tma_3d(&ml, klo, p.NBcap, p.H, D, 128))
+        !make_tma_3d(&mh, khi, p.NBcap, p.H, D, kb_box) ||
+        !make_tma_3d(&ml, klo, p.NBcap, p.H, D, kb_box))
         return cudaErrorInvalidValue;
     // an upper bound of the units; CTAs beyond the real count return at once
     const long long units_max =
         (long long)p.H * (((long long)p.total + gate_tc::kRows - 1) / gate_tc::kRows + p.num_seqs);
-    const int grid = (int)std::min<long long>(sm_count(), units_max);
+    const int grid = (int)std::min<long long>(std::min(sm_count(), kMaxGateCtas), units_max);
     const int km1 = p.topk - 1;
     using L = gate_tc::Smem<D>;
     const int smem = (int)(L::tiles(a.nq, a.kb_rows) + 1008 + L::kMisc);
 #define MOBA_GATE_TC_CASE(KC)                                                                   \
     {                                                                                           \
-        constexpr int nwg = (KC) <= 8 ? 3 : 2;                                                  \
+        constexpr int nwg = (KC) <= 2 ? gate_tc::kNwgShort : (KC) <= 8 ? 3 : 2;                          \
         auto kern = gate_tc::gate_tc_kernel<D, KC, nwg>;                                        \
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                                              smem);                                             \
         if (e != cudaSuccess) return e;                                                         \
         kern<<<grid, gate_tc::threads_for(nwg), smem, st>>>(mq, mh, ml, a);                    \
         if ((e = cudaGetLastError()) != cudaSuccess) return e;                                  \
-        gate_tc::gate_exact_kernel<D, KC><<<4 * sm_count(), 32 * gate_tc::kExactWarps, 0,   \
-                                             st>>>(a.g, a.q, a.kbar, a.idx, a.topk, a.counts,  \
-                                                   a.need_list, a.need_count);                 \
+        gate_tc::gate_exact_kernel<D, KC><<<grid * gate_tc::kExactSplit,                        \
+                                            32 * gate_tc::kExactWarps, 0, st>>>(                \
+            a.g, a.q, a.kbar, a.idx, a.topk, a.counts, a.need_list, a.need_count, a.gtile,    \
+            grid);                                                                              \
         return cudaGetLastError();                                                              \
     }
     if (km1 <= 1) MOBA_GATE_TC_CASE(1)
@@ -716,8 +789,9 @@ cudaError_t launch_gate_tc(const Plan &p, const Workspace &ws, const __nv_bfloat
     // or 256 columns; as many q stages as the shared memory left holds
     const int nmax = (p.max_len + p.bs - 1) / p.bs;
     const int W = nmax <= 64 ? 64 : nmax <= 128 ? 128 : 256;
-    a.nslots = 512 / W;
-    a.kb_rows = W <= 128 ? 128 : 256;
+    a.cat = W == 64 ? 1 : 0;
+    a.nslots = a.cat ? 4 : 512 / W;          // a cat slot holds 64 hi + 64 lo columns
+    a.kb_rows = a.cat ? 64 : W <= 128 ? 128 : 256;
     const uint32_t budget = p.D == 64 ? gate_tc::Smem<64>::kTileBudget : gate_tc::Smem<128>::kTileBudget;
     const uint32_t kb = p.D == 64 ? gate_tc::Smem<64>::kb_bytes(a.kb_rows)
                                   : gate_tc::Smem<128>::kb_bytes(a.kb_rows);

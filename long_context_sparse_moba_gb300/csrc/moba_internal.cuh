@@ -18,6 +18,7 @@ namespace moba {
 constexpr int kMaxPastSlots = 31;      // topk - 1 limit when gating is needed
 constexpr int kSlotBits = 5;           // regroup entry = token << 5 | slot
 constexpr int kMaxTokens = 1 << 26;
+constexpr int kMaxGateCtas = 1024;     // CTAs of the tensor-core gate at most
 
 // Device status word of the current device (defined in moba_api.cu); kernels
 // with bounded waits record MOBA_ERR_TIMEOUT there.  moba_get_status reads
@@ -56,7 +57,7 @@ struct Workspace {
     int32_t *idx;     // [total][H][topk]
     int *counts;      // [NBcap * H]   queries per (block, head) past list (zero
                       //               again once the scatter has used them)
-    int *need_count;  // [1] rows the tensor-core gate left to its exact kernel
+    int *need_count;  // [kMaxGateCtas] rows each tensor-core gate CTA left to the exact kernel
     unsigned long long *need_list;  // [2 * total * H] those rows and their candidates
     int *list_off;    // [NBcap * H + 1]
     int *tile_off;    // [NBcap * H + 1]  first attention job of each list
@@ -147,8 +148,9 @@ cudaError_t launch_kbar_split(const Plan &p, const float *kbar, __nv_bfloat16 *h
                               __nv_bfloat16 *lo, float *norm, cudaStream_t st);
 // tensor-core gate (scores on tcgen05, exact fp32 re-score of the candidates);
 // with counts != nullptr it also adds every past selection into counts.
-// need_list (room for every row) and *need_count (zero on entry) carry the rows
-// whose selection the score margin cannot settle to the exact follow-up kernel
+// need_list (room for every row) and need_count (kMaxGateCtas ints, written by
+// the gate) carry the rows whose selection the score margin cannot settle to
+// the exact follow-up kernel
 bool gate_tc_supported(const Plan &p);
 cudaError_t launch_gate_tc(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
                            const float *kbar, const __nv_bfloat16 *khi, const __nv_bfloat16 *klo,
@@ -164,6 +166,14 @@ size_t decode_ticket_offset(int B, int H, int D, int topk);
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *kbar,
                           const int32_t *lens, void *out, float *lse, int32_t *idx, int B, int H,
                           int S_max, int D, int bs, int topk, void *scratch, cudaStream_t st);
+// backward dk, dv and dq accumulation on the tcgen05 tensor cores (head size
+// 128 with the tcgen05 attention kernels selected); ws.delta must hold dO . O
+// and ws.dq_acc must be zero
+bool bwd_tc_supported(const Plan &p);
+cudaError_t launch_bwd_kv_tc(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
+                             const __nv_bfloat16 *k, const __nv_bfloat16 *v,
+                             const float *lse, const __nv_bfloat16 *dout, __nv_bfloat16 *dk,
+                             __nv_bfloat16 *dv, cudaStream_t st);
 // idx of the rows the gate does not run for (top-1, or top-k covering every
 // block): the own block and every earlier one, ascending, -1 padded
 cudaError_t launch_fill_idx(const Plan &p, const Workspace &ws, int32_t *idx, cudaStream_t st);

@@ -116,7 +116,7 @@ def test_backward_workspace_variant_and_determinism():
     b = gpu_backward(inp, w, 3, out, lse, dout, workspace=ws)
     assert ops.get_status() == ops.MOBA_OK
     # the summation order is not fixed (the regroup lists fill in any order, dq
-    # adds fp32 atomics): the two calls agree to rounding, not bit for bit
+    # adds fp32 reductions): the two calls agree to rounding, not bit for bit
     for x, y in zip(a, b):
         d = (x.float() - y.float()).abs()
         assert d.max() <= 1e-2 * x.float().abs().max(), d.max()
@@ -146,6 +146,17 @@ def test_backward_train32k_sampled_and_identities():
                                   r["idx"])
     got = flat(dq).float().cpu().numpy()[toks, heads]
     check("dq", got[~differ], ref[~differ])
+    # dq, dk and dv of two whole heads element by element: the oracle's backward
+    # on the head's own slice (gate, selection and attention are per head)
+    for h in (0, w.H - 1):
+        sl = lambda t: t[:, h:h + 1, :].contiguous()
+        refh = oracle.moba_bwd(sl(q), sl(k), sl(v), sl(g), cu, 1, w.D, w.block_size, topk)
+        fwdh = oracle.moba_full(sl(q), sl(k), sl(v), cu, 1, w.D, w.block_size, topk)
+        wh = workloads.Workload(**{**w.__dict__, "H": 1})
+        row_ok, key_ok = tie_masks(wh, idx.cpu().numpy()[:, h:h + 1, :], refh["idx"],
+                                   fwdh["gap"])
+        for name, t, keep in (("dq", dq, row_ok), ("dk", dk, key_ok), ("dv", dv, key_ok)):
+            check(name, flat(t)[:, h:h + 1, :].float().cpu().numpy(), refh[name], keep)
     # sum over keys of dv = sum over rows of dO; sum over keys of dk = 0 (per head)
     dvs = flat(dv).double().sum(0)
     gs = flat(dout).double().sum(0)
