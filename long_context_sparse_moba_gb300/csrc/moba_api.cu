@@ -125,6 +125,10 @@ size_t workspace_bytes(const Plan &p, Workspace *ws, char *base, bool backward) 
         const size_t rows = (size_t)p.total * p.H;
         w.dq_acc = static_cast<float *>(take(sizeof(float) * rows * p.D));
         w.delta = static_cast<float *>(take(sizeof(float) * rows));
+        if (gate) {
+            w.list_l2 = static_cast<float *>(take(sizeof(float) * rows * p.km1));
+            w.list_dl = static_cast<float *>(take(sizeof(float) * rows * p.km1));
+        }
     }
     if (ws) *ws = w;
     return off;

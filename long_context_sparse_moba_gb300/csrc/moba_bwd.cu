@@ -54,7 +54,7 @@ struct Args {
     Geometry g;
     const __nv_bfloat16 *q, *k, *v, *dout;
     const float *lse;           // forward lse, natural log, forward layout
-    const float *delta;         // [total][H]
+    const float *delta;         // [H][total]
     float *dq_acc;              // [total][H][D], zero on entry
     __nv_bfloat16 *dq_out, *dk, *dv;  // [total][H][D]
     int fixed, S_fixed, dense, km1;
@@ -89,7 +89,7 @@ template <int D>
 __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16 *__restrict__ out,
                                                         const __nv_bfloat16 *__restrict__ dout,
                                                         float *__restrict__ delta,
-                                                        long long rows) {
+                                                        long long rows, int H, int total) {
     const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     if (r >= rows) return;  // whole warps leave together
     const int lane = threadIdx.x & 31;
@@ -106,7 +106,8 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16 *__r
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) delta[r] = acc;
+    // [H][total]: each head's rows contiguous
+    if (lane == 0) delta[(size_t)(r % H) * total + r / H] = acc;
 }
 
 template <int D>
@@ -177,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_kv_kernel(Args a) {
                     const size_t li = a.fixed ? ((size_t)b * H + h) * a.S_fixed + (tok - seq0)
                                               : (size_t)h * a.g.total + tok;
                     l2 = __ldg(a.lse + li) * kLog2e;
-                    dl = __ldg(a.delta + (size_t)tok * H + h);
+                    dl = __ldg(a.delta + (size_t)h * a.g.total + tok);
                 }
                 r_tok[mb * kM + r] = tok;
                 r_lse[mb * kM + r] = l2;
@@ -375,7 +376,8 @@ static cudaError_t launch_bwd_d(const Plan &p, const Workspace &ws, const bwd::A
                                 const __nv_bfloat16 *out, cudaStream_t st) {
     using namespace bwd;
     const long long rows = (long long)p.total * p.H;
-    bwd_delta_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(out, a.dout, ws.delta, rows);
+    bwd_delta_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(out, a.dout, ws.delta, rows,
+                                                                      p.H, p.total);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (bwd_tc_supported(p)) {

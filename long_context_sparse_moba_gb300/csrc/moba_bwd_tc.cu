@@ -26,8 +26,8 @@
 //   dV  += P^T dO       (A = P^T from TMEM, B = dO MN-major)
 //   dK  += dS^T Q       (A = dS^T from shared memory, B = Q MN-major)
 //   dQ^T = K^T dS^T     (A = K MN-major, B = dS^T MN-major; M = 128 dims)
-// and the dQ^T tile (lanes = head dims, columns = rows) is added into an fp32
-// accumulator with one coalesced reduction per (row, 32 dims).
+// and the dQ^T tile (lanes = head dims, columns = rows) is re-laid by rows in
+// shared memory and added into an fp32 accumulator with 16-byte reductions.
 //
 // Roles (320 threads):
 //   warp 0      producer: K and V of the unit (TMA), per tile Q and dO (TMA
@@ -41,8 +41,9 @@
 //   warps 2..9  two groups of four warps: group n % 2 takes tile n.  Thread
 //               = key (its TMEM lane): P^T and dS^T of its key over the 64
 //               rows, P^T packed into TMEM over S^T, dS^T into shared memory;
-//               then the tile's dQ^T epilogue (thread = head dim).  At the end
-//               of a unit group 0 writes dV, group 1 dK.
+//               then the tile's dQ^T epilogue (thread = head dim; staged by
+//               rows through the group's dS^T buffer for 16-byte reductions).
+//               At the end of a unit group 0 writes dV, group 1 dK.
 // TMEM (512 columns): dV [0, 128), dK [128, 256), tile buffer b at 256 + 128 b:
 // S^T / P^T / dQ^T in its first 64 columns, dP^T in the next 64.  dQ^T is
 // written over P^T: MMAs from one thread run in order, so the dV MMA has read
@@ -73,7 +74,8 @@ struct Args {
     Geometry g;
     const __nv_bfloat16 *q, *k, *v, *dout;
     const float *lse;           // forward lse, natural log, forward layout
-    const float *delta;         // [total][H]
+    const float *delta;         // [H][total]
+    const float *list_l2, *list_dl;  // per list entry: its row's lse (log2) and delta
     float *dq_acc;              // [total][H][D], zero on entry, unscaled dS K
     __nv_bfloat16 *dk, *dv;     // [total][H][D]
     int fixed, S_fixed, dense, km1;
@@ -108,6 +110,13 @@ struct Smem {
     static_assert(kRequest <= 227 * 1024, "shared memory per CTA");
 };
 
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float x) {
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(x) : "memory");
+}
+// barrier of the `count` threads of one softmax group (ids 1, 2; 0 is the CTA's)
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 // instruction descriptor of kind::f16 with either operand MN-major
 __host__ __device__ constexpr uint32_t idesc(int M, int N, int a_mn, int b_mn) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
@@ -239,10 +248,110 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ================= producer =================
+        // Row metadata of a tile, two rows per lane; the loads of tile t + 1
+        // are issued before the copies of tile t and used one tile later.
+        struct TileMeta {
+            int tok[2], lim[2];
+            float l2[2], dl[2];
+        };
+        auto fetch = [&](int t, TileMeta &m) {
+            const bool own = t < U.n_own;
+            const int row0 = U.key0 + t * kRowsT;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int r = 2 * lane + j;
+                m.tok[j] = -1;
+                m.lim[j] = -1;
+                m.l2[j] = 0.f;
+                m.dl[j] = 0.f;
+                if (own) {
+                    const int g = row0 + r;
+                    if (g < U.own_end) {
+                        m.tok[j] = g;
+                        m.lim[j] = min(g - U.key0, U.nkeys - 1);
+                        const size_t li = a.fixed
+                                              ? ((size_t)U.b * H + U.h) * a.S_fixed + (g - U.seq0)
+                                              : (size_t)U.h * a.g.total + g;
+                        m.l2[j] = __ldg(a.lse + li) * kLog2e;
+                        m.dl[j] = __ldg(a.delta + (size_t)U.h * a.g.total + g);
+                    }
+                } else {
+                    const int pr = (t - U.n_own) * kRowsT + r;
+                    if (pr < U.lcnt) {
+                        const int pos = U.lbeg + pr;
+                        m.tok[j] = __ldg(a.list + pos) >> kSlotBits;
+                        m.lim[j] = U.nkeys - 1;
+                        m.l2[j] = __ldg(a.list_l2 + pos);
+                        m.dl[j] = __ldg(a.list_dl + pos);
+                    }
+                }
+            }
+        };
         int n = 0, ui = 0;
         bool go = true;
-        int kvpend = -1;                 // unit whose K/V copy is in flight
+        int kvpend = -1;                    // unit whose K/V copy is in flight
         int qpend[kStages] = {-1, -1, -1};  // tile whose Q/dO copy is in flight per stage
+        // stage tile t of the unit (metadata m), fetching tile t + 1 into nx
+        auto do_tile = [&](int t, const TileMeta &m, TileMeta &nx) -> bool {
+            if (t + 1 < U.n_tiles) fetch(t + 1, nx);
+            const int s = n % kStages;
+            if (n >= kStages) {
+                const uint32_t par = (uint32_t)((n / kStages - 1) & 1);
+                if (!wait_fast(bar(L::kBarQE + s), par, ctl) ||
+                    !wait_fast(bar(L::kBarME + s), par, ctl))
+                    return false;
+            }
+            const bool own = t < U.n_own;
+            const int row0 = U.key0 + t * kRowsT;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int r = 2 * lane + j;
+                meta_i(s)[r] = m.tok[j];
+                meta_i(s)[kRowsT + r] = m.lim[j];
+                meta_f(s)[2 * kRowsT + r] = m.l2[j];
+                meta_f(s)[3 * kRowsT + r] = m.dl[j];
+            }
+            const uint32_t q_s = sQ + s * 2 * L::kRBox, o_s = sO + s * 2 * L::kRBox;
+            if (own) {
+                if (lane == 0) {
+                    mbar_expect_tx(bar(L::kBarQF + s), 4 * L::kRBox);
+                    for (int x = 0; x < 2; ++x) {
+                        tma_load_3d(q_s + x * L::kRBox, &tmap_q, bar(L::kBarQF + s), x * 64, U.h,
+                                    row0);
+                        tma_load_3d(o_s + x * L::kRBox, &tmap_o, bar(L::kBarQF + s), x * 64, U.h,
+                                    row0);
+                    }
+                } else {
+                    mbar_arrive(bar(L::kBarQF + s));
+                }
+            } else {
+                // the tile's 64 rows of Q and dO, 16 bytes per lane: an instruction
+                // moves 128 bytes (one box row) of each of four rows, lane ->
+                // (row it * 4 + lane / 8, chunk lane % 8), into the
+                // 128-byte-swizzled layout the TMA would write
+                const int ch = lane & 7;
+#pragma unroll 4
+                for (int it = 0; it < kRowsT / 4; ++it) {
+                    const int r = it * 4 + (lane >> 3);
+                    const int t0 = __shfl_sync(0xffffffffu, m.tok[0], r >> 1);
+                    const int t1 = __shfl_sync(0xffffffffu, m.tok[1], r >> 1);
+                    const int tok = (r & 1) ? t1 : t0;
+                    const bool ok = tok >= 0;
+                    const size_t src_row = ((size_t)(ok ? tok : 0) * H + U.h) * D + ch * 8;
+                    const uint32_t off = (uint32_t)r * 128 + ((uint32_t)(ch ^ (r & 7)) << 4);
+#pragma unroll
+                    for (int x = 0; x < 2; ++x) {
+                        cp_async16(q_s + x * L::kRBox + off, a.q + src_row + x * 64, ok);
+                        cp_async16(o_s + x * L::kRBox + off, a.dout + src_row + x * 64, ok);
+                    }
+                }
+                cp_async_arrive_noinc(bar(L::kBarQF + s));
+            }
+            qpend[s] = n;
+            mbar_arrive(bar(L::kBarMF + s));
+            ++n;
+            return true;
+        };
         while (go && walk.next(a, U)) {
             if (ui > 0 && !wait_fast(bar(L::kBarKVE), (ui - 1) & 1, ctl)) break;
             if (lane == 0) {
@@ -253,85 +362,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             kvpend = ui;
-            for (int t = 0; t < U.n_tiles; ++t, ++n) {
-                const int s = n % kStages;
-                if (n >= kStages) {
-                    const uint32_t par = (uint32_t)((n / kStages - 1) & 1);
-                    if (!wait_fast(bar(L::kBarQE + s), par, ctl) ||
-                        !wait_fast(bar(L::kBarME + s), par, ctl)) {
-                        go = false;
-                        break;
-                    }
-                }
-                const bool own = t < U.n_own;
-                const int row0 = U.key0 + t * kRowsT;  // own tiles: first row's token
-                int toks[2];
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int r = 2 * lane + j;
-                    int tok = -1, lim = -1;
-                    if (own) {
-                        const int g = row0 + r;
-                        if (g < U.own_end) {
-                            tok = g;
-                            lim = min(g - U.key0, U.nkeys - 1);
-                        }
-                    } else {
-                        const int pr = (t - U.n_own) * kRowsT + r;
-                        if (pr < U.lcnt) {
-                            tok = __ldg(a.list + U.lbeg + pr) >> kSlotBits;
-                            lim = U.nkeys - 1;
-                        }
-                    }
-                    float l2 = 0.f, dl = 0.f;
-                    if (tok >= 0) {
-                        const size_t li = a.fixed
-                                              ? ((size_t)U.b * H + U.h) * a.S_fixed + (tok - U.seq0)
-                                              : (size_t)U.h * a.g.total + tok;
-                        l2 = __ldg(a.lse + li) * kLog2e;
-                        dl = __ldg(a.delta + (size_t)tok * H + U.h);
-                    }
-                    meta_i(s)[r] = tok;
-                    meta_i(s)[kRowsT + r] = lim;
-                    meta_f(s)[2 * kRowsT + r] = l2;
-                    meta_f(s)[3 * kRowsT + r] = dl;
-                    toks[j] = tok;
-                }
-                const uint32_t q_s = sQ + s * 2 * L::kRBox, o_s = sO + s * 2 * L::kRBox;
-                if (own) {
-                    if (lane == 0) {
-                        mbar_expect_tx(bar(L::kBarQF + s), 4 * L::kRBox);
-                        for (int x = 0; x < 2; ++x) {
-                            tma_load_3d(q_s + x * L::kRBox, &tmap_q, bar(L::kBarQF + s), x * 64, U.h,
-                                        row0);
-                            tma_load_3d(o_s + x * L::kRBox, &tmap_o, bar(L::kBarQF + s), x * 64, U.h,
-                                        row0);
-                        }
-                    } else {
-                        mbar_arrive(bar(L::kBarQF + s));
-                    }
-                } else {
-                    // this lane's two rows of Q and dO, 16 bytes at a time, into
-                    // the 128-byte-swizzled layout the TMA would write
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        const int r = 2 * lane + j;
-                        const bool ok = toks[j] >= 0;
-                        const size_t src_row = ((size_t)(ok ? toks[j] : 0) * H + U.h) * D;
-#pragma unroll
-                        for (int x = 0; x < 2; ++x)
-#pragma unroll
-                            for (int ch = 0; ch < 8; ++ch) {
-                                const uint32_t off = x * L::kRBox + (uint32_t)r * 128 +
-                                                     ((uint32_t)(ch ^ (r & 7)) << 4);
-                                cp_async16(q_s + off, a.q + src_row + x * 64 + ch * 8, ok);
-                                cp_async16(o_s + off, a.dout + src_row + x * 64 + ch * 8, ok);
-                            }
-                    }
-                    cp_async_arrive_noinc(bar(L::kBarQF + s));
-                }
-                qpend[s] = n;
-                mbar_arrive(bar(L::kBarMF + s));
+            // two metadata sets in turn, so a tile's loads are in flight while
+            // the previous tile is staged
+            TileMeta ma, mb;
+            fetch(0, ma);
+            for (int t = 0; go && t < U.n_tiles; t += 2) {
+                go = do_tile(t, ma, mb);
+                if (go && t + 1 < U.n_tiles) go = do_tile(t + 1, mb, ma);
             }
             ++ui;
         }
@@ -511,7 +548,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(L::kBarPF + wg));
 
-                // dQ^T of the tile: lane = head dim kl, column = row
+                // dQ^T of the tile, lane = head dim kl, column = row: re-laid by
+                // rows through this group's dS^T buffer (free once the dQ^T MMAs
+                // have completed), 32 rows at a time, then added into the fp32
+                // accumulator with 16-byte reductions, a warp covering one row's
+                // 128 dims per instruction
                 if (!__all_sync(0xffffffffu, wait_fast(bar(L::kBarDQF + wg), (n / 2) & 1, ctl))) {
                     ok = false;
                     break;
@@ -524,24 +565,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(L::kBarDQE + wg));
-                float *dq_col = a.dq_acc + (size_t)U.h * D + kl;
+                // rows quarter * 8 + i of each pass are this warp's to reduce
+                int rtok[2][8];
 #pragma unroll
-                for (int r = 0; r < kRowsT; r += 4) {
-                    const int4 tk = *reinterpret_cast<const int4 *>(mtok + r);
-                    const int tks[4] = {tk.x, tk.y, tk.z, tk.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int rr = r + e;
-                        const float val = __uint_as_float(rr < 32 ? q0[rr] : q1[rr - 32]);
-                        if (tks[e] >= 0)
-                            asm volatile("red.global.add.f32 [%0], %1;" ::"l"(
-                                             dq_col + (size_t)tks[e] * H * D),
-                                         "f"(val)
-                                         : "memory");
-                    }
+                for (int pass = 0; pass < 2; ++pass) {
+                    const int4 t0 = *reinterpret_cast<const int4 *>(mtok + 32 * pass + quarter * 8);
+                    const int4 t1 = *reinterpret_cast<const int4 *>(mtok + 32 * pass + quarter * 8 + 4);
+                    rtok[pass][0] = t0.x; rtok[pass][1] = t0.y; rtok[pass][2] = t0.z; rtok[pass][3] = t0.w;
+                    rtok[pass][4] = t1.x; rtok[pass][5] = t1.y; rtok[pass][6] = t1.z; rtok[pass][7] = t1.w;
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(L::kBarME + s));
+                if (lane == 0) mbar_arrive(bar(L::kBarME + s));  // the tile's metadata is read
+                const uint32_t stg = sDS + (uint32_t)wg * kKeys * 128;
+                float *dq_h = a.dq_acc + (size_t)U.h * D + 4 * lane;
+#pragma unroll
+                for (int pass = 0; pass < 2; ++pass) {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        st_shared_f32(stg + (uint32_t)c * 512 + (uint32_t)kl * 4,
+                                      __uint_as_float(pass == 0 ? q0[c] : q1[c]));
+                    named_bar_sync(1 + wg, 128);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int tk = rtok[pass][i];
+                        const uint4 v4 = ld_shared_v4(stg + (uint32_t)(quarter * 8 + i) * 512 + lane * 16);
+                        if (tk >= 0)
+                            atomicAdd(reinterpret_cast<float4 *>(dq_h + (size_t)tk * H * D),
+                                      make_float4(__uint_as_float(v4.x), __uint_as_float(v4.y),
+                                                  __uint_as_float(v4.z), __uint_as_float(v4.w)));
+                    }
+                    named_bar_sync(1 + wg, 128);  // the staging rows may be written again
+                }
             }
             if (!ok) break;
             // the unit's dV (group 0) and dK (group 1): thread = key
@@ -587,6 +641,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// lse (log2) and dO . O of every list entry's row, next to the list, so that
+// the producer of the kernel above reads a tile's metadata with independent
+// loads; one warp per (block, head) list
+__global__ void __launch_bounds__(256)
+    bwd_list_meta_kernel(Geometry g, const int *__restrict__ list,
+                         const int *__restrict__ list_off, int n_lists,
+                         const float *__restrict__ lse, const float *__restrict__ delta, int fixed,
+                         int S_fixed, float *__restrict__ list_l2, float *__restrict__ list_dl) {
+    MOBA_RETURN_IF_BAD(g);
+    const int lane = threadIdx.x & 31;
+    for (int Lid = blockIdx.x * 8 + (threadIdx.x >> 5); Lid < n_lists; Lid += gridDim.x * 8) {
+        const int h = Lid % g.H;
+        const int gblk = Lid / g.H;
+        const int b = upper_index(g.blk_base, g.num_seqs, gblk);
+        const int seq0 = __ldg(g.cu + b);
+        const int p1 = __ldg(list_off + Lid + 1);
+        for (int pos = __ldg(list_off + Lid) + lane; pos < p1; pos += 32) {
+            const int tok = __ldg(list + pos) >> kSlotBits;
+            const size_t li = fixed ? ((size_t)b * g.H + h) * S_fixed + (tok - seq0)
+                                    : (size_t)h * g.total + tok;
+            list_l2[pos] = __ldg(lse + li) * kLog2e;
+            list_dl[pos] = __ldg(delta + (size_t)h * g.total + tok);
+        }
+    }
+}
+
 }  // namespace bwd_tc
 
 bool bwd_tc_supported(const Plan &p) { return p.D == bwd_tc::D && p.attn_kind == MOBA_ATTN_TCGEN05; }
@@ -616,6 +696,8 @@ cudaError_t launch_bwd_kv_tc(const Plan &p, const Workspace &ws, const __nv_bflo
     a.dout = dout;
     a.lse = lse;
     a.delta = ws.delta;
+    a.list_l2 = ws.list_l2;
+    a.list_dl = ws.list_dl;
     a.dq_acc = ws.dq_acc;
     a.dk = dk;
     a.dv = dv;
@@ -631,6 +713,16 @@ cudaError_t launch_bwd_kv_tc(const Plan &p, const Workspace &ws, const __nv_bflo
     a.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)D));
     a.status = status_word();
     a.wait_limit = p.wait_limit;
+    if (!p.dense && p.km1 > 0) {
+        const int n_lists = p.NBcap * p.H;
+        const int blocks = std::min((n_lists + 7) / 8, 8 * sm_count());
+        bwd_list_meta_kernel<<<blocks, 256, 0, st>>>(a.g, ws.list, ws.list_off, n_lists, lse,
+                                                      ws.delta, a.fixed, a.S_fixed, ws.list_l2,
+                                                      ws.list_dl);
+        note_launches(1);
+        cudaError_t e1 = cudaGetLastError();
+        if (e1 != cudaSuccess) return e1;
+    }
     auto kern = bwd_tc_kernel;
     static int checked = 0;
     if (!checked) {

@@ -69,7 +69,8 @@ struct Workspace {
     float *part_lse;  // [total * H * km1]     partial log2-sum-exp
     // backward pass only (part_o / part_lse are not carved then)
     float *dq_acc;    // [total][H][D]  fp32 dq accumulator
-    float *delta;     // [total][H]     dO . O per row
+    float *delta;     // [H][total]     dO . O per row
+    float *list_l2, *list_dl;  // [total * H * km1] lse (log2) and dO . O of each list entry's row
 };
 
 struct Plan {
