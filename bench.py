@@ -408,9 +408,10 @@ class Forward:
     """One workload's inputs resident on the GPU and a forward step through
     the C ABI (caller workspace, so the timed step allocates nothing)."""
 
-    def __init__(self, ops, torch, w, dev):
+    def __init__(self, ops, torch, w, dev, **opts):
         from long_context_sparse_moba_gb300 import workloads
         self.ops, self.torch, self.w, self.dev = ops, torch, w, dev
+        self.opts = opts  # per-call options of every step
         self.inp = workloads.make_inputs(w, device=dev)
         H, D = w.H, w.D
         if w.varlen:
@@ -438,6 +439,7 @@ class Forward:
     def step(self, topk, **kw):
         w, inp = self.w, self.inp
         ws = self.workspace(topk)
+        kw = {**self.opts, **kw}
         if w.varlen:
             self.ops.attn_fwd_varlen(inp.q, inp.k, inp.v, self.cu, w.S, w.block_size, topk,
                                      out=self.out, lse=self.lse, workspace=ws, **kw)
@@ -673,6 +675,19 @@ def main():
             rng[name] = workload_entry(fo, t, steps, 3, peaks, peak_src)
             if not args.no_cpu_baseline:
                 near.append(near_tie_report(fo.w, fo, t))
+            del fo
+        # the adaptive schedule against the block-major one on inputs whose
+        # 256-row tiles agree on their past blocks (the adaptive schedule is the
+        # default everywhere above)
+        for name, steps in (("coherent32k", 20), ("coherent128k", 10)):
+            torch.cuda.empty_cache()
+            fo = Forward(ops, torch, workloads.WORKLOADS[name], dev)
+            t = fo.w.topks[0]
+            ent = {"adaptive": workload_entry(fo, t, steps, 3, peaks, peak_src)}
+            fo.opts = {"schedule": ops.SCHEDULE_BLOCK_MAJOR}
+            ent["block_major"] = workload_entry(fo, t, steps, 3, peaks, peak_src)
+            ent["speedup"] = ent["block_major"]["ms_per_step"] / ent["adaptive"]["ms_per_step"]
+            rng[name] = ent
             del fo
         if w.name != "varlen":
             torch.cuda.empty_cache()

@@ -98,6 +98,15 @@ typedef enum {
  *                selected blocks ascending, -1 padded), written also on the
  *                paths that run no gate (top-1, and top-k covering every
  *                block).  4-byte aligned.
+ *   schedule     forward only: MOBA_SCHEDULE_ADAPTIVE (default) lets a
+ *                256-row job of one block and head whose rows together selected
+ *                at most topk - 1 distinct past blocks attend to them in the
+ *                own-block pass (query-major, each row masked to its own
+ *                selection, no partial outputs; block sizes that are multiples
+ *                of 256, topk <= 9, tcgen05 attention); every other row goes
+ *                through the per-block lists.  MOBA_SCHEDULE_BLOCK_MAJOR sends
+ *                every row through the lists.  Same results either way (within
+ *                the stated tolerances).
  *   phase_events forward only, optional: an array of 7 cudaEvent_t (passed as
  *                void *) owned by the caller; the call records event i on its
  *                stream before phase i and event 6 after the last one.  Phases:
@@ -111,6 +120,7 @@ typedef enum {
 enum { MOBA_POOL_MEAN = 0, MOBA_POOL_MAX = 1 };
 enum { MOBA_GATE_TENSOR_CORES = 0, MOBA_GATE_CUDA_CORES = 1 };
 enum { MOBA_ATTN_TCGEN05 = 0, MOBA_ATTN_MMA_SYNC = 1 };
+enum { MOBA_SCHEDULE_ADAPTIVE = 0, MOBA_SCHEDULE_BLOCK_MAJOR = 1 };
 enum { MOBA_NUM_PHASES = 6 };
 
 typedef struct moba_options {
@@ -121,6 +131,7 @@ typedef struct moba_options {
     long long wait_limit_cycles;
     int32_t *idx_out;
     void *const *phase_events;
+    int schedule;
 } moba_options_t;
 
 /* Number of blocks of a sequence: ceil(len / block_size) (the tail block may

@@ -116,6 +116,10 @@ size_t workspace_bytes(const Plan &p, Workspace *ws, char *base, bool backward) 
         w.knorm = static_cast<float *>(take(sizeof(float) * N));
         w.list = static_cast<int *>(take(sizeof(int) * rows * p.km1));
         if (!backward) {
+            const size_t jobs =
+                (size_t)((p.max_len + kFuseRows - 1) / kFuseRows) * p.num_seqs * p.H;
+            w.job_nu = static_cast<int *>(take(sizeof(int) * jobs));
+            w.job_ub = static_cast<int *>(take(sizeof(int) * jobs * kMaxUnion));
             w.part_o =
                 static_cast<__nv_bfloat16 *>(take(sizeof(__nv_bfloat16) * rows * p.km1 * p.D));
             w.part_lse = static_cast<float *>(take(sizeof(float) * rows * p.km1));
@@ -158,6 +162,7 @@ static int make_plan(int num_seqs, long long total, int max_len, int H, int D, i
     p->attn_kind = MOBA_ATTN_TCGEN05;
     p->debug_flags = 0;
     p->wait_limit = kDefaultWaitLimit;
+    p->schedule = MOBA_SCHEDULE_ADAPTIVE;
     p->dense = topk >= n_max;
     p->km1 = p->dense ? 0 : topk - 1;
     const long long nbcap = fixed ? (long long)num_seqs * n_max : total / bs + num_seqs;
@@ -177,6 +182,9 @@ static int apply_options(const moba_options_t *o, Plan *p) {
     if (o->attn_kernel != MOBA_ATTN_TCGEN05 && o->attn_kernel != MOBA_ATTN_MMA_SYNC)
         return MOBA_ERR_INVALID_ARG;
     if (o->debug_flags < 0) return MOBA_ERR_INVALID_ARG;
+    if (o->schedule != MOBA_SCHEDULE_ADAPTIVE && o->schedule != MOBA_SCHEDULE_BLOCK_MAJOR)
+        return MOBA_ERR_INVALID_ARG;
+    p->schedule = o->schedule;
     p->pool = o->pooling;
     p->gate_kind = o->gate_kernel;
     p->attn_kind = o->attn_kernel;
@@ -233,7 +241,9 @@ static int run_forward(const Plan &p, const int *cu_dev, const void *q, const vo
         MOBA_TRY(launch_fill_idx(p, ws, idx_out, st));
     }
     prof_mark(ev, 3, st);
-    if (gate) MOBA_TRY(launch_regroup(p, ws, tc_gate, st));
+    const bool fuse = gate && fusion_enabled(p);
+    if (fuse) MOBA_TRY(launch_union(p, ws, tc_gate, st));
+    if (gate) MOBA_TRY(launch_regroup(p, ws, tc_gate, fuse, st));
     prof_mark(ev, 4, st);
     MOBA_TRY(launch_attn_past(p, ws, qb, kb, vb, st));
     prof_mark(ev, 5, st);
@@ -267,7 +277,7 @@ static int run_backward(const Plan &p, const int *cu_dev, const void *q, const v
         } else {
             MOBA_TRY(launch_gate(p, ws, qb, ws.kbar, ws.idx, st));
         }
-        MOBA_TRY(launch_regroup(p, ws, tc_gate, st));
+        MOBA_TRY(launch_regroup(p, ws, tc_gate, false, st));
     }
     MOBA_TRY(cudaMemsetAsync(ws.dq_acc, 0, sizeof(float) * (size_t)p.total * p.H * p.D, st));
     MOBA_TRY(launch_attn_bwd(p, ws, qb, kb, static_cast<const __nv_bfloat16 *>(v),

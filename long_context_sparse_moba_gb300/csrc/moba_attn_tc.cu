@@ -86,6 +86,12 @@ struct Args {
     __nv_bfloat16 *part_o;  // partial outputs, bf16
     float *part_lse;
     float scale_log2;
+    // own-block mode: fused jobs (query-major over their rows' past blocks)
+    int fused;                    // job tables below are valid
+    const int *job_nu, *job_ub;   // [jobs], [jobs][kMaxUnion]
+    // set by the fusion test when some job is fused: of the two own-block
+    // variants launched, only the one that matches runs
+    const int *any_fused;
     int *status;
     long long wait_limit;  // clock64 budget of one wait
     int debug_flags;       // bit 0: the producer skips its first K/V load
@@ -129,12 +135,15 @@ struct Smem {
 // One unit of work: up to 256 query rows and the K/V tiles they visit.
 // rows: tile g holds job rows [g*128, g*128 + 128) (valid below nrows); K/V
 // tiles [0, nkv) start at token kv_tok0; tile g visits K/V tiles [tb[g], te[g]).
+// Fused own-block jobs visit their union blocks' tiles first (nut of them,
+// bs / 128 per block), then their own tiles.
 struct Job {
     int h, b, seq0, L_len, r0, nrows, kv_tok0, kv_end, kv_lo, nkv, lbeg;
+    int nu;               // own-block mode: past blocks of a fused job (0: not fused)
     int tb[kG], te[kG];
 };
 
-template <int MODE>
+template <int MODE, bool FUSE = false>
 __device__ __forceinline__ bool get_job(const Args &a, int job, Job &J) {
     const int H = a.g.H;
     if (MODE == kPast) {
@@ -154,6 +163,7 @@ __device__ __forceinline__ bool get_job(const Args &a, int job, Job &J) {
         J.nrows = min(kRows, lcnt - J.r0);
         J.lbeg = lbeg + J.r0;
         J.nkv = (J.kv_end - J.kv_tok0 + kN - 1) / kN;
+        J.nu = 0;
 #pragma unroll
         for (int g = 0; g < kG; ++g) {
             J.tb[g] = 0;
@@ -188,14 +198,43 @@ __device__ __forceinline__ bool get_job(const Args &a, int job, Job &J) {
         J.tb[g] = (lo_key - J.kv_lo) / kN;
         J.te[g] = (last - J.kv_lo) / kN + 1;
     }
+    // a fused job's past blocks; their tiles are added by add_union_tiles when
+    // the job starts (the load is in flight until then)
+    J.nu = FUSE ? __ldg(a.job_nu + job) : 0;
     return true;
+}
+
+// A fused job (block size a multiple of 256: its rows share one block, so
+// every one of its tiles starts at the block's first key) visits its union
+// blocks' tiles before its own.
+template <bool FUSE>
+__device__ __forceinline__ void add_union_tiles(const Args &a, Job &J) {
+    if (!FUSE || J.nu == 0) return;
+    const int nut = J.nu * (a.g.bs / kN);
+    J.nkv += nut;
+#pragma unroll
+    for (int g = 0; g < kG; ++g)
+        if (J.te[g] > J.tb[g]) J.te[g] += nut;
+}
+
+// first token of K/V tile j of job J (number `job`)
+template <bool FUSE>
+__device__ __forceinline__ int tile_tok(const Args &a, const Job &J, int job, int j) {
+    if (!FUSE) return J.kv_tok0 + j * kN;
+    const int tpb = a.g.bs / kN;  // K/V tiles per block
+    const int nut = J.nu * tpb;
+    if (j < nut) {
+        const int u = j / tpb;
+        return J.seq0 + __ldg(a.job_ub + job * kMaxUnion + u) * a.g.bs + (j - u * tpb) * kN;
+    }
+    return J.kv_tok0 + (j - nut) * kN;
 }
 
 // Persistent kernel: one CTA per SM walks the jobs blockIdx.x, +gridDim.x,
 // ...; every barrier phase is counted across jobs, the K/V rings run ahead
 // into the next job, and in the past-block mode the next job's Q rows are
 // gathered while the current job's partial outputs are written.
-template <int D, int MODE>
+template <int D, int MODE, bool FUSE>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                    const __grid_constant__ CUtensorMap tmap_k,
@@ -209,6 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.g.H;
     MOBA_RETURN_IF_BAD(a.g);
+    if (MODE == kCurrent && a.fused && (*a.any_fused != 0) != FUSE) return;
     const int njobs = (MODE == kPast) ? __ldg(a.tile_off + a.n_lists) : a.n_jobs;
     if ((int)blockIdx.x >= njobs) return;
 
@@ -267,12 +307,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool go = true;
             int job = blockIdx.x;
             Job J;
-            while (job < njobs && !get_job<MODE>(a, job, J)) job += gridDim.x;
+            while (job < njobs && !get_job<MODE, FUSE>(a, job, J)) job += gridDim.x;
             while (go && job < njobs) {
+                add_union_tiles<FUSE>(a, J);
                 // the next job's descriptor is fetched one job ahead
                 int njob = job + gridDim.x;
                 Job NJ;
-                while (njob < njobs && !get_job<MODE>(a, njob, NJ)) njob += gridDim.x;
+                while (njob < njobs && !get_job<MODE, FUSE>(a, njob, NJ)) njob += gridDim.x;
                 if (MODE == kCurrent && is_k) {
                     for (int g = 0; g < kG && go; ++g) {
                         // the previous job's S_g MMAs have read Q_g before it is replaced
@@ -300,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_expect_tx(bar(bfull + s), kTileBytes);
                     for (int x = 0; x < L::NB; ++x)
                         tma_load_3d(ring + (s * L::NB + x) * L::kKVBox, map, bar(bfull + s),
-                                    x * kBox, J.h, J.kv_tok0 + j * kN);
+                                    x * kBox, J.h, tile_tok<FUSE>(a, J, job, j));
                     pend[s] = t;
                 }
                 job = njob;
@@ -326,11 +367,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             int job = blockIdx.x;
             Job J;
-            while (job < njobs && !get_job<MODE>(a, job, J)) job += gridDim.x;
+            while (job < njobs && !get_job<MODE, FUSE>(a, job, J)) job += gridDim.x;
             while (ok && job < njobs) {
+                add_union_tiles<FUSE>(a, J);
                 int njob = job + gridDim.x;  // next descriptor, fetched one job ahead
                 Job NJ;
-                while (njob < njobs && !get_job<MODE>(a, njob, NJ)) njob += gridDim.x;
+                while (njob < njobs && !get_job<MODE, FUSE>(a, njob, NJ)) njob += gridDim.x;
                 // a Q tile without S MMAs in this job is released at once
 #pragma unroll
                 for (int g = 0; g < kG; ++g)
@@ -455,18 +497,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         int job = blockIdx.x;
         Job J;
-        while (job < njobs && !get_job<MODE>(a, job, J)) job += gridDim.x;
+        while (job < njobs && !get_job<MODE, FUSE>(a, job, J)) job += gridDim.x;
         int entry = 0;  // this row's regroup entry in the current job, past mode
         if (MODE == kPast && job < njobs) {
             entry = list_entry(J);
             gather(J, entry);
         }
         while (ok && job < njobs) {
+            add_union_tiles<FUSE>(a, J);
             // the next job's descriptor, fetched one job ahead, and (past mode)
             // this row's entry in it, loaded now and used after the last tile
             int njob = job + gridDim.x;
             Job NJ;
-            while (njob < njobs && !get_job<MODE>(a, njob, NJ)) njob += gridDim.x;
+            while (njob < njobs && !get_job<MODE, FUSE>(a, njob, NJ)) njob += gridDim.x;
             const int next_entry = (MODE == kPast && njob < njobs) ? list_entry(NJ) : 0;
             const int seq0 = J.seq0, h = J.h;
             const bool row_valid = jrow < J.nrows;
@@ -478,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 row_tok = seq0 + J.r0 + jrow;
                 // warm L2 with this row's past partials; the merge reads them only
                 // after the last tile, so the fetch overlaps the attention loop
-                if (row_valid && !a.dense && a.km1 > 0) {
+                if (row_valid && !a.dense && a.km1 > 0 && J.nu == 0) {
                     // every earlier block was a candidate, so the row holds
                     // min(topk - 1, its block index) partials, slots 0, 1, ...
                     const int npre = min(a.km1, (row_tok - seq0) / a.g.bs);
@@ -492,6 +535,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             const int i_loc = row_tok - seq0;  // position inside the sequence
+            // fused job: bit u = this row selected union block u
+            unsigned row_bits = 0u;
+            const int tpb = a.g.bs / kN;           // K/V tiles per block
+            const int nut = FUSE ? J.nu * tpb : 0;  // union tiles of a fused job
+            if (FUSE && J.nu > 0 && row_valid) {
+                const int ci = i_loc / a.g.bs;
+                const int32_t *sel = a.idx + ((size_t)row_tok * H + h) * a.topk;
+                for (int s2 = 0; s2 < a.km1; ++s2) {
+                    const int c = __ldg(sel + s2);
+                    if (c < 0 || c >= ci) break;
+                    for (int u = 0; u < J.nu; ++u)
+                        if (__ldg(a.job_ub + job * kMaxUnion + u) == c) row_bits |= 1u << u;
+                }
+            }
             const int rb = (MODE == kCurrent && !a.dense) ? (i_loc / a.g.bs) * a.g.bs : 0;
             const int g_first = J.r0 + g * kM;
             const int g_last = min(J.r0 + (g + 1) * kM, J.r0 + J.nrows) - 1;
@@ -501,6 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int kv_lo = J.kv_lo, kv_tok0 = J.kv_tok0, kv_end = J.kv_end;
 
             float m_run = -INFINITY, l_run = 0.f;
+            int ucur = 0, usub = 0;  // union block and tile within it (fused jobs start at tile 0)
             for (int jl = 0; jl < ntile; ++jl) {
                 const int j = my_tb + jl;
                 // S_g(j) is ready; the commit behind it also covers PV_g(j-1), so
@@ -510,20 +568,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const int key0 = kv_lo + j * kN;  // sequence-local position of column 0
+                // a fused job's union tiles come first: a full past block, off
+                // for the rows that did not select it
+                const bool uni = FUSE && j < nut;
+                bool row_off = false;
+                if (uni) {
+                    row_off = !((row_bits >> ucur) & 1u);
+                    if (++usub == tpb) {
+                        usub = 0;
+                        ++ucur;
+                    }
+                }
+                const int jo = j - nut;            // own tile index
+                const int key0 = kv_lo + jo * kN;  // sequence-local position of column 0
                 const bool need_mask =
                     (MODE == kPast) ? (kv_tok0 + (j + 1) * kN > kv_end)
+                    : uni           ? row_off
                                     : (key0 + kN - 1 > g_first || key0 < rb_max ||
                                        seq0 + key0 + kN > kv_end);
                 // masked columns are set to -inf (raw fp32 bits) in place; only the
                 // tiles on the diagonal / at the end of a block need it
-                const int kt0 = kv_tok0 + j * kN;  // token of column 0
+                const int kt0 = kv_tok0 + jo * kN;  // token of column 0
 #define MOBA_MASK64(SR, BASE)                                                         \
     if (need_mask) {                                                                  \
         _Pragma("unroll") for (int c = 0; c < 64; ++c) {                              \
             const int col = (BASE) + c;                                               \
             const int kp = key0 + col;                                                \
-            if (kt0 + col >= kv_end || (MODE == kCurrent && (kp > i_loc || kp < rb))) \
+            if (uni || kt0 + col >= kv_end || (MODE == kCurrent && (kp > i_loc || kp < rb))) \
                 SR[c >> 5][c & 31] = 0xff800000u;                                     \
         }                                                                             \
     }
@@ -692,7 +763,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const size_t rowid = (size_t)row_tok * H + h;
                     int np = 0;
                     float mmax = lse2;
-                    if (row_valid && !a.dense && a.km1 > 0) {
+                    if (row_valid && !a.dense && a.km1 > 0 && J.nu == 0) {
                         np = min(a.km1, i_loc / a.g.bs);
                         for (int s2 = 0; s2 < np; ++s2)
                             mmax = fmaxf(mmax, __ldg(a.part_lse + rowid * a.km1 + s2));
@@ -884,6 +955,10 @@ static tc::Args make_tc_args(const Plan &p, const Workspace &ws, const __nv_bflo
     a.n_jobs = a.n_rtiles * p.num_seqs * p.H;
     a.part_o = ws.part_o;
     a.part_lse = ws.part_lse;
+    a.fused = fusion_enabled(p) ? 1 : 0;
+    a.any_fused = ws.counts ? ws.counts + (size_t)p.NBcap * p.H : nullptr;
+    a.job_nu = ws.job_nu;
+    a.job_ub = ws.job_ub;
     a.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)p.D));
     a.status = status_word();
     a.wait_limit = p.wait_limit;
@@ -891,7 +966,7 @@ static tc::Args make_tc_args(const Plan &p, const Workspace &ws, const __nv_bflo
     return a;
 }
 
-template <int D, int MODE>
+template <int D, int MODE, bool FUSE>
 static cudaError_t launch_tc(const Plan &p, const tc::Args &a, const __nv_bfloat16 *q,
                              const __nv_bfloat16 *k, const __nv_bfloat16 *v, cudaStream_t st) {
     CUtensorMap mq, mk, mv;
@@ -900,11 +975,11 @@ static cudaError_t launch_tc(const Plan &p, const tc::Args &a, const __nv_bfloat
         !make_tma_3d(&mv, v, p.total, p.H, D, tc::kN))
         return cudaErrorInvalidValue;
     const int smem = tc::Smem<D>::kRequest;
-    auto kern = tc::attn_tc_kernel<D, MODE>;
+    auto kern = tc::attn_tc_kernel<D, MODE, FUSE>;
     // The block needs all of its 320 threads resident (warp roles are fixed);
     // refuse to launch if the build's register use would not allow that.
-    static int checked[2][2] = {{0, 0}, {0, 0}};
-    int &chk = checked[D == 128][MODE];
+    static int checked[2][2][2] = {};
+    int &chk = checked[D == 128][MODE][FUSE ? 1 : 0];
     if (!chk) {
         cudaFuncAttributes fa;
         cudaError_t e0 = cudaFuncGetAttributes(&fa, kern);
@@ -927,16 +1002,22 @@ cudaError_t launch_attn_past_tc(const Plan &p, const Workspace &ws, const __nv_b
                                 const __nv_bfloat16 *k, const __nv_bfloat16 *v, cudaStream_t st) {
     if (p.dense || p.km1 == 0) return cudaSuccess;
     auto a = make_tc_args(p, ws, q, nullptr, nullptr);
-    return p.D == 64 ? launch_tc<64, tc::kPast>(p, a, q, k, v, st)
-                     : launch_tc<128, tc::kPast>(p, a, q, k, v, st);
+    return p.D == 64 ? launch_tc<64, tc::kPast, false>(p, a, q, k, v, st)
+                     : launch_tc<128, tc::kPast, false>(p, a, q, k, v, st);
 }
 
 cudaError_t launch_attn_current_tc(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
                                    const __nv_bfloat16 *k, const __nv_bfloat16 *v,
                                    __nv_bfloat16 *out, float *lse, cudaStream_t st) {
     auto a = make_tc_args(p, ws, q, out, lse);
-    return p.D == 64 ? launch_tc<64, tc::kCurrent>(p, a, q, k, v, st)
-                     : launch_tc<128, tc::kCurrent>(p, a, q, k, v, st);
+    // with fusion possible, both variants are launched and the fusion test's
+    // flag lets one of them run: the variant without union tiles keeps the
+    // own-block kernel's speed when no job fused
+    cudaError_t e = p.D == 64 ? launch_tc<64, tc::kCurrent, false>(p, a, q, k, v, st)
+                              : launch_tc<128, tc::kCurrent, false>(p, a, q, k, v, st);
+    if (e != cudaSuccess || !a.fused) return e;
+    return p.D == 64 ? launch_tc<64, tc::kCurrent, true>(p, a, q, k, v, st)
+                     : launch_tc<128, tc::kCurrent, true>(p, a, q, k, v, st);
 }
 
 }  // namespace moba

@@ -485,13 +485,30 @@ cudaError_t launch_gate(const Plan &p, const Workspace &ws, const __nv_bfloat16 
 constexpr int kRgThreads = 512;
 constexpr int kRgSmemBins = 48 * 1024;  // 192 KB of shared-memory histogram at most
 
+// Which own-block jobs are fused (job_nu[job] > 0); null when none is.  Job
+// numbering of the own-block attention kernel: heads fastest, then sequences,
+// then 256-row tiles from the last.
+struct FusedJobs {
+    const int *job_nu;
+    int n_rtiles;
+    __device__ __forceinline__ bool row_fused(const Geometry &g, int b, int i_loc, int h) const {
+        if (!job_nu) return false;
+        const int x = i_loc / kFuseRows;
+        const int job = ((n_rtiles - 1 - x) * g.num_seqs + b) * g.H + h;
+        return __ldg(job_nu + job) > 0;
+    }
+};
+
 // calls f(bin, entry) for every past selection of row r = token * H + head
+// (none for the rows of fused own-block jobs)
 template <typename F>
 __device__ __forceinline__ void for_each_selection(const Geometry &g, const int32_t *__restrict__ idx,
-                                                   int topk, size_t r, F f) {
+                                                   int topk, size_t r, const FusedJobs &fj, F f) {
     const int t = (int)(r / g.H), h = (int)(r % g.H);
     const int b = upper_index(g.cu, g.num_seqs, t);
-    const int ci = (t - __ldg(g.cu + b)) / g.bs;
+    const int seq0 = __ldg(g.cu + b);
+    const int ci = (t - seq0) / g.bs;
+    if (fj.row_fused(g, b, t - seq0, h)) return;
     const int bbase = __ldg(g.blk_base + b);
     const int32_t *row = idx + r * topk;
     for (int s = 0; s < topk - 1; ++s) {
@@ -504,7 +521,7 @@ __device__ __forceinline__ void for_each_selection(const Geometry &g, const int3
 template <bool SMEM>
 __global__ void __launch_bounds__(kRgThreads)
     regroup_count_kernel(Geometry g, const int32_t *__restrict__ idx, int topk, int rows_per_cta,
-                         int N, int *__restrict__ counts) {
+                         int N, int *__restrict__ counts, FusedJobs fj) {
     extern __shared__ int hist[];
     MOBA_RETURN_IF_BAD(g);
     const size_t R = (size_t)g.total * g.H;
@@ -514,7 +531,7 @@ __global__ void __launch_bounds__(kRgThreads)
         __syncthreads();
     }
     for (size_t r = r0 + threadIdx.x; r < r1; r += kRgThreads)
-        for_each_selection(g, idx, topk, r, [&](int bin, int) {
+        for_each_selection(g, idx, topk, r, fj, [&](int bin, int) {
             if (SMEM) atomicAdd(&hist[bin], 1);
             else atomicAdd(counts + bin, 1);
         });
@@ -544,7 +561,7 @@ template <bool SMEM>
 __global__ void __launch_bounds__(kRgThreads)
     regroup_scatter_kernel(Geometry g, const int32_t *__restrict__ idx, int topk, int rows_per_cta,
                            int N, int *__restrict__ counts, const int *__restrict__ list_off,
-                           int *__restrict__ list) {
+                           int *__restrict__ list, FusedJobs fj) {
     extern __shared__ int hist[];
     MOBA_RETURN_IF_BAD(g);
     const size_t R = (size_t)g.total * g.H;
@@ -553,7 +570,7 @@ __global__ void __launch_bounds__(kRgThreads)
         for (int x = threadIdx.x; x < N; x += kRgThreads) hist[x] = 0;
         __syncthreads();
         for (size_t r = r0 + threadIdx.x; r < r1; r += kRgThreads)
-            for_each_selection(g, idx, topk, r, [&](int bin, int) { atomicAdd(&hist[bin], 1); });
+            for_each_selection(g, idx, topk, r, fj, [&](int bin, int) { atomicAdd(&hist[bin], 1); });
         __syncthreads();
         // this CTA's range in list x: [list_off + remaining - n, list_off + remaining)
         for (int x = threadIdx.x; x < N; x += kRgThreads) {
@@ -563,14 +580,18 @@ __global__ void __launch_bounds__(kRgThreads)
         __syncthreads();
     }
     for (size_t r = r0 + threadIdx.x; r < r1; r += kRgThreads)
-        for_each_selection(g, idx, topk, r, [&](int bin, int entry) {
+        for_each_selection(g, idx, topk, r, fj, [&](int bin, int entry) {
             const int pos = SMEM ? atomicAdd(&hist[bin], 1)
                                  : __ldg(list_off + bin) + atomicSub(counts + bin, 1) - 1;
             list[pos] = entry;
         });
 }
 
-cudaError_t launch_regroup(const Plan &p, const Workspace &ws, bool counted, cudaStream_t st) {
+cudaError_t launch_regroup(const Plan &p, const Workspace &ws, bool counted, bool skip_fused,
+                           cudaStream_t st) {
+    FusedJobs fj;
+    fj.job_nu = skip_fused ? ws.job_nu : nullptr;
+    fj.n_rtiles = (p.max_len + kFuseRows - 1) / kFuseRows;
     const int N = p.NBcap * p.H;
     const size_t R = (size_t)p.total * p.H;
     const bool smem = N <= kRgSmemBins;
@@ -591,10 +612,10 @@ cudaError_t launch_regroup(const Plan &p, const Workspace &ws, bool counted, cud
     if (!counted) {
         if (smem)
             regroup_count_kernel<true><<<grid, kRgThreads, hbytes, st>>>(g, ws.idx, p.topk,
-                                                                          rows_per_cta, N, ws.counts);
+                                                                          rows_per_cta, N, ws.counts, fj);
         else
             regroup_count_kernel<false><<<grid, kRgThreads, 0, st>>>(g, ws.idx, p.topk,
-                                                                     rows_per_cta, N, ws.counts);
+                                                                     rows_per_cta, N, ws.counts, fj);
         note_launches(1);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
@@ -603,10 +624,10 @@ cudaError_t launch_regroup(const Plan &p, const Workspace &ws, bool counted, cud
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (smem)
         regroup_scatter_kernel<true><<<grid, kRgThreads, hbytes, st>>>(
-            g, ws.idx, p.topk, rows_per_cta, N, ws.counts, ws.list_off, ws.list);
+            g, ws.idx, p.topk, rows_per_cta, N, ws.counts, ws.list_off, ws.list, fj);
     else
         regroup_scatter_kernel<false><<<grid, kRgThreads, 0, st>>>(
-            g, ws.idx, p.topk, rows_per_cta, N, ws.counts, ws.list_off, ws.list);
+            g, ws.idx, p.topk, rows_per_cta, N, ws.counts, ws.list_off, ws.list, fj);
     note_launches(2);
     return cudaGetLastError();
 }
@@ -615,6 +636,108 @@ cudaError_t launch_fill_idx(const Plan &p, const Workspace &ws, int32_t *idx, cu
     const size_t R = (size_t)p.total * p.H;
     const unsigned blocks = (unsigned)std::min<size_t>((R + 255) / 256, 8192);
     fill_idx_kernel<<<blocks, 256, 0, st>>>(make_geo(p, ws), idx, p.topk, p.dense ? p.topk - 1 : p.km1);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Fusion test of each own-block job (256 rows of one block and head; block
+// sizes a multiple of 256 keep a job inside one block, so its rows share one
+// block index c > topk - 1).  The union of the rows' past selections has at
+// most topk - 1 blocks exactly when every row selected the same topk - 1
+// blocks.  Such a job is fused: the own-block kernel attends its rows to
+// those blocks directly (no row does more work than on the block-major path)
+// and its rows stay out of the regroup lists.  The rows of the first blocks
+// (c <= topk - 1, which take every past block) are left to the lists, where
+// they share long jobs with the rest of the sequence.  One warp per job
+// compares every row's selection with the first row's and stops at the first
+// difference.
+// ---------------------------------------------------------------------------
+constexpr int kUnionWarps = 8;
+
+__global__ void __launch_bounds__(32 * kUnionWarps)
+    union_kernel(Geometry g, const int32_t *__restrict__ idx, int topk, int n_rtiles,
+                 int n_jobs, int *__restrict__ job_nu, int *__restrict__ job_ub,
+                 int *__restrict__ counts, int *__restrict__ any_fused) {
+    MOBA_RETURN_IF_BAD(g);
+    const int job = blockIdx.x * kUnionWarps + (threadIdx.x >> 5);
+    if (job >= n_jobs) return;  // whole warps leave together
+    const int lane = threadIdx.x & 31, H = g.H, km1 = topk - 1;
+    const int h = job % H, tt = job / H;
+    const int b = tt % g.num_seqs;
+    const int x = n_rtiles - 1 - tt / g.num_seqs;
+    const int seq0 = __ldg(g.cu + b), L = __ldg(g.cu + b + 1) - seq0;
+    const int r0 = x * kFuseRows;
+    const int nrows = min(kFuseRows, L - r0);
+    int nu = 0;
+    int first[kMaxUnion];  // the first row's past blocks
+#pragma unroll
+    for (int s2 = 0; s2 < kMaxUnion; ++s2) first[s2] = -1;
+    const int ci = r0 / g.bs;
+    if (nrows > 0 && ci > km1) {
+        const int32_t *row0 = idx + ((size_t)(seq0 + r0) * H + h) * topk;
+#pragma unroll
+        for (int s2 = 0; s2 < kMaxUnion; ++s2)
+            if (s2 < km1) {
+                const int c = __ldg(row0 + s2);
+                if (c >= 0 && c < ci) first[s2] = c;
+            }
+        bool same = true;
+        // warp-uniform trip count: every lane reaches each vote
+        for (int base = 0; base < nrows; base += 32) {
+            const int r = base + lane;
+            if (r < nrows) {
+                const int32_t *row = idx + ((size_t)(seq0 + r0 + r) * H + h) * topk;
+#pragma unroll
+                for (int s2 = 0; s2 < kMaxUnion; ++s2)
+                    if (s2 < km1) {
+                        int c = __ldg(row + s2);
+                        if (c < 0 || c >= ci) c = -1;
+                        same = same && c == first[s2];
+                    }
+            }
+            if (!__all_sync(0xffffffffu, same)) break;
+        }
+        if (__all_sync(0xffffffffu, same)) {
+#pragma unroll
+            for (int s2 = 0; s2 < kMaxUnion; ++s2) nu += first[s2] >= 0;
+        }
+    }
+    if (nu > 0 && lane < nu) {
+        if (lane == 0) *any_fused = 1;
+        if (counts) {
+            // the job's selections leave the per-list counts the gate accumulated
+            const int bbase = __ldg(g.blk_base + b);
+            int c = -1;
+#pragma unroll
+            for (int s2 = 0; s2 < kMaxUnion; ++s2)
+                if (s2 == lane) c = first[s2];
+            atomicSub(counts + (size_t)(bbase + c) * H + h, nrows);
+        }
+    }
+    if (lane == 0) job_nu[job] = nu;
+    if (lane < kMaxUnion) {
+        int c = -1;
+#pragma unroll
+        for (int s2 = 0; s2 < kMaxUnion; ++s2)
+            if (s2 == lane) c = first[s2];
+        job_ub[(size_t)job * kMaxUnion + lane] = lane < nu ? c : -1;
+    }
+}
+
+bool fusion_enabled(const Plan &p) {
+    return !p.dense && p.km1 > 0 && p.km1 <= kMaxUnion && p.bs % kFuseRows == 0 &&
+           p.attn_kind == 0 && p.schedule == 0;
+}
+
+
+
+cudaError_t launch_union(const Plan &p, const Workspace &ws, bool counted, cudaStream_t st) {
+    const int n_rtiles = (p.max_len + kFuseRows - 1) / kFuseRows;
+    const long long jobs = (long long)n_rtiles * p.num_seqs * p.H;
+    union_kernel<<<(unsigned)((jobs + kUnionWarps - 1) / kUnionWarps), 32 * kUnionWarps, 0, st>>>(
+        make_geo(p, ws), ws.idx, p.topk, n_rtiles, (int)jobs, ws.job_nu,
+        ws.job_ub, counted ? ws.counts : nullptr, ws.counts + (size_t)p.NBcap * p.H);
     note_launches(1);
     return cudaGetLastError();
 }

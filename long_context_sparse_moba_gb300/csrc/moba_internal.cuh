@@ -19,6 +19,9 @@ constexpr int kMaxPastSlots = 31;      // topk - 1 limit when gating is needed
 constexpr int kSlotBits = 5;           // regroup entry = token << 5 | slot
 constexpr int kMaxTokens = 1 << 26;
 constexpr int kMaxGateCtas = 1024;     // CTAs of the tensor-core gate at most
+// query-major fusion of the own-block jobs (256 rows of one block and head)
+constexpr int kFuseRows = 256;         // rows per own-block job
+constexpr int kMaxUnion = 8;           // past blocks a fused job may visit
 
 // Device status word of the current device (defined in moba_api.cu); kernels
 // with bounded waits record MOBA_ERR_TIMEOUT there.  moba_get_status reads
@@ -56,7 +59,8 @@ struct Workspace {
     float *kbar;      // [NBcap][H][D]
     int32_t *idx;     // [total][H][topk]
     int *counts;      // [NBcap * H]   queries per (block, head) past list (zero
-                      //               again once the scatter has used them)
+                      //               again once the scatter has used them),
+                      //               then one word: some own-block job fused
     int *need_count;  // [kMaxGateCtas] rows each tensor-core gate CTA left to the exact kernel
     unsigned long long *need_list;  // [2 * total * H] those rows and their candidates
     int *list_off;    // [NBcap * H + 1]
@@ -65,6 +69,8 @@ struct Workspace {
     __nv_bfloat16 *kbhi, *kblo;  // [NBcap][H][D] bf16 split of kbar (tensor-core gate)
     float *knorm;                // [NBcap][H] L2 norm of each pooled key
     int *list;        // [total * H * km1]  entries token << 5 | slot
+    int *job_nu;      // [own-block jobs]  past blocks of a fused job (0: not fused)
+    int *job_ub;      // [own-block jobs][kMaxUnion]  those blocks, ascending
     __nv_bfloat16 *part_o;  // [total * H * km1][D]  normalised partial outputs (bf16)
     float *part_lse;  // [total * H * km1]     partial log2-sum-exp
     // backward pass only (part_o / part_lse are not carved then)
@@ -85,6 +91,7 @@ struct Plan {
     int attn_kind;          // 0 tcgen05 / TMEM / TMA, 1 warp-level mma.sync
     int debug_flags;        // bit 0: the K/V producer skips its first load
     long long wait_limit;   // clock64 budget of one bounded wait
+    int schedule;           // 0 adaptive (fused own-block jobs where it pays), 1 block-major
 };
 
 // clock64 budget of one bounded wait when the caller gives none (~2 s at 2 GHz)
@@ -108,9 +115,22 @@ cudaError_t launch_kpool(const Plan &p, const Workspace &ws, const __nv_bfloat16
                          float *kbar, cudaStream_t st);
 cudaError_t launch_gate(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
                         const float *kbar, int32_t *idx, cudaStream_t st);
+// Own-block jobs (256-row tiles x of a sequence) run heavy (late) tiles
+// first: job id = ((n_rtiles - 1 - x) * num_seqs + b) * H + h.
+// Query-major fusion: an own-block job (256 rows of one block and head) whose
+// rows all chose the same topk - 1 past blocks (among more candidates than
+// that) attends to those blocks itself, so its rows leave the regroup lists
+// and write no partial outputs.  Available with the tcgen05 attention, block
+// sizes that are multiples of 256 and topk <= 9.
+bool fusion_enabled(const Plan &p);
+// the own-block jobs' unions of past selections (ws.job_nu, ws.job_ub); with
+// counted, the fused rows' selections are taken back out of ws.counts
+cudaError_t launch_union(const Plan &p, const Workspace &ws, bool counted, cudaStream_t st);
 // per-(block, head) lists of the past selections: count (unless the gate has
-// already added its selections into ws.counts), scan, scatter
-cudaError_t launch_regroup(const Plan &p, const Workspace &ws, bool counted, cudaStream_t st);
+// already added its selections into ws.counts), scan, scatter; with
+// skip_fused, the rows of fused own-block jobs are left out
+cudaError_t launch_regroup(const Plan &p, const Workspace &ws, bool counted, bool skip_fused,
+                           cudaStream_t st);
 // attention over the selected past blocks (skipped on the dense / top-1 paths)
 cudaError_t launch_attn_past(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
                              const __nv_bfloat16 *k, const __nv_bfloat16 *v, cudaStream_t st);

@@ -76,6 +76,8 @@ GATE_TCGEN05 = 0
 GATE_CUDA_CORES = 1
 ATTN_TCGEN05 = 0
 ATTN_MMA_SYNC = 1
+SCHEDULE_ADAPTIVE = 0
+SCHEDULE_BLOCK_MAJOR = 1
 
 
 class Options(ctypes.Structure):
@@ -83,14 +85,15 @@ class Options(ctypes.Structure):
     _fields_ = [("pooling", ctypes.c_int), ("gate_kernel", ctypes.c_int),
                 ("attn_kernel", ctypes.c_int), ("debug_flags", ctypes.c_int),
                 ("wait_limit_cycles", ctypes.c_longlong), ("idx_out", ctypes.c_void_p),
-                ("phase_events", ctypes.c_void_p)]
+                ("phase_events", ctypes.c_void_p), ("schedule", ctypes.c_int)]
 
 
 def _options(pooling=POOL_MEAN, gate_kernel=GATE_TCGEN05, attn_kernel=ATTN_TCGEN05,
-             debug_flags=0, wait_limit_cycles=0, idx_out=None, phase_events=None):
+             debug_flags=0, wait_limit_cycles=0, idx_out=None, phase_events=None,
+             schedule=SCHEDULE_ADAPTIVE):
     """An Options structure and the objects that must outlive the call."""
     o = Options(int(pooling), int(gate_kernel), int(attn_kernel), int(debug_flags),
-                int(wait_limit_cycles), None, None)
+                int(wait_limit_cycles), None, None, int(schedule))
     keep = []
     if idx_out is not None:
         o.idx_out = idx_out.data_ptr()

@@ -15,7 +15,13 @@ block (so the mean-pooled keys differ between blocks and the gate is not
 degenerate), then for the "needle" workload: the ids of the needle blocks, the
 ids of the needle queries and one direction u ~ N(0, 1)^D shared by all heads,
 added to every key of the needle blocks and to every head of the needle
-queries.  Values are drawn in fp32 and rounded to bf16 (round to nearest even).
+queries; for a "coherent" workload, per (sequence, head, 256-row tile) the
+ids of `coherent` distinct past blocks (uniform among the tile's earlier
+blocks; all of them when there are fewer) and, added to every query of the
+tile, 0.5 times the sum of those blocks' key offsets, so that the tile's rows
+agree on their past blocks (the locality real queries often show, which the
+other recipes lack).  Values are drawn in fp32 and rounded to bf16 (round to
+nearest even).
 """
 from __future__ import annotations
 
@@ -39,6 +45,7 @@ class Workload:
     needle_block_frac: float = 0.0
     needle_query_frac: float = 0.0
     varlen: bool = False      # packed [total, H, D] + cu_seqlens instead of [B, S, H, D]
+    coherent: int = 0         # > 0: queries of each 256-row tile agree on this many past blocks
     notes: str = ""
 
     @property
@@ -83,6 +90,16 @@ WORKLOADS = {
     "prefill1m": Workload("prefill1m", (1048576,), H=8, D=128, block_size=4096, topks=(3,),
                           seed=3, offset_std=0.5,
                           notes="B1 H8 S1048576 D128 bs4096 (256 blocks) top-k 3"),
+    "coherent32k": Workload("coherent32k", (32768,), H=32, D=128, block_size=512, topks=(3,),
+                            seed=5, qkv_scale=1.0 / math.sqrt(128.0), offset_std=0.5,
+                            coherent=2,
+                            notes="the 32K training shape with each 256-row tile's queries "
+                                  "agreeing on 2 past blocks"),
+    "coherent128k": Workload("coherent128k", (131072,), H=32, D=128, block_size=2048,
+                             topks=(3,), seed=7, qkv_scale=1.0 / math.sqrt(128.0),
+                             offset_std=0.5, coherent=2,
+                             notes="the 128K shape (block 2048) with each 256-row tile's "
+                                   "queries agreeing on 2 past blocks"),
     "varlen": Workload("varlen", _varlen_lengths(4, 8, 4096, 65536), H=16, D=128,
                        block_size=512, topks=(1, 2, 3, 4, 8), seed=4, varlen=True,
                        notes="8 sequences, lengths U{4096..65536} (partial tail blocks), "
@@ -91,13 +108,14 @@ WORKLOADS = {
 
 
 def custom(seqlens, H, D, block_size, topk, seed=0, qkv_scale=1.0, offset_std=0.5,
-           varlen=None, name="custom") -> Workload:
+           varlen=None, name="custom", coherent=0) -> Workload:
     """A small workload for tests (same recipe, any shape)."""
     seqlens = tuple(int(s) for s in seqlens)
     if varlen is None:
         varlen = len(set(seqlens)) > 1
     return Workload(name, seqlens, H=H, D=D, block_size=block_size, topks=(topk,), seed=seed,
-                    qkv_scale=qkv_scale, offset_std=offset_std, varlen=varlen)
+                    qkv_scale=qkv_scale, offset_std=offset_std, varlen=varlen,
+                    coherent=coherent)
 
 
 @dataclass
@@ -147,6 +165,20 @@ def make_inputs(w: Workload, device="cpu") -> Inputs:
         for c in needle_blocks:
             k[c * bs:(c + 1) * bs] += u
         q[torch.tensor(needle_queries, device=device)] += u
+    if w.coherent > 0:
+        assert w.offset_std > 0
+        tile = 256
+        for b, L in enumerate(w.seqlens):
+            for t0 in range(0, L, tile):
+                c = t0 // bs  # the tile's block (tiles of 256 rows stay in one block when
+                #               the block size is a multiple of 256)
+                if c == 0:
+                    continue
+                base_blk = sum(nblk[:b])
+                for h in range(H):
+                    pick = torch.randperm(c, generator=g, device=device)[:w.coherent]
+                    direction = off[base_blk + pick, h, :].sum(0)
+                    q[cu[b] + t0: cu[b] + min(t0 + tile, L), h, :] += 0.5 * direction
     q, k, v = (x.to(torch.bfloat16) for x in (q, k, v))
     if not w.varlen:
         q, k, v = (x.view(w.B, w.S, H, D) for x in (q, k, v))

@@ -55,7 +55,7 @@ def test_options_validate_on_the_host(lib):
     pointers are never dereferenced)."""
     fake = ctypes.c_void_p(0x10000)
     for field, bad in (("pooling", 7), ("pooling", -1), ("gate_kernel", 2), ("attn_kernel", 5),
-                       ("debug_flags", -1)):
+                       ("debug_flags", -1), ("schedule", 2)):
         o = ops.Options()
         setattr(o, field, bad)
         assert lib.moba_kpool_ex(fake, fake, 1, 1, 64, 64, 64, ctypes.byref(o),
@@ -73,10 +73,11 @@ def test_options_validate_on_the_host(lib):
 
 def test_options_struct_layout():
     """The ctypes mirror of moba_options_t has the C layout (LP64: int x4,
-    long long, two pointers = 40 bytes)."""
-    assert ctypes.sizeof(ops.Options) == 40
+    long long, two pointers, int, padding = 48 bytes)."""
+    assert ctypes.sizeof(ops.Options) == 48
     assert ops.Options.wait_limit_cycles.offset == 16
     assert ops.Options.idx_out.offset == 24 and ops.Options.phase_events.offset == 32
+    assert ops.Options.schedule.offset == 40
 
 
 def test_no_process_wide_switches(lib):

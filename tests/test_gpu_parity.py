@@ -254,3 +254,36 @@ def test_inconsistent_cu_seqlens_are_reported_not_used(cu, max_seqlen):
     w = workloads.custom((2048, 2048), H, D, bs, topk=3, seed=44)
     *_, st = run_case(w, 3)
     print("after invalid offsets", st)
+
+
+# ---------------------------------------------------------------------------
+# query-major fusion of own-block jobs whose rows agree on their past blocks
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("seqlens,H,bs,topk,coherent", [
+    ((4096,), 4, 512, 3, 2),            # every tile's rows agree on 2 blocks: fused
+    ((4096, 2500), 2, 256, 3, 2),       # varlen, block 256, partial tail tile
+    ((8192,), 2, 1024, 2, 1),           # top-2: a single past block per tile
+    ((4096,), 2, 512, 4, 2),            # union 2 <= topk - 1 = 3: fused
+    ((4096,), 2, 512, 3, 3),            # union 3 > topk - 1: block-major
+    ((6144,), 2, 512, 9, 8),            # the widest union a fused job may hold
+])
+def test_fused_own_block_jobs(seqlens, H, bs, topk, coherent):
+    """Rows of a 256-row tile that agree on their past blocks are attended by
+    the own-block pass (query-major, each row masked to its selection): the
+    results match the oracle, and the block-major schedule on the same inputs."""
+    w = workloads.custom(seqlens, H, 128, bs, topk=topk, seed=51, qkv_scale=128 ** -0.5,
+                         coherent=coherent)
+    inp, _, idx, out, lse, st = run_case(w, topk)
+    o2, l2, i2 = gpu_forward(inp, w, topk, with_idx=True, schedule=ops.SCHEDULE_BLOCK_MAJOR)
+    assert ops.get_status() == ops.MOBA_OK
+    assert torch.equal(idx, i2)
+    compare(w, inp, topk, o2, l2, idx_gpu=i2)
+    print(seqlens, bs, topk, coherent, st)
+
+
+def test_coherent32k_sampled():
+    w = workloads.WORKLOADS["coherent32k"]
+    rows = workloads.sample_rows(w, 4096)
+    *_, st = run_case(w, 3, rows=rows)
+    print("coherent32k", st)
