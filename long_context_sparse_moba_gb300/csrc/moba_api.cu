@@ -132,6 +132,8 @@ size_t workspace_bytes(const Plan &p, Workspace *ws, char *base, bool backward) 
         if (gate) {
             w.list_l2 = static_cast<float *>(take(sizeof(float) * rows * p.km1));
             w.list_dl = static_cast<float *>(take(sizeof(float) * rows * p.km1));
+            w.cta_hist = static_cast<int *>(
+                take(sizeof(int) * (size_t)stable_regroup_ctas(p) * p.NBcap * p.H));
         }
     }
     if (ws) *ws = w;
@@ -277,7 +279,7 @@ static int run_backward(const Plan &p, const int *cu_dev, const void *q, const v
         } else {
             MOBA_TRY(launch_gate(p, ws, qb, ws.kbar, ws.idx, st));
         }
-        MOBA_TRY(launch_regroup(p, ws, tc_gate, false, st));
+        MOBA_TRY(launch_regroup_stable(p, ws, st));
     }
     MOBA_TRY(cudaMemsetAsync(ws.dq_acc, 0, sizeof(float) * (size_t)p.total * p.H * p.D, st));
     MOBA_TRY(launch_attn_bwd(p, ws, qb, kb, static_cast<const __nv_bfloat16 *>(v),

@@ -632,6 +632,164 @@ cudaError_t launch_regroup(const Plan &p, const Workspace &ws, bool counted, boo
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// The same lists in a fixed order (the backward's: it sums each key's dK and
+// dV over its list tile by tile, so an order that changes from call to call
+// changes their rounding).  Every CTA owns a range of whole tokens, all heads.
+// (a) count: the CTA's histogram of its selections becomes its row of a
+// [CTA][list] table; (b) a column scan turns every column into the CTAs'
+// first positions inside that list (CTAs in token order) and its total into
+// ws.counts; (c) the list and tile offsets as above; (d) scatter: warp w owns
+// the heads h = w (mod 16) of its CTA -- so no other thread touches the lists
+// of those heads -- and walks the CTA's tokens 32 at a time, slot by slot; the
+// lanes that chose the same list take consecutive positions in lane order
+// (__match_any_sync).  A list thus holds its entries ordered by CTA, 32-token
+// group, slot and token, whatever the timing.
+// ---------------------------------------------------------------------------
+constexpr int kRgWarps = kRgThreads / 32;
+
+static int stable_tokens_per_cta(const Plan &p) {
+    const long long N = (long long)p.NBcap * p.H;
+    const long long rows = std::max<long long>(4096, 4 * N);  // as the histogram kernels above
+    long long t = (rows + p.H - 1) / p.H;
+    t = std::min<long long>(t, p.total);
+    return (int)((t + 31) / 32 * 32);
+}
+
+int stable_regroup_ctas(const Plan &p) {
+    const int tpc = stable_tokens_per_cta(p);
+    return (p.total + tpc - 1) / tpc;
+}
+
+template <bool SMEM>
+__global__ void __launch_bounds__(kRgThreads)
+    regroup_count_cta_kernel(Geometry g, const int32_t *__restrict__ idx, int topk, int tpc, int N,
+                             int *__restrict__ cta_hist) {
+    extern __shared__ int hist[];
+    MOBA_RETURN_IF_BAD(g);
+    int *row = cta_hist + (size_t)blockIdx.x * N;  // zeroed beforehand without SMEM
+    const size_t r0 = (size_t)blockIdx.x * tpc * g.H;
+    const size_t r1 = min((size_t)g.total * g.H, r0 + (size_t)tpc * g.H);
+    const FusedJobs none{nullptr, 0};
+    if (SMEM) {
+        for (int x = threadIdx.x; x < N; x += kRgThreads) hist[x] = 0;
+        __syncthreads();
+    }
+    for (size_t r = r0 + threadIdx.x; r < r1; r += kRgThreads)
+        for_each_selection(g, idx, topk, r, none, [&](int bin, int) {
+            atomicAdd(SMEM ? &hist[bin] : row + bin, 1);
+        });
+    if (SMEM) {
+        __syncthreads();
+        for (int x = threadIdx.x; x < N; x += kRgThreads) row[x] = hist[x];
+    }
+}
+
+// one thread per list: exclusive prefix of its column over the CTAs, total into counts
+__global__ void regroup_colscan_kernel(int G, int N, int *__restrict__ cta_hist,
+                                       int *__restrict__ counts) {
+    const int x = blockIdx.x * blockDim.x + threadIdx.x;
+    if (x >= N) return;
+    constexpr int kBatch = 8;  // loads in flight per thread
+    int run = 0;
+    for (int b0 = 0; b0 < G; b0 += kBatch) {
+        int v[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+            v[u] = b0 + u < G ? cta_hist[(size_t)(b0 + u) * N + x] : 0;
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+            if (b0 + u < G) {
+                cta_hist[(size_t)(b0 + u) * N + x] = run;
+                run += v[u];
+            }
+    }
+    counts[x] = run;
+}
+
+template <bool SMEM>
+__global__ void __launch_bounds__(kRgThreads)
+    regroup_scatter_stable_kernel(Geometry g, const int32_t *__restrict__ idx, int topk, int tpc,
+                                  int N, int *__restrict__ cta_hist,
+                                  const int *__restrict__ list_off, int *__restrict__ list) {
+    extern __shared__ int hist[];
+    MOBA_RETURN_IF_BAD(g);
+    int *row = cta_hist + (size_t)blockIdx.x * N;
+    int *pos = SMEM ? hist : row;  // next free position of each list
+    for (int x = threadIdx.x; x < N; x += kRgThreads) pos[x] = row[x] + __ldg(list_off + x);
+    __syncthreads();
+    const int t0 = blockIdx.x * tpc, t1 = min(g.total, t0 + tpc);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const unsigned below = (1u << lane) - 1u;
+    for (int h = warp; h < g.H; h += kRgWarps) {
+        for (int tb = t0; tb < t1; tb += 32) {
+            const int t = tb + lane;
+            bool live = t < t1;
+            int ci = 0, bbase = 0;
+            const int32_t *sel = idx;
+            if (live) {
+                const int b = upper_index(g.cu, g.num_seqs, t);
+                ci = (t - __ldg(g.cu + b)) / g.bs;
+                bbase = __ldg(g.blk_base + b);
+                sel = idx + ((size_t)t * g.H + h) * topk;
+            }
+            for (int s = 0; s < topk - 1; ++s) {
+                const int c = live ? __ldg(sel + s) : -1;
+                live = live && c >= 0 && c < ci;  // a row's selections end at its first invalid slot
+                if (__ballot_sync(~0u, live) == 0u) break;
+                const int bin = live ? (bbase + c) * g.H + h : -1;
+                const unsigned peers = __match_any_sync(~0u, bin);
+                const int base = live ? pos[bin] : 0;
+                __syncwarp();
+                if (live) {
+                    list[base + __popc(peers & below)] = (t << kSlotBits) | s;
+                    if ((peers >> lane) == 1u) pos[bin] = base + __popc(peers);  // last of its group
+                }
+                __syncwarp();
+            }
+        }
+    }
+}
+
+cudaError_t launch_regroup_stable(const Plan &p, const Workspace &ws, cudaStream_t st) {
+    const int N = p.NBcap * p.H;
+    const int tpc = stable_tokens_per_cta(p);
+    const int G = stable_regroup_ctas(p);
+    const bool smem = N <= kRgSmemBins;
+    const size_t hbytes = smem ? sizeof(int) * (size_t)N : 0;
+    const Geometry g = make_geo(p, ws);
+    cudaError_t e;
+    if (smem) {
+        e = cudaFuncSetAttribute(regroup_count_cta_kernel<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hbytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(regroup_scatter_stable_kernel<true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hbytes);
+        if (e != cudaSuccess) return e;
+        regroup_count_cta_kernel<true><<<G, kRgThreads, hbytes, st>>>(g, ws.idx, p.topk, tpc, N,
+                                                                      ws.cta_hist);
+    } else {
+        if ((e = cudaMemsetAsync(ws.cta_hist, 0, sizeof(int) * (size_t)G * N, st)) != cudaSuccess)
+            return e;
+        regroup_count_cta_kernel<false><<<G, kRgThreads, 0, st>>>(g, ws.idx, p.topk, tpc, N,
+                                                                  ws.cta_hist);
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    regroup_colscan_kernel<<<(N + 255) / 256, 256, 0, st>>>(G, N, ws.cta_hist, ws.counts);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    regroup_scan_kernel<<<1, 1024, 0, st>>>(ws.counts, N, past_tile_rows(p), ws.list_off,
+                                            ws.tile_off, ws.job_list);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (smem)
+        regroup_scatter_stable_kernel<true><<<G, kRgThreads, hbytes, st>>>(
+            g, ws.idx, p.topk, tpc, N, ws.cta_hist, ws.list_off, ws.list);
+    else
+        regroup_scatter_stable_kernel<false><<<G, kRgThreads, 0, st>>>(
+            g, ws.idx, p.topk, tpc, N, ws.cta_hist, ws.list_off, ws.list);
+    note_launches(4);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_fill_idx(const Plan &p, const Workspace &ws, int32_t *idx, cudaStream_t st) {
     const size_t R = (size_t)p.total * p.H;
     const unsigned blocks = (unsigned)std::min<size_t>((R + 255) / 256, 8192);

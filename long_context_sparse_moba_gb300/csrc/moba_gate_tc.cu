@@ -104,11 +104,13 @@ struct Smem {
     // NB boxes of kb_rows x 64 dims
     // mbarriers: q_full[kMaxQ], q_empty[kMaxQ], kb_full, kb_empty,
     // s_full[kMaxSlots], s_empty[kMaxSlots], drain; then the TMEM address slot,
-    // the abort flag and the count of rows left to the exact kernel
+    // the abort flag, the count of rows left to the exact kernel and, per q
+    // stage, the scored-block count of the unit it holds (written by the
+    // producer before it arms the stage's barrier)
     static constexpr int kBarQF = 0, kBarQE = kBarQF + kMaxQ, kBarKF = kBarQE + kMaxQ,
                          kBarKE = kBarKF + 1, kBarSF = kBarKE + 1, kBarSE = kBarSF + kMaxSlots,
                          kBarDrain = kBarSE + kMaxSlots, kNumBars = kBarDrain + 1;
-    static constexpr uint32_t kMisc = kNumBars * 8 + 16;
+    static constexpr uint32_t kMisc = kNumBars * 8 + 16 + 4 * kMaxQ;
     // the misc words go into the alignment slack when it is large enough, else
     // after the tiles
     static constexpr uint32_t kTileBudget = 227 * 1024 - 1008 - kMisc;
@@ -186,6 +188,7 @@ __global__ void __launch_bounds__(threads_for(NWG), 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gmisc + L::kNumBars * 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gmisc + L::kNumBars * 8 + 4);
     int *need_cnt = reinterpret_cast<int *>(gmisc + L::kNumBars * 8 + 8);
+    volatile int *stage_cmax = reinterpret_cast<volatile int *>(gmisc + L::kNumBars * 8 + 16);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     MOBA_RETURN_IF_BAD(a.g);
     const int H = a.g.H, km1 = a.topk - 1;
@@ -273,6 +276,7 @@ __global__ void __launch_bounds__(threads_for(NWG), 1)
                     break;
                 }
                 qpend[s] = -1;
+                stage_cmax[s] = U.cmax;  // released to the MMA thread by the arrive below
                 mbar_expect_tx(bar(L::kBarQF + s), L::kQStage);
                 for (int x = 0; x < L::NB; ++x)
                     tma_load_3d(sQ + s * L::kQStage + x * L::kQBox, &tmap_q, bar(L::kBarQF + s),
@@ -295,7 +299,6 @@ __global__ void __launch_bounds__(threads_for(NWG), 1)
     } else if (warp == 1) {
         // ================= MMA issuer =================
         if (lane == 0) {
-            int cur = -1;
             int nload = 0, i = 0;
             int s = 0, qround = 0, w = 0, wround = 0;  // q stage, TMEM slot of unit i
             bool ok = true;
@@ -303,13 +306,15 @@ __global__ void __launch_bounds__(threads_for(NWG), 1)
             // 16-byte units) is advanced by plain addition below
             const uint64_t dhi = sdesc(sHi, 16, 1024), dlo = sdesc(sLo, 16, 1024);
             const uint32_t kbox16 = kKBox >> 4;
+            // the unit's (sequence, head) is decoded only when it changes; the
+            // scored-block count comes with the q stage
             UnitCursor cur_u;
-            Unit U, NU;  // this unit and the next
-            cur_u.unit(a, u0, km1, U);
-            for (int u = u0; ok && u < u1; ++u, ++i, U = NU) {
-                if (u + 1 < u1) cur_u.unit(a, u + 1, km1, NU);
-                const int pair = U.b * H + U.h;
-                if (pair != cur) {
+            Unit U;
+            int left = 0;  // units of the current (sequence, head) still to come
+            for (int u = u0; ok && u < u1; ++u, ++i, --left) {
+                if (left == 0) {
+                    cur_u.unit(a, u, km1, U);
+                    left = cur_u.nt - ((u - cur_u.ub0) - U.h * cur_u.nt);
                     // the previous keys may be replaced once these MMAs complete
                     if (nload > 0) tc_commit(bar(L::kBarKE));
                     if (!wait_bar(bar(L::kBarKF), nload & 1, ctl)) {
@@ -317,15 +322,15 @@ __global__ void __launch_bounds__(threads_for(NWG), 1)
                         break;
                     }
                     ++nload;
-                    cur = pair;
                 }
                 if (!wait_fast(bar(L::kBarQF + s), qround & 1, ctl) ||
                     (wround > 0 && !wait_fast(bar(L::kBarSE + w), (wround - 1) & 1, ctl))) {
                     ok = false;
                     break;
                 }
+                const int cmax = stage_cmax[s];
                 tc_fence_after();
-                if (U.cmax > 0 && a.cat) {
+                if (cmax > 0 && a.cat) {
                     // one chain: N = 128 rows of [hi; lo]
                     const uint32_t idesc = idesc_bf16(kRows, 128, 0);
                     const uint32_t tS = tmem + w * slot_cols;
@@ -337,8 +342,8 @@ __global__ void __launch_bounds__(threads_for(NWG), 1)
                         tc_mma(tS, dq + aoff, dhi + boff, idesc, k > 0);
                     }
                     tc_commit(bar(L::kBarSF + w));
-                } else if (U.cmax > 0) {
-                    const int n = min((int)slot_cols, (U.cmax + 15) & ~15);
+                } else if (cmax > 0) {
+                    const int n = min((int)slot_cols, (cmax + 15) & ~15);
                     const uint32_t idesc = idesc_bf16(kRows, n, 0);
                     const uint32_t tS = tmem + w * slot_cols;
                     const uint64_t dq = sdesc(sQ + s * L::kQStage, 16, 1024);

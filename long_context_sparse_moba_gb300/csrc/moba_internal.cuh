@@ -77,6 +77,7 @@ struct Workspace {
     float *dq_acc;    // [total][H][D]  fp32 dq accumulator
     float *delta;     // [H][total]     dO . O per row
     float *list_l2, *list_dl;  // [total * H * km1] lse (log2) and dO . O of each list entry's row
+    int *cta_hist;    // [stable regroup CTAs][NBcap * H]  selections per CTA and list
 };
 
 struct Plan {
@@ -131,6 +132,11 @@ cudaError_t launch_union(const Plan &p, const Workspace &ws, bool counted, cudaS
 // skip_fused, the rows of fused own-block jobs are left out
 cudaError_t launch_regroup(const Plan &p, const Workspace &ws, bool counted, bool skip_fused,
                            cudaStream_t st);
+// the same lists with their entries in an order fixed by the selection alone
+// (every call places them alike); needs ws.cta_hist, rewrites ws.counts
+cudaError_t launch_regroup_stable(const Plan &p, const Workspace &ws, cudaStream_t st);
+// CTAs of the stable regroup (rows of ws.cta_hist)
+int stable_regroup_ctas(const Plan &p);
 // attention over the selected past blocks (skipped on the dense / top-1 paths)
 cudaError_t launch_attn_past(const Plan &p, const Workspace &ws, const __nv_bfloat16 *q,
                              const __nv_bfloat16 *k, const __nv_bfloat16 *v, cudaStream_t st);
