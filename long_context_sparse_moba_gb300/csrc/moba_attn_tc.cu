@@ -45,6 +45,9 @@
 //             log-sum-exp merge with the row's past partials -> bf16 out, lse.
 //             Each tile only visits the K/V tiles its rows can see.
 //
+// The MMA lane polls its barriers (a suspended wait wakes up late, and every
+// cycle it sleeps past a phase leaves the tensor core idle); the other roles
+// wait suspended, leaving their issue slots to the softmax warps beside them.
 // Every mbarrier wait is bounded (clock64 budget); a wait that runs out sets
 // MOBA_ERR_TIMEOUT in the device status word and an abort flag that makes the
 // other roles leave their loops; the producer then waits (bounded) for its
@@ -72,6 +75,7 @@ constexpr int kTmemCols = 512;
 constexpr uint32_t kBox = 64;     // dims per TMA box (128 bytes of bf16)
 
 enum Mode { kPast = 0, kCurrent = 1 };
+
 
 struct Args {
     Geometry g;
@@ -377,21 +381,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int g = 0; g < kG; ++g)
                     if (ok && J.te[g] <= J.tb[g]) {
-                        ok = wait_bar(bar(L::kBarQ + g), qj & 1, ctl);
+                        ok = wait_poll(bar(L::kBarQ + g), qj & 1, ctl);
                         if (ok) mbar_arrive(bar(L::kBarQE + g));
                     }
                 if (!ok) break;
                 for (int j = 0; j <= J.nkv; ++j) {
                     const int tk = t + j, s = tk % kStages;
                     if (j < J.nkv) {
-                        if (!wait_bar(bar(L::kBarKF + s), (tk / kStages) & 1, ctl)) {
+                        if (!wait_poll(bar(L::kBarKF + s), (tk / kStages) & 1, ctl)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
                     }
                     const int jp = j - 1, tp = tk - 1, sp = (tp + kStages) % kStages;
-                    if (jp >= 0 && !wait_bar(bar(L::kBarVF + sp), (tp / kStages) & 1, ctl)) {
+                    if (jp >= 0 && !wait_poll(bar(L::kBarVF + sp), (tp / kStages) & 1, ctl)) {
                         ok = false;
                         break;
                     }
@@ -403,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (ok && jp >= J.tb[g] && jp < J.te[g]) {
                             // O_g += P_g V: P_g sits in the first 64 columns of S_g
                             const int jl = jp - J.tb[g];
-                            if (!wait_bar(bar(L::kBarP + g), (gt[g] + jl) & 1, ctl)) {
+                            if (!wait_poll(bar(L::kBarP + g), (gt[g] + jl) & 1, ctl)) {
                                 ok = false;
                                 break;
                             }
@@ -420,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 // Q_g of this job is in shared memory (TMA, or the
                                 // softmax warps' cp.async gather: generic-proxy
                                 // writes, ordered before the MMA's reads here)
-                                if (!wait_bar(bar(L::kBarQ + g), qj & 1, ctl)) {
+                                if (!wait_poll(bar(L::kBarQ + g), qj & 1, ctl)) {
                                     ok = false;
                                     break;
                                 }

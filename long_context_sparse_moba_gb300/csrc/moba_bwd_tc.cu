@@ -48,8 +48,9 @@
 // S^T / P^T / dQ^T in its first 64 columns, dP^T in the next 64.  dQ^T is
 // written over P^T: MMAs from one thread run in order, so the dV MMA has read
 // P^T before it.
-// Every mbarrier wait is bounded; a wait that runs out records
-// MOBA_ERR_TIMEOUT and makes every role leave its loops.
+// The MMA lane polls its barriers (no late wake-up of a suspended wait); the
+// other roles wait suspended.  Every mbarrier wait is bounded; a wait that
+// runs out records MOBA_ERR_TIMEOUT and makes every role leave its loops.
 #include <cuda.h>
 
 #include <algorithm>
@@ -396,8 +397,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // previous unit's accumulators were read)
             auto finish = [&](int m, bool first) -> bool {
                 const int bm = m & 1, sm = m % kStages;
-                if (!wait_fast(bar(L::kBarPF + bm), (m / 2) & 1, ctl)) return false;
-                if (first && ui > 0 && !wait_fast(bar(L::kBarAE), (ui - 1) & 1, ctl)) return false;
+                if (!wait_poll(bar(L::kBarPF + bm), (m / 2) & 1, ctl)) return false;
+                if (first && ui > 0 && !wait_poll(bar(L::kBarAE), (ui - 1) & 1, ctl)) return false;
                 fence_proxy_async();
                 tc_fence_after();
                 const uint32_t q_s = sQ + sm * 2 * L::kRBox, o_s = sO + sm * 2 * L::kRBox;
@@ -425,15 +426,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
             while (ok && walk.next(a, U)) {
-                if (!wait_fast(bar(L::kBarKVF), ui & 1, ctl)) {
+                if (!wait_poll(bar(L::kBarKVF), ui & 1, ctl)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 for (int t = 0; t < U.n_tiles; ++t, ++n) {
                     const int s = n % kStages, b = n & 1;
-                    if (!wait_fast(bar(L::kBarQF + s), (n / kStages) & 1, ctl) ||
-                        (n >= 2 && !wait_fast(bar(L::kBarDQE + b), ((n - 2) / 2) & 1, ctl))) {
+                    if (!wait_poll(bar(L::kBarQF + s), (n / kStages) & 1, ctl) ||
+                        (n >= 2 && !wait_poll(bar(L::kBarDQE + b), ((n - 2) / 2) & 1, ctl))) {
                         ok = false;
                         break;
                     }

@@ -34,7 +34,8 @@
 //        sums), so the selection -- and its lower-index tie-break -- equals
 //        that kernel's bit for bit.
 // Rows whose own block has at most k-1 predecessors take them all.
-// Every wait is bounded; a wait that runs out records MOBA_ERR_TIMEOUT.
+// The MMA lane polls its barriers, the other roles wait suspended.  Every
+// wait is bounded; a wait that runs out records MOBA_ERR_TIMEOUT.
 #include <algorithm>
 
 #include "moba.h"
@@ -317,14 +318,14 @@ __global__ void __launch_bounds__(threads_for(NWG), 1)
                     left = cur_u.nt - ((u - cur_u.ub0) - U.h * cur_u.nt);
                     // the previous keys may be replaced once these MMAs complete
                     if (nload > 0) tc_commit(bar(L::kBarKE));
-                    if (!wait_bar(bar(L::kBarKF), nload & 1, ctl)) {
+                    if (!wait_poll(bar(L::kBarKF), nload & 1, ctl)) {
                         ok = false;
                         break;
                     }
                     ++nload;
                 }
-                if (!wait_fast(bar(L::kBarQF + s), qround & 1, ctl) ||
-                    (wround > 0 && !wait_fast(bar(L::kBarSE + w), (wround - 1) & 1, ctl))) {
+                if (!wait_poll(bar(L::kBarQF + s), qround & 1, ctl) ||
+                    (wround > 0 && !wait_poll(bar(L::kBarSE + w), (wround - 1) & 1, ctl))) {
                     ok = false;
                     break;
                 }

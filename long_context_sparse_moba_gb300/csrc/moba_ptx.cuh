@@ -212,7 +212,21 @@ struct Ctl {
     long long limit;
 };
 
+// A wait ran out: the abort flag makes every role leave its loops, and the
+// first timeout of the device records which wait gave up.
+static __device__ __noinline__ void record_timeout(uint32_t bar, uint32_t parity, const Ctl &c) {
+    *c.abort = 1;
+    if (atomicExch(c.status, (int)MOBA_ERR_TIMEOUT) == 0) {
+        c.status[1] = (int)(bar & 0xffff);
+        c.status[2] = (int)parity;
+        c.status[3] = (int)blockIdx.x;
+        c.status[4] = (int)threadIdx.x;
+    }
+}
+
 // Bounded wait; false when it ran out (status set) or another role aborted.
+// The test suspends the thread while the phase is incomplete (no issue slots
+// taken from the warps beside it), at the price of a late wake-up.
 static __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl &c) {
     if (mbar_test(bar, parity)) return true;
     const long long t0 = clock64();
@@ -220,17 +234,40 @@ static __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, cons
         if (mbar_test(bar, parity)) return true;
         if (*c.abort) return false;
         if (clock64() - t0 > c.limit) {
-            *c.abort = 1;
-            if (atomicExch(c.status, (int)MOBA_ERR_TIMEOUT) == 0) {
-                // first timeout of this device: which wait gave up
-                c.status[1] = (int)(bar & 0xffff);
-                c.status[2] = (int)parity;
-                c.status[3] = (int)blockIdx.x;
-                c.status[4] = (int)threadIdx.x;
-            }
+            record_timeout(bar, parity, c);
             return false;
         }
     }
+}
+// Non-blocking test of a phase.
+__device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait by polling: it sees the phase complete within a few cycles,
+// for the single threads (MMA issuers) whose every late wake-up leaves the
+// tensor core idle; it takes issue slots, so the warps that do arithmetic
+// wait with wait_bar.
+static __device__ __noinline__ bool wait_poll_slow(uint32_t bar, uint32_t parity, const Ctl &c) {
+    const long long t0 = clock64();
+    while (true) {
+        for (int k = 0; k < 64; ++k)
+            if (mbar_poll(bar, parity)) return true;
+        if (*c.abort) return false;
+        if (clock64() - t0 > c.limit) {
+            record_timeout(bar, parity, c);
+            return false;
+        }
+    }
+}
+__device__ __forceinline__ bool wait_poll(uint32_t bar, uint32_t parity, const Ctl &c) {
+    return mbar_poll(bar, parity) || wait_poll_slow(bar, parity, c);
 }
 // one inline test first: the bounded wait is a call
 __device__ __forceinline__ bool wait_fast(uint32_t bar, uint32_t parity, const Ctl &c) {
