@@ -76,6 +76,15 @@ constexpr uint32_t kBox = 64;     // dims per TMA box (128 bytes of bf16)
 
 enum Mode { kPast = 0, kCurrent = 1 };
 
+// The softmax warps' waits at a job boundary (the job's last PV, the next
+// job's first S): in the past mode, whose jobs are a few tiles long, they poll
+// -- every warp of the CTA is waiting on the same chain then, and a late
+// wake-up adds to it; elsewhere they wait suspended.
+template <int MODE>
+__device__ __forceinline__ bool boundary_wait(uint32_t bar, uint32_t parity, const Ctl &c) {
+    return MODE == kPast ? wait_poll(bar, parity, c) : wait_bar(bar, parity, c);
+}
+
 
 struct Args {
     Geometry g;
@@ -567,7 +576,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int j = my_tb + jl;
                 // S_g(j) is ready; the commit behind it also covers PV_g(j-1), so
                 // O_g is stable and P_g's columns are free
-                if (!__all_sync(0xffffffffu, wait_bar(bar(L::kBarS + g), (gt + jl) & 1, ctl))) {
+                const bool sready = jl == 0 ? boundary_wait<MODE>(bar(L::kBarS + g), (gt + jl) & 1, ctl)
+                                            : wait_bar(bar(L::kBarS + g), (gt + jl) & 1, ctl);
+                if (!__all_sync(0xffffffffu, sready)) {
                     ok = false;
                     break;
                 }
@@ -711,7 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             // ---------------- epilogue ----------------
             if (ntile > 0) {
-                if (!__all_sync(0xffffffffu, wait_bar(bar(L::kBarPV + g), gj & 1, ctl))) {
+                if (!__all_sync(0xffffffffu, boundary_wait<MODE>(bar(L::kBarPV + g), gj & 1, ctl))) {
                     ok = false;
                     break;
                 }
