@@ -70,8 +70,8 @@ TRAFFIC_SOURCES = ("long_context_sparse_moba_gb300/csrc/moba_attn_tc.cu",
                    "long_context_sparse_moba_gb300/csrc/moba_internal.cuh")
 MEASURED_TRAFFIC = {
     # (workload, topk, phase): (bytes per launch, sources_sha256() of the code measured)
-    ("train32k", 3, "attn_past"): (1031735808 + 538555904,
-                                   "b3849337b3be598e6afa581d8c98fb9c0bea5bf54ecee09c4948743f726e599e"),
+    ("train32k", 3, "attn_past"): (1031219712 + 538434560,
+                                   "1331857265599531e743b45436cc1490f18acad8cdc97abcfea663378409ce21"),
 }
 
 
