@@ -542,16 +542,22 @@ __global__ void __launch_bounds__(kRgThreads)
     }
 }
 
+// After an earlier kernel has recorded an error in the device status word
+// (a bounded wait gave up: the selection may be incomplete), the lists are
+// published empty and the scatters write nothing, so that no later phase
+// gathers through entries that were never written; the status stays set until
+// the caller reads it.
 __global__ void regroup_scan_kernel(const int *__restrict__ counts, int N, int tile_m,
                                     int *__restrict__ list_off, int *__restrict__ tile_off,
-                                    int *__restrict__ job_list) {
+                                    int *__restrict__ job_list, const int *__restrict__ status) {
+    const bool ok = status == nullptr || *(volatile const int *)status == 0;
     cta_exclusive_scan(
-        N, [&](int i) { return counts[i]; }, [&](int i, int v) { list_off[i] = v; });
+        N, [&](int i) { return ok ? counts[i] : 0; }, [&](int i, int v) { list_off[i] = v; });
     cta_exclusive_scan(
-        N, [&](int i) { return (counts[i] + tile_m - 1) / tile_m; },
+        N, [&](int i) { return ok ? (counts[i] + tile_m - 1) / tile_m : 0; },
         [&](int i, int v) {
             tile_off[i] = v;
-            if (i < N)  // the attention jobs of list i
+            if (i < N && ok)  // the attention jobs of list i
                 for (int t = 0, nt = (counts[i] + tile_m - 1) / tile_m; t < nt; ++t)
                     job_list[v + t] = i;
         });
@@ -561,9 +567,10 @@ template <bool SMEM>
 __global__ void __launch_bounds__(kRgThreads)
     regroup_scatter_kernel(Geometry g, const int32_t *__restrict__ idx, int topk, int rows_per_cta,
                            int N, int *__restrict__ counts, const int *__restrict__ list_off,
-                           int *__restrict__ list, FusedJobs fj) {
+                           int *__restrict__ list, FusedJobs fj, const int *__restrict__ status) {
     extern __shared__ int hist[];
     MOBA_RETURN_IF_BAD(g);
+    if (status && *(volatile const int *)status != 0) return;  // the lists were published empty
     const size_t R = (size_t)g.total * g.H;
     const size_t r0 = (size_t)blockIdx.x * rows_per_cta, r1 = min(R, r0 + rows_per_cta);
     if (SMEM) {
@@ -572,18 +579,29 @@ __global__ void __launch_bounds__(kRgThreads)
         for (size_t r = r0 + threadIdx.x; r < r1; r += kRgThreads)
             for_each_selection(g, idx, topk, r, fj, [&](int bin, int) { atomicAdd(&hist[bin], 1); });
         __syncthreads();
-        // this CTA's range in list x: [list_off + remaining - n, list_off + remaining)
+        // this CTA's range in list x: [list_off + remaining - n, list_off + remaining);
+        // a range that would start below the list (only when the counts and the
+        // selection disagree) is refused whole: a negative start skips its writes
         for (int x = threadIdx.x; x < N; x += kRgThreads) {
             const int n = hist[x];
-            if (n) hist[x] = __ldg(list_off + x) + atomicSub(counts + x, n) - n;
+            if (n) {
+                const int rem = atomicSub(counts + x, n);
+                hist[x] = rem >= n ? __ldg(list_off + x) + rem - n : INT_MIN / 2;
+            }
         }
         __syncthreads();
     }
     for (size_t r = r0 + threadIdx.x; r < r1; r += kRgThreads)
         for_each_selection(g, idx, topk, r, fj, [&](int bin, int entry) {
-            const int pos = SMEM ? atomicAdd(&hist[bin], 1)
-                                 : __ldg(list_off + bin) + atomicSub(counts + bin, 1) - 1;
-            list[pos] = entry;
+            // positions stay inside the list: ranges are reserved downwards from
+            // its end and never below its start
+            if (SMEM) {
+                const int pos = atomicAdd(&hist[bin], 1);
+                if (pos >= 0) list[pos] = entry;
+            } else {
+                const int rem = atomicSub(counts + bin, 1);
+                if (rem > 0) list[__ldg(list_off + bin) + rem - 1] = entry;
+            }
         });
 }
 
@@ -620,14 +638,14 @@ cudaError_t launch_regroup(const Plan &p, const Workspace &ws, bool counted, boo
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     regroup_scan_kernel<<<1, 1024, 0, st>>>(ws.counts, N, past_tile_rows(p), ws.list_off,
-                                            ws.tile_off, ws.job_list);
+                                            ws.tile_off, ws.job_list, status_word());
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (smem)
         regroup_scatter_kernel<true><<<grid, kRgThreads, hbytes, st>>>(
-            g, ws.idx, p.topk, rows_per_cta, N, ws.counts, ws.list_off, ws.list, fj);
+            g, ws.idx, p.topk, rows_per_cta, N, ws.counts, ws.list_off, ws.list, fj, status_word());
     else
         regroup_scatter_kernel<false><<<grid, kRgThreads, 0, st>>>(
-            g, ws.idx, p.topk, rows_per_cta, N, ws.counts, ws.list_off, ws.list, fj);
+            g, ws.idx, p.topk, rows_per_cta, N, ws.counts, ws.list_off, ws.list, fj, status_word());
     note_launches(2);
     return cudaGetLastError();
 }
@@ -711,9 +729,11 @@ template <bool SMEM>
 __global__ void __launch_bounds__(kRgThreads)
     regroup_scatter_stable_kernel(Geometry g, const int32_t *__restrict__ idx, int topk, int tpc,
                                   int N, int *__restrict__ cta_hist,
-                                  const int *__restrict__ list_off, int *__restrict__ list) {
+                                  const int *__restrict__ list_off, int *__restrict__ list,
+                                  const int *__restrict__ status) {
     extern __shared__ int hist[];
     MOBA_RETURN_IF_BAD(g);
+    if (status && *(volatile const int *)status != 0) return;  // the lists were published empty
     int *row = cta_hist + (size_t)blockIdx.x * N;
     int *pos = SMEM ? hist : row;  // next free position of each list
     for (int x = threadIdx.x; x < N; x += kRgThreads) pos[x] = row[x] + __ldg(list_off + x);
@@ -778,14 +798,14 @@ cudaError_t launch_regroup_stable(const Plan &p, const Workspace &ws, cudaStream
     regroup_colscan_kernel<<<(N + 255) / 256, 256, 0, st>>>(G, N, ws.cta_hist, ws.counts);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     regroup_scan_kernel<<<1, 1024, 0, st>>>(ws.counts, N, past_tile_rows(p), ws.list_off,
-                                            ws.tile_off, ws.job_list);
+                                            ws.tile_off, ws.job_list, status_word());
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (smem)
         regroup_scatter_stable_kernel<true><<<G, kRgThreads, hbytes, st>>>(
-            g, ws.idx, p.topk, tpc, N, ws.cta_hist, ws.list_off, ws.list);
+            g, ws.idx, p.topk, tpc, N, ws.cta_hist, ws.list_off, ws.list, status_word());
     else
         regroup_scatter_stable_kernel<false><<<G, kRgThreads, 0, st>>>(
-            g, ws.idx, p.topk, tpc, N, ws.cta_hist, ws.list_off, ws.list);
+            g, ws.idx, p.topk, tpc, N, ws.cta_hist, ws.list_off, ws.list, status_word());
     note_launches(4);
     return cudaGetLastError();
 }

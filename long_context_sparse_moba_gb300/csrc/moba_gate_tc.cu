@@ -14,7 +14,8 @@
 //   warp 0      TMA: a ring of q tiles (as many stages as the shared memory
 //               left beside the keys holds) and, whenever the (sequence, head)
 //               changes, the head's pooled keys split into two bf16 terms,
-//               kbar ~= hi + lo (hi = bf16(kbar), lo = bf16(kbar - hi));
+//               kbar ~= hi + lo (hi = bf16(kbar), lo = bf16(kbar - hi)); it
+//               leaves each unit's fields beside its q stage;
 //   warp 1      allocates TMEM; lane 0 issues one MMA chain per unit,
 //               approx[r][c] = q_r . hi_c + q_r . lo_c (M128, N = the unit's
 //               scored blocks rounded up to 16, fp32 in TMEM), into as many
@@ -106,12 +107,12 @@ struct Smem {
     // mbarriers: q_full[kMaxQ], q_empty[kMaxQ], kb_full, kb_empty,
     // s_full[kMaxSlots], s_empty[kMaxSlots], drain; then the TMEM address slot,
     // the abort flag, the count of rows left to the exact kernel and, per q
-    // stage, the scored-block count of the unit it holds (written by the
+    // stage, the fields of the unit it holds (StageMeta, written by the
     // producer before it arms the stage's barrier)
     static constexpr int kBarQF = 0, kBarQE = kBarQF + kMaxQ, kBarKF = kBarQE + kMaxQ,
                          kBarKE = kBarKF + 1, kBarSF = kBarKE + 1, kBarSE = kBarSF + kMaxSlots,
                          kBarDrain = kBarSE + kMaxSlots, kNumBars = kBarDrain + 1;
-    static constexpr uint32_t kMisc = kNumBars * 8 + 16 + 4 * kMaxQ;
+    static constexpr uint32_t kMisc = kNumBars * 8 + 16 + 32 * kMaxQ;
     // the misc words go into the alignment slack when it is large enough, else
     // after the tiles
     static constexpr uint32_t kTileBudget = 227 * 1024 - 1008 - kMisc;
@@ -124,6 +125,16 @@ struct Smem {
 struct Unit {
     int b, h, t, seq0, L, bbase, nb, cmax;
 };
+
+// A unit's fields as the producer leaves them beside its q stage: the MMA lane
+// and the selection warpgroups read them after the stage's barrier (no unit
+// decoding, no integer division per unit or row there).
+struct StageMeta {
+    int cmax;       // blocks scored by some row of the unit (0: none)
+    int h, t, seq0, L, bbase, nb;
+    int c0;         // block of the unit's first row
+};
+static_assert(sizeof(StageMeta) == 32, "eight words per stage");
 
 // unit u -> (sequence, head, row tile); cmax = blocks scored by some row of
 // the tile (0 when no row is scored).  Each role walks increasing units and
@@ -189,7 +200,7 @@ __global__ void __launch_bounds__(threads_for(NWG), 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gmisc + L::kNumBars * 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gmisc + L::kNumBars * 8 + 4);
     int *need_cnt = reinterpret_cast<int *>(gmisc + L::kNumBars * 8 + 8);
-    volatile int *stage_cmax = reinterpret_cast<volatile int *>(gmisc + L::kNumBars * 8 + 16);
+    StageMeta *stage_meta = reinterpret_cast<StageMeta *>(gmisc + L::kNumBars * 8 + 16);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     MOBA_RETURN_IF_BAD(a.g);
     const int H = a.g.H, km1 = a.topk - 1;
@@ -203,6 +214,7 @@ __global__ void __launch_bounds__(threads_for(NWG), 1)
     }
     Ctl ctl{abort_flag, a.status, a.wait_limit};
     const int nq = a.nq, nslots = a.nslots;
+    const int nwg = min(NWG, nslots);  // selection warpgroups in use
     const uint32_t slot_cols = 512u / nslots;
     const uint32_t sQ = base, sHi = base + nq * L::kQStage;
     const uint32_t sLo = a.cat ? sHi + (uint32_t)a.kb_rows * 128 : sHi + L::NB * kKBox;
@@ -277,7 +289,17 @@ __global__ void __launch_bounds__(threads_for(NWG), 1)
                     break;
                 }
                 qpend[s] = -1;
-                stage_cmax[s] = U.cmax;  // released to the MMA thread by the arrive below
+                {  // released to the selection warps by the arrive below
+                    StageMeta &m = stage_meta[s];
+                    m.cmax = U.cmax;
+                    m.h = U.h;
+                    m.t = U.t;
+                    m.seq0 = U.seq0;
+                    m.L = U.L;
+                    m.bbase = U.bbase;
+                    m.nb = U.nb;
+                    m.c0 = U.t * kRows / a.g.bs;
+                }
                 mbar_expect_tx(bar(L::kBarQF + s), L::kQStage);
                 for (int x = 0; x < L::NB; ++x)
                     tma_load_3d(sQ + s * L::kQStage + x * L::kQBox, &tmap_q, bar(L::kBarQF + s),
@@ -329,7 +351,7 @@ __global__ void __launch_bounds__(threads_for(NWG), 1)
                     ok = false;
                     break;
                 }
-                const int cmax = stage_cmax[s];
+                const int cmax = stage_meta[s].cmax;
                 tc_fence_after();
                 if (cmax > 0 && a.cat) {
                     // one chain: N = 128 rows of [hi; lo]
@@ -384,27 +406,39 @@ __global__ void __launch_bounds__(threads_for(NWG), 1)
         // warpgroup wg takes units wg, wg + nwg, ...; no more warpgroups than
         // TMEM slots
         const int wg = (warp - 2) >> 2, quarter = warp & 3;
-        const int nwg = min(NWG, nslots);
         const int row = quarter * 32 + lane;  // my TMEM lane and q row
         const uint32_t tlane = tmem + ((uint32_t)(quarter * 32) << 16);
-        UnitCursor cur_u;
-        Unit U, NU;  // this unit and the warpgroup's next
         int kn_pair = -1;  // (sequence, head) whose key-norm maximum is in kn
         float kn = 0.f;
-        if (wg < nwg && u0 + wg < u1) cur_u.unit(a, u0 + wg, km1, U);
-        for (int u = u0 + wg, i = wg; wg < nwg && u < u1; u += nwg, i += nwg, U = NU) {
-            if (u + nwg < u1) cur_u.unit(a, u + nwg, km1, NU);
+        for (int u = u0 + wg, i = wg; wg < nwg && u < u1; u += nwg, i += nwg) {
             const int s = i % nq, slot = i % nslots;
             const uint32_t tS = tlane + slot * slot_cols;
             const uint32_t sq = sQ + s * L::kQStage;
+            // the unit's fields, copied before the stage is handed back
+            if (!__all_sync(0xffffffffu, wait_fast(bar(L::kBarQF + s), (i / nq) & 1, ctl))) break;
+            Unit U;
+            {
+                const StageMeta &m = stage_meta[s];
+                U.cmax = m.cmax;
+                U.h = m.h;
+                U.t = m.t;
+                U.seq0 = m.seq0;
+                U.L = m.L;
+                U.bbase = m.bbase;
+                U.nb = m.nb;
+                U.b = m.c0;  // (the block of the unit's first row, below)
+            }
             const int my_i = U.t * kRows + row;
             const bool valid = my_i < U.L;
-            const int ci = valid ? my_i / a.g.bs : 0;
+            // my row's block: the unit's 128 rows span at most three blocks
+            // (block sizes are multiples of 64)
+            const int x_in = U.t * kRows - U.b * a.g.bs + row;
+            const int ci = valid ? U.b + (x_in >= a.g.bs) + (x_in >= 2 * a.g.bs) : 0;
             const int tok = U.seq0 + my_i;
             const bool scored = valid && km1 > 0 && ci > km1;
             // largest pooled-key norm of the head's blocks (the margin), once per
             // (sequence, head)
-            const int pair = U.b * H + U.h;
+            const int pair = U.bbase * H + U.h;
             if (pair != kn_pair) {
                 kn = 0.f;
                 for (int c = lane; c < U.nb; c += 32)
@@ -420,24 +454,30 @@ __global__ void __launch_bounds__(threads_for(NWG), 1)
             bool need = false;  // the exact kernel writes this row
             unsigned long long cand = ~0ull;  // its candidate blocks, one byte each
             int ncand = 0;
-            // ||q_r||^2 for the margin, read from the q stage as soon as it has
-            // landed, so that it overlaps the unit's MMAs
-            if (!__all_sync(0xffffffffu, wait_fast(bar(L::kBarQF + s), (i / nq) & 1, ctl))) break;
+            // ||q_r||^2 for the margin, from the q stage while the unit's MMAs
+            // run: four independent f32x2 accumulators (a bf16 is the top half
+            // of its fp32)
             float qq = 0.f;
             if (scored) {
+                float2 acc[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[e] = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int d = 0; d < D; d += 8) {
                     uint32_t w[4];
+                    // volatile: kept after the wait for the stage's barrier
                     asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                                  : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
                                  : "r"(q_addr<D>(sq, row, d)));
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float2 f =
-                            __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[e]));
-                        qq = fmaf(f.x, f.x, fmaf(f.y, f.y, qq));
+                        const float2 f = make_float2(__uint_as_float(w[e] << 16),
+                                                     __uint_as_float(w[e] & 0xffff0000u));
+                        acc[e] = ffma2(f, f, acc[e]);
                     }
                 }
+                qq = ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
+                     ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
             }
             if (!__all_sync(0xffffffffu, wait_fast(bar(L::kBarSF + slot), (i / nslots) & 1, ctl))) break;
             tc_fence_after();
@@ -534,7 +574,7 @@ __global__ void __launch_bounds__(threads_for(NWG), 1)
                     }
                 }
             }
-            release_slot();  // the slot is free for the unit after next
+            release_slot();  // the slot is free for the warpgroup's next unit
             // rows left to the exact kernel go to this CTA's own region of the
             // list (room for all of its rows), reserved with a shared-memory count
             const unsigned nmask = __ballot_sync(0xffffffffu, need);
