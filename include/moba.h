@@ -222,6 +222,34 @@ int moba_attn_fwd_ex(const void *q, const void *k, const void *v, void *out, flo
                      void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * moba_attn_fwd on HOST buffers: the same operation and layouts, with q, k,
+ * v, out and lse in host memory (page-locked for asynchronous copies; other
+ * host memory works but the copies then block).  Enqueued on `stream` and
+ * returning before completion: k, q and v are copied to the device scratch in
+ * that order, each in two halves on two streams of the call's own (two copy
+ * engines), starting after the earlier work on `stream`; the pooling, the gate
+ * and the attention each wait only for the inputs they read, so the first
+ * phases run while v is still arriving; out and lse come back the same way,
+ * and `stream` reaches its next work once they have.  The host buffers must
+ * stay valid, and out / lse unread, until then.  Two calls on different
+ * streams with different scratch run side by side (one call's copies beside
+ * the other's kernels).
+ *   dev_scratch : device memory, 256-byte aligned, at least
+ *                 moba_attn_fwd_host_scratch_size bytes (MOBA_ERR_WORKSPACE
+ *                 otherwise): the device copies of q, k, v, out, lse and the
+ *                 forward's workspace; not used by anything else until the
+ *                 call's work has finished.
+ *   options     : as moba_attn_fwd_ex (idx_out, if given, is device memory).
+ * Errors: as moba_attn_fwd_ex; a failed copy or stream/event creation
+ * returns MOBA_ERR_CUDA.
+ */
+int moba_attn_fwd_host(const void *q, const void *k, const void *v, void *out, float *lse, int B,
+                       int H, int S, int D, int block_size, int topk,
+                       const moba_options_t *options, void *dev_scratch, size_t scratch_bytes,
+                       void *stream);
+size_t moba_attn_fwd_host_scratch_size(int B, int H, int S, int D, int block_size, int topk);
+
+/*
  * Varlen forward: q, k, v, out [total_tokens][H][D] bf16; lse
  * [H][total_tokens] fp32; cu_seqlens DEVICE int32 [num_seqs + 1];
  * max_seqlen >= every sequence length.  Each sequence is partitioned into

@@ -208,9 +208,23 @@ static thread_local cudaError_t g_last_cuda_error = cudaSuccess;
         }                                                \
     } while (0)
 
+// Events the forward waits for just before the phase that reads each input
+// (moba_attn_fwd_host: the copies of k, q and v land while earlier phases run).
+struct InputWaits {
+    cudaEvent_t k[2], q[2], v[2];
+};
+static cudaError_t wait_all(cudaStream_t st, const cudaEvent_t (&ev)[2]) {
+    for (cudaEvent_t e : ev) {
+        const cudaError_t r = cudaStreamWaitEvent(st, e, 0);
+        if (r != cudaSuccess) return r;
+    }
+    return cudaSuccess;
+}
+
 static int run_forward(const Plan &p, const int *cu_dev, const void *q, const void *k,
                        const void *v, void *out, float *lse, void *workspace, size_t ws_bytes,
-                       const moba_options_t *opt, cudaStream_t st) {
+                       const moba_options_t *opt, cudaStream_t st,
+                       const InputWaits *iw = nullptr) {
     Workspace ws;
     const size_t need = workspace_bytes(p, &ws, static_cast<char *>(workspace));
     if (!workspace || ws_bytes < need) return MOBA_ERR_WORKSPACE;
@@ -226,9 +240,11 @@ static int run_forward(const Plan &p, const int *cu_dev, const void *q, const vo
     const bool gate = !p.dense && p.km1 > 0;
     // the selection goes straight to the caller's buffer when one is given
     if (gate && idx_out) ws.idx = idx_out;
+    if (iw) MOBA_TRY(wait_all(st, iw->k));
     if (gate) MOBA_TRY(launch_kpool(p, ws, kb, ws.kbar, st));
     prof_mark(ev, 2, st);
     const bool tc_gate = p.gate_kind == MOBA_GATE_TENSOR_CORES && gate_tc_supported(p);
+    if (iw) MOBA_TRY(wait_all(st, iw->q));
     if (gate) {
         // the per-list counts
         MOBA_TRY(cudaMemsetAsync(ws.counts, 0, sizeof(int) * ((size_t)p.NBcap * p.H + 1), st));
@@ -247,6 +263,7 @@ static int run_forward(const Plan &p, const int *cu_dev, const void *q, const vo
     if (fuse) MOBA_TRY(launch_union(p, ws, tc_gate, st));
     if (gate) MOBA_TRY(launch_regroup(p, ws, tc_gate, fuse, st));
     prof_mark(ev, 4, st);
+    if (iw) MOBA_TRY(wait_all(st, iw->v));
     MOBA_TRY(launch_attn_past(p, ws, qb, kb, vb, st));
     prof_mark(ev, 5, st);
     MOBA_TRY(launch_attn_current(p, ws, qb, kb, vb, static_cast<__nv_bfloat16 *>(out), lse, st));
@@ -534,6 +551,112 @@ MOBA_EXPORT int moba_attn_fwd(const void *q, const void *k, const void *v, void 
                               int B, int H, int S, int D, int block_size, int topk, void *stream) {
     return moba_attn_fwd_ex(q, k, v, out, lse, B, H, S, D, block_size, topk, nullptr, nullptr, 0,
                             stream);
+}
+
+// ---------------------------------------------------------------------------
+// forward on host buffers: copies in, the forward, copies out, one call
+// ---------------------------------------------------------------------------
+// Device scratch: q, k, v, out (bf16), lse (fp32) and the forward's workspace,
+// each from a 256-byte boundary.
+struct HostScratch {
+    size_t q, k, v, out, lse, ws, end;
+};
+static HostScratch host_scratch(const Plan &p) {
+    HostScratch h;
+    const size_t qkv = align256((size_t)p.total * p.H * p.D * 2);
+    h.q = 0;
+    h.k = h.q + qkv;
+    h.v = h.k + qkv;
+    h.out = h.v + qkv;
+    h.lse = h.out + qkv;
+    h.ws = h.lse + align256((size_t)p.total * p.H * 4);
+    h.end = h.ws + workspace_bytes(p, nullptr, nullptr);
+    return h;
+}
+
+MOBA_EXPORT size_t moba_attn_fwd_host_scratch_size(int B, int H, int S, int D, int block_size,
+                                                   int topk) {
+    Plan p;
+    if (make_plan(B, (long long)B * S, S, H, D, block_size, topk, true, &p) != MOBA_OK) return 0;
+    return host_scratch(p).end;
+}
+
+// Copies a host range to or from the device in two halves on two streams (two
+// copy engines), recording an event on each after its half.
+static cudaError_t copy_halves(void *dst, const void *src, size_t bytes, cudaMemcpyKind kind,
+                               const cudaStream_t (&cs)[2], cudaEvent_t (&done)[2]) {
+    const size_t half = (bytes / 2) & ~size_t(255);
+    const size_t part[2] = {half, bytes - half};
+    size_t off = 0;
+    for (int i = 0; i < 2; ++i) {
+        cudaError_t e = cudaSuccess;
+        if (part[i])
+            e = cudaMemcpyAsync(static_cast<char *>(dst) + off, static_cast<const char *>(src) + off,
+                                part[i], kind, cs[i]);
+        if (e == cudaSuccess) e = cudaEventRecord(done[i], cs[i]);
+        if (e != cudaSuccess) return e;
+        off += part[i];
+    }
+    return cudaSuccess;
+}
+
+MOBA_EXPORT int moba_attn_fwd_host(const void *q, const void *k, const void *v, void *out,
+                                   float *lse, int B, int H, int S, int D, int block_size,
+                                   int topk, const moba_options_t *opt, void *dev_scratch,
+                                   size_t scratch_bytes, void *stream) {
+    int rc = check_tensors(q, k, v, out, lse);
+    if (rc || (rc = check_options_buffers(opt))) return rc;
+    Plan p;
+    rc = make_plan(B, (long long)B * S, S, H, D, block_size, topk, true, &p);
+    if (rc || (rc = apply_options(opt, &p))) return rc;
+    const HostScratch hs = host_scratch(p);
+    if (!dev_scratch || scratch_bytes < hs.end || (reinterpret_cast<uintptr_t>(dev_scratch) & 255))
+        return MOBA_ERR_WORKSPACE;
+    char *base = static_cast<char *>(dev_scratch);
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t qkv = (size_t)p.total * p.H * p.D * 2, lse_bytes = (size_t)p.total * p.H * 4;
+    // two copy streams and their events, made for this call and released once
+    // the work enqueued on them has run
+    cudaStream_t cs[2] = {nullptr, nullptr};
+    InputWaits iw;
+    cudaEvent_t start = nullptr, fin = nullptr, back[2] = {nullptr, nullptr};
+    cudaEvent_t *evs[] = {&start, &fin, &back[0], &back[1], &iw.k[0], &iw.k[1],
+                          &iw.q[0], &iw.q[1], &iw.v[0], &iw.v[1]};
+    for (cudaEvent_t *e : evs) *e = nullptr;
+    cudaError_t e = cudaSuccess;
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i)
+        e = cudaStreamCreateWithFlags(&cs[i], cudaStreamNonBlocking);
+    for (cudaEvent_t *ev : evs)
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    // the copies in start after the caller's earlier work on its stream, in the
+    // order the phases read them: k (pooling), q (gate), v (attention)
+    if (e == cudaSuccess) e = cudaEventRecord(start, st);
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaStreamWaitEvent(cs[i], start, 0);
+    if (e == cudaSuccess) e = copy_halves(base + hs.k, k, qkv, cudaMemcpyHostToDevice, cs, iw.k);
+    if (e == cudaSuccess) e = copy_halves(base + hs.q, q, qkv, cudaMemcpyHostToDevice, cs, iw.q);
+    if (e == cudaSuccess) e = copy_halves(base + hs.v, v, qkv, cudaMemcpyHostToDevice, cs, iw.v);
+    if (e == cudaSuccess) {
+        rc = run_forward(p, nullptr, base + hs.q, base + hs.k, base + hs.v, base + hs.out,
+                         reinterpret_cast<float *>(base + hs.lse), base + hs.ws, hs.end - hs.ws,
+                         opt, st, &iw);
+        // the results out, then the caller's stream waits for them
+        if (rc == MOBA_OK) {
+            e = cudaEventRecord(fin, st);
+            for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaStreamWaitEvent(cs[i], fin, 0);
+            if (e == cudaSuccess) e = copy_halves(out, base + hs.out, qkv, cudaMemcpyDeviceToHost, cs, back);
+            // lse is small: one copy on the first stream, after its half of out
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync(lse, base + hs.lse, lse_bytes, cudaMemcpyDeviceToHost, cs[0]);
+            if (e == cudaSuccess) e = cudaEventRecord(back[0], cs[0]);
+            for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaStreamWaitEvent(st, back[i], 0);
+        }
+    }
+    for (cudaEvent_t *ev : evs)
+        if (*ev) cudaEventDestroy(*ev);
+    for (cudaStream_t c : cs)
+        if (c) cudaStreamDestroy(c);
+    if (rc != MOBA_OK) return rc;
+    return cuda_status(e);
 }
 
 MOBA_EXPORT int moba_attn_fwd_varlen_ex(const void *q, const void *k, const void *v, void *out,

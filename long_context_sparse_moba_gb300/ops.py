@@ -62,6 +62,8 @@ _SIGNATURES = {
     "moba_gate_topk_ex": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "moba_gate_topk_varlen_ex": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "moba_attn_fwd_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "moba_attn_fwd_host": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "moba_attn_fwd_host_scratch_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "moba_attn_fwd_varlen_ex": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P,
                                      _P, _SZ, _P]),
     "moba_attn_bwd_ex": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P,
@@ -291,6 +293,36 @@ def attn_fwd(q, k, v, block_size: int, topk: int, out=None, lse=None, workspace=
                                 workspace.numel() if workspace is not None else 0,
                                 _stream(stream))
     _check(rc, "moba_attn_fwd")
+    return out, lse
+
+
+def host_scratch_size(B: int, H: int, S: int, D: int, block_size: int, topk: int) -> int:
+    """Bytes of device scratch :func:`attn_fwd_host` needs."""
+    return int(lib().moba_attn_fwd_host_scratch_size(B, H, S, D, block_size, topk))
+
+
+def attn_fwd_host(q, k, v, block_size: int, topk: int, out, lse, scratch, stream=None,
+                  **options):
+    """The forward on host tensors (page-locked for asynchronous copies): q, k,
+    v [B, S, H, D] bf16 in, out [B, S, H, D] bf16 and lse [B, H, S] fp32 filled
+    in once ``stream`` has reached the end of the call's work.  ``scratch`` is a
+    uint8 CUDA tensor of at least :func:`host_scratch_size` bytes; the library
+    copies the inputs in and the results out itself."""
+    for t, n, dt in ((q, "q", torch.bfloat16), (k, "k", torch.bfloat16),
+                     (v, "v", torch.bfloat16), (out, "out", torch.bfloat16),
+                     (lse, "lse", torch.float32)):
+        if t.dtype != dt or t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous host {dt} tensor")
+    B, S, H, D = q.shape
+    if k.shape != q.shape or v.shape != q.shape or out.shape != q.shape or \
+            tuple(lse.shape) != (B, H, S):
+        raise ValueError("q, k, v, out must be [B, S, H, D] and lse [B, H, S]")
+    _need(scratch, torch.uint8, "scratch")
+    o, _keep = _options(**options)
+    rc = lib().moba_attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, S, D,
+                                  block_size, topk, ctypes.byref(o), _ptr(scratch),
+                                  scratch.numel(), _stream(stream))
+    _check(rc, "moba_attn_fwd_host")
     return out, lse
 
 

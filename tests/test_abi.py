@@ -88,6 +88,17 @@ def test_no_process_wide_switches(lib):
         assert not hasattr(lib, name), name
 
 
+def test_host_scratch_size(lib):
+    # device copies of q, k, v, out (bf16) and lse (fp32), each from a 256-byte
+    # boundary, then the forward's own workspace
+    B, H, S, D = 1, 32, 32768, 128
+    a256 = lambda x: (x + 255) // 256 * 256
+    want = 4 * a256(B * S * H * D * 2) + a256(B * S * H * 4) + \
+        lib.moba_attn_fwd_workspace_size(B, H, S, D, 512, 3)
+    assert lib.moba_attn_fwd_host_scratch_size(B, H, S, D, 512, 3) == want
+    assert lib.moba_attn_fwd_host_scratch_size(B, H, S, 96, 512, 3) == 0  # unsupported D
+
+
 def test_workspace_size_alias(lib):
     assert lib.moba_workspace_size(1, 32, 32768, 128, 512, 3) == \
         lib.moba_attn_fwd_workspace_size(1, 32, 32768, 128, 512, 3) > 0
