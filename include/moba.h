@@ -226,8 +226,8 @@ int moba_attn_fwd_ex(const void *q, const void *k, const void *v, void *out, flo
  * v, out and lse in host memory (page-locked for asynchronous copies; other
  * host memory works but the copies then block).  Enqueued on `stream` and
  * returning before completion: k, q and v are copied to the device scratch in
- * that order, each in two halves on two streams of the call's own (two copy
- * engines), starting after the earlier work on `stream`; the pooling, the gate
+ * that order on a stream of the call's own, starting after the earlier work
+ * on `stream`; the pooling, the gate
  * and the attention each wait only for the inputs they read, so the first
  * phases run while v is still arriving; out and lse come back the same way,
  * and `stream` reaches its next work once they have.  The host buffers must
