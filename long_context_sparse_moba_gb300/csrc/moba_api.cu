@@ -287,6 +287,9 @@ static int run_backward(const Plan &p, const int *cu_dev, const void *q, const v
     const auto *qb = static_cast<const __nv_bfloat16 *>(q);
     const auto *kb = static_cast<const __nv_bfloat16 *>(k);
     MOBA_TRY(launch_setup(p, cu_dev, ws, st));
+    // delta first: the regroup writes it beside every list entry
+    MOBA_TRY(launch_bwd_delta(p, ws, static_cast<const __nv_bfloat16 *>(out),
+                              static_cast<const __nv_bfloat16 *>(dout), st));
     const bool gate = !p.dense && p.km1 > 0;
     const bool tc_gate = p.gate_kind == MOBA_GATE_TENSOR_CORES && gate_tc_supported(p);
     if (gate) {
@@ -299,7 +302,7 @@ static int run_backward(const Plan &p, const int *cu_dev, const void *q, const v
         } else {
             MOBA_TRY(launch_gate(p, ws, qb, ws.kbar, ws.idx, st));
         }
-        MOBA_TRY(launch_regroup_stable(p, ws, st));
+        MOBA_TRY(launch_regroup_stable(p, ws, lse, st));
     }
     MOBA_TRY(cudaMemsetAsync(ws.dq_acc, 0, sizeof(float) * (size_t)p.total * p.H * p.D, st));
     MOBA_TRY(launch_attn_bwd(p, ws, qb, kb, static_cast<const __nv_bfloat16 *>(v),

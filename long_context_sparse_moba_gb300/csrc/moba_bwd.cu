@@ -36,6 +36,8 @@
 // 32 (w / 4) .. +31; for dV and dK keys 16 (w % 4) .. +15 x the column half
 // w / 4 of D; for dQ query rows 16 (w % 4) .. +15 x the same column half.
 // P^T, dS^T and dS pass between the phases through shared memory (bf16).
+#include <algorithm>
+
 #include "moba_internal.cuh"
 #include "moba_mma.cuh"
 
@@ -85,29 +87,48 @@ __device__ __forceinline__ void load_rows(uint32_t s_base, const __nv_bfloat16 *
     }
 }
 
+// delta = dO . O per (token, head) row: D / 8 lanes per row, 16 bytes of each
+// tensor per lane, four row groups of the warp in flight per pass
 template <int D>
 __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16 *__restrict__ out,
                                                         const __nv_bfloat16 *__restrict__ dout,
                                                         float *__restrict__ delta,
                                                         long long rows, int H, int total) {
-    const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (r >= rows) return;  // whole warps leave together
-    const int lane = threadIdx.x & 31;
-    constexpr int PER = D / 32;
-    const __nv_bfloat16 *o = out + r * D + lane * PER;
-    const __nv_bfloat16 *g = dout + r * D + lane * PER;
-    float acc = 0.f;
+    constexpr int LPR = D / 8;       // lanes per row
+    constexpr int RPW = 32 / LPR;    // rows per warp and pass
+    constexpr int U = 4;             // passes in flight
+    const int lane = threadIdx.x & 31, sub = lane / LPR, li = lane % LPR;
+    const long long warps = (long long)gridDim.x * 8;
+    for (long long r0 = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * RPW * U; r0 < rows;
+         r0 += warps * RPW * U) {
+        uint4 x[U], y[U];
 #pragma unroll
-    for (int i = 0; i < PER; i += 2) {
-        const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(o + i));
-        const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(g + i));
-        acc = fmaf(x.x, y.x, acc);
-        acc = fmaf(x.y, y.y, acc);
+        for (int u = 0; u < U; ++u) {
+            const long long r = r0 + u * RPW + sub;
+            if (r < rows) {
+                x[u] = __ldg(reinterpret_cast<const uint4 *>(out + r * D) + li);
+                y[u] = __ldg(reinterpret_cast<const uint4 *>(dout + r * D) + li);
+            } else {
+                x[u] = y[u] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const __nv_bfloat162 *xa = reinterpret_cast<const __nv_bfloat162 *>(&x[u]);
+            const __nv_bfloat162 *ya = reinterpret_cast<const __nv_bfloat162 *>(&y[u]);
+            float acc = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 a2 = __bfloat1622float2(xa[e]), b2 = __bfloat1622float2(ya[e]);
+                acc = fmaf(a2.x, b2.x, fmaf(a2.y, b2.y, acc));
+            }
+#pragma unroll
+            for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            const long long r = r0 + u * RPW + sub;
+            // [H][total]: each head's rows contiguous
+            if (li == 0 && r < rows) delta[(size_t)(r % H) * total + r / H] = acc;
+        }
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    // [H][total]: each head's rows contiguous
-    if (lane == 0) delta[(size_t)(r % H) * total + r / H] = acc;
 }
 
 template <int D>
@@ -376,10 +397,7 @@ static cudaError_t launch_bwd_d(const Plan &p, const Workspace &ws, const bwd::A
                                 const __nv_bfloat16 *out, cudaStream_t st) {
     using namespace bwd;
     const long long rows = (long long)p.total * p.H;
-    bwd_delta_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(out, a.dout, ws.delta, rows,
-                                                                      p.H, p.total);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
     if (bwd_tc_supported(p)) {
         // dk, dv and the dq accumulator on the tcgen05 tensor cores
         e = launch_bwd_kv_tc(p, ws, a.q, a.k, a.v, a.lse, a.dout, a.dk, a.dv, st);
@@ -398,7 +416,22 @@ static cudaError_t launch_bwd_d(const Plan &p, const Workspace &ws, const bwd::A
     bwd_dq_kernel<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, st>>>(
         reinterpret_cast<const float4 *>(ws.dq_acc), reinterpret_cast<uint2 *>(a.dq_out), n4,
         a.scale);
-    note_launches(2);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_delta(const Plan &p, const Workspace &ws, const __nv_bfloat16 *out,
+                             const __nv_bfloat16 *dout, cudaStream_t st) {
+    const long long rows = (long long)p.total * p.H;
+    const long long warps_needed = (rows + 4 * (256 / p.D) - 1) / (4 * (256 / p.D));
+    const long long blocks = std::min<long long>((warps_needed + 7) / 8, 16ll * sm_count());
+    if (p.D == 64)
+        bwd::bwd_delta_kernel<64><<<(unsigned)blocks, 256, 0, st>>>(out, dout, ws.delta, rows, p.H,
+                                                                    p.total);
+    else
+        bwd::bwd_delta_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(out, dout, ws.delta, rows,
+                                                                     p.H, p.total);
+    note_launches(1);
     return cudaGetLastError();
 }
 

@@ -642,32 +642,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// lse (log2) and dO . O of every list entry's row, next to the list, so that
-// the producer of the kernel above reads a tile's metadata with independent
-// loads; one warp per (block, head) list
-__global__ void __launch_bounds__(256)
-    bwd_list_meta_kernel(Geometry g, const int *__restrict__ list,
-                         const int *__restrict__ list_off, int n_lists,
-                         const float *__restrict__ lse, const float *__restrict__ delta, int fixed,
-                         int S_fixed, float *__restrict__ list_l2, float *__restrict__ list_dl) {
-    MOBA_RETURN_IF_BAD(g);
-    const int lane = threadIdx.x & 31;
-    for (int Lid = blockIdx.x * 8 + (threadIdx.x >> 5); Lid < n_lists; Lid += gridDim.x * 8) {
-        const int h = Lid % g.H;
-        const int gblk = Lid / g.H;
-        const int b = upper_index(g.blk_base, g.num_seqs, gblk);
-        const int seq0 = __ldg(g.cu + b);
-        const int p1 = __ldg(list_off + Lid + 1);
-        for (int pos = __ldg(list_off + Lid) + lane; pos < p1; pos += 32) {
-            const int tok = __ldg(list + pos) >> kSlotBits;
-            const size_t li = fixed ? ((size_t)b * g.H + h) * S_fixed + (tok - seq0)
-                                    : (size_t)h * g.total + tok;
-            list_l2[pos] = __ldg(lse + li) * kLog2e;
-            list_dl[pos] = __ldg(delta + (size_t)h * g.total + tok);
-        }
-    }
-}
-
 }  // namespace bwd_tc
 
 bool bwd_tc_supported(const Plan &p) { return p.D == bwd_tc::D && p.attn_kind == MOBA_ATTN_TCGEN05; }
@@ -714,16 +688,6 @@ cudaError_t launch_bwd_kv_tc(const Plan &p, const Workspace &ws, const __nv_bflo
     a.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)D));
     a.status = status_word();
     a.wait_limit = p.wait_limit;
-    if (!p.dense && p.km1 > 0) {
-        const int n_lists = p.NBcap * p.H;
-        const int blocks = std::min((n_lists + 7) / 8, 8 * sm_count());
-        bwd_list_meta_kernel<<<blocks, 256, 0, st>>>(a.g, ws.list, ws.list_off, n_lists, lse,
-                                                      ws.delta, a.fixed, a.S_fixed, ws.list_l2,
-                                                      ws.list_dl);
-        note_launches(1);
-        cudaError_t e1 = cudaGetLastError();
-        if (e1 != cudaSuccess) return e1;
-    }
     auto kern = bwd_tc_kernel;
     static int checked = 0;
     if (!checked) {

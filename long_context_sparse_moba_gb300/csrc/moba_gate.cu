@@ -666,6 +666,14 @@ cudaError_t launch_regroup(const Plan &p, const Workspace &ws, bool counted, boo
 // ---------------------------------------------------------------------------
 constexpr int kRgWarps = kRgThreads / 32;
 
+// What the backward keeps beside each list entry: its row's forward lse (in
+// log2 units) and delta; lse == nullptr when not asked for.
+struct EntryMeta {
+    const float *lse, *delta;  // lse [B][H][S] (fixed) or [H][total]; delta [H][total]
+    int fixed, S_fixed;
+    float *list_l2, *list_dl;
+};
+
 static int stable_tokens_per_cta(const Plan &p) {
     const long long N = (long long)p.NBcap * p.H;
     const long long rows = std::max<long long>(4096, 4 * N);  // as the histogram kernels above
@@ -730,7 +738,7 @@ __global__ void __launch_bounds__(kRgThreads)
     regroup_scatter_stable_kernel(Geometry g, const int32_t *__restrict__ idx, int topk, int tpc,
                                   int N, int *__restrict__ cta_hist,
                                   const int *__restrict__ list_off, int *__restrict__ list,
-                                  const int *__restrict__ status) {
+                                  const int *__restrict__ status, EntryMeta em) {
     extern __shared__ int hist[];
     MOBA_RETURN_IF_BAD(g);
     if (status && *(volatile const int *)status != 0) return;  // the lists were published empty
@@ -746,12 +754,20 @@ __global__ void __launch_bounds__(kRgThreads)
             const int t = tb + lane;
             bool live = t < t1;
             int ci = 0, bbase = 0;
+            float l2 = 0.f, dl = 0.f;  // my row's lse (log2) and delta, when asked for
             const int32_t *sel = idx;
             if (live) {
                 const int b = upper_index(g.cu, g.num_seqs, t);
-                ci = (t - __ldg(g.cu + b)) / g.bs;
+                const int seq0 = __ldg(g.cu + b);
+                ci = (t - seq0) / g.bs;
                 bbase = __ldg(g.blk_base + b);
                 sel = idx + ((size_t)t * g.H + h) * topk;
+                if (em.lse) {
+                    const size_t li = em.fixed ? ((size_t)b * g.H + h) * em.S_fixed + (t - seq0)
+                                               : (size_t)h * g.total + t;
+                    l2 = __ldg(em.lse + li) * 1.4426950408889634f;
+                    dl = __ldg(em.delta + (size_t)h * g.total + t);
+                }
             }
             for (int s = 0; s < topk - 1; ++s) {
                 const int c = live ? __ldg(sel + s) : -1;
@@ -762,7 +778,12 @@ __global__ void __launch_bounds__(kRgThreads)
                 const int base = live ? pos[bin] : 0;
                 __syncwarp();
                 if (live) {
-                    list[base + __popc(peers & below)] = (t << kSlotBits) | s;
+                    const int at = base + __popc(peers & below);
+                    list[at] = (t << kSlotBits) | s;
+                    if (em.lse) {
+                        em.list_l2[at] = l2;
+                        em.list_dl[at] = dl;
+                    }
                     if ((peers >> lane) == 1u) pos[bin] = base + __popc(peers);  // last of its group
                 }
                 __syncwarp();
@@ -771,7 +792,11 @@ __global__ void __launch_bounds__(kRgThreads)
     }
 }
 
-cudaError_t launch_regroup_stable(const Plan &p, const Workspace &ws, cudaStream_t st) {
+cudaError_t launch_regroup_stable(const Plan &p, const Workspace &ws, const float *lse,
+                                  cudaStream_t st) {
+    EntryMeta em{nullptr, nullptr, 0, 0, nullptr, nullptr};
+    if (lse && ws.delta && ws.list_l2 && ws.list_dl)
+        em = EntryMeta{lse, ws.delta, p.fixed ? 1 : 0, p.max_len, ws.list_l2, ws.list_dl};
     const int N = p.NBcap * p.H;
     const int tpc = stable_tokens_per_cta(p);
     const int G = stable_regroup_ctas(p);
@@ -802,10 +827,10 @@ cudaError_t launch_regroup_stable(const Plan &p, const Workspace &ws, cudaStream
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (smem)
         regroup_scatter_stable_kernel<true><<<G, kRgThreads, hbytes, st>>>(
-            g, ws.idx, p.topk, tpc, N, ws.cta_hist, ws.list_off, ws.list, status_word());
+            g, ws.idx, p.topk, tpc, N, ws.cta_hist, ws.list_off, ws.list, status_word(), em);
     else
         regroup_scatter_stable_kernel<false><<<G, kRgThreads, 0, st>>>(
-            g, ws.idx, p.topk, tpc, N, ws.cta_hist, ws.list_off, ws.list, status_word());
+            g, ws.idx, p.topk, tpc, N, ws.cta_hist, ws.list_off, ws.list, status_word(), em);
     note_launches(4);
     return cudaGetLastError();
 }

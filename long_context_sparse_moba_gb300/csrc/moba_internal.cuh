@@ -133,8 +133,14 @@ cudaError_t launch_union(const Plan &p, const Workspace &ws, bool counted, cudaS
 cudaError_t launch_regroup(const Plan &p, const Workspace &ws, bool counted, bool skip_fused,
                            cudaStream_t st);
 // the same lists with their entries in an order fixed by the selection alone
-// (every call places them alike); needs ws.cta_hist, rewrites ws.counts
-cudaError_t launch_regroup_stable(const Plan &p, const Workspace &ws, cudaStream_t st);
+// (every call places them alike); needs ws.cta_hist, rewrites ws.counts.  With
+// lse (the forward's, its layout per the plan) and ws.delta, each entry's
+// row lse (log2) and delta go into ws.list_l2 / ws.list_dl beside it.
+cudaError_t launch_regroup_stable(const Plan &p, const Workspace &ws, const float *lse,
+                                  cudaStream_t st);
+// delta = dO . O per row into ws.delta ([H][total])
+cudaError_t launch_bwd_delta(const Plan &p, const Workspace &ws, const __nv_bfloat16 *out,
+                             const __nv_bfloat16 *dout, cudaStream_t st);
 // CTAs of the stable regroup (rows of ws.cta_hist)
 int stable_regroup_ctas(const Plan &p);
 // attention over the selected past blocks (skipped on the dense / top-1 paths)
