@@ -12,7 +12,11 @@
 //   warp 0      TMA producers: lane 0 loads the Q tiles (own-block mode) and a
 //               2-stage ring of K tiles, lane 1 a 2-stage ring of V tiles (one
 //               TMA stream per thread tops out well below what the tensor core
-//               consumes); the rings run ahead into the next job;
+//               consumes); the rings run ahead into the next job.  In the past
+//               mode lane 0 also leaves each next job's descriptor in one of two
+//               shared-memory slots for the softmax warps (a descriptor is a chain
+//               of dependent table loads, which the producer, running ahead,
+//               takes off their job boundary);
 //   warp 1      allocates all 512 TMEM columns; lane 0 issues the MMAs
 //                 S_g = Q_g K_j^T   (M128 N128 K=D, A and B from shared memory)
 //                 O_g += P_g V_j    (M128 N=D K128, A = P_g from TMEM)
@@ -134,8 +138,13 @@ struct Smem {
                          kBarKE = kBarKF + kStages,
                          kBarVF = kBarKE + kStages, kBarVE = kBarVF + kStages,
                          kBarS = kBarVE + kStages, kBarP = kBarS + kG, kBarPV = kBarP + kG,
-                         kBarDrain = kBarPV + kG, kNumBars = kBarDrain + 1;
-    static constexpr uint32_t kMisc = kNumBars * 8 + 8;
+                         kBarDrain = kBarPV + kG, kBarDF = kBarDrain + 1, kBarDE = kBarDF + 2,
+                         kNumBars = kBarDE + 2;
+    // past mode: two slots of the next job's descriptor, written by the K
+    // producer (desc_full / desc_empty above) for the softmax warps
+    static constexpr uint32_t kDesc = (kNumBars * 8 + 8 + 15) & ~15u;
+    static constexpr uint32_t kDescSlot = 80;  // a Job and its number
+    static constexpr uint32_t kMisc = kDesc + 2 * kDescSlot;
     // The tiles need a 1024-byte aligned base; the dynamic window is at least
     // 16-byte aligned, so up to 1008 bytes of slack; the misc words go into
     // the slack when it is large enough, else right after the staging.  The
@@ -155,6 +164,7 @@ struct Job {
     int nu;               // own-block mode: past blocks of a fused job (0: not fused)
     int tb[kG], te[kG];
 };
+static_assert(sizeof(Job) + 4 <= Smem<128>::kDescSlot, "a descriptor slot holds a Job and its number");
 
 template <int MODE, bool FUSE = false>
 __device__ __forceinline__ bool get_job(const Args &a, int job, Job &J) {
@@ -290,6 +300,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(L::kBarPV + g), 1);
         }
         mbar_init(bar(L::kBarDrain), 1);
+        for (int d = 0; d < 2; ++d) {
+            mbar_init(bar(L::kBarDF + d), 1);
+            mbar_init(bar(L::kBarDE + d), 4 * kG);  // one arrival per softmax warp
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -317,6 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < kStages; ++s) pend[s] = -1;
             int qpend[kG] = {-1, -1};  // own-block mode: Q phase in flight per tile
             int t = 0, qj = 0;  // K/V tiles and Q tiles loaded so far
+            int dn = 0;         // past mode: descriptors handed to the softmax warps
             bool go = true;
             int job = blockIdx.x;
             Job J;
@@ -327,6 +342,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int njob = job + gridDim.x;
                 Job NJ;
                 while (njob < njobs && !get_job<MODE, FUSE>(a, njob, NJ)) njob += gridDim.x;
+                if (MODE == kPast && is_k) {
+                    // and handed to the softmax warps, which would otherwise wait
+                    // on the same chain of table loads at their job boundary
+                    const int d = dn & 1;
+                    if (dn >= 2 && !wait_bar(bar(L::kBarDE + d), ((dn - 2) >> 1) & 1, ctl)) {
+                        go = false;
+                        break;
+                    }
+                    uint8_t *slot = gmisc + L::kDesc + d * L::kDescSlot;
+                    *reinterpret_cast<Job *>(slot) = NJ;
+                    *reinterpret_cast<int *>(slot + sizeof(Job)) = njob;
+                    mbar_arrive(bar(L::kBarDF + d));
+                    ++dn;
+                }
                 if (MODE == kCurrent && is_k) {
                     for (int g = 0; g < kG && go; ++g) {
                         // the previous job's S_g MMAs have read Q_g before it is replaced
@@ -516,14 +545,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             entry = list_entry(J);
             gather(J, entry);
         }
+        int dn = 0;  // past mode: descriptors taken from the producer
         while (ok && job < njobs) {
             add_union_tiles<FUSE>(a, J);
-            // the next job's descriptor, fetched one job ahead, and (past mode)
-            // this row's entry in it, loaded now and used after the last tile
+            // the next job's descriptor, one job ahead (past mode: from the
+            // producer), and this row's entry in it, loaded now and used after
+            // the last tile
             int njob = job + gridDim.x;
-            Job NJ;
-            while (njob < njobs && !get_job<MODE, FUSE>(a, njob, NJ)) njob += gridDim.x;
-            const int next_entry = (MODE == kPast && njob < njobs) ? list_entry(NJ) : 0;
+            Job NJ;  // (own-block mode; the past mode reads it from its slot when needed)
+            const Job *pnj = &NJ;
+            if (MODE == kPast) {
+                if (!__all_sync(0xffffffffu, wait_bar(bar(L::kBarDF + (dn & 1)), (dn >> 1) & 1, ctl))) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t *slot = gmisc + L::kDesc + (dn & 1) * L::kDescSlot;
+                pnj = reinterpret_cast<const Job *>(slot);
+                njob = *reinterpret_cast<const int *>(slot + sizeof(Job));
+            } else {
+                while (njob < njobs && !get_job<MODE, FUSE>(a, njob, NJ)) njob += gridDim.x;
+            }
+            const int next_entry = (MODE == kPast && njob < njobs) ? list_entry(*pnj) : 0;
             const int seq0 = J.seq0, h = J.h;
             const bool row_valid = jrow < J.nrows;
             int row_tok = -1, slot = 0;
@@ -717,7 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 ++qj;
-                gather(NJ, next_entry);
+                gather(*pnj, next_entry);
             }
 
             // ---------------- epilogue ----------------
@@ -886,8 +928,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
             }
             job = njob;
-            J = NJ;
+            J = *pnj;
             entry = next_entry;
+            if (MODE == kPast) {
+                // the slot may take the descriptor after the next
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(L::kBarDE + (dn & 1)));
+                ++dn;
+            }
         }
         cp_async_wait_all();  // no copy of ours may land after the exit
     }
