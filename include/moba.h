@@ -44,6 +44,11 @@
  *     failed launch or allocation.  A kernel that gives up a bounded wait
  *     records MOBA_ERR_TIMEOUT in a device-side status word that
  *     moba_get_status reads.
+ *   - Per-device state (that status word, the scratch of the allocation-free
+ *     forward, the SM count) is allocated on first use and cached for the
+ *     process, thread-safely.  cudaDeviceReset frees it behind the library's
+ *     back: a process that resets a device must not call the library on that
+ *     device again.
  */
 #ifndef MOBA_GB300_H
 #define MOBA_GB300_H

@@ -121,7 +121,7 @@ template <int D>
 struct Smem {
     static constexpr int NB = D / kBox;                       // 64-dim boxes per row
     static constexpr uint32_t kQBox = kM * 128;               // 16 KB
-    static constexpr uint32_t kKVBox = kN * 128;              // 8 KB
+    static constexpr uint32_t kKVBox = kN * 128;              // 16 KB
     static constexpr uint32_t kQ = 0;                         // [g][box]
     static constexpr uint32_t kK = kQ + kG * NB * kQBox;      // [stage][box]
     static constexpr uint32_t kV = kK + kStages * NB * kKVBox;
