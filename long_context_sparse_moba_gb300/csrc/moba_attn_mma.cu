@@ -236,7 +236,8 @@ __global__ __launch_bounds__(kThreads, 2) void past_kernel(Args a) {
             const int row = warp * 16 + (lane >> 2) + r * 8;
             if (row >= nrows) continue;
             const int e = __ldg(ent + row);
-            const size_t slot = ((size_t)(e >> kSlotBits) * H + h) * a.km1 + (e & ((1 << kSlotBits) - 1));
+            // head-major partials, [head][token][slot]
+            const size_t slot = ((size_t)h * a.g.total + (e >> kSlotBits)) * a.km1 + (e & ((1 << kSlotBits) - 1));
             const float inv = 1.f / st.l[r];
             __nv_bfloat16 *dst = a.part_o + slot * D + 2 * (lane & 3);
 #pragma unroll
@@ -294,7 +295,7 @@ __global__ __launch_bounds__(kThreads, 2) void current_kernel(Args a) {
             for (; np < a.km1; ++np) {
                 const int c = __ldg(sel + np);
                 if (c < 0 || c >= ci) break;
-                mmax = fmaxf(mmax, __ldg(a.part_lse + ((size_t)tok * H + h) * a.km1 + np));
+                mmax = fmaxf(mmax, __ldg(a.part_lse + ((size_t)h * a.g.total + tok) * a.km1 + np));
             }
             if (np > 0) {
                 float wsum = fast_exp2(lse_cur - mmax);
@@ -304,7 +305,7 @@ __global__ __launch_bounds__(kThreads, 2) void current_kernel(Args a) {
                     acc[j][1] *= wsum;
                 }
                 for (int s = 0; s < np; ++s) {
-                    const size_t slot = ((size_t)tok * H + h) * a.km1 + s;
+                    const size_t slot = ((size_t)h * a.g.total + tok) * a.km1 + s;
                     const float w = fast_exp2(__ldg(a.part_lse + slot) - mmax);
                     wsum += w;
                     const __nv_bfloat16 *src = a.part_o + slot * D + 2 * (lane & 3);

@@ -580,9 +580,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // every earlier block was a candidate, so the row holds
                     // min(topk - 1, its block index) partials, slots 0, 1, ...
                     const int npre = min(a.km1, (row_tok - seq0) / a.g.bs);
-                    const size_t rowid = (size_t)row_tok * H + h;
+                    const size_t prow = (size_t)h * a.g.total + row_tok;  // head-major partials
                     for (int s2 = 0; s2 < npre; ++s2) {
-                        const char *po = reinterpret_cast<const char *>(a.part_o + (rowid * a.km1 + s2) * D);
+                        const char *po = reinterpret_cast<const char *>(a.part_o + (prow * a.km1 + s2) * D);
 #pragma unroll
                         for (int ln = 0; ln < D * 2; ln += 128)
                             asm volatile("prefetch.global.L2 [%0];" ::"l"(po + ln));
@@ -773,7 +773,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
                 const float lse2 = m_run + __log2f(l_run);
                 if (MODE == kPast) {
-                    const size_t pslot = ((size_t)row_tok * H + h) * a.km1 + slot;
+                    // partials are head-major, [head][token][slot]: a later
+                    // own-block job reads its rows' partials as one run
+                    const size_t pslot = ((size_t)h * a.g.total + row_tok) * a.km1 + slot;
                     const unsigned long long my_dst =
                         reinterpret_cast<unsigned long long>(a.part_o + pslot * D);
 #pragma unroll
@@ -818,19 +820,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // ascending block order; every earlier block was a candidate,
                     // so there are min(topk - 1, block index) of them)
                     const size_t rowid = (size_t)row_tok * H + h;
+                    const size_t prow = (size_t)h * a.g.total + row_tok;  // head-major partials
                     int np = 0;
                     float mmax = lse2;
                     if (row_valid && !a.dense && a.km1 > 0 && J.nu == 0) {
                         np = min(a.km1, i_loc / a.g.bs);
                         for (int s2 = 0; s2 < np; ++s2)
-                            mmax = fmaxf(mmax, __ldg(a.part_lse + rowid * a.km1 + s2));
+                            mmax = fmaxf(mmax, __ldg(a.part_lse + prow * a.km1 + s2));
                     }
                     float w_cur = 1.f, wsum = 1.f;
                     if (np > 0) {
                         w_cur = fast_exp2(lse2 - mmax);
                         wsum = w_cur;
                         for (int s2 = 0; s2 < np; ++s2)
-                            wsum += fast_exp2(__ldg(a.part_lse + rowid * a.km1 + s2) - mmax);
+                            wsum += fast_exp2(__ldg(a.part_lse + prow * a.km1 + s2) - mmax);
                     }
                     const float iw = 1.f / wsum;
                     const float fcur = w_cur * inv * iw;
@@ -849,14 +852,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int it = 0; it < 4; ++it) {
                                 const int r = it * 8 + (lane >> 2), q4 = lane & 3;
-                                const unsigned long long rid =
-                                    __shfl_sync(0xffffffffu, (unsigned long long)rowid, r);
+                                const unsigned long long prid =
+                                    __shfl_sync(0xffffffffu, (unsigned long long)prow, r);
                                 const int npr = __shfl_sync(0xffffffffu, np, r);
 #pragma unroll
                                 for (int ss = 0; ss < 2; ++ss) {
                                     const bool v = s0 + ss < npr;
                                     const __nv_bfloat16 *src =
-                                        a.part_o + (rid * a.km1 + s0 + ss) * D + c0 + q4 * 8;
+                                        a.part_o + (prid * a.km1 + s0 + ss) * D + c0 + q4 * 8;
                                     cp_async16(stg + ss * 2048 + r * 64 +
                                                    ((uint32_t)(q4 ^ ((r >> 1) & 3)) << 4),
                                                v ? (const void *)src : (const void *)a.part_o, v);
@@ -868,7 +871,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int ss = 0; ss < 2; ++ss) {
                                 if (s0 + ss < np) {
                                     const float w =
-                                        fast_exp2(__ldg(a.part_lse + rowid * a.km1 + s0 + ss) - mmax) * iw;
+                                        fast_exp2(__ldg(a.part_lse + prow * a.km1 + s0 + ss) - mmax) * iw;
 #pragma unroll
                                     for (int q4 = 0; q4 < 4; ++q4) {
                                         const uint4 f =

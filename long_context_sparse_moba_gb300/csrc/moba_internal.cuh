@@ -71,8 +71,8 @@ struct Workspace {
     int *list;        // [total * H * km1]  entries token << 5 | slot
     int *job_nu;      // [own-block jobs]  past blocks of a fused job (0: not fused)
     int *job_ub;      // [own-block jobs][kMaxUnion]  those blocks, ascending
-    __nv_bfloat16 *part_o;  // [total * H * km1][D]  normalised partial outputs (bf16)
-    float *part_lse;  // [total * H * km1]     partial log2-sum-exp
+    __nv_bfloat16 *part_o;  // [H][total][km1][D]  normalised partial outputs (bf16), head-major
+    float *part_lse;  // [H][total][km1]     partial log2-sum-exp
     // backward pass only (part_o / part_lse are not carved then)
     float *dq_acc;    // [total][H][D]  fp32 dq accumulator
     float *delta;     // [H][total]     dO . O per row
