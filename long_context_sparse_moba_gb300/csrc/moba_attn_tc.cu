@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(L::kBarDrain), 1);
         for (int d = 0; d < 2; ++d) {
             mbar_init(bar(L::kBarDF + d), 1);
-            mbar_init(bar(L::kBarDE + d), 4 * kG);  // one arrival per softmax warp
+            mbar_init(bar(L::kBarDE + d), 4 * kG + 1);  // each softmax warp and the MMA lane
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -406,15 +406,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc_o = idesc_bf16(kM, D, 1);
             int t = 0, qj = 0;          // K/V tiles consumed, jobs started
             int gt[kG] = {0, 0};        // per tile g: S/P tiles so far
+            int dn = 0;                 // past mode: descriptors taken from the producer
             bool ok = true;
             int job = blockIdx.x;
             Job J;
             while (job < njobs && !get_job<MODE, FUSE>(a, job, J)) job += gridDim.x;
             while (ok && job < njobs) {
                 add_union_tiles<FUSE>(a, J);
-                int njob = job + gridDim.x;  // next descriptor, fetched one job ahead
+                // next descriptor, one job ahead (past mode: from the producer's slot)
+                int njob = job + gridDim.x;
                 Job NJ;
-                while (njob < njobs && !get_job<MODE, FUSE>(a, njob, NJ)) njob += gridDim.x;
+                if (MODE == kPast) {
+                    if (!wait_poll(bar(L::kBarDF + (dn & 1)), (dn >> 1) & 1, ctl)) break;
+                    const uint8_t *slot = gmisc + L::kDesc + (dn & 1) * L::kDescSlot;
+                    NJ = *reinterpret_cast<const Job *>(slot);
+                    njob = *reinterpret_cast<const int *>(slot + sizeof(Job));
+                    mbar_arrive(bar(L::kBarDE + (dn & 1)));
+                    ++dn;
+                } else {
+                    while (njob < njobs && !get_job<MODE, FUSE>(a, njob, NJ)) njob += gridDim.x;
+                }
                 // a Q tile without S MMAs in this job is released at once
 #pragma unroll
                 for (int g = 0; g < kG; ++g)
