@@ -614,7 +614,7 @@ cudaError_t launch_regroup(const Plan &p, const Workspace &ws, bool counted, boo
     const size_t R = (size_t)p.total * p.H;
     const bool smem = N <= kRgSmemBins;
     // enough rows per CTA that clearing and flushing the histogram stays cheap
-    const int rows_per_cta = smem ? (int)std::max<long long>(4096, 4ll * N) : 4096;
+    const int rows_per_cta = smem ? (int)std::max<long long>(2048, 2ll * N) : 4096;
     const unsigned grid = (unsigned)((R + rows_per_cta - 1) / rows_per_cta);
     const size_t hbytes = smem ? sizeof(int) * (size_t)N : 0;
     const Geometry g = make_geo(p, ws);
