@@ -170,42 +170,55 @@ def decode_bench(ops, torch, dev, H, D, bs, topk, B=8, S=32768, steps=50):
 def backward_bench(ops, torch, w, inp, topk, out, lse, flops_fwd, steps=10):
     """The backward pass (dq, dk, dv for a seeded upstream gradient) after the
     timed forward: time per call and its issued tensor-core work, five
-    products per (query, key) pair against the forward's two, over the time."""
+    products per (query, key) pair against the forward's two, over the time.
+    A training step keeps the forward's selection beside lse (``idx_out``),
+    and the call takes it back (``idx_in``); the time of the call that
+    recomputes the selection is reported beside it."""
     from long_context_sparse_moba_gb300 import workloads
     dev = inp.q.device
     dout = workloads.make_grad(w, device=dev)
     dq, dk, dv = (torch.empty_like(inp.q) for _ in range(3))
-    ws = None
+    ws = idx = None
     if not w.varlen:
         ws = torch.empty(ops.bwd_workspace_size(w.B, w.H, w.S, w.D, w.block_size, topk),
                          dtype=torch.uint8, device=dev)
+        idx = torch.empty(w.B, w.S, w.H, topk, dtype=torch.int32, device=dev)
+        out, lse = ops.attn_fwd(inp.q, inp.k, inp.v, w.block_size, topk, idx_out=idx)
         cu = None
     else:
         cu = torch.tensor(inp.cu_seqlens, dtype=torch.int32, device=dev)
 
-    def call():
+    def call(saved):
         if w.varlen:
             ops.attn_bwd_varlen(inp.q, inp.k, inp.v, out, lse, dout, cu, w.S, w.block_size, topk)
         else:
             ops.attn_bwd(inp.q, inp.k, inp.v, out, lse, dout, w.block_size, topk, dq=dq, dk=dk,
-                         dv=dv, workspace=ws)
+                         dv=dv, workspace=ws, idx_in=idx if saved else None)
 
-    for _ in range(3):
-        call()
-    torch.cuda.synchronize()
-    stream = torch.cuda.current_stream()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        call()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    assert ops.get_status() == ops.MOBA_OK
-    ms = e0.elapsed_time(e1) / steps
+    def timed(saved):
+        for _ in range(3):
+            call(saved)
+        torch.cuda.synchronize()
+        stream = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            call(saved)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        assert ops.get_status() == ops.MOBA_OK
+        return e0.elapsed_time(e1) / steps
+
+    saved = idx is not None
+    ms = timed(saved)
     flops = 2.5 * flops_fwd
-    return {"topk": topk, "ms_per_step": ms, "tokens_per_s": w.total / (ms * 1e-3),
-            "issued_flops": flops, "effective_tflops": flops / (ms * 1e-3) / 1e12,
-            "steps": steps}
+    res = {"topk": topk, "ms_per_step": ms, "tokens_per_s": w.total / (ms * 1e-3),
+           "issued_flops": flops, "effective_tflops": flops / (ms * 1e-3) / 1e12,
+           "steps": steps,
+           "selection": "the forward's (idx_out -> idx_in)" if saved else "recomputed"}
+    if saved:
+        res["ms_per_step_recomputing_selection"] = timed(False)
+    return res
 
 
 def load_peaks():

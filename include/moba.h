@@ -119,6 +119,14 @@ typedef enum {
  *                4 attention over past blocks, 5 attention over the own block
  *                + merge (a phase a path skips is empty).  A NULL entry is
  *                skipped.
+ *   idx_in       backward only, optional DEVICE int32 [tokens][H][topk]: the
+ *                selection of the forward pass (its idx_out), saved by the
+ *                caller like lse.  The backward then regroups this selection
+ *                instead of recomputing it (no key pooling, no gate).  A row's
+ *                past blocks are read in order up to the first entry that is
+ *                negative or not below the row's own block; values are not
+ *                otherwise checked (a different selection gives the gradients
+ *                of that selection).  4-byte aligned.  NULL: recompute.
  * An option value outside its set returns MOBA_ERR_INVALID_ARG before any
  * launch.
  */
@@ -137,6 +145,7 @@ typedef struct moba_options {
     int32_t *idx_out;
     void *const *phase_events;
     int schedule;
+    const int32_t *idx_in;
 } moba_options_t;
 
 /* Number of blocks of a sequence: ceil(len / block_size) (the tail block may

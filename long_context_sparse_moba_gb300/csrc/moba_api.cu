@@ -165,6 +165,7 @@ static int make_plan(int num_seqs, long long total, int max_len, int H, int D, i
     p->debug_flags = 0;
     p->wait_limit = kDefaultWaitLimit;
     p->schedule = MOBA_SCHEDULE_ADAPTIVE;
+    p->idx_in = nullptr;
     p->dense = topk >= n_max;
     p->km1 = p->dense ? 0 : topk - 1;
     const long long nbcap = fixed ? (long long)num_seqs * n_max : total / bs + num_seqs;
@@ -192,6 +193,8 @@ static int apply_options(const moba_options_t *o, Plan *p) {
     p->attn_kind = o->attn_kernel;
     p->debug_flags = o->debug_flags;
     p->wait_limit = o->wait_limit_cycles > 0 ? o->wait_limit_cycles : kDefaultWaitLimit;
+    if (o->idx_in && (reinterpret_cast<uintptr_t>(o->idx_in) & 3)) return MOBA_ERR_INVALID_ARG;
+    p->idx_in = o->idx_in;
     return MOBA_OK;
 }
 
@@ -292,7 +295,11 @@ static int run_backward(const Plan &p, const int *cu_dev, const void *q, const v
                               static_cast<const __nv_bfloat16 *>(dout), st));
     const bool gate = !p.dense && p.km1 > 0;
     const bool tc_gate = p.gate_kind == MOBA_GATE_TENSOR_CORES && gate_tc_supported(p);
-    if (gate) {
+    if (gate && p.idx_in) {
+        // the forward's selection: regroup it as it is
+        ws.idx = const_cast<int32_t *>(p.idx_in);
+        MOBA_TRY(launch_regroup_stable(p, ws, lse, st));
+    } else if (gate) {
         MOBA_TRY(launch_kpool(p, ws, kb, ws.kbar, st));
         MOBA_TRY(cudaMemsetAsync(ws.counts, 0, sizeof(int) * ((size_t)p.NBcap * p.H + 1), st));
         if (tc_gate) {

@@ -93,6 +93,7 @@ struct Plan {
     int debug_flags;        // bit 0: the K/V producer skips its first load
     long long wait_limit;   // clock64 budget of one bounded wait
     int schedule;           // 0 adaptive (fused own-block jobs where it pays), 1 block-major
+    const int32_t *idx_in;  // backward: the forward's selection, or nullptr (recompute)
 };
 
 // clock64 budget of one bounded wait when the caller gives none (~2 s at 2 GHz)

@@ -87,18 +87,23 @@ class Options(ctypes.Structure):
     _fields_ = [("pooling", ctypes.c_int), ("gate_kernel", ctypes.c_int),
                 ("attn_kernel", ctypes.c_int), ("debug_flags", ctypes.c_int),
                 ("wait_limit_cycles", ctypes.c_longlong), ("idx_out", ctypes.c_void_p),
-                ("phase_events", ctypes.c_void_p), ("schedule", ctypes.c_int)]
+                ("phase_events", ctypes.c_void_p), ("schedule", ctypes.c_int),
+                ("idx_in", ctypes.c_void_p)]
 
 
 def _options(pooling=POOL_MEAN, gate_kernel=GATE_TCGEN05, attn_kernel=ATTN_TCGEN05,
              debug_flags=0, wait_limit_cycles=0, idx_out=None, phase_events=None,
-             schedule=SCHEDULE_ADAPTIVE):
+             schedule=SCHEDULE_ADAPTIVE, idx_in=None):
     """An Options structure and the objects that must outlive the call."""
     o = Options(int(pooling), int(gate_kernel), int(attn_kernel), int(debug_flags),
-                int(wait_limit_cycles), None, None, int(schedule))
+                int(wait_limit_cycles), None, None, int(schedule), None)
     keep = []
     if idx_out is not None:
         o.idx_out = idx_out.data_ptr()
+    if idx_in is not None:
+        if idx_in.dtype != torch.int32 or not idx_in.is_cuda or not idx_in.is_contiguous():
+            raise ValueError("idx_in must be a contiguous int32 CUDA tensor")
+        o.idx_in = idx_in.data_ptr()
     if phase_events is not None:
         if len(phase_events) != len(PHASES) + 1:
             raise ValueError(f"phase_events needs {len(PHASES) + 1} events")
@@ -399,7 +404,9 @@ def attn_bwd(q, k, v, out, lse, dout, block_size: int, topk: int, dq=None, dk=No
     """MoBA backward for the forward ``attn_fwd(q, k, v, block_size, topk)``:
     q, k, v, out, dout [B, S, H, D] bf16 and lse [B, H, S] fp32 (as the forward
     returned them) -> (dq, dk, dv) [B, S, H, D] bf16.  The gate's selection is
-    recomputed (with the same ``options`` as the forward) and held fixed."""
+    recomputed (with the same ``options`` as the forward) and held fixed, or,
+    with ``idx_in`` ([B, S, H, topk] int32, the forward's ``idx_out``), taken
+    as it is."""
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
         _need(t, torch.bfloat16, n)
     _need(lse, torch.float32, "lse")

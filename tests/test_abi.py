@@ -69,15 +69,20 @@ def test_options_validate_on_the_host(lib):
     o.idx_out = 0x10002  # not 4-byte aligned
     assert lib.moba_attn_fwd_ex(fake, fake, fake, fake, fake, 1, 1, 64, 64, 64, 3,
                                 ctypes.byref(o), None, 0, None) == ops.MOBA_ERR_INVALID_ARG
+    o = ops.Options()
+    o.idx_in = 0x10002  # not 4-byte aligned
+    assert lib.moba_attn_bwd_ex(fake, fake, fake, fake, fake, fake, fake, fake, fake, 1, 1,
+                                64, 64, 64, 3, ctypes.byref(o), None, 0,
+                                None) == ops.MOBA_ERR_INVALID_ARG
 
 
 def test_options_struct_layout():
     """The ctypes mirror of moba_options_t has the C layout (LP64: int x4,
-    long long, two pointers, int, padding = 48 bytes)."""
-    assert ctypes.sizeof(ops.Options) == 48
+    long long, two pointers, int, padding, pointer = 56 bytes)."""
+    assert ctypes.sizeof(ops.Options) == 56
     assert ops.Options.wait_limit_cycles.offset == 16
     assert ops.Options.idx_out.offset == 24 and ops.Options.phase_events.offset == 32
-    assert ops.Options.schedule.offset == 40
+    assert ops.Options.schedule.offset == 40 and ops.Options.idx_in.offset == 48
 
 
 def test_no_process_wide_switches(lib):

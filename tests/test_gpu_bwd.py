@@ -131,6 +131,27 @@ def test_backward_workspace_variant_and_determinism(seqlens, D, varlen):
     assert d.mean() <= 2e-3 * a[0].float().abs().mean(), d.mean()
 
 
+@pytest.mark.parametrize("seqlens,D,bs,topk", [((1536,), 128, 128, 3), ((2048,), 64, 256, 4),
+                                               ((4096,), 128, 512, 3)])
+def test_backward_with_the_forwards_selection(seqlens, D, bs, topk):
+    # the forward's idx_out handed back as idx_in: the backward regroups that
+    # selection instead of recomputing it, and the gradients are those of the
+    # recomputing backward (dk, dv bit for bit; dq to the rounding of its
+    # fp32 reductions)
+    w = workloads.custom(seqlens, 2, D, bs, topk, seed=34, qkv_scale=D ** -0.5)
+    inp = workloads.make_inputs(w, device="cuda")
+    dout = workloads.make_grad(w, device="cuda")
+    idx = torch.empty(w.B, w.S, w.H, topk, dtype=torch.int32, device="cuda")
+    out, lse = ops.attn_fwd(inp.q, inp.k, inp.v, bs, topk, idx_out=idx)
+    a = ops.attn_bwd(inp.q, inp.k, inp.v, out, lse, dout, bs, topk)
+    b = ops.attn_bwd(inp.q, inp.k, inp.v, out, lse, dout, bs, topk, idx_in=idx)
+    assert ops.get_status() == ops.MOBA_OK
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    d = (a[0].float() - b[0].float()).abs()
+    assert d.max() <= 1e-2 * a[0].float().abs().max(), d.max()
+    assert d.mean() <= 2e-3 * a[0].float().abs().mean(), d.mean()
+
+
 def test_backward_train32k_sampled_and_identities():
     # the 32K-token training shape: dq of sampled rows against the oracle, and
     # two exact identities of attention gradients over every key
