@@ -152,6 +152,24 @@ def test_backward_with_the_forwards_selection(seqlens, D, bs, topk):
     assert d.mean() <= 2e-3 * a[0].float().abs().mean(), d.mean()
 
 
+def test_backward_varlen_with_the_forwards_selection():
+    # the same for packed sequences (a partial tail block in each)
+    w = workloads.custom((1100, 900, 300), 2, 128, 128, 3, seed=35, qkv_scale=128 ** -0.5,
+                         varlen=True)
+    inp = workloads.make_inputs(w, device="cuda")
+    dout = workloads.make_grad(w, device="cuda")
+    cu = torch.tensor(inp.cu_seqlens, dtype=torch.int32, device="cuda")
+    idx = torch.empty(w.total, w.H, 3, dtype=torch.int32, device="cuda")
+    out, lse = ops.attn_fwd_varlen(inp.q, inp.k, inp.v, cu, w.S, w.block_size, 3, idx_out=idx)
+    a = ops.attn_bwd_varlen(inp.q, inp.k, inp.v, out, lse, dout, cu, w.S, w.block_size, 3)
+    b = ops.attn_bwd_varlen(inp.q, inp.k, inp.v, out, lse, dout, cu, w.S, w.block_size, 3,
+                            idx_in=idx)
+    assert ops.get_status() == ops.MOBA_OK
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    d = (a[0].float() - b[0].float()).abs()
+    assert d.max() <= 1e-2 * a[0].float().abs().max(), d.max()
+
+
 def test_backward_train32k_sampled_and_identities():
     # the 32K-token training shape: dq of sampled rows against the oracle, and
     # two exact identities of attention gradients over every key
